@@ -1,0 +1,208 @@
+"""CPU oracle for the FarSkip-Collective MoE layer stack -- TEST INFRASTRUCTURE.
+
+A ctypes wrapper around ``oracle.c`` (plain C, fp64 accumulation).  Only the
+tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference
+arm may import this package.  It imports nothing from the CUDA library and the
+library imports nothing from it.
+
+Every function takes numpy arrays.  bf16 tensors are passed as ``uint16`` arrays
+(the raw bit patterns) together with ``dtype="bf16"``.
+
+Source of the formulas: "FarSkip-Collective: Unhobbling Blocking Communication
+in Mixture of Experts Models" (papercache.org summary), §2.1 (MLP and MoE
+equations, Dispatch/Combine) and §3 (FarSkip equation, eq. 8a/8b).  The readings
+taken where the page is silent are stated in ``oracle.c``.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, hand-derived golden values, brute force, reductions to a dense
+MLP, invariants).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16, F64 = 0, 1, 2
+EXACT, STORE_BF16, STORE_F32 = 0, 1, 2
+GATES = {"softmax": 0, "softmax_renorm": 1, "sigmoid": 2, "sigmoid_norm": 3}
+WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (OpenMP over tokens).  Returns its path."""
+    with _lock:
+        stale = (not os.path.exists(_LIB)) or any(
+            os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+        if force or stale:
+            tmp = _LIB + ".%d.tmp" % os.getpid()
+            subprocess.check_call(["gcc", "-O2", "-fopenmp", "-std=c11", "-shared", "-fPIC",
+                                   "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("d", "E", "k", "c", "n_shared", "c_shared", "gate", "in_dtype", "storage")]
+
+
+class _W(ctypes.Structure):
+    _fields_ = [("w_r", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("w1", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w3", ctypes.c_void_p),
+                ("w1s", ctypes.c_void_p), ("w2s", ctypes.c_void_p), ("w3s", ctypes.c_void_p)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        L.oracle_round.restype = ctypes.c_double
+        L.oracle_round.argtypes = [ctypes.c_double, ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def _dt(a: np.ndarray, dtype: str | None = None) -> int:
+    if dtype == "bf16" or a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError("unsupported oracle input dtype %s" % a.dtype)
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def round_storage(x: float, storage: int) -> float:
+    return float(lib().oracle_round(float(x), int(storage)))
+
+
+def make_cfg(d, E, k, c, n_shared=0, c_shared=0, gate="softmax_renorm", in_dtype=F32,
+             storage=EXACT) -> _Cfg:
+    g = GATES[gate] if isinstance(gate, str) else int(gate)
+    return _Cfg(d, E, k, c, n_shared, c_shared, g, in_dtype, storage)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError("oracle %s failed (rc=%d)" % (what, rc))
+
+
+def router(cfg: _Cfg, u: np.ndarray, w_r: np.ndarray, bias: np.ndarray | None = None):
+    """Logits z = u W_R^T + b (fp64), top-k indices and gate weights."""
+    u = np.ascontiguousarray(u)
+    n = u.shape[0]
+    logits = np.zeros((n, cfg.E), np.float64)
+    idx = np.zeros((n, cfg.k), np.int32)
+    w = np.zeros((n, cfg.k), np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    _check(lib().oracle_router(ctypes.byref(cfg), ctypes.c_int(n), _p(u), ctypes.c_int(_dt(u)),
+                               _p(np.ascontiguousarray(w_r)), _p(b),
+                               _p(logits), _p(idx), _p(w)), "router")
+    return logits, idx, w
+
+
+def expert_rows(cfg: _Cfg, a: np.ndarray, expert: np.ndarray, w1, w2, w3):
+    """Per row r: h = SiLU(a W2[e]^T) * (a W1[e]^T) and y = h W3[e]^T (rounded per storage)."""
+    a = np.ascontiguousarray(a)
+    n = a.shape[0]
+    h = np.zeros((n, cfg.c), np.float64)
+    y = np.zeros((n, cfg.d), np.float64)
+    ex = np.ascontiguousarray(expert, dtype=np.int32)
+    _check(lib().oracle_expert_rows(ctypes.byref(cfg), ctypes.c_int(n), _p(a), ctypes.c_int(_dt(a)),
+                                    _p(ex), _p(np.ascontiguousarray(w1)), _p(np.ascontiguousarray(w2)),
+                                    _p(np.ascontiguousarray(w3)), _p(h), _p(y)), "expert_rows")
+    return h, y
+
+
+class Weights:
+    """One block's weights in the page's layout (numpy; bf16 as uint16)."""
+
+    def __init__(self, w_r, w1, w2, w3, bias=None, w1s=None, w2s=None, w3s=None):
+        c = np.ascontiguousarray
+        self.w_r, self.w1, self.w2, self.w3 = c(w_r), c(w1), c(w2), c(w3)
+        self.bias = None if bias is None else c(bias, dtype=np.float32)
+        self.w1s = None if w1s is None else c(w1s)
+        self.w2s = None if w2s is None else c(w2s)
+        self.w3s = None if w3s is None else c(w3s)
+
+    def struct(self) -> _W:
+        return _W(_p(self.w_r), _p(self.bias), _p(self.w1), _p(self.w2), _p(self.w3),
+                  _p(self.w1s), _p(self.w2s), _p(self.w3s))
+
+
+def stack(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, want_rs: bool = False,
+          want_logits: bool = True):
+    """Run L = len(weights) FarSkip blocks on the rows of x.
+
+    Returns a dict with o (= o_L), o_star (= o_L*), topk_idx [L,n,k], topk_w [L,n,k],
+    logits [L,n,E] and, with want_rs, R and S [L,n,d]."""
+    x = np.ascontiguousarray(x)
+    L = len(weights)
+    n = x.shape[0]
+    arr = (_W * L)(*[w.struct() for w in weights])
+    out = {
+        "o": np.zeros((n, cfg.d), np.float64),
+        "o_star": np.zeros((n, cfg.d), np.float64),
+        "topk_idx": np.zeros((L, n, cfg.k), np.int32),
+        "topk_w": np.zeros((L, n, cfg.k), np.float64),
+        "logits": np.zeros((L, n, cfg.E), np.float64) if want_logits else None,
+        "R": np.zeros((L, n, cfg.d), np.float64) if want_rs else None,
+        "S": np.zeros((L, n, cfg.d), np.float64) if want_rs else None,
+    }
+    _check(lib().oracle_stack(ctypes.byref(cfg), arr, ctypes.c_int(L), ctypes.c_int(WIRINGS[wiring]),
+                              ctypes.c_int(n), _p(x), ctypes.c_int(_dt(x)),
+                              _p(out["o"]), _p(out["o_star"]), _p(out["topk_idx"]), _p(out["topk_w"]),
+                              _p(out["logits"]), _p(out["R"]), _p(out["S"])), "stack")
+    return out
+
+
+def dispatch(T: int, k: int, E: int, topk_idx: np.ndarray):
+    """Counting-sort Dispatch: counts[E], offsets[E+1], pos[T*k], perm_src[T*k]."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    pos = np.zeros(T * k, np.int32)
+    perm = np.zeros(T * k, np.int32)
+    _check(lib().oracle_dispatch(ctypes.c_int(T), ctypes.c_int(k), ctypes.c_int(E), _p(idx),
+                                 _p(counts), _p(offsets), _p(pos), _p(perm)), "dispatch")
+    return counts, offsets, pos, perm
+
+
+def combine(T, k, d, y_perm, pos, topk_w, o_prev, shared_out=None, storage=EXACT):
+    """o* = o_prev + S and o = o_prev + S + sum_s w_s y_perm[pos] (fp64, rounded per storage)."""
+    y_perm = np.ascontiguousarray(y_perm)
+    o_prev = np.ascontiguousarray(o_prev)
+    dt = _dt(y_perm)
+    assert _dt(o_prev) == dt and (shared_out is None or _dt(shared_out) == dt)
+    o_star = np.zeros((T, d), np.float64)
+    o = np.zeros((T, d), np.float64)
+    _check(lib().oracle_combine(ctypes.c_int(T), ctypes.c_int(k), ctypes.c_int(d), ctypes.c_int(dt),
+                                ctypes.c_int(storage), _p(y_perm),
+                                _p(np.ascontiguousarray(pos, dtype=np.int32)),
+                                _p(np.ascontiguousarray(topk_w, dtype=np.float32)), _p(o_prev),
+                                _p(None if shared_out is None else np.ascontiguousarray(shared_out)),
+                                _p(o_star), _p(o)), "combine")
+    return o_star, o

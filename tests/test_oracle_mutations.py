@@ -1,0 +1,84 @@
+"""The oracle's pins are strong enough: plant plausible mistakes in copies of the
+oracle (on the CPU only) and check that at least one pin fails for each.
+
+Each mutant is compiled from a string-edited copy of ``oracle/oracle.c`` into a
+temporary library; the pin functions of ``test_oracle_pins`` run against it.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "silu_on_up_projection": ("silu(gate) * up", "silu(up) * gate"),
+    "w3_transposed": ("elem(w3, base3 + (size_t)i * c + j, wdt)", "elem(w3, base3 + (size_t)j * d + i, wdt)"),
+    "ties_to_higher_index": ("if (best < 0 || z[j] > z[best]) best = j;", "if (best < 0 || z[j] >= z[best]) best = j;"),
+    "renorm_over_all_experts": ("for (int s = 0; s < k; ++s) den += exp(z[e[s]] - zmax);",
+                                "for (int j = 0; j < E; ++j) den += exp(z[j] - zmax);"),
+    "sigmoid_norm_unnormalised": ("w[s] = sigmoid(z[e[s]]) / den;", "w[s] = sigmoid(z[e[s]]);"),
+    "bias_dropped": ("if (bias) acc += (double)bias[j];", ""),
+    "partial_wiring_uses_o_k": ("if (wiring == ORACLE_WIRE_PARTIAL) u = os_k;", "if (wiring == ORACLE_WIRE_PARTIAL) u = o_k;"),
+    "outdated_wiring_uses_o_star": ("else if (wiring == ORACLE_WIRE_OUTDATED) u = o_km1;",
+                                    "else if (wiring == ORACLE_WIRE_OUTDATED) u = os_k;"),
+    "o_star_without_shared": ("o_star[(size_t)t * d + i] = oracle_round(op + sv, cfg->storage);",
+                              "o_star[(size_t)t * d + i] = oracle_round(op, cfg->storage);"),
+    "gate_weight_dropped": ("for (int i = 0; i < d; ++i) R[i] += w * oracle_round(y[i], cfg->storage);",
+                            "for (int i = 0; i < d; ++i) R[i] += oracle_round(y[i], cfg->storage);"),
+    "dispatch_unstable": ("for (int t = 0; t < T; ++t) {\n        for (int s = 0; s < k; ++s) {\n            int e = topk_idx[(size_t)t * k + s];\n            int p = cursor[e]++;",
+                          "for (int t = T - 1; t >= 0; --t) {\n        for (int s = 0; s < k; ++s) {\n            int e = topk_idx[(size_t)t * k + s];\n            int p = cursor[e]++;"),
+    "combine_weight_dropped": ("r += (double)topk_w[(size_t)t * k + s] * elem(y_perm, p * d + i, in_dtype);",
+                               "r += elem(y_perm, p * d + i, in_dtype);"),
+    "rounding_ties_away": ("double r = nearbyint(x / q) * q;", "double r = round(x / q) * q;"),
+    "shared_sum_rounded_per_expert": ("for (int i = 0; i < d; ++i) S[i] += y[i];",
+                                      "for (int i = 0; i < d; ++i) S[i] += (sh == 0 ? y[i] : 0.0);"),
+}
+
+PIN_TESTS = [
+    lambda: [pins.test_golden_gates(g) for g in ("softmax", "softmax_renorm", "sigmoid", "sigmoid_norm")],
+    pins.test_golden_tie_and_bias,
+    pins.test_golden_mlp,
+    pins.test_golden_dispatch,
+    pins.test_golden_rounding,
+    lambda: [pins.test_router_vs_library(g) for g in ("softmax", "softmax_renorm", "sigmoid", "sigmoid_norm")],
+    pins.test_dispatch_vs_library,
+    lambda: [pins.test_brute_force_dense_moe(g) for g in ("softmax", "softmax_renorm", "sigmoid", "sigmoid_norm")],
+    pins.test_tp_slice_identity,
+    lambda: [pins.test_telescoping_and_wiring(w) for w in ("partial", "outdated", "disabled")],
+    pins.test_disabled_is_plain_recurrence_and_L1_agrees,
+    lambda: [pins.test_dispatch_combine_round_trip(k, w) for k, w in ((1, 1.0), (2, 0.5), (4, 0.25))],
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: %s" % name
+    mut = src.replace(old, new)
+    cpath = tmp_path / "oracle_mut.c"
+    cpath.write_text(mut)
+    so = tmp_path / "liboracle_mut.so"
+    subprocess.check_call(["gcc", "-O1", "-fopenmp", "-std=c11", "-shared", "-fPIC",
+                           "-I", os.path.dirname(SRC), "-o", str(so), str(cpath), "-lm"])
+    mutant = ctypes.CDLL(str(so))
+    mutant.oracle_round.restype = ctypes.c_double
+    mutant.oracle_round.argtypes = [ctypes.c_double, ctypes.c_int]
+    saved = oracle.lib()
+    oracle._lib = mutant
+    caught = []
+    try:
+        for t in PIN_TESTS:
+            try:
+                t()
+            except (AssertionError, RuntimeError):
+                caught.append(t)
+    finally:
+        oracle._lib = saved
+    assert caught, "no pin catches the mutant %s" % name
