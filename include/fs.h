@@ -1,0 +1,194 @@
+/*
+ * fs.h -- C ABI of libfs, the GB300 (sm_103a) FarSkip-Collective MoE layer library.
+ *
+ * What is computed ("FarSkip-Collective: Unhobbling Blocking Communication in
+ * Mixture of Experts Models", papercache.org summary):
+ *   §2.1 MLP equation   MLP(A) = sigma(A W1^T . g(A W2^T)) W3^T, read as
+ *                       (SiLU(A W2^T) * (A W1^T)) W3^T  (W1 = up, W2 = gate, W3 = down)
+ *   §2.1 MoE equation   MoE(A) = sum_j G(A)_j MLP^j(A),  G(A) = s(A W_R^T)
+ *   §2.1 Dispatch / Combine: on one GPU a local stable permutation of token rows
+ *                       by expert and the gate-weighted sum back to token order;
+ *                       a shared expert processes every token
+ *   §3 FarSkip equation o_k = o_0 + f_1(o_0) + f_2(o_1*) + ... + f_k(o_{k-1}*)
+ *   §3 eq. (8a)/(8b)    o_k* = o_{k-1} (outdated) | o_{k-1} + f_k*(o_{k-1}*) (partial),
+ *                       f_k* = the shared-expert part of block k
+ *
+ * Conventions for every entry point:
+ *   - All pointers except `desc`/`blocks` are DEVICE pointers owned by the caller.
+ *     The library never allocates, frees or synchronises; every call is
+ *     asynchronous on `stream` (a cudaStream_t, NULL = the legacy default stream).
+ *   - Argument errors return before any launch and leave outputs untouched.
+ *     A failed launch returns FS_ERR_CUDA.  No exception crosses the ABI.
+ *   - Device-side faults that the kernels detect (an expert index out of range,
+ *     inconsistent offsets, a pipeline wait that ran out of time) never trap:
+ *     the kernel records a code in the library's device error word and skips
+ *     the work; fs_get_error() reads and clears it.
+ *   - Row-major layouts throughout.  Activations are [rows, d] with dtype
+ *     desc->dtype (bf16 or fp32); gate weights and logits are fp32; indices int32.
+ *   - Pointers must be 16-byte aligned; d and c must be multiples of 64;
+ *     n_shared * c_shared must be a multiple of 64.  Otherwise FS_ERR_UNSUPPORTED.
+ *   - Workspace: `ws` is caller-owned device scratch of at least
+ *     fs_workspace_bytes(desc, L) bytes (L = 0 for the single-step calls),
+ *     256-byte aligned.  Contents need not be initialised.
+ */
+#ifndef FARSKIP_FS_H
+#define FARSKIP_FS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FS_OK = 0,
+    FS_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, k > E, bad enum */
+    FS_ERR_UNSUPPORTED = 2,   /* shape/alignment outside what the kernels handle */
+    FS_ERR_WORKSPACE = 3,     /* ws too small or misaligned */
+    FS_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+    FS_ERR_DEVICE_STATE = 5   /* fs_get_error: a kernel recorded a device-side fault */
+} fs_status;
+
+typedef enum { FS_BF16 = 0, FS_F32 = 1 } fs_dtype;
+
+/* Gate rule s() applied to the top-k logits z (after the optional bias):
+ *   SOFTMAX         w_s = exp(z_s) / sum over ALL experts of exp(z_j)
+ *   SOFTMAX_RENORM  w_s = exp(z_s) / sum over the k chosen of exp(z_s')
+ *   SIGMOID         w_s = sigmoid(z_s)
+ *   SIGMOID_NORM    w_s = sigmoid(z_s) / sum over the k chosen of sigmoid(z_s')
+ * Selection: the k largest z, descending, ties to the lower expert index. */
+typedef enum {
+    FS_GATE_SOFTMAX = 0,
+    FS_GATE_SOFTMAX_RENORM = 1,
+    FS_GATE_SIGMOID = 2,
+    FS_GATE_SIGMOID_NORM = 3
+} fs_gate;
+
+/* Input of block k+1 (§3, eq. 8a/8b): PARTIAL u = o_k* = o_{k-1} + S_k,
+ * OUTDATED u = o_{k-1}, DISABLED u = o_k (plain residual recurrence). */
+typedef enum { FS_WIRE_PARTIAL = 0, FS_WIRE_OUTDATED = 1, FS_WIRE_DISABLED = 2 } fs_wiring;
+
+/* One MoE layer: T tokens of width d, E routed experts of width c, top-k,
+ * n_shared shared experts of width c_shared (0 = none), activation dtype, gate. */
+typedef struct {
+    int32_t T, d, E, k, c, n_shared, c_shared;
+    int32_t dtype;   /* fs_dtype */
+    int32_t gate;    /* fs_gate */
+} fs_layer_desc;
+
+/* One block's weights in the library's packed layout (see fs_pack_w13 /
+ * fs_pack_w3_shared).  Element type = desc->dtype. */
+typedef struct {
+    const void* w_r;        /* [E, d] router (W_R) */
+    const float* bias;      /* [E] router bias added to the logits, or NULL */
+    const void* w13;        /* [E, 2c, d] packed gate/up (fs_pack_w13) */
+    const void* w3;         /* [E, d, c] down (W3) */
+    const void* w13_shared; /* [2 n_shared c_shared, d] packed, NULL when n_shared = 0 */
+    const void* w3_shared;  /* [d, n_shared c_shared] (fs_pack_w3_shared) */
+} fs_block_weights;
+
+/* Bytes of workspace needed by the single-step calls (L = 0) or by
+ * fs_farskip_stack with L blocks (L >= 1).  Returns 0 for an invalid desc. */
+size_t fs_workspace_bytes(const fs_layer_desc* desc, int L);
+
+/* Repack the page's W1 (up) and W2 (gate), each [G, c, d], into w13 [G, 2c, d]:
+ * for each group of 64 expert columns b, rows [128b, 128b+64) of w13 are W2
+ * rows [64b, 64b+64) (gate) and rows [128b+64, 128b+128) are W1 rows (up).
+ * The SwiGLU epilogue then finds gate and up of one column in the same tile.
+ * c must be a multiple of 64.  Element type = dtype. */
+fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype,
+                      const void* w1, const void* w2, void* w13, void* stream);
+
+/* Concatenate n_shared shared-expert down projections, each [d, c_shared],
+ * along the expert width: w3cat[i, s c_shared + j] = w3s[s, i, j], giving
+ * [d, n_shared c_shared].  By the TP-slicing identity of §2.1 the sum of the
+ * shared experts equals one MLP over the concatenated width; their gate/up
+ * weights [n_shared, c_shared, d] are already concatenated in memory and are
+ * packed with fs_pack_w13(G = 1, c = n_shared c_shared). */
+fs_status fs_pack_w3_shared(int32_t n_shared, int32_t c_shared, int32_t d, int32_t dtype,
+                            const void* w3s, void* w3cat, void* stream);
+
+/* Router (§2.1, G(A) = s(A W_R^T)): logits z = u W_R^T + bias (fp32 accumulate;
+ * bf16 operands on the tensor cores for FS_BF16, fp32 FMA for FS_F32), then the
+ * top-k selection and gate weights of desc->gate.
+ *   u [T, d], w_r [E, d], bias [E] fp32 or NULL
+ *   -> topk_idx [T, k] int32 (slot order = descending z), topk_w [T, k] fp32,
+ *      logits [T, E] fp32 (z without the bias; NULL = kept in ws only).
+ * Needs ws of fs_workspace_bytes(desc, 0) bytes.  E <= 512, k <= 16. */
+fs_status fs_router_topk(const fs_layer_desc* desc, const void* u, const void* w_r,
+                         const float* bias, int32_t* topk_idx, float* topk_w, float* logits,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch (§2.1, local form): stable counting sort of the (token, slot) pairs
+ * by expert, in token order within each expert, and the permuted copy of u.
+ *   topk_idx [T, k], u [T, d]
+ *   -> counts [E], offsets [E+1] (exclusive prefix, offsets[E] = T k),
+ *      pos [T k] (pos[t k + s] = permuted row of (t, s)),
+ *      perm_src [T k] (perm_src[p] = token of permuted row p),
+ *      x_perm [T k, d] (x_perm[p] = u[perm_src[p]]).
+ * An index outside [0, E) sets the device error word (reported by
+ * fs_get_error) and that pair is dropped. */
+fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u,
+                      int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
+                      void* x_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Routed experts (§2.1 MLP and MoE equations), grouped by expert: for every
+ * expert e and every row p in [offsets[e], offsets[e+1]):
+ *   h = SiLU(x W2_e^T) * (x W1_e^T)  (fp32 accumulate, stored bf16/fp32 in ws)
+ *   y_perm[p] = h W3_e^T             (fp32 accumulate, stored in desc->dtype)
+ *   x_perm [T k, d], offsets [E+1] (device; the host never reads them),
+ *   w13 [E, 2c, d] packed, w3 [E, d, c] -> y_perm [T k, d].
+ * bf16: persistent tcgen05/TMEM grouped GEMMs fed by TMA; fp32: fp32 FMA. */
+fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets,
+                            const void* w13, const void* w3, void* y_perm,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Shared expert(s) (§2.1): S = sum_i MLP_shared_i(u) over all T tokens, as one
+ * MLP of width n_shared c_shared.  u [T, d] -> s_out [T, d]. */
+fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void* w13_shared,
+                           const void* w3_shared, void* s_out, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Combine (§2.1, local form) fused with the FarSkip update (§3, eq. 8b):
+ *   R[t]  = sum_{s<k} topk_w[t, s] * y_perm[pos[t k + s]]   (fp32, slot order)
+ *   o_partial[t] = o_prev[t] + S[t]                          (o_k*)
+ *   o_full[t]    = o_prev[t] + S[t] + R[t]                   (o_k)
+ * all sums in fp32, each output rounded once.  shared_out NULL = no shared
+ * expert (S = 0); o_partial NULL = not written. */
+fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_t* pos,
+                     const float* topk_w, const void* o_prev, const void* shared_out,
+                     void* o_partial, void* o_full, void* stream);
+
+/* L FarSkip blocks (§3): o_0 = u_1 = x; block k runs router, dispatch, routed
+ * experts, shared expert and combine on u_k and o_{k-1}, producing
+ * o_k* = o_{k-1} + S_k and o_k = o_k* + R_k; u_{k+1} follows `wiring`.
+ *   blocks [L] (host array of device pointers), x [T, d]
+ *   -> o_full = o_L, o_partial = o_L* (NULL = not written).
+ * Needs ws of fs_workspace_bytes(desc, L) bytes.  Everything is enqueued on
+ * `stream` with no host synchronisation. */
+fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
+                           const fs_block_weights* blocks, const void* x,
+                           void* o_full, void* o_partial, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Read and clear the device error word (synchronises the device).  FS_OK when
+ * no kernel recorded a fault; FS_ERR_DEVICE_STATE otherwise, with the raw code
+ * in *code when code != NULL (1 = expert index out of range, 2 = inconsistent
+ * offsets, 3 = pipeline wait timed out, 4 = size beyond a kernel limit). */
+fs_status fs_get_error(int32_t* code);
+
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t fs_launch_count(void);
+
+/* Text of the last CUDA error behind an FS_ERR_CUDA on this host thread
+ * ("" if none).  The string is owned by the library. */
+const char* fs_last_cuda_error(void);
+
+/* Human-readable name of a status. */
+const char* fs_status_string(fs_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,391 @@
+// api.cu -- the C ABI of libfs: argument validation, workspace planning, the
+// single-step entry points and the L-block FarSkip driver.
+//
+// "FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
+// Models" (papercache.org summary): §2.1 (MLP, MoE, router, Dispatch, Combine,
+// shared expert) and §3 (FarSkip equation, eq. 8a/8b).  Every step of the
+// path runs in this library's kernels; the host side only validates, plans
+// buffers inside the caller's workspace and enqueues launches.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/fs.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fs {
+
+__device__ int g_fs_dev_error;
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static thread_local char g_last_cuda[256] = "";
+
+static int* g_err_ptr[64] = {nullptr};
+
+int* dev_error_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fs_dev_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+static fs_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FS_OK;
+    std::snprintf(g_last_cuda, sizeof g_last_cuda, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return FS_ERR_CUDA;
+}
+
+#define FS_TRY(expr)                               \
+    do {                                           \
+        cudaError_t e_ = (expr);                   \
+        if (e_ != cudaSuccess) return cuda_status(e_); \
+    } while (0)
+
+// ------------------------------------------------------------- validation
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static fs_status check_desc(const fs_layer_desc* d) {
+    if (!d) return FS_ERR_INVALID_ARG;
+    if (d->T < 1 || d->d < 1 || d->E < 1 || d->k < 1 || d->c < 1 || d->n_shared < 0) return FS_ERR_INVALID_ARG;
+    if (d->k > d->E) return FS_ERR_INVALID_ARG;
+    if (d->dtype != FS_BF16 && d->dtype != FS_F32) return FS_ERR_INVALID_ARG;
+    if (d->gate < FS_GATE_SOFTMAX || d->gate > FS_GATE_SIGMOID_NORM) return FS_ERR_INVALID_ARG;
+    if (d->n_shared > 0 && d->c_shared < 1) return FS_ERR_INVALID_ARG;
+    if (d->d % 64 || d->c % 64) return FS_ERR_UNSUPPORTED;
+    if (d->n_shared > 0 && d->c_shared % 64) return FS_ERR_UNSUPPORTED;
+    if (d->E > kMaxExperts || d->k > kMaxTopK) return FS_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(d->T) * d->k;
+    if (rows > 0x7fffffffLL - 1024) return FS_ERR_UNSUPPORTED;
+    return FS_OK;
+}
+
+static inline int elem_bytes(const fs_layer_desc* d) { return d->dtype == FS_BF16 ? 2 : 4; }
+
+// ------------------------------------------------------------- workspace
+struct Layout {
+    // single-step regions (L = 0)
+    size_t logits, disp, plan_z, plan_r, h_r, plan_s, h_s, end0;
+    // stack regions (L >= 1)
+    size_t topk_idx, topk_w, counts, offsets, pos, perm, x_perm, y_perm, s_out, ring[3], star[2], end;
+};
+
+static Layout layout(const fs_layer_desc* d, int L) {
+    const size_t A = 256;
+    const size_t es = elem_bytes(d);
+    const size_t T = d->T, E = d->E, k = d->k, dm = d->d;
+    const size_t rows = T * k;
+    const size_t cw = static_cast<size_t>(d->n_shared) * d->c_shared;
+    Layout l;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, A); return at; };
+    l.logits = take(T * E * 4);
+    l.disp = take(dispatch_ws_bytes(d->T, d->E));
+    l.plan_z = take(4 * sizeof(int));
+    l.plan_r = take(2 * (E + 1) * sizeof(int));
+    l.h_r = take(rows * d->c * es);
+    l.plan_s = take(4 * sizeof(int));
+    l.h_s = take(T * cw * es);
+    l.end0 = o;
+    l.topk_idx = take(rows * 4);
+    l.topk_w = take(rows * 4);
+    l.counts = take(E * 4);
+    l.offsets = take((E + 1) * 4);
+    l.pos = take(rows * 4);
+    l.perm = take(rows * 4);
+    l.x_perm = take(rows * dm * es);
+    l.y_perm = take(rows * dm * es);
+    l.s_out = take(cw ? T * dm * es : 0);
+    const int nring = L > 1 ? (L - 1 < 3 ? L - 1 : 3) : 0;
+    const int nstar = L > 1 ? (L - 1 < 2 ? L - 1 : 2) : 0;
+    for (int i = 0; i < 3; ++i) l.ring[i] = i < nring ? take(T * dm * es) : 0;
+    for (int i = 0; i < 2; ++i) l.star[i] = i < nstar ? take(T * dm * es) : 0;
+    l.end = o;
+    return l;
+}
+
+static fs_status check_ws(const fs_layer_desc* d, int L, const void* ws, size_t ws_bytes) {
+    if (!ws) return FS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return FS_ERR_WORKSPACE;
+    const Layout l = layout(d, L);
+    if (ws_bytes < (L >= 1 ? l.end : l.end0)) return FS_ERR_WORKSPACE;
+    return FS_OK;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+static inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// ------------------------------------------------------------ step bodies
+static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* w_r, const float* bias,
+                             int32_t* idx, float* w, float* logits, void* ws, cudaStream_t st) {
+    const Layout l = layout(d, 0);
+    float* z = logits ? logits : at<float>(ws, l.logits);
+    int* plan = at<int>(ws, l.plan_z);
+    if (d->dtype == FS_BF16) {
+        const int bm = tc_block_m();
+        FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
+        FS_TRY(launch_tc_gemm(EPI_F32, u, d->T, w_r, 1, d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E,
+                              st));
+    } else {
+        const int bm = simt_block_m();
+        FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
+        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(u), static_cast<const float*>(w_r), 1, d->E,
+                                d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E, st));
+    }
+    FS_TRY(launch_topk(z, bias, d->T, d->E, d->k, d->gate, idx, w, st));
+    return FS_OK;
+}
+
+static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const void* u, int32_t* counts,
+                               int32_t* offsets, int32_t* pos, int32_t* perm, void* x_perm, void* ws,
+                               cudaStream_t st) {
+    const Layout l = layout(d, 0);
+    FS_TRY(launch_dispatch(idx, u, d->T, d->d, d->E, d->k, elem_bytes(d), counts, offsets, pos, perm, x_perm,
+                           at<int32_t>(ws, l.disp), st));
+    return FS_OK;
+}
+
+// Two grouped GEMMs over `rows` rows split into G groups by `offsets`
+// (nullptr = one group): h = SiLU(x W2^T) * (x W1^T), then y = h W3^T.
+static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, int rows, const int32_t* offsets, int G,
+                             int cw, const void* w13, const void* w3, void* y, int* plan, void* h,
+                             cudaStream_t st) {
+    if (d->dtype == FS_BF16) {
+        const int bm = tc_block_m();
+        const int max_mt = ceil_div(rows, bm) + G;
+        FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
+        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, st));
+        FS_TRY(launch_tc_gemm(EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d, st));
+    } else {
+        const int bm = simt_block_m();
+        const int max_mt = ceil_div(rows, bm) + G;
+        FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
+        FS_TRY(launch_simt_gemm(EPI_SWIGLU, static_cast<const float*>(x), static_cast<const float*>(w13), G, 2 * cw,
+                                d->d, plan, max_mt, static_cast<float*>(h), cw, cw, st));
+        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(h), static_cast<const float*>(w3), G, d->d, cw,
+                                plan, max_mt, static_cast<float*>(y), d->d, d->d, st));
+    }
+    return FS_OK;
+}
+
+static fs_status routed_impl(const fs_layer_desc* d, const void* x_perm, const int32_t* offsets, const void* w13,
+                             const void* w3, void* y_perm, void* ws, cudaStream_t st) {
+    const Layout l = layout(d, 0);
+    return swiglu_impl(d, x_perm, d->T * d->k, offsets, d->E, d->c, w13, w3, y_perm, at<int>(ws, l.plan_r),
+                       at<void>(ws, l.h_r), st);
+}
+
+static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* w13s, const void* w3s, void* s_out,
+                             void* ws, cudaStream_t st) {
+    const Layout l = layout(d, 0);
+    return swiglu_impl(d, u, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out,
+                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), st);
+}
+
+static fs_status combine_impl(const fs_layer_desc* d, const void* y_perm, const int32_t* pos, const float* w,
+                              const void* o_prev, const void* s, void* o_partial, void* o_full, cudaStream_t st) {
+    FS_TRY(launch_combine(y_perm, pos, w, o_prev, s, o_partial, o_full, d->T, d->d, d->k, d->dtype == FS_BF16, st));
+    return FS_OK;
+}
+
+}  // namespace fs
+
+using namespace fs;
+
+#define FS_CHECK(expr)              \
+    do {                            \
+        fs_status s_ = (expr);      \
+        if (s_ != FS_OK) return s_; \
+    } while (0)
+
+static fs_status need(const void* p) {
+    if (!p) return FS_ERR_INVALID_ARG;
+    return aligned16(p) ? FS_OK : FS_ERR_UNSUPPORTED;
+}
+
+extern "C" {
+
+size_t fs_workspace_bytes(const fs_layer_desc* desc, int L) {
+    if (check_desc(desc) != FS_OK || L < 0) return 0;
+    const Layout l = layout(desc, L);
+    return L >= 1 ? l.end : l.end0;
+}
+
+fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype, const void* w1, const void* w2, void* w13,
+                      void* stream) {
+    if (G < 1 || c < 1 || d < 1 || (dtype != FS_BF16 && dtype != FS_F32)) return FS_ERR_INVALID_ARG;
+    if (c % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w1));
+    FS_CHECK(need(w2));
+    FS_CHECK(need(w13));
+    FS_TRY(launch_pack_w13(G, c, d, dtype == FS_BF16 ? 2 : 4, w1, w2, w13, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+fs_status fs_pack_w3_shared(int32_t n_shared, int32_t c_shared, int32_t d, int32_t dtype, const void* w3s,
+                            void* w3cat, void* stream) {
+    if (n_shared < 1 || c_shared < 1 || d < 1 || (dtype != FS_BF16 && dtype != FS_F32)) return FS_ERR_INVALID_ARG;
+    if (c_shared % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w3s));
+    FS_CHECK(need(w3cat));
+    FS_TRY(launch_pack_w3_shared(n_shared, c_shared, d, dtype == FS_BF16 ? 2 : 4, w3s, w3cat,
+                                 static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+fs_status fs_router_topk(const fs_layer_desc* desc, const void* u, const void* w_r, const float* bias,
+                         int32_t* topk_idx, float* topk_w, float* logits, void* ws, size_t ws_bytes, void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(u));
+    FS_CHECK(need(w_r));
+    FS_CHECK(need(topk_idx));
+    FS_CHECK(need(topk_w));
+    if (bias && !aligned16(bias)) return FS_ERR_UNSUPPORTED;
+    if (logits && !aligned16(logits)) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    return router_impl(desc, u, w_r, bias, topk_idx, topk_w, logits, ws, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u, int32_t* counts,
+                      int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm, void* ws, size_t ws_bytes,
+                      void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(topk_idx));
+    FS_CHECK(need(u));
+    FS_CHECK(need(counts));
+    FS_CHECK(need(offsets));
+    FS_CHECK(need(pos));
+    FS_CHECK(need(perm_src));
+    FS_CHECK(need(x_perm));
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    return dispatch_impl(desc, topk_idx, u, counts, offsets, pos, perm_src, x_perm, ws,
+                         static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets, const void* w13,
+                            const void* w3, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(x_perm));
+    FS_CHECK(need(offsets));
+    FS_CHECK(need(w13));
+    FS_CHECK(need(w3));
+    FS_CHECK(need(y_perm));
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    return routed_impl(desc, x_perm, offsets, w13, w3, y_perm, ws, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void* w13_shared, const void* w3_shared,
+                           void* s_out, void* ws, size_t ws_bytes, void* stream) {
+    FS_CHECK(check_desc(desc));
+    if (desc->n_shared < 1) return FS_ERR_INVALID_ARG;
+    FS_CHECK(need(u));
+    FS_CHECK(need(w13_shared));
+    FS_CHECK(need(w3_shared));
+    FS_CHECK(need(s_out));
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    return shared_impl(desc, u, w13_shared, w3_shared, s_out, ws, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_t* pos, const float* topk_w,
+                     const void* o_prev, const void* shared_out, void* o_partial, void* o_full, void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(y_perm));
+    FS_CHECK(need(pos));
+    FS_CHECK(need(topk_w));
+    FS_CHECK(need(o_prev));
+    FS_CHECK(need(o_full));
+    if (shared_out && !aligned16(shared_out)) return FS_ERR_UNSUPPORTED;
+    if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
+    return combine_impl(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full,
+                        static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring, const fs_block_weights* blocks,
+                           const void* x, void* o_full, void* o_partial, void* ws, size_t ws_bytes, void* stream) {
+    FS_CHECK(check_desc(desc));
+    if (L < 1 || !blocks) return FS_ERR_INVALID_ARG;
+    if (wiring < FS_WIRE_PARTIAL || wiring > FS_WIRE_DISABLED) return FS_ERR_INVALID_ARG;
+    FS_CHECK(need(x));
+    FS_CHECK(need(o_full));
+    if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
+    for (int b = 0; b < L; ++b) {
+        FS_CHECK(need(blocks[b].w_r));
+        FS_CHECK(need(blocks[b].w13));
+        FS_CHECK(need(blocks[b].w3));
+        if (blocks[b].bias && !aligned16(blocks[b].bias)) return FS_ERR_UNSUPPORTED;
+        if (desc->n_shared > 0) {
+            FS_CHECK(need(blocks[b].w13_shared));
+            FS_CHECK(need(blocks[b].w3_shared));
+        }
+    }
+    FS_CHECK(check_ws(desc, L, ws, ws_bytes));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Layout l = layout(desc, L);
+    int32_t* idx = at<int32_t>(ws, l.topk_idx);
+    float* w = at<float>(ws, l.topk_w);
+    int32_t* counts = at<int32_t>(ws, l.counts);
+    int32_t* offsets = at<int32_t>(ws, l.offsets);
+    int32_t* pos = at<int32_t>(ws, l.pos);
+    int32_t* perm = at<int32_t>(ws, l.perm);
+    void* x_perm = at<void>(ws, l.x_perm);
+    void* y_perm = at<void>(ws, l.y_perm);
+    void* s_out = desc->n_shared > 0 ? at<void>(ws, l.s_out) : nullptr;
+
+    const void* u = x;        // u_k   (= o_{k-1}* in the page's notation)
+    const void* o_prev = x;   // o_{k-1}
+    for (int b = 1; b <= L; ++b) {
+        const fs_block_weights& bw = blocks[b - 1];
+        void* o_k = (b == L) ? o_full : at<void>(ws, l.ring[b % 3]);
+        void* os_k = (b == L) ? o_partial : at<void>(ws, l.star[b % 2]);
+        FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
+        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
+        FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
+        if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st));
+        FS_CHECK(combine_impl(desc, y_perm, pos, w, o_prev, s_out, os_k, o_k, st));
+        if (wiring == FS_WIRE_PARTIAL) u = os_k;
+        else if (wiring == FS_WIRE_OUTDATED) u = o_prev;
+        else u = o_k;
+        o_prev = o_k;
+    }
+    return FS_OK;
+}
+
+fs_status fs_get_error(int32_t* code) {
+    int* p = dev_error_ptr();
+    if (!p) return cuda_status(cudaGetLastError());
+    int v = 0;
+    FS_TRY(cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost));
+    const int zero = 0;
+    FS_TRY(cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice));
+    if (code) *code = v;
+    return v ? FS_ERR_DEVICE_STATE : FS_OK;
+}
+
+uint64_t fs_launch_count(void) { return g_launches.load(); }
+
+const char* fs_last_cuda_error(void) { return g_last_cuda; }
+
+const char* fs_status_string(fs_status s) {
+    switch (s) {
+        case FS_OK: return "FS_OK";
+        case FS_ERR_INVALID_ARG: return "FS_ERR_INVALID_ARG";
+        case FS_ERR_UNSUPPORTED: return "FS_ERR_UNSUPPORTED";
+        case FS_ERR_WORKSPACE: return "FS_ERR_WORKSPACE";
+        case FS_ERR_CUDA: return "FS_ERR_CUDA";
+        case FS_ERR_DEVICE_STATE: return "FS_ERR_DEVICE_STATE";
+        default: return "FS_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+// dispatch.cu -- local Dispatch: stable counting sort of (token, slot) pairs by
+// expert and the permuted copy of the token rows.
+//
+// "FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
+// Models", §2.1 Dispatch paragraph: tokens are grouped by the experts the
+// router chose for them and the activations are permuted accordingly (on one
+// GPU the all-to-all that follows is a local copy).  The order is deterministic
+// and stable: expert-major, token order inside an expert.
+//
+// Four launches, no atomics on global memory, no host synchronisation:
+//   1 count   chunk of 1024 tokens per CTA -> per-chunk expert histogram
+//   2 scan    one CTA: column scan over chunks, counts, exclusive offsets
+//   3 rank    chunk per CTA, one warp per 32 tokens: lane bitmasks per expert
+//             give the rank inside the warp, a scan over the CTA's warps the
+//             rank inside the chunk -> pos[t k + s], perm_src[p]
+//   4 copy    one warp per token: read the row of u once (16-byte vectors),
+//             write it to its k permuted rows
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fs {
+
+constexpr int kChunk = 1024;          // tokens per chunk (= threads of count/rank CTAs)
+constexpr int kChunkWarps = kChunk / 32;
+
+static inline int n_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+
+size_t dispatch_ws_bytes(int T, int E) { return static_cast<size_t>(n_chunks(T)) * E * sizeof(int32_t); }
+
+__global__ void __launch_bounds__(kChunk)
+dispatch_count_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k, int32_t* __restrict__ chunk_hist,
+                      int* err) {
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + threadIdx.x;
+    if (t < T) {
+        for (int s = 0; s < k; ++s) {
+            const int e = topk_idx[static_cast<long long>(t) * k + s];
+            if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+            else set_dev_error(err, DEV_ERR_EXPERT_INDEX);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_hist[static_cast<long long>(blockIdx.x) * E + e] = hist[e];
+}
+
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+dispatch_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E, int32_t* __restrict__ counts,
+                     int32_t* __restrict__ offsets) {
+    __shared__ int warp_sums[32];
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < E) {
+        int b = 0;
+        for (; b + 8 <= nchunks; b += 8) {        // 8 independent loads in flight
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = chunk_hist[static_cast<long long>(b + j) * E + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                chunk_hist[static_cast<long long>(b + j) * E + e] = total;
+                total += c[j];
+            }
+        }
+        for (; b < nchunks; ++b) {
+            const int c = chunk_hist[static_cast<long long>(b) * E + e];
+            chunk_hist[static_cast<long long>(b) * E + e] = total;
+            total += c;
+        }
+        counts[e] = total;
+    }
+    // exclusive scan of totals over experts
+    const int lane = e & 31, wid = e >> 5;
+    int v = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int excl = v - total + (wid > 0 ? warp_sums[wid - 1] : 0);
+    if (e < E) {
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + total;
+        for (int b = 0; b < nchunks; ++b) chunk_hist[static_cast<long long>(b) * E + e] += excl;
+    }
+}
+
+// chunk_base[b][e] = first permuted row of expert e for chunk b.
+__global__ void __launch_bounds__(kChunk)
+dispatch_rank_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ pos,
+                     int32_t* __restrict__ perm_src) {
+    extern __shared__ uint32_t wmask[];     // [kChunkWarps][E]: lane masks, then counts, then prefixes
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wmask[i] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + threadIdx.x;
+    int ex[kMaxTopK];
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+        ex[s] = -1;
+        if (s < k && t < T) {
+            const int e = topk_idx[static_cast<long long>(t) * k + s];
+            if (e >= 0 && e < E) {
+                ex[s] = e;
+                atomicOr(&wmask[w * E + e], 1u << lane);
+            }
+        }
+    }
+    __syncwarp();
+    const uint32_t lt = (1u << lane) - 1u;
+    int rank[kMaxTopK];
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) rank[s] = ex[s] >= 0 ? __popc(wmask[w * E + ex[s]] & lt) : 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wmask[i] = __popc(wmask[i]);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        uint32_t run = 0;
+        for (int ww = 0; ww < kChunkWarps; ++ww) {
+            const uint32_t c = wmask[ww * E + e];
+            wmask[ww * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    if (t < T) {
+        const int32_t* base = chunk_base + static_cast<long long>(blockIdx.x) * E;
+#pragma unroll
+        for (int s = 0; s < kMaxTopK; ++s) {
+            if (s >= k) break;
+            int p = -1;
+            if (ex[s] >= 0) {
+                p = base[ex[s]] + static_cast<int>(wmask[w * E + ex[s]]) + rank[s];
+                perm_src[p] = t;
+            }
+            pos[static_cast<long long>(t) * k + s] = p;
+        }
+    }
+}
+
+constexpr int kCopyWarps = 8;
+
+// One warp per token: x_perm[pos[t, s]] = u[t] for every slot s.
+__global__ void __launch_bounds__(kCopyWarps * 32)
+dispatch_copy_kernel(const uint4* __restrict__ u, int T, int row_vecs, int k, const int32_t* __restrict__ pos,
+                     uint4* __restrict__ x_perm) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kCopyWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int my_p = lane < k ? pos[static_cast<long long>(t) * k + lane] : -1;
+    const uint4* src = u + static_cast<long long>(t) * row_vecs;
+    for (int i0 = 0; i0 < row_vecs; i0 += 4 * 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * 32 + lane;
+            if (i < row_vecs) v[j] = __ldg(src + i);
+        }
+        for (int s = 0; s < k; ++s) {
+            const int p = __shfl_sync(0xffffffffu, my_p, s);
+            if (p < 0) continue;
+            uint4* dst = x_perm + static_cast<long long>(p) * row_vecs;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * 32 + lane;
+                if (i < row_vecs) dst[i] = v[j];
+            }
+        }
+    }
+}
+
+static cudaError_t set_smem_attr(const void* fn, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
+                            int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
+                            int32_t* scratch, cudaStream_t st) {
+    const int nc = n_chunks(T);
+    int* err = dev_error_ptr();
+    dispatch_count_kernel<<<nc, kChunk, E * sizeof(int32_t), st>>>(topk_idx, T, E, k, scratch, err);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(scratch, nc, E, counts, offsets);
+    count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t rank_smem = static_cast<size_t>(kChunkWarps) * E * sizeof(uint32_t);
+    e = set_smem_attr(reinterpret_cast<const void*>(dispatch_rank_kernel), rank_smem);
+    if (e != cudaSuccess) return e;
+    dispatch_rank_kernel<<<nc, kChunk, rank_smem, st>>>(topk_idx, T, E, k, scratch, pos, perm_src);
+    count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int row_vecs = d * elem_bytes / 16;
+    dispatch_copy_kernel<<<(T + kCopyWarps - 1) / kCopyWarps, kCopyWarps * 32, 0, st>>>(
+        reinterpret_cast<const uint4*>(u), T, row_vecs, k, pos, reinterpret_cast<uint4*>(x_perm));
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace fs

@@ -1,0 +1,472 @@
+// gemm_tc.cu -- persistent grouped GEMM on the 5th-generation tensor cores
+// (tcgen05.mma kind::f16, bf16 operands, fp32 accumulators in TMEM), operands
+// staged in shared memory by TMA with the 128-byte swizzle.
+//
+// One GEMM shape serves every dense contraction of the MoE layer
+// ("FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
+// Models", §2.1 MLP and MoE equations):
+//   EPI_SWIGLU : H = SiLU(X W2^T) * (X W1^T) from the packed [2c, d] gate/up weight
+//   EPI_BF16   : Y = H W3^T                       (down projection, bf16 out)
+//   EPI_F32    : Z = U W_R^T                      (router logits, fp32 out)
+// Rows are grouped (one group per expert; offsets live on the device and the
+// host never reads them).  Each group's rows [row_start[g], row_start[g+1]) are
+// multiplied by the group's own B = W[g] ([N, K], K-major).
+//
+// CTA = 6 warps, one CTA per SM, persistent over a static tile order:
+//   warp 0      TMA producer (one lane): A tile 128 x 64 and B tile 256 x 64 per stage
+//   warp 1      TMEM owner + MMA issuer (one lane): 4 x (128 x 256 x 16) MMAs per stage
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, activation, stores
+// TMEM holds two 128 x 256 fp32 accumulators (512 columns) so the epilogue of
+// tile i overlaps the MMAs of tile i + 1.  Every wait is bounded in time.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fs {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;                 // 64 bf16 = 128 B = one swizzle row
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KB
+constexpr int B_STAGE = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NACC = 2;
+constexpr int TMEM_COLS = NACC * BN;   // 512
+constexpr int THREADS = 192;
+constexpr int BAR_BYTES = 256;
+constexpr size_t SMEM_BYTES =
+    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * sizeof(int);
+
+struct Args {
+    const int* plan;   // [2 (G + 1)]: m-tile prefix (BM rows), then row_start
+    int G;
+    int N;             // B rows per group
+    int K;
+    int n_tiles;       // ceil(N / BN)
+    int max_mtiles;    // upper bound of the m-tile count (capacity check)
+    void* out;
+    long long ldo;     // output row stride in elements
+    int out_cols;      // valid output columns (EPI_F32 / EPI_BF16), c for EPI_SWIGLU
+    int* err;          // device error word
+};
+
+struct Tile {
+    int g, m, n, a_row, rows_valid, b_row;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const int* row_start, int G,
+                                            int n_tiles, int BNrows, int N) {
+    const int q = t / n_tiles;
+    int lo = 0, hi = G;            // last g with mt_start[g] <= q
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (mt_start[mid] <= q) lo = mid; else hi = mid;
+    }
+    Tile r;
+    r.g = lo;
+    const int mtiles = mt_start[lo + 1] - mt_start[lo];
+    const int local = t - mt_start[lo] * n_tiles;
+    r.n = local / mtiles;
+    r.m = local - r.n * mtiles;
+    r.a_row = row_start[lo] + r.m * BM;
+    const int rem = row_start[lo + 1] - r.a_row;
+    r.rows_valid = rem < BM ? rem : BM;
+    r.b_row = lo * N + r.n * BNrows;
+    return r;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const Args args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full = bars;                 // [STAGES]
+    uint64_t* empty = bars + STAGES;       // [STAGES]
+    uint64_t* tfull = bars + 2 * STAGES;   // [NACC]
+    uint64_t* tempty = tfull + NACC;       // [NACC]
+    uint64_t* fin = tempty + NACC;         // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* mt_start = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);
+    int* row_start = mt_start + (args.G + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = args.G;
+
+    for (int i = threadIdx.x; i < 2 * (G + 1); i += THREADS) mt_start[i] = args.plan[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 4);
+        }
+        mbar_init(smem_u32(fin), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int total_mtiles = mt_start[G];
+    if (total_mtiles < 0 || total_mtiles > args.max_mtiles) {
+        if (threadIdx.x == 0) set_dev_error(args.err, DEV_ERR_OFFSETS);
+        total_mtiles = 0;
+    }
+    const int total = total_mtiles * args.n_tiles;
+    const int num_kb = args.K / BK;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, tl.a_row);
+                    tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: the last loads (at most STAGES) must land before the CTA exits.
+            const int pending = issued < STAGES ? issued : STAGES;
+            for (int j = 1; j <= pending; ++j) {
+                int s = stage - j;
+                uint32_t ph = phase;
+                if (s < 0) { s += STAGES; ph ^= 1u; }
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(&full[s]), ph)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t use = static_cast<uint32_t>(it >> 1);
+                if (!mbar_wait(smem_u32(&tempty[acc]), (use & 1u) ^ 1u, abort_flag, args.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err)) { ok = false; break; }
+                    tc_fence_after();
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sa));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sa + A_STAGE));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // +32 bytes along K inside the 128-byte swizzle row = +2 in the >>4 address field
+                        tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&tfull[acc]));
+            }
+            // every MMA issued by this thread completes before TMEM is released
+            tc_commit(smem_u32(fin));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(fin), 0)) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;          // TMEM lanes [32 quarter, 32 quarter + 32)
+        const int r = quarter * 32 + lane;     // row of the tile owned by this thread
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N);
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            const bool row_ok = r < tl.rows_valid;
+            const long long orow = static_cast<long long>(tl.a_row + r);
+            if constexpr (EPI == EPI_SWIGLU) {
+                // packed tile columns: [gate 64 | up 64] x 2 -> 128 expert columns
+                const int rem = args.N - tl.n * BN;
+                const int npk = (rem >= BN ? BN : rem) / 128;
+                __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
+                for (int g2 = 0; g2 < npk; ++g2) {
+#pragma unroll 1
+                    for (int j0 = 0; j0 < 64; j0 += 32) {
+                        uint32_t gv[32], uv[32];
+                        tmem_ld32(tbase + g2 * 128 + j0, gv);
+                        tmem_ld32(tbase + g2 * 128 + 64 + j0, uv);
+                        tmem_ld_wait();
+                        if (row_ok) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const float h0 = silu_f(__uint_as_float(gv[2 * q])) * __uint_as_float(uv[2 * q]);
+                                const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
+                                pk[q] = pack_bf16x2(h0, h1);
+                            }
+                            uint4* dst = reinterpret_cast<uint4*>(H + orow * args.ldo + tl.n * 128 + g2 * 64 + j0);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        }
+                    }
+                }
+            } else if constexpr (EPI == EPI_BF16) {
+                const int rem = args.out_cols - tl.n * BN;
+                const int ncols = rem >= BN ? BN : rem;
+                __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c0, v);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                        uint4* dst = reinterpret_cast<uint4*>(Y + orow * args.ldo + tl.n * BN + c0);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    }
+                }
+            } else {  // EPI_F32
+                const int rem = args.out_cols - tl.n * BN;
+                const int ncols = rem >= BN ? BN : rem;
+                float* Z = reinterpret_cast<float*>(args.out);
+                const bool vec = (args.ldo & 3) == 0;
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c0, v);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        float* dst = Z + orow * args.ldo + tl.n * BN + c0;
+                        const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
+                        if (vec && nv == 32) {
+#pragma unroll
+                            for (int w = 0; w < 8; ++w)
+                                reinterpret_cast<uint4*>(dst)[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+                        } else {
+                            for (int j = 0; j < nv; ++j) dst[j] = __uint_as_float(v[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------- plan
+// m-tile prefix and row starts of G groups; offsets == nullptr means one group
+// of n_rows rows.  Inconsistent offsets record DEV_ERR_OFFSETS and yield an
+// empty plan (every GEMM over it then does nothing).
+__global__ void plan_kernel(const int* __restrict__ offsets, int G, int n_rows, int bm, int* plan, int* err) {
+    __shared__ int warp_sums[32];
+    __shared__ int s_bad;
+    __shared__ int s_carry;
+    if (threadIdx.x == 0) { s_bad = 0; s_carry = 0; }
+    __syncthreads();
+    int* mt = plan;
+    int* rs = plan + (G + 1);
+    for (int base = 0; base < G; base += blockDim.x) {
+        const int g = base + threadIdx.x;
+        int cnt = 0;
+        if (g < G) {
+            const int a = offsets ? offsets[g] : 0;
+            const int b = offsets ? offsets[g + 1] : n_rows;
+            if (a < 0 || b < a || b > n_rows) s_bad = 1;
+            rs[g] = a;
+            if (g == G - 1) rs[G] = b;
+            cnt = b > a ? (b - a + bm - 1) / bm : 0;
+        }
+        // block-wide exclusive scan of cnt
+        int v = cnt;
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (lane == 31) warp_sums[wid] = v;
+        __syncthreads();
+        if (wid == 0) {
+            int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int n = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += n;
+            }
+            warp_sums[lane] = w;   // inclusive
+        }
+        __syncthreads();
+        const int excl = v - cnt + (wid > 0 ? warp_sums[wid - 1] : 0) + s_carry;
+        if (g < G) mt[g] = excl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) s_carry = excl + cnt;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        mt[G] = s_carry;
+        if (s_bad) {
+            for (int g = 0; g <= G; ++g) mt[g] = 0;
+            set_dev_error(err, DEV_ERR_OFFSETS);
+        }
+    }
+}
+
+}  // namespace tc
+
+// ------------------------------------------------------------------- host
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static cudaError_t get_encode() {
+    if (g_encode) return cudaSuccess;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// 2D bf16 tensor map over a [rows, cols] row-major matrix with a box of
+// box_rows x 64 elements and the 128-byte swizzle.
+static cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static int g_num_sms = 0;
+
+static cudaError_t num_sms(int* out) {
+    if (!g_num_sms) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    *out = g_num_sms;
+    return cudaSuccess;
+}
+
+cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st) {
+    tc::plan_kernel<<<1, 1024, 0, st>>>(offsets, G, n_rows, bm, plan, dev_error_ptr());
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int EPI>
+static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,
+                                  const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
+                                  cudaStream_t st) {
+    static bool attr_set = false;
+    cudaError_t e;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap ta, tb;
+    e = make_map(&ta, A, a_rows, K, tc::BM);
+    if (e != cudaSuccess) return e;
+    e = make_map(&tb, B, static_cast<long long>(G) * N, K, tc::BN);
+    if (e != cudaSuccess) return e;
+    tc::Args args;
+    args.plan = plan;
+    args.G = G;
+    args.N = N;
+    args.K = K;
+    args.n_tiles = (N + tc::BN - 1) / tc::BN;
+    args.max_mtiles = max_mtiles;
+    args.out = out;
+    args.ldo = ldo;
+    args.out_cols = out_cols;
+    args.err = dev_error_ptr();
+    int sms = 0;
+    e = num_sms(&sms);
+    if (e != cudaSuccess) return e;
+    long long max_tiles = static_cast<long long>(max_mtiles) * args.n_tiles;
+    int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+    if (grid < 1) grid = 1;
+    tc::grouped_gemm_kernel<EPI><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
+                           const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
+                           cudaStream_t st) {
+    switch (epi) {
+        case EPI_SWIGLU:
+            return launch_tc_impl<EPI_SWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols, st);
+        case EPI_BF16:
+            return launch_tc_impl<EPI_BF16>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols, st);
+        case EPI_F32:
+            return launch_tc_impl<EPI_F32>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols, st);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+int tc_block_m() { return tc::BM; }
+
+}  // namespace fs

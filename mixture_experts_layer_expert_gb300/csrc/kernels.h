@@ -1,0 +1,51 @@
+// kernels.h -- internal launchers of libfs (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fs {
+
+constexpr int kMaxGroups = 1024;   // groups (experts) one grouped GEMM handles
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 512;   // router top-k kernel limit
+
+enum { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2 };
+
+void count_launch();
+int* dev_error_ptr();
+
+// gemm_tc.cu (bf16 operands, tcgen05)
+int tc_block_m();
+cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st);
+cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
+                           const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
+                           cudaStream_t st);
+
+// gemm_simt.cu (fp32 operands, fp32 FMA)
+int simt_block_m();
+cudaError_t launch_simt_gemm(int epi, const float* A, const float* B, int G, int N, int K, const int* plan,
+                             int max_mtiles, float* out, long long ldo, int out_cols, cudaStream_t st);
+
+// router.cu
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int gate,
+                        int32_t* topk_idx, float* topk_w, cudaStream_t st);
+
+// dispatch.cu
+size_t dispatch_ws_bytes(int T, int E);
+cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
+                            int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
+                            int32_t* scratch, cudaStream_t st);
+
+// combine.cu
+cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* topk_w, const void* o_prev,
+                           const void* shared_out, void* o_partial, void* o_full, int T, int d, int k,
+                           int is_bf16, cudaStream_t st);
+
+// pack.cu
+cudaError_t launch_pack_w13(int G, int c, int d, int elem_bytes, const void* w1, const void* w2, void* w13,
+                            cudaStream_t st);
+cudaError_t launch_pack_w3_shared(int ns, int cs, int d, int elem_bytes, const void* w3s, void* w3cat,
+                                  cudaStream_t st);
+
+}  // namespace fs

@@ -1,0 +1,214 @@
+"""Thin Python binding of libfs (the C ABI in include/fs.h).
+
+Argument marshalling only: every function passes tensor data pointers, sizes
+and the current CUDA stream to the library entry point of the same name.  The
+library is loaded from the in-tree build (``_build/libfs.so``); if it is
+missing, ``lib()`` raises -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .configs import LayerConfig
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfs.so")
+_lib = None
+
+FS_BF16, FS_F32 = 0, 1
+GATES = {"softmax": 0, "softmax_renorm": 1, "sigmoid": 2, "sigmoid_norm": 3}
+WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2}
+STATUS = {0: "FS_OK", 1: "FS_ERR_INVALID_ARG", 2: "FS_ERR_UNSUPPORTED", 3: "FS_ERR_WORKSPACE",
+          4: "FS_ERR_CUDA", 5: "FS_ERR_DEVICE_STATE"}
+
+
+class FsError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        super().__init__("%s failed: %s%s" % (what, STATUS.get(status, status), (" (%s)" % detail) if detail else ""))
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "E", "k", "c", "n_shared", "c_shared", "dtype", "gate")]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [("w_r", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("w13", ctypes.c_void_p),
+                ("w3", ctypes.c_void_p), ("w13_shared", ctypes.c_void_p), ("w3_shared", ctypes.c_void_p)]
+
+
+_VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_SIGS = {
+    "fs_workspace_bytes": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
+    "fs_pack_w13": (_I32, [_I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "fs_pack_w3_shared": (_I32, [_I32, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "fs_router_topk": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_dispatch": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_grouped_swiglu": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_shared_expert": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "fs_farskip_stack": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP, _VP,
+                                _VP, _VP, _SZ, _VP]),
+    "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
+    "fs_launch_count": (ctypes.c_uint64, []),
+    "fs_last_cuda_error": (ctypes.c_char_p, []),
+    "fs_status_string": (ctypes.c_char_p, [_I32]),
+}
+
+
+def lib():
+    """Load libfs.so (built in-tree).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfs.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        detail = ""
+        if status == 4:
+            detail = (lib().fs_last_cuda_error() or b"").decode()
+        raise FsError(status, what, detail)
+
+
+def _p(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def make_desc(cfg: LayerConfig, T: int | None = None) -> LayerDesc:
+    return LayerDesc(cfg.T if T is None else T, cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared,
+                     FS_BF16 if cfg.dtype == "bf16" else FS_F32, GATES[cfg.gate])
+
+
+# ----------------------------------------------------------------- entry points
+
+def fs_workspace_bytes(desc: LayerDesc, L: int = 0) -> int:
+    return int(lib().fs_workspace_bytes(ctypes.byref(desc), L))
+
+
+def fs_pack_w13(G, c, d, dtype, w1, w2, w13, stream=None):
+    _check(lib().fs_pack_w13(G, c, d, dtype, _p(w1), _p(w2), _p(w13), _stream(stream)), "fs_pack_w13")
+
+
+def fs_pack_w3_shared(n_shared, c_shared, d, dtype, w3s, w3cat, stream=None):
+    _check(lib().fs_pack_w3_shared(n_shared, c_shared, d, dtype, _p(w3s), _p(w3cat), _stream(stream)),
+           "fs_pack_w3_shared")
+
+
+def fs_router_topk(desc, u, w_r, bias, topk_idx, topk_w, logits, ws, stream=None):
+    _check(lib().fs_router_topk(ctypes.byref(desc), _p(u), _p(w_r), _p(bias), _p(topk_idx), _p(topk_w),
+                                _p(logits), _p(ws), _nbytes(ws), _stream(stream)), "fs_router_topk")
+
+
+def fs_dispatch(desc, topk_idx, u, counts, offsets, pos, perm_src, x_perm, ws, stream=None):
+    _check(lib().fs_dispatch(ctypes.byref(desc), _p(topk_idx), _p(u), _p(counts), _p(offsets), _p(pos),
+                             _p(perm_src), _p(x_perm), _p(ws), _nbytes(ws), _stream(stream)), "fs_dispatch")
+
+
+def fs_grouped_swiglu(desc, x_perm, offsets, w13, w3, y_perm, ws, stream=None):
+    _check(lib().fs_grouped_swiglu(ctypes.byref(desc), _p(x_perm), _p(offsets), _p(w13), _p(w3), _p(y_perm),
+                                   _p(ws), _nbytes(ws), _stream(stream)), "fs_grouped_swiglu")
+
+
+def fs_shared_expert(desc, u, w13_shared, w3_shared, s_out, ws, stream=None):
+    _check(lib().fs_shared_expert(ctypes.byref(desc), _p(u), _p(w13_shared), _p(w3_shared), _p(s_out), _p(ws),
+                                  _nbytes(ws), _stream(stream)), "fs_shared_expert")
+
+
+def fs_combine(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full, stream=None):
+    _check(lib().fs_combine(ctypes.byref(desc), _p(y_perm), _p(pos), _p(topk_w), _p(o_prev), _p(shared_out),
+                            _p(o_partial), _p(o_full), _stream(stream)), "fs_combine")
+
+
+def block_struct(packed: dict) -> BlockWeights:
+    return BlockWeights(_p(packed["w_r"]), _p(packed.get("bias")), _p(packed["w13"]), _p(packed["w3"]),
+                        _p(packed.get("w13_shared")), _p(packed.get("w3_shared")))
+
+
+def fs_farskip_stack(desc, L, wiring, blocks, x, o_full, o_partial, ws, stream=None):
+    """`blocks`: list of L packed-weight dicts (see pack_block)."""
+    arr = (BlockWeights * L)(*[block_struct(b) for b in blocks])
+    w = WIRINGS[wiring] if isinstance(wiring, str) else int(wiring)
+    _check(lib().fs_farskip_stack(ctypes.byref(desc), L, w, arr, _p(x), _p(o_full), _p(o_partial), _p(ws),
+                                  _nbytes(ws), _stream(stream)), "fs_farskip_stack")
+
+
+def fs_get_error():
+    code = ctypes.c_int32(0)
+    st = lib().fs_get_error(ctypes.byref(code))
+    return int(st), int(code.value)
+
+
+def fs_launch_count() -> int:
+    return int(lib().fs_launch_count())
+
+
+# -------------------------------------------------------------- conveniences
+
+def alloc_workspace(desc: LayerDesc, L: int, device="cuda") -> torch.Tensor:
+    n = fs_workspace_bytes(desc, L)
+    if n == 0:
+        raise FsError(1, "fs_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def pack_block(cfg: LayerConfig, w: dict, stream=None) -> dict:
+    """Repack one block's page-layout weights (on the GPU) into the library layout."""
+    dt = FS_BF16 if cfg.dtype == "bf16" else FS_F32
+    E, c, d = cfg.E, cfg.c, cfg.d
+    out = {"w_r": w["w_r"].contiguous(), "bias": None if w.get("bias") is None else w["bias"].contiguous().float()}
+    out["w13"] = torch.empty((E, 2 * c, d), dtype=w["w1"].dtype, device=w["w1"].device)
+    fs_pack_w13(E, c, d, dt, w["w1"].contiguous(), w["w2"].contiguous(), out["w13"], stream)
+    out["w3"] = w["w3"].contiguous()
+    if cfg.n_shared:
+        cw = cfg.n_shared * cfg.c_shared
+        out["w13_shared"] = torch.empty((2 * cw, d), dtype=w["w1s"].dtype, device=w["w1s"].device)
+        fs_pack_w13(1, cw, d, dt, w["w1s"].contiguous(), w["w2s"].contiguous(), out["w13_shared"], stream)
+        out["w3_shared"] = torch.empty((d, cw), dtype=w["w3s"].dtype, device=w["w3s"].device)
+        fs_pack_w3_shared(cfg.n_shared, cfg.c_shared, d, dt, w["w3s"].contiguous(), out["w3_shared"], stream)
+    return out
+
+
+class FarSkipStack:
+    """L FarSkip MoE blocks on one GPU: packed weights + workspace, one
+    fs_farskip_stack call per forward."""
+
+    def __init__(self, cfg: LayerConfig, raw_blocks: list, wiring: str | None = None, T: int | None = None,
+                 device="cuda"):
+        self.cfg = cfg
+        self.T = cfg.T if T is None else T
+        self.wiring = wiring or cfg.wiring
+        self.desc = make_desc(cfg, self.T)
+        self.blocks = [pack_block(cfg, b) for b in raw_blocks]
+        self.ws = alloc_workspace(self.desc, len(self.blocks), device)
+        dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        self.o_full = torch.empty((self.T, cfg.d), dtype=dt, device=device)
+        self.o_partial = torch.empty((self.T, cfg.d), dtype=dt, device=device)
+
+    def forward(self, x: torch.Tensor, stream=None):
+        fs_farskip_stack(self.desc, len(self.blocks), self.wiring, self.blocks, x, self.o_full, self.o_partial,
+                         self.ws, stream)
+        return self.o_full, self.o_partial

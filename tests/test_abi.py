@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/fs.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_expert_gb300 import build, configs, fs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fs.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return fs.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fs_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fs_router_topk", "fs_dispatch", "fs_grouped_swiglu", "fs_combine", "fs_farskip_stack",
+              "fs_shared_expert", "fs_workspace_bytes", "fs_get_error", "fs_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_functions():
+        assert hasattr(L, n), "libfs.so does not export %s" % n
+
+
+def test_binding_covers_the_header():
+    for n in declared_functions():
+        assert n in fs._SIGS, "fs.py has no binding for %s" % n
+
+
+def test_status_strings(L):
+    for code, name in fs.STATUS.items():
+        assert L.fs_status_string(code).decode() == name
+
+
+def desc(**kw):
+    cfg = configs.CONFIGS["v3"]
+    d = fs.make_desc(cfg)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_workspace_bytes(L):
+    assert fs.fs_workspace_bytes(desc(), 0) > 0
+    assert fs.fs_workspace_bytes(desc(), 1) > fs.fs_workspace_bytes(desc(), 0)
+    assert fs.fs_workspace_bytes(desc(), 4) > fs.fs_workspace_bytes(desc(), 1)
+    # invalid descriptors -> 0
+    for bad in (dict(T=0), dict(k=300), dict(d=100), dict(c=100), dict(E=1024), dict(dtype=7), dict(gate=9),
+                dict(k=17, E=64)):
+        assert fs.fs_workspace_bytes(desc(**bad), 1) == 0, bad
+    # the V3 stack: X_perm and Y_perm dominate (2 x 7.5 GB)
+    v3 = fs.fs_workspace_bytes(desc(), 1)
+    assert 15.0e9 < v3 < 25.0e9
+
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced: every call below fails validation first
+MIS = 0x10001
+
+
+def _vp(x):
+    return ctypes.c_void_p(x)
+
+
+def test_router_rejects_bad_args(L):
+    d = desc()
+    ws_ok = fs.fs_workspace_bytes(d, 0)
+    f = L.fs_router_topk
+    args = [ctypes.byref(d), _vp(FAKE), _vp(FAKE), None, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256), ws_ok, None]
+    a = list(args); a[1] = None
+    assert f(*a) == 1                                     # null u
+    a = list(args); a[1] = _vp(MIS)
+    assert f(*a) == 2                                     # misaligned u
+    a = list(args); a[8] = ws_ok - 1
+    assert f(*a) == 3                                     # workspace too small
+    a = list(args); a[7] = _vp(FAKE * 256 + 16)
+    assert f(*a) == 3                                     # workspace misaligned
+    bad = desc(k=9, E=8)
+    a = list(args); a[0] = ctypes.byref(bad)
+    assert f(*a) == 1                                     # k > E
+    bad = desc(d=7100)
+    a = list(args); a[0] = ctypes.byref(bad)
+    assert f(*a) == 2                                     # d not a multiple of 64
+
+
+def test_other_entry_points_reject_bad_args(L):
+    d = desc()
+    assert L.fs_dispatch(ctypes.byref(d), None, _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE),
+                         _vp(FAKE * 256), 1 << 40, None) == 1
+    assert L.fs_grouped_swiglu(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE),
+                               _vp(FAKE * 256), 16, None) == 3
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), None, None, None, None) == 1
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(MIS), None, _vp(FAKE),
+                        None) == 2
+    nd = desc(n_shared=0)
+    assert L.fs_shared_expert(ctypes.byref(nd), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE * 256),
+                              1 << 40, None) == 1
+    assert L.fs_pack_w13(0, 64, 64, 0, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 1
+    assert L.fs_pack_w13(1, 65, 64, 0, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_pack_w3_shared(1, 64, 64, 3, _vp(FAKE), _vp(FAKE), None) == 1
+    blocks = (fs.BlockWeights * 1)()
+    assert L.fs_farskip_stack(ctypes.byref(d), 1, 0, blocks, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256),
+                              1 << 40, None) == 1              # null block weights
+    assert L.fs_farskip_stack(ctypes.byref(d), 0, 0, blocks, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256),
+                              1 << 40, None) == 1              # L = 0
+    assert L.fs_farskip_stack(ctypes.byref(d), 1, 5, blocks, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256),
+                              1 << 40, None) == 1              # bad wiring
+
+
+def test_no_launch_on_rejected_calls(L):
+    assert fs.fs_launch_count() == 0
