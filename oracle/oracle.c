@@ -33,7 +33,10 @@
  *   - Storage: the configurations store activations in bf16 (or fp32) between
  *     steps.  With storage != ORACLE_EXACT the oracle rounds (RNE) exactly the
  *     tensors the layer writes out: the expert hidden h, each routed expert
- *     output y, the shared output S, and o_k*, o_k.  All sums stay fp64.
+ *     output y, the shared output S, every block input u_k (k >= 2; the
+ *     operand of the block's GEMMs), and the stack outputs o_L*, o_L.  Inside
+ *     a stack the residual stream o_k, o_k* (k < L) is carried in fp32.  All
+ *     sums stay fp64.
  */
 #include <math.h>
 #include <stdint.h>
@@ -200,11 +203,11 @@ int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_d
  * Computes, per token (§2.1 MoE and shared expert; §3 FarSkip, eq. 8b):
  *   R    = sum_s w_s * y_{e_s}(u)       (y_e stored, so rounded per storage)
  *   S    = sum_i MLP_shared_i(u)        (rounded once)
- *   o*   = o_prev + S                   (rounded)
- *   o    = o_prev + S + R               (rounded)
+ *   o*   = o_prev + S                   (rounded per out_storage)
+ *   o    = o_prev + S + R               (rounded per out_storage)
  */
 int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
-                 const double* u, const double* o_prev,
+                 const double* u, const double* o_prev, int out_storage,
                  double* o_star, double* o_full,
                  int32_t* topk_idx, double* topk_w, double* logits,
                  double* R_out, double* S_out) {
@@ -247,8 +250,8 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
         for (int i = 0; i < d; ++i) {
             double sv = oracle_round(S[i], cfg->storage);
             double op = o_prev[(size_t)t * d + i];
-            o_star[(size_t)t * d + i] = oracle_round(op + sv, cfg->storage);
-            o_full[(size_t)t * d + i] = oracle_round(op + sv + R[i], cfg->storage);
+            o_star[(size_t)t * d + i] = oracle_round(op + sv, out_storage);
+            o_full[(size_t)t * d + i] = oracle_round(op + sv + R[i], out_storage);
             if (R_out) R_out[(size_t)t * d + i] = R[i];
             if (S_out) S_out[(size_t)t * d + i] = sv;
         }
@@ -266,6 +269,8 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
  *     ORACLE_WIRE_PARTIAL  : u_{k+1} = o_k*          (eq. 8b, f* = shared expert)
  *     ORACLE_WIRE_OUTDATED : u_{k+1} = o_{k-1}       (eq. 8a)
  *     ORACLE_WIRE_DISABLED : u_{k+1} = o_k           (the plain residual recurrence)
+ * Storage (when not exact): o_k, o_k* of blocks k < L are rounded to fp32 (the
+ * residual stream), u_{k+1} to the storage type, o_L and o_L* to the storage type.
  * Outputs o_L and o_L*; per-block routing and R/S when the pointers are set
  * ([L, n_tok, ...], block-major).  Token rows are independent, so any subset
  * of the rows of x can be passed. */
@@ -278,6 +283,7 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
     const size_t n = (size_t)n_tok * d;
     if (L < 1 || n_tok < 0) return -1;
     double* x64 = (double*)malloc(sizeof(double) * (n ? n : 1));
+    double* ubuf = (double*)malloc(sizeof(double) * (n ? n : 1));
     double* ring[3];
     double* star[2];
     for (int i = 0; i < 3; ++i) ring[i] = (double*)malloc(sizeof(double) * (n ? n : 1));
@@ -285,7 +291,8 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
     int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_tok ? n_tok : 1) * k);
     double* w = (double*)malloc(sizeof(double) * (size_t)(n_tok ? n_tok : 1) * k);
     int rc = 0;
-    if (!x64 || !ring[0] || !ring[1] || !ring[2] || !star[0] || !star[1] || !idx || !w) rc = -2;
+    if (!x64 || !ubuf || !ring[0] || !ring[1] || !ring[2] || !star[0] || !star[1] || !idx || !w) rc = -2;
+    const int resid = cfg->storage == ORACLE_STORE_BF16 ? ORACLE_STORE_F32 : cfg->storage;
     if (!rc) {
         for (size_t i = 0; i < n; ++i) x64[i] = elem(x, i, x_dtype);
         const double* o_km1 = x64;  /* o_{k-1} */
@@ -294,7 +301,7 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
             double* o_k = ring[b % 3];
             double* os_k = star[b % 2];
             const oracle_weights* wb = wts + (b - 1);
-            rc = oracle_block(cfg, wb, n_tok, u, o_km1, os_k, o_k, idx, w,
+            rc = oracle_block(cfg, wb, n_tok, u, o_km1, b == L ? cfg->storage : resid, os_k, o_k, idx, w,
                               logits_all ? logits_all + (size_t)(b - 1) * n_tok * E : NULL,
                               R_all ? R_all + (size_t)(b - 1) * n : NULL,
                               S_all ? S_all + (size_t)(b - 1) * n : NULL);
@@ -304,13 +311,17 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
                 memcpy(o_last, o_k, sizeof(double) * n);
                 memcpy(o_last_star, os_k, sizeof(double) * n);
             }
-            if (wiring == ORACLE_WIRE_PARTIAL) u = os_k;
-            else if (wiring == ORACLE_WIRE_OUTDATED) u = o_km1;
-            else u = o_k;
+            const double* nxt;
+            if (wiring == ORACLE_WIRE_PARTIAL) nxt = os_k;
+            else if (wiring == ORACLE_WIRE_OUTDATED) nxt = o_km1;
+            else nxt = o_k;
+            for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(nxt[i], cfg->storage);
+            u = ubuf;
             o_km1 = o_k;
         }
     }
     free(x64);
+    free(ubuf);
     for (int i = 0; i < 3; ++i) free(ring[i]);
     for (int i = 0; i < 2; ++i) free(star[i]);
     free(idx);

@@ -47,7 +47,8 @@ int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_d
                        const int32_t* expert, const void* w1, const void* w2, const void* w3,
                        double* h_out, double* y_out);
 int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
-                 const double* u, const double* o_prev, double* o_star, double* o_full,
+                 const double* u, const double* o_prev, int out_storage,
+                 double* o_star, double* o_full,
                  int32_t* topk_idx, double* topk_w, double* logits,
                  double* R_out, double* S_out);
 int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wiring,

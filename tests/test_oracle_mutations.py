@@ -24,11 +24,11 @@ MUTANTS = {
                                 "for (int j = 0; j < E; ++j) den += exp(z[j] - zmax);"),
     "sigmoid_norm_unnormalised": ("w[s] = sigmoid(z[e[s]]) / den;", "w[s] = sigmoid(z[e[s]]);"),
     "bias_dropped": ("if (bias) acc += (double)bias[j];", ""),
-    "partial_wiring_uses_o_k": ("if (wiring == ORACLE_WIRE_PARTIAL) u = os_k;", "if (wiring == ORACLE_WIRE_PARTIAL) u = o_k;"),
-    "outdated_wiring_uses_o_star": ("else if (wiring == ORACLE_WIRE_OUTDATED) u = o_km1;",
-                                    "else if (wiring == ORACLE_WIRE_OUTDATED) u = os_k;"),
-    "o_star_without_shared": ("o_star[(size_t)t * d + i] = oracle_round(op + sv, cfg->storage);",
-                              "o_star[(size_t)t * d + i] = oracle_round(op, cfg->storage);"),
+    "partial_wiring_uses_o_k": ("if (wiring == ORACLE_WIRE_PARTIAL) nxt = os_k;", "if (wiring == ORACLE_WIRE_PARTIAL) nxt = o_k;"),
+    "outdated_wiring_uses_o_star": ("else if (wiring == ORACLE_WIRE_OUTDATED) nxt = o_km1;",
+                                    "else if (wiring == ORACLE_WIRE_OUTDATED) nxt = os_k;"),
+    "o_star_without_shared": ("o_star[(size_t)t * d + i] = oracle_round(op + sv, out_storage);",
+                              "o_star[(size_t)t * d + i] = oracle_round(op, out_storage);"),
     "gate_weight_dropped": ("for (int i = 0; i < d; ++i) R[i] += w * oracle_round(y[i], cfg->storage);",
                             "for (int i = 0; i < d; ++i) R[i] += oracle_round(y[i], cfg->storage);"),
     "dispatch_unstable": ("for (int t = 0; t < T; ++t) {\n        for (int s = 0; s < k; ++s) {\n            int e = topk_idx[(size_t)t * k + s];\n            int p = cursor[e]++;",
