@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the FarSkip-Collective MoE layer stack on GB300.
+
+Default workload: the DeepSeek-V3-shaped MoE layer, T = 65,536 tokens
+(32 x 2,048 prefill), d = 7168, 256 routed experts, top-8 normalised sigmoid,
+expert width 2048, one shared expert of width 2048, bf16 storage with fp32
+accumulation.  One step = one pass of the whole hot path (router + top-k,
+dispatch, routed grouped SwiGLU GEMMs, shared expert, combine + FarSkip
+update) over the T tokens, through the library's C ABI.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own T tokens
+(data-parallel, no collective on the data path): weak scaling.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (test infrastructure, plain C fp64) on a
+bounded token sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_layer_expert_gb300 import configs, synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s, DeepSeek-V3 shape, 64K tokens; % of roofline (BF16/HBM)"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        load = [s for s, p in zip(sm, power) if p > 0.25 * max(power)] if power else sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def cuda_events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def gemm_traffic(cfg_name):
+    """DRAM bytes per launch of the gate/up GEMM from the committed ncu summary,
+    valid only while the kernel source is unchanged (null otherwise)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "mixture_experts_layer_expert_gb300", "csrc", "gemm_tc.cu")
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if rec.get("gemm_tc_sha") != h:
+            return None
+        return rec.get("per_launch", {}).get(cfg_name)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, cfg, rank, world, local):
+    from mixture_experts_layer_expert_gb300 import build, fs
+
+    build.build()
+    fs.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    prob = synth.make_problem(cfg, device=dev)
+    stack = fs.FarSkipStack(cfg, prob["blocks"], device=dev)
+    host_blocks = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_blocks = [{k: synth.to_numpy(v) for k, v in b.items()} for b in prob["blocks"]]
+    x = prob["x"]
+    del prob
+    torch.cuda.empty_cache()
+    T, L = cfg.T, cfg.L
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ------------------------------------------------ timed region 1: the stack
+    for _ in range(args.warmup):
+        stack.forward(x)
+    torch.cuda.synchronize()
+    st, code = fs.fs_get_error()
+    if st != 0:
+        raise RuntimeError("device error word after warm-up: %d" % code)
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier()
+    torch.cuda.synchronize()
+    l0 = fs.fs_launch_count()
+    e0, e1 = cuda_events(2)
+    e0.record(stream)
+    for _ in range(args.steps):
+        stack.forward(x)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = (fs.fs_launch_count() - l0) // args.steps
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+
+    # ------------------------- timed region 2: per-stage events (same kernels)
+    stage_ms = per_stage_timing(cfg, stack, x, args.steps, stream)
+
+    # ------------------------------------------- timed region 3: end to end
+    e2e_ms, h2d, d2h = e2e_timing(cfg, stack, x, max(2, args.steps // 2), stream)
+    clocks = sampler.stop() if sampler else None
+    st, code = fs.fs_get_error()
+    if st != 0:
+        raise RuntimeError("device error word after timing: %d" % code)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    tokens = T * world
+    value = tokens / (ms / 1e3)
+    # layer roofline: max(FLOPs / bf16 peak, algorithmic bytes / HBM)
+    flops = cfg.flops_per_block() * L
+    bytes_ = cfg.alg_bytes_per_block() * L
+    t_roof = max(flops / (pk["bf16_tflops"] * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9))
+    # dominant kernel: the routed grouped SwiGLU GEMMs (gate/up + down)
+    routed_flops = 6.0 * T * cfg.k * cfg.d * cfg.c
+    routed_ms = stage_ms["routed"] / L
+    achieved = routed_flops / (routed_ms / 1e3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), uniform router",
+        "config": {"workload": configs.describe(cfg), "T_per_gpu": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+                   "c": cfg.c, "n_shared": cfg.n_shared, "c_shared": cfg.c_shared, "L": L, "gate": cfg.gate,
+                   "wiring": cfg.wiring,
+                   "l2": "inputs larger than L2 (x %.2f GB, weights %.1f GB per block)" % (
+                       T * cfg.d * 2 / 1e9, cfg.alg_bytes_per_block() / 1e9)},
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (routed gate/up + down, tcgen05)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": "bf16 sustained, %s" % pk_src,
+                     "traffic": gemm_traffic(cfg.name),
+                     "flops_per_launch_pair": routed_flops, "ms_per_launch_pair": round(routed_ms, 4)},
+        "layer_roofline": {"bound": "tensor" if flops / (pk["bf16_tflops"] * 1e12) >= bytes_ / (pk["hbm_gbs"] * 1e9)
+                           else "hbm", "tokens_per_s_at_roofline": round(T / t_roof, 1),
+                           "frac": round((T / (ms / 1e3)) / (T / t_roof), 4),
+                           "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                           "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"], "source": pk_src}},
+        "breakdown_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": int(launches * args.steps),
+        "gpu_launches_per_step": int(launches),
+        "clocks": clocks,
+    }
+    if host_blocks is not None:
+        line["cpu_baseline"] = cpu_baseline(cfg, host_blocks, x, args.cpu_sample)
+    return line
+
+
+def per_stage_timing(cfg, stack, x, steps, stream):
+    """The same stack driven through the single-step C-ABI entry points with
+    CUDA events between stages (launch sequence identical to fs_farskip_stack)."""
+    from mixture_experts_layer_expert_gb300 import fs
+    T, d, k, E = cfg.T, cfg.d, cfg.k, cfg.E
+    desc = stack.desc
+    ws = fs.alloc_workspace(desc, 0)
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    pos, perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
+    x_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
+    y_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
+    s = torch.empty((T, d), dtype=x.dtype, device=dev) if cfg.n_shared else None
+    L = len(stack.blocks)
+    o_bufs = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(3)]
+    os_bufs = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    u_bufs = [torch.empty((T, d), dtype=x.dtype, device=dev) for _ in range(2)]
+    names = ["router", "dispatch", "routed", "shared", "combine"]
+    tot = {n: 0.0 for n in names}
+    for it in range(steps + 1):     # the first pass warms the extra buffers
+        u, o_prev = x, x
+        for b, pw in enumerate(stack.blocks):
+            last = b == L - 1
+            ev = cuda_events(6)
+            ev[0].record(stream)
+            fs.fs_router_topk(desc, u, pw["w_r"], pw["bias"], idx, w, None, ws)
+            ev[1].record(stream)
+            fs.fs_dispatch(desc, idx, u, counts, offsets, pos, perm, x_perm, ws)
+            ev[2].record(stream)
+            fs.fs_grouped_swiglu(desc, x_perm, offsets, pw["w13"], pw["w3"], y_perm, ws)
+            ev[3].record(stream)
+            if s is not None:
+                fs.fs_shared_expert(desc, u, pw["w13_shared"], pw["w3_shared"], s, ws)
+            ev[4].record(stream)
+            o_k = stack.o_full if last else o_bufs[b % 3]
+            os_k = stack.o_partial if last else os_bufs[b % 2]
+            u_next = None if last else u_bufs[b % 2]
+            fs.fs_combine(desc, y_perm, pos, w, o_prev, s, os_k, o_k, u_next, stack.wiring)
+            ev[5].record(stream)
+            torch.cuda.synchronize()
+            if it > 0:
+                for i, n in enumerate(names):
+                    tot[n] += ev[i].elapsed_time(ev[i + 1])
+            u = u_next
+            o_prev = o_k
+    return {n: v / steps for n, v in tot.items()}
+
+
+def e2e_timing(cfg, stack, x, steps, stream):
+    """Host buffers in, host buffer out: pinned H2D of x, the stack, D2H of o_L."""
+    x_host = x.cpu().pin_memory()
+    o_host = torch.empty(stack.o_full.shape, dtype=stack.o_full.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        stack.forward(x_dev)
+        o_host.copy_(stack.o_full, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = cuda_events(2)
+    e0.record(stream)
+    for _ in range(steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        stack.forward(x_dev)
+        o_host.copy_(stack.o_full, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    nb = x.numel() * x.element_size()
+    return e0.elapsed_time(e1) / steps, nb, stack.o_full.numel() * stack.o_full.element_size()
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(cfg, host_blocks, x, sample):
+    import oracle
+    oracle.build()
+    rows = np.arange(sample)
+    xs = synth.to_numpy(x[:sample])
+    dt = oracle.BF16 if cfg.dtype == "bf16" else oracle.F32
+    st = oracle.STORE_BF16 if cfg.dtype == "bf16" else oracle.STORE_F32
+    oc = oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st)
+    ws = [oracle.Weights(**b) for b in host_blocks]
+    t0 = time.perf_counter()
+    oracle.stack(oc, ws, cfg.wiring, xs, want_logits=False)
+    dt_s = time.perf_counter() - t0
+    return {"value": round(len(rows) / dt_s, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "first %d of the %d tokens, all L=%d blocks (plain C fp64, OpenMP over tokens)"
+            % (sample, cfg.T, cfg.L), "seconds": round(dt_s, 2)}
+
+
+# -------------------------------------------------------- reference arm
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    T = args.ref_sample
+    x = synth.make_x(cfg, device=dev, T=cfg.T)[:T]
+    blocks = [synth.make_block_weights(cfg, b, device=dev) for b in range(cfg.L)]
+    hb = [oracle.Weights(**{k: synth.to_numpy(v) for k, v in b.items()}) for b in blocks]
+    del blocks
+    xs = synth.to_numpy(x)
+    dt = oracle.BF16 if cfg.dtype == "bf16" else oracle.F32
+    st = oracle.STORE_BF16 if cfg.dtype == "bf16" else oracle.STORE_F32
+    oc = oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st)
+    for _ in range(args.warmup):
+        oracle.stack(oc, hb, cfg.wiring, xs[: max(1, T // 8)], want_logits=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.stack(oc, hb, cfg.wiring, xs, want_logits=False)
+    sec = (time.perf_counter() - t0) / args.steps
+    value = T / sec
+    sample = "%d of the %d tokens per step, all L=%d blocks" % (T, cfg.T, cfg.L)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in)",
+            "config": {"workload": configs.describe(cfg), "tokens_per_step": T},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="v3", choices=sorted(configs.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--ref-sample", type=int, default=64)
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    cfg = configs.CONFIGS[args.config]
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    if args.impl == "reference":
+        line = run_reference(args, cfg, rank, world)
+    else:
+        line = run_ours(args, cfg, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -150,21 +150,29 @@ fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void*
                            const void* w3_shared, void* s_out, void* ws, size_t ws_bytes,
                            void* stream);
 
-/* Combine (§2.1, local form) fused with the FarSkip update (§3, eq. 8b):
+/* Combine (§2.1, local form) fused with the FarSkip update (§3, eq. 8a/8b):
  *   R[t]  = sum_{s<k} topk_w[t, s] * y_perm[pos[t k + s]]   (fp32, slot order)
  *   o_partial[t] = o_prev[t] + S[t]                          (o_k*)
  *   o_full[t]    = o_prev[t] + S[t] + R[t]                   (o_k)
- * all sums in fp32, each output rounded once.  shared_out NULL = no shared
- * expert (S = 0); o_partial NULL = not written. */
+ *   u_next[t]    = the next block's input per `wiring`: o_k* (PARTIAL),
+ *                  o_prev (OUTDATED) or o_k (DISABLED)
+ * All sums in fp32, each output rounded once.  y_perm, shared_out and u_next
+ * have the activation type desc->dtype; the residual stream o_prev (prev_dtype)
+ * and o_partial / o_full (out_dtype) are FS_BF16 or FS_F32 each, so a stack can
+ * carry its residual in fp32.  shared_out NULL = no shared expert (S = 0);
+ * o_partial NULL and u_next NULL = not written (wiring is then ignored). */
 fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_t* pos,
-                     const float* topk_w, const void* o_prev, const void* shared_out,
-                     void* o_partial, void* o_full, void* stream);
+                     const float* topk_w, const void* o_prev, int32_t prev_dtype,
+                     const void* shared_out, void* o_partial, void* o_full, int32_t out_dtype,
+                     void* u_next, int32_t wiring, void* stream);
 
 /* L FarSkip blocks (§3): o_0 = u_1 = x; block k runs router, dispatch, routed
  * experts, shared expert and combine on u_k and o_{k-1}, producing
  * o_k* = o_{k-1} + S_k and o_k = o_k* + R_k; u_{k+1} follows `wiring`.
+ * Between blocks the residual stream o_k, o_k* is kept in fp32 (in ws) and
+ * u_{k+1} is its rounding to the activation type (the GEMM operand).
  *   blocks [L] (host array of device pointers), x [T, d]
- *   -> o_full = o_L, o_partial = o_L* (NULL = not written).
+ *   -> o_full = o_L, o_partial = o_L* (NULL = not written), activation type.
  * Needs ws of fs_workspace_bytes(desc, L) bytes.  Everything is enqueued on
  * `stream` with no host synchronisation. */
 fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,

@@ -74,7 +74,8 @@ struct Layout {
     // single-step regions (L = 0)
     size_t logits, disp, plan_z, plan_r, h_r, plan_s, h_s, end0;
     // stack regions (L >= 1)
-    size_t topk_idx, topk_w, counts, offsets, pos, perm, x_perm, y_perm, s_out, ring[3], star[2], end;
+    size_t topk_idx, topk_w, counts, offsets, pos, perm, x_perm, y_perm, s_out, ring[3], star[2], ubuf[2], end;
+    int nring, nstar, nu;   // fp32 o_k / o_k* and activation-type u_{k+1} buffers of blocks 1..L-1
 };
 
 static Layout layout(const fs_layer_desc* d, int L) {
@@ -103,10 +104,17 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.x_perm = take(rows * dm * es);
     l.y_perm = take(rows * dm * es);
     l.s_out = take(cw ? T * dm * es : 0);
+    // The residual stream between blocks is fp32; the last block writes the
+    // caller's outputs.  o_{b-2}, o_{b-1} (and o_{b-1}*) stay live while block
+    // b writes, so 3 (2) slots suffice for any L.
     const int nring = L > 1 ? (L - 1 < 3 ? L - 1 : 3) : 0;
     const int nstar = L > 1 ? (L - 1 < 2 ? L - 1 : 2) : 0;
-    for (int i = 0; i < 3; ++i) l.ring[i] = i < nring ? take(T * dm * es) : 0;
-    for (int i = 0; i < 2; ++i) l.star[i] = i < nstar ? take(T * dm * es) : 0;
+    l.nring = nring;
+    l.nstar = nstar;
+    l.nu = nstar;
+    for (int i = 0; i < 3; ++i) l.ring[i] = i < nring ? take(T * dm * 4) : 0;
+    for (int i = 0; i < 2; ++i) l.star[i] = i < nstar ? take(T * dm * 4) : 0;
+    for (int i = 0; i < 2; ++i) l.ubuf[i] = i < nstar ? take(T * dm * es) : 0;
     l.end = o;
     return l;
 }
@@ -194,8 +202,10 @@ static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* 
 }
 
 static fs_status combine_impl(const fs_layer_desc* d, const void* y_perm, const int32_t* pos, const float* w,
-                              const void* o_prev, const void* s, void* o_partial, void* o_full, cudaStream_t st) {
-    FS_TRY(launch_combine(y_perm, pos, w, o_prev, s, o_partial, o_full, d->T, d->d, d->k, d->dtype == FS_BF16, st));
+                              const void* o_prev, int prev_dtype, const void* s, void* o_partial, void* o_full,
+                              int out_dtype, void* u_next, int wiring, cudaStream_t st) {
+    FS_TRY(launch_combine(y_perm, pos, w, o_prev, prev_dtype == FS_BF16, s, o_partial, o_full, out_dtype == FS_BF16,
+                          u_next, wiring, d->T, d->d, d->k, d->dtype == FS_BF16, st));
     return FS_OK;
 }
 
@@ -298,17 +308,22 @@ fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void*
 }
 
 fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_t* pos, const float* topk_w,
-                     const void* o_prev, const void* shared_out, void* o_partial, void* o_full, void* stream) {
+                     const void* o_prev, int32_t prev_dtype, const void* shared_out, void* o_partial, void* o_full,
+                     int32_t out_dtype, void* u_next, int32_t wiring, void* stream) {
     FS_CHECK(check_desc(desc));
     FS_CHECK(need(y_perm));
     FS_CHECK(need(pos));
     FS_CHECK(need(topk_w));
     FS_CHECK(need(o_prev));
     FS_CHECK(need(o_full));
+    if ((prev_dtype != FS_BF16 && prev_dtype != FS_F32) || (out_dtype != FS_BF16 && out_dtype != FS_F32))
+        return FS_ERR_INVALID_ARG;
+    if (u_next && (wiring < FS_WIRE_PARTIAL || wiring > FS_WIRE_DISABLED)) return FS_ERR_INVALID_ARG;
     if (shared_out && !aligned16(shared_out)) return FS_ERR_UNSUPPORTED;
     if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
-    return combine_impl(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full,
-                        static_cast<cudaStream_t>(stream));
+    if (u_next && !aligned16(u_next)) return FS_ERR_UNSUPPORTED;
+    return combine_impl(desc, y_perm, pos, topk_w, o_prev, prev_dtype, shared_out, o_partial, o_full, out_dtype,
+                        u_next, wiring, static_cast<cudaStream_t>(stream));
 }
 
 fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring, const fs_block_weights* blocks,
@@ -342,21 +357,25 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
     void* y_perm = at<void>(ws, l.y_perm);
     void* s_out = desc->n_shared > 0 ? at<void>(ws, l.s_out) : nullptr;
 
-    const void* u = x;        // u_k   (= o_{k-1}* in the page's notation)
-    const void* o_prev = x;   // o_{k-1}
+    const void* u = x;        // u_k   (= o_{k-1}* in the page's notation), activation type
+    const void* o_prev = x;   // o_{k-1}: the caller's x for k = 1, then the fp32 residual stream
+    int prev_dtype = desc->dtype;
     for (int b = 1; b <= L; ++b) {
         const fs_block_weights& bw = blocks[b - 1];
-        void* o_k = (b == L) ? o_full : at<void>(ws, l.ring[b % 3]);
-        void* os_k = (b == L) ? o_partial : at<void>(ws, l.star[b % 2]);
+        const bool last = (b == L);
+        void* o_k = last ? o_full : at<void>(ws, l.ring[(b - 1) % l.nring]);
+        void* os_k = last ? o_partial : at<void>(ws, l.star[(b - 1) % l.nstar]);
+        void* u_next = last ? nullptr : at<void>(ws, l.ubuf[(b - 1) % l.nu]);
+        const int out_dtype = last ? desc->dtype : FS_F32;
         FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
         FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
         FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
         if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st));
-        FS_CHECK(combine_impl(desc, y_perm, pos, w, o_prev, s_out, os_k, o_k, st));
-        if (wiring == FS_WIRE_PARTIAL) u = os_k;
-        else if (wiring == FS_WIRE_OUTDATED) u = o_prev;
-        else u = o_k;
+        FS_CHECK(combine_impl(desc, y_perm, pos, w, o_prev, prev_dtype, s_out, os_k, o_k, out_dtype, u_next, wiring,
+                              st));
+        u = u_next;
         o_prev = o_k;
+        prev_dtype = out_dtype;
     }
     return FS_OK;
 }

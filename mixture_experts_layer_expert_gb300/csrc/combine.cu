@@ -4,12 +4,16 @@
 // "FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
 // Models": §2.1 Combine (aggregate and sum the routed expert activations back
 // to token order), §3 eq. (8b) (o_k* = o_{k-1} + f_k*(o_{k-1}*), f* = shared
-// expert) and the FarSkip equation (o_k = o_{k-1} + f_k(o_{k-1}*)).
+// expert), eq. (8a) and the FarSkip equation (o_k = o_{k-1} + f_k(o_{k-1}*)).
 //   R[t]   = sum_{s<k} w[t, s] * y_perm[pos[t k + s]]     (fp32, slot order: no atomics)
 //   o*[t]  = o_prev[t] + S[t]
 //   o[t]   = o_prev[t] + S[t] + R[t]
-// One warp per token, 16-byte vectors: each lane loads the k expert rows of
-// its columns together (k loads in flight), sums in fp32, rounds once.
+//   u'[t]  = the next block's input, rounded to the activation type:
+//            o*[t] (partial), o_prev[t] (outdated) or o[t] (disabled)
+// The residual stream (o_prev, o*, o) may be fp32 or the activation type; the
+// expert rows, S and u' are in the activation type.  One warp per token, 8
+// columns per lane step: each lane loads the k expert rows of its columns
+// together (k loads in flight), sums in fp32, rounds once per output.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,12 +21,75 @@ namespace fs {
 
 constexpr int kCombineWarps = 8;
 
+// 8 consecutive elements at element offset `off` (a multiple of 8)
+__device__ __forceinline__ void load8(const void* base, long long off, bool bf16, float (&v)[8]) {
+    if (bf16) {
+        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[2 * q] = bf16lo(w[q]);
+            v[2 * q + 1] = bf16hi(w[q]);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+        const float4 a = p[0], b = p[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ void store8(void* base, long long off, bool bf16, const float (&v)[8]) {
+    if (bf16) {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off) =
+            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                       pack_bf16x2(v[6], v[7]));
+    } else {
+        float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+        p[0] = make_float4(v[0], v[1], v[2], v[3]);
+        p[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+
+// raw 16-byte vectors of 8 elements of a row (1 for bf16, 2 for fp32)
 template <bool BF16>
+struct Raw8 {
+    uint4 v[BF16 ? 1 : 2];
+};
+
+template <bool BF16>
+__device__ __forceinline__ void load_raw8(const void* base, long long off, Raw8<BF16>& r) {
+    if constexpr (BF16) {
+        r.v[0] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+    } else {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + off);
+        r.v[0] = p[0];
+        r.v[1] = p[1];
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void fma_raw8(float w, const Raw8<BF16>& r, float (&acc)[8]) {
+    if constexpr (BF16) {
+        const uint32_t q[4] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(w, bf16lo(q[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(w, bf16hi(q[i]), acc[2 * i + 1]);
+        }
+    } else {
+        const uint32_t q[8] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w, r.v[1].x, r.v[1].y, r.v[1].z, r.v[1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, __uint_as_float(q[i]), acc[i]);
+    }
+}
+
+template <bool BF16, int KMAX>   // BF16: activation type of y_perm, shared_out and u_next
 __global__ void __launch_bounds__(kCombineWarps * 32)
-combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ pos, const float* __restrict__ topk_w,
-               const uint4* __restrict__ o_prev, const uint4* __restrict__ shared_out, uint4* __restrict__ o_partial,
-               uint4* __restrict__ o_full, int T, int row_vecs, int k) {
-    constexpr int EPV = BF16 ? 8 : 4;   // elements per 16-byte vector
+combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos, const float* __restrict__ topk_w,
+               const void* __restrict__ o_prev, bool prev_bf16, const void* __restrict__ shared_out,
+               void* __restrict__ o_partial, void* __restrict__ o_full, bool out_bf16, void* __restrict__ u_next,
+               int u_src, int T, int d, int k) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -32,85 +99,64 @@ combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ pos
         my_p = pos[static_cast<long long>(t) * k + lane];
         my_w = topk_w[static_cast<long long>(t) * k + lane];
     }
-    int ps[kMaxTopK];
-    float ws[kMaxTopK];
+    int ps[KMAX];
+    float ws[KMAX];
 #pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
+    for (int s = 0; s < KMAX; ++s) {
         ps[s] = __shfl_sync(0xffffffffu, my_p, s);
         ws[s] = __shfl_sync(0xffffffffu, my_w, s);
     }
-    const long long row = static_cast<long long>(t) * row_vecs;
-    for (int i = lane; i < row_vecs; i += 32) {
-        float acc[EPV];
-        float base[EPV];
-        {
-            const uint4 a = o_prev[row + i];
-            const uint4 b = shared_out ? shared_out[row + i] : make_uint4(0, 0, 0, 0);
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-            const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+    const long long row = static_cast<long long>(t) * d;
+    for (int c8 = lane * 8; c8 < d; c8 += 32 * 8) {
+        Raw8<BF16> yr[KMAX];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if constexpr (BF16) {
-                    base[2 * q] = bf16lo(av[q]) + bf16lo(bv[q]);
-                    base[2 * q + 1] = bf16hi(av[q]) + bf16hi(bv[q]);
-                } else {
-                    base[q] = __uint_as_float(av[q]) + __uint_as_float(bv[q]);
-                }
-            }
+        for (int s = 0; s < KMAX; ++s)
+            if (s < k && ps[s] >= 0) load_raw8<BF16>(y_perm, static_cast<long long>(ps[s]) * d + c8, yr[s]);
+        float base[8], sv[8], acc[8];
+        load8(o_prev, row + c8, prev_bf16, base);
+        if (shared_out) {
+            load8(shared_out, row + c8, BF16, sv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) base[j] += sv[j];
         }
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) acc[j] = 0.f;
-        uint4 yv[kMaxTopK];
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll
-        for (int s = 0; s < kMaxTopK; ++s)
-            if (s < k && ps[s] >= 0) yv[s] = y_perm[static_cast<long long>(ps[s]) * row_vecs + i];
+        for (int s = 0; s < KMAX; ++s)
+            if (s < k && ps[s] >= 0) fma_raw8<BF16>(ws[s], yr[s], acc);
+        float full[8];
 #pragma unroll
-        for (int s = 0; s < kMaxTopK; ++s) {
-            if (s < k && ps[s] >= 0) {
-                const uint32_t v[4] = {yv[s].x, yv[s].y, yv[s].z, yv[s].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if constexpr (BF16) {
-                        acc[2 * q] = fmaf(ws[s], bf16lo(v[q]), acc[2 * q]);
-                        acc[2 * q + 1] = fmaf(ws[s], bf16hi(v[q]), acc[2 * q + 1]);
-                    } else {
-                        acc[q] = fmaf(ws[s], __uint_as_float(v[q]), acc[q]);
-                    }
-                }
-            }
-        }
-        uint32_t op[4], of[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if constexpr (BF16) {
-                op[q] = pack_bf16x2(base[2 * q], base[2 * q + 1]);
-                of[q] = pack_bf16x2(base[2 * q] + acc[2 * q], base[2 * q + 1] + acc[2 * q + 1]);
+        for (int j = 0; j < 8; ++j) full[j] = base[j] + acc[j];
+        if (o_partial) store8(o_partial, row + c8, out_bf16, base);
+        store8(o_full, row + c8, out_bf16, full);
+        if (u_next) {
+            if (u_src == 0) {
+                store8(u_next, row + c8, BF16, base);
+            } else if (u_src == 1) {
+                float op[8];
+                load8(o_prev, row + c8, prev_bf16, op);
+                store8(u_next, row + c8, BF16, op);
             } else {
-                op[q] = __float_as_uint(base[q]);
-                of[q] = __float_as_uint(base[q] + acc[q]);
+                store8(u_next, row + c8, BF16, full);
             }
         }
-        if (o_partial) o_partial[row + i] = make_uint4(op[0], op[1], op[2], op[3]);
-        o_full[row + i] = make_uint4(of[0], of[1], of[2], of[3]);
     }
 }
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* topk_w, const void* o_prev,
-                           const void* shared_out, void* o_partial, void* o_full, int T, int d, int k,
-                           int is_bf16, cudaStream_t st) {
-    const int row_vecs = d * (is_bf16 ? 2 : 4) / 16;
+                           int prev_bf16, const void* shared_out, void* o_partial, void* o_full, int out_bf16,
+                           void* u_next, int u_src, int T, int d, int k, int is_bf16, cudaStream_t st) {
     const int grid = (T + kCombineWarps - 1) / kCombineWarps;
     const int threads = kCombineWarps * 32;
-    if (is_bf16)
-        combine_kernel<true><<<grid, threads, 0, st>>>(
-            static_cast<const uint4*>(y_perm), pos, topk_w, static_cast<const uint4*>(o_prev),
-            static_cast<const uint4*>(shared_out), static_cast<uint4*>(o_partial), static_cast<uint4*>(o_full), T,
-            row_vecs, k);
-    else
-        combine_kernel<false><<<grid, threads, 0, st>>>(
-            static_cast<const uint4*>(y_perm), pos, topk_w, static_cast<const uint4*>(o_prev),
-            static_cast<const uint4*>(shared_out), static_cast<uint4*>(o_partial), static_cast<uint4*>(o_full), T,
-            row_vecs, k);
+#define FS_COMBINE(BF, KM)                                                                                  \
+    combine_kernel<BF, KM><<<grid, threads, 0, st>>>(y_perm, pos, topk_w, o_prev, prev_bf16 != 0, shared_out, \
+                                                     o_partial, o_full, out_bf16 != 0, u_next, u_src, T, d, k)
+    if (is_bf16) {
+        if (k <= 8) FS_COMBINE(true, 8); else FS_COMBINE(true, 16);
+    } else {
+        if (k <= 8) FS_COMBINE(false, 8); else FS_COMBINE(false, 16);
+    }
+#undef FS_COMBINE
     count_launch();
     return cudaGetLastError();
 }

@@ -49,7 +49,8 @@ _SIGS = {
     "fs_dispatch": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_grouped_swiglu": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_shared_expert": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
-    "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32,
+                          _VP]),
     "fs_farskip_stack": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP, _VP,
                                 _VP, _VP, _SZ, _VP]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
@@ -138,9 +139,19 @@ def fs_shared_expert(desc, u, w13_shared, w3_shared, s_out, ws, stream=None):
                                   _nbytes(ws), _stream(stream)), "fs_shared_expert")
 
 
-def fs_combine(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full, stream=None):
-    _check(lib().fs_combine(ctypes.byref(desc), _p(y_perm), _p(pos), _p(topk_w), _p(o_prev), _p(shared_out),
-                            _p(o_partial), _p(o_full), _stream(stream)), "fs_combine")
+def _dtype_code(t):
+    return FS_BF16 if t.dtype == torch.bfloat16 else FS_F32
+
+
+def fs_combine(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full, u_next=None, wiring="partial",
+               stream=None):
+    """Residual dtypes (bf16 or fp32) are taken from the o_prev and o_full tensors."""
+    if o_partial is not None:
+        assert o_partial.dtype == o_full.dtype
+    w = WIRINGS[wiring] if isinstance(wiring, str) else int(wiring)
+    _check(lib().fs_combine(ctypes.byref(desc), _p(y_perm), _p(pos), _p(topk_w), _p(o_prev), _dtype_code(o_prev),
+                            _p(shared_out), _p(o_partial), _p(o_full), _dtype_code(o_full), _p(u_next), w,
+                            _stream(stream)), "fs_combine")
 
 
 def block_struct(packed: dict) -> BlockWeights:

@@ -33,10 +33,11 @@
  *   - Storage: the configurations store activations in bf16 (or fp32) between
  *     steps.  With storage != ORACLE_EXACT the oracle rounds (RNE) exactly the
  *     tensors the layer writes out: the expert hidden h, each routed expert
- *     output y, the shared output S, every block input u_k (k >= 2; the
- *     operand of the block's GEMMs), and the stack outputs o_L*, o_L.  Inside
- *     a stack the residual stream o_k, o_k* (k < L) is carried in fp32.  All
- *     sums stay fp64.
+ *     output y, the shared output S and every block input u_k (k >= 2; the
+ *     operand of the block's GEMMs).  The residual stream o_k, o_k* is carried
+ *     in fp32, and the stack outputs o_L, o_L* are returned at that precision:
+ *     storing them in bf16 is the layer's own output rounding, which the
+ *     comparison tolerance covers.  All sums stay fp64.
  */
 #include <math.h>
 #include <stdint.h>
@@ -269,8 +270,9 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
  *     ORACLE_WIRE_PARTIAL  : u_{k+1} = o_k*          (eq. 8b, f* = shared expert)
  *     ORACLE_WIRE_OUTDATED : u_{k+1} = o_{k-1}       (eq. 8a)
  *     ORACLE_WIRE_DISABLED : u_{k+1} = o_k           (the plain residual recurrence)
- * Storage (when not exact): o_k, o_k* of blocks k < L are rounded to fp32 (the
- * residual stream), u_{k+1} to the storage type, o_L and o_L* to the storage type.
+ * Storage (when not exact): o_k, o_k* are rounded to fp32 (the residual
+ * stream) and u_{k+1} to the storage type; the fp32-storage configuration
+ * rounds everything to fp32.
  * Outputs o_L and o_L*; per-block routing and R/S when the pointers are set
  * ([L, n_tok, ...], block-major).  Token rows are independent, so any subset
  * of the rows of x can be passed. */
@@ -301,7 +303,7 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
             double* o_k = ring[b % 3];
             double* os_k = star[b % 2];
             const oracle_weights* wb = wts + (b - 1);
-            rc = oracle_block(cfg, wb, n_tok, u, o_km1, b == L ? cfg->storage : resid, os_k, o_k, idx, w,
+            rc = oracle_block(cfg, wb, n_tok, u, o_km1, resid, os_k, o_k, idx, w,
                               logits_all ? logits_all + (size_t)(b - 1) * n_tok * E : NULL,
                               R_all ? R_all + (size_t)(b - 1) * n : NULL,
                               S_all ? S_all + (size_t)(b - 1) * n : NULL);

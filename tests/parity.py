@@ -94,17 +94,21 @@ def gpu_stack_stepwise(cfg, packed_blocks, x, wiring, DEV="cuda"):
     u, o_prev = x, x
     routing = []
     o_k = o_star = None
+    L = len(packed_blocks)
     for b, pw in enumerate(packed_blocks):
+        last = b == L - 1
         fs.fs_router_topk(desc, u, pw["w_r"], pw["bias"], idx, w, None, ws)
         routing.append(idx.cpu().numpy().copy())
         fs.fs_dispatch(desc, idx, u, counts, offsets, pos, perm, x_perm, ws)
         fs.fs_grouped_swiglu(desc, x_perm, offsets, pw["w13"], pw["w3"], y_perm, ws)
         if s is not None:
             fs.fs_shared_expert(desc, u, pw["w13_shared"], pw["w3_shared"], s, ws)
-        o_k = torch.empty((T, d), dtype=dt, device=DEV)
-        o_star = torch.empty((T, d), dtype=dt, device=DEV)
-        fs.fs_combine(desc, y_perm, pos, w, o_prev, s, o_star, o_k)
-        u = {"partial": o_star, "outdated": o_prev, "disabled": o_k}[wiring]
+        rdt = dt if last else torch.float32          # fp32 residual stream between blocks
+        o_k = torch.empty((T, d), dtype=rdt, device=DEV)
+        o_star = torch.empty((T, d), dtype=rdt, device=DEV)
+        u_next = None if last else torch.empty((T, d), dtype=dt, device=DEV)
+        fs.fs_combine(desc, y_perm, pos, w, o_prev, s, o_star, o_k, u_next, wiring)
+        u = u_next
         o_prev = o_k
     torch.cuda.synchronize()
     return o_k, o_star, routing

@@ -102,9 +102,14 @@ def test_other_entry_points_reject_bad_args(L):
                          _vp(FAKE * 256), 1 << 40, None) == 1
     assert L.fs_grouped_swiglu(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE),
                                _vp(FAKE * 256), 16, None) == 3
-    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), None, None, None, None) == 1
-    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(MIS), None, _vp(FAKE),
-                        None) == 2
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, None, None, 0, None,
+                        0, None) == 1                                       # null o_full
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, _vp(MIS), None, _vp(FAKE),
+                        0, None, 0, None) == 2                              # misaligned S
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 3, None, None, _vp(FAKE),
+                        0, None, 0, None) == 1                              # bad residual dtype
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, None, _vp(FAKE),
+                        0, _vp(FAKE), 9, None) == 1                         # bad wiring for u_next
     nd = desc(n_shared=0)
     assert L.fs_shared_expert(ctypes.byref(nd), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE * 256),
                               1 << 40, None) == 1

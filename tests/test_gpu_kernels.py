@@ -180,11 +180,15 @@ def test_shared_expert(fs, dtype, ns, cs, T):
 
 # ----------------------------------------------------------------- combine
 
-@pytest.mark.parametrize("dtype,T,k,d,shared,partial", [
-    ("bf16", 300, 2, 256, True, True), ("bf16", 77, 8, 512, False, True),
-    ("bf16", 1, 1, 64, True, False), ("f32", 256, 2, 128, True, True), ("bf16", 1000, 16, 128, True, True),
+@pytest.mark.parametrize("dtype,T,k,d,shared,partial,resid", [
+    ("bf16", 300, 2, 256, True, True, "act"), ("bf16", 77, 8, 512, False, True, "act"),
+    ("bf16", 1, 1, 64, True, False, "act"), ("f32", 256, 2, 128, True, True, "act"),
+    ("bf16", 1000, 16, 128, True, True, "act"), ("bf16", 300, 8, 256, True, True, "f32"),
+    ("bf16", 200, 4, 192, True, True, "f32_in"),
 ])
-def test_combine(fs, dtype, T, k, d, shared, partial):
+def test_combine(fs, dtype, T, k, d, shared, partial, resid):
+    """resid: 'act' = residual in the activation type; 'f32' = fp32 in and out;
+    'f32_in' = fp32 in, activation type out (the last block of a stack)."""
     E = max(k, 8)
     cfg = small(dtype, T=T, E=E, k=k, d=d)
     sdt = synth.storage_dtype(cfg)
@@ -193,21 +197,35 @@ def test_combine(fs, dtype, T, k, d, shared, partial):
     _, _, pos, _ = oracle.dispatch(T, k, E, idx.numpy())
     y = torch.randn((T * k, d), generator=g, device=DEV).to(sdt)
     w = torch.rand((T, k), generator=g, device=DEV)
-    op = torch.randn((T, d), generator=g, device=DEV).to(sdt)
+    pdt = sdt if resid == "act" else torch.float32
+    odt = torch.float32 if resid == "f32" else sdt
+    op = torch.randn((T, d), generator=g, device=DEV).to(pdt)
     s = torch.randn((T, d), generator=g, device=DEV).to(sdt) if shared else None
-    o_star = torch.empty((T, d), dtype=sdt, device=DEV) if partial else None
-    o = torch.empty((T, d), dtype=sdt, device=DEV)
-    fs.fs_combine(fs.make_desc(cfg), y, torch.from_numpy(pos).to(DEV), w, op, s, o_star, o)
+    o_star = torch.empty((T, d), dtype=odt, device=DEV) if partial else None
+    o = torch.empty((T, d), dtype=odt, device=DEV)
+    u_next = {wi: torch.empty((T, d), dtype=sdt, device=DEV) for wi in ("partial", "outdated", "disabled")}
+    for wi, un in u_next.items():
+        fs.fs_combine(fs.make_desc(cfg), y, torch.from_numpy(pos).to(DEV), w, op, s, o_star, o, un, wi)
     _no_dev_error()
-    st = oracle.STORE_BF16 if dtype == "bf16" else oracle.STORE_F32
-    r_star, r = oracle.combine(T, k, d, synth.to_numpy(y), pos, w.cpu().numpy(), synth.to_numpy(op),
-                               synth.to_numpy(s), storage=st)
+    ost = oracle.STORE_BF16 if odt == torch.bfloat16 else oracle.STORE_F32
+    sn = None if s is None else synth.to_numpy(s.to(pdt)) if pdt == torch.float32 else synth.to_numpy(s)
+    y_in = synth.to_numpy(y.to(pdt)) if pdt == torch.float32 else synth.to_numpy(y)
+    r_star, r = oracle.combine(T, k, d, y_in, pos, w.cpu().numpy(), synth.to_numpy(op), sn, storage=ost)
     # fp32 sums vs fp64 sums, each rounded once: equal but for 1-ulp rounding flips
     # plus the fp32 accumulation error, bounded by a few fp32 ulps of the term magnitudes
-    ulp = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -23
+    ulp = 2.0 ** -7 if odt == torch.bfloat16 else 2.0 ** -23
     yv = np.abs(to64(y))[pos.reshape(T, k)]                      # [T, k, d]
     mag = np.abs(to64(op)) + (np.abs(to64(s)) if shared else 0.0) + np.einsum("tk,tkd->td", w.cpu().numpy(), yv)
     diff = np.abs(to64(o) - r)
     assert np.all(diff <= ulp * np.abs(r) + k * 2.0 ** -22 * mag + 1e-30), diff.max()
     if partial:
-        np.testing.assert_array_equal(to64(o_star), r_star)   # o* = o_prev + S: one exact-ish add
+        d_star = np.abs(to64(o_star) - r_star)
+        assert np.all(d_star <= ulp * np.abs(r_star) + 2.0 ** -23 * mag + 1e-30), d_star.max()
+    # next-block inputs: the chosen residual rounded to the activation type
+    act = oracle.STORE_BF16 if dtype == "bf16" else oracle.STORE_F32
+    r_star_u, r_u = oracle.combine(T, k, d, y_in, pos, w.cpu().numpy(), synth.to_numpy(op), sn, storage=act)
+    ulp_u = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -23
+    for wi, want in (("partial", r_star_u), ("disabled", r_u)):
+        du = np.abs(to64(u_next[wi]) - want)
+        assert np.all(du <= ulp_u * np.abs(want) + k * 2.0 ** -22 * mag + 1e-30), (wi, du.max())
+    assert torch.equal(u_next["outdated"], op.to(sdt))

@@ -391,17 +391,26 @@ def test_dispatch_combine_round_trip(k, wval):
 
 # --------------------------------------------------------------- storage modes
 
-def test_bf16_storage_outputs_are_bf16_and_close():
+def test_bf16_storage_outputs_are_fp32_and_close():
+    """With bf16 storage the stack returns the fp32 residual stream; the block
+    inputs in between are bf16 values (checked through block 2's logits)."""
     cfg, ws, x = _stack_problem(17, 2)
-    ex = oracle.stack(cfg, [W(w) for w in ws], "partial", x)
+    ex = oracle.stack(cfg, [W(w) for w in ws], "partial", x, want_rs=True)
     cfg_b = cfg_of(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, storage=oracle.STORE_BF16)
-    bf = oracle.stack(cfg_b, [W(w) for w in ws], "partial", x)
+    bf = oracle.stack(cfg_b, [W(w) for w in ws], "partial", x, want_rs=True)
     for key in ("o", "o_star"):
         v = bf[key]
-        rt = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
-        np.testing.assert_array_equal(v, rt)          # every stored value is a bf16 value
+        np.testing.assert_array_equal(v, v.astype(np.float32).astype(np.float64))   # fp32 values
         rel = np.linalg.norm(v - ex[key]) / np.linalg.norm(ex[key])
         assert rel < 1e-2, rel
+    # S is a stored tensor: bf16 values
+    s1 = bf["S"][0]
+    np.testing.assert_array_equal(s1, torch.from_numpy(s1.astype(np.float32)).to(torch.bfloat16).double().numpy())
+    # block 2 sees u_2 = bf16(o_1*) with o_1* = fp32(x + S_1)
+    o1s = (x + s1).astype(np.float32)
+    u2 = torch.from_numpy(o1s).to(torch.bfloat16).double().numpy()
+    z2 = u2 @ ws[1]["w_r"].T + ws[1]["bias"].astype(np.float64)
+    np.testing.assert_allclose(bf["logits"][1], z2, rtol=1e-12, atol=1e-12)
 
 
 def test_bf16_inputs_widen_exactly():
