@@ -267,7 +267,7 @@ def per_stage_timing(cfg, stack, x, steps, stream):
     pos, perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
     x_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
     y_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
-    s = torch.empty((T, d), dtype=x.dtype, device=dev) if cfg.n_shared else None
+    s = torch.empty((T, d), dtype=torch.float32, device=dev) if cfg.n_shared else None
     L = len(stack.blocks)
     o_bufs = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(3)]
     os_bufs = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(2)]

@@ -145,7 +145,8 @@ fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const
                             void* ws, size_t ws_bytes, void* stream);
 
 /* Shared expert(s) (§2.1): S = sum_i MLP_shared_i(u) over all T tokens, as one
- * MLP of width n_shared c_shared.  u [T, d] -> s_out [T, d]. */
+ * MLP of width n_shared c_shared.  u [T, d] -> s_out [T, d] in fp32 (S is only
+ * ever added into the residual stream, so it keeps fp32 accumulator precision). */
 fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void* w13_shared,
                            const void* w3_shared, void* s_out, void* ws, size_t ws_bytes,
                            void* stream);
@@ -156,8 +157,9 @@ fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void*
  *   o_full[t]    = o_prev[t] + S[t] + R[t]                   (o_k)
  *   u_next[t]    = the next block's input per `wiring`: o_k* (PARTIAL),
  *                  o_prev (OUTDATED) or o_k (DISABLED)
- * All sums in fp32, each output rounded once.  y_perm, shared_out and u_next
- * have the activation type desc->dtype; the residual stream o_prev (prev_dtype)
+ * All sums in fp32, each output rounded once.  y_perm and u_next have the
+ * activation type desc->dtype, shared_out is fp32 (fs_shared_expert's output);
+ * the residual stream o_prev (prev_dtype)
  * and o_partial / o_full (out_dtype) are FS_BF16 or FS_F32 each, so a stack can
  * carry its residual in fp32.  shared_out NULL = no shared expert (S = 0);
  * o_partial NULL and u_next NULL = not written (wiring is then ignored). */

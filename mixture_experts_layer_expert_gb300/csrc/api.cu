@@ -103,7 +103,7 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.perm = take(rows * 4);
     l.x_perm = take(rows * dm * es);
     l.y_perm = take(rows * dm * es);
-    l.s_out = take(cw ? T * dm * es : 0);
+    l.s_out = take(cw ? T * dm * 4 : 0);     // S in fp32
     // The residual stream between blocks is fp32; the last block writes the
     // caller's outputs.  o_{b-2}, o_{b-1} (and o_{b-1}*) stay live while block
     // b writes, so 3 (2) slots suffice for any L.
@@ -165,16 +165,18 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 }
 
 // Two grouped GEMMs over `rows` rows split into G groups by `offsets`
-// (nullptr = one group): h = SiLU(x W2^T) * (x W1^T), then y = h W3^T.
+// (nullptr = one group): h = SiLU(x W2^T) * (x W1^T), then y = h W3^T, with
+// y stored in the activation type (y_f32 = false) or in fp32.
 static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, int rows, const int32_t* offsets, int G,
-                             int cw, const void* w13, const void* w3, void* y, int* plan, void* h,
+                             int cw, const void* w13, const void* w3, void* y, bool y_f32, int* plan, void* h,
                              cudaStream_t st) {
     if (d->dtype == FS_BF16) {
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
         FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, st));
-        FS_TRY(launch_tc_gemm(EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d, st));
+        FS_TRY(launch_tc_gemm(y_f32 ? EPI_F32 : EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d,
+                              st));
     } else {
         const int bm = simt_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -190,14 +192,14 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, int rows, co
 static fs_status routed_impl(const fs_layer_desc* d, const void* x_perm, const int32_t* offsets, const void* w13,
                              const void* w3, void* y_perm, void* ws, cudaStream_t st) {
     const Layout l = layout(d, 0);
-    return swiglu_impl(d, x_perm, d->T * d->k, offsets, d->E, d->c, w13, w3, y_perm, at<int>(ws, l.plan_r),
+    return swiglu_impl(d, x_perm, d->T * d->k, offsets, d->E, d->c, w13, w3, y_perm, false, at<int>(ws, l.plan_r),
                        at<void>(ws, l.h_r), st);
 }
 
 static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* w13s, const void* w3s, void* s_out,
                              void* ws, cudaStream_t st) {
     const Layout l = layout(d, 0);
-    return swiglu_impl(d, u, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out,
+    return swiglu_impl(d, u, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
                        at<int>(ws, l.plan_s), at<void>(ws, l.h_s), st);
 }
 

@@ -10,8 +10,8 @@
 //   o[t]   = o_prev[t] + S[t] + R[t]
 //   u'[t]  = the next block's input, rounded to the activation type:
 //            o*[t] (partial), o_prev[t] (outdated) or o[t] (disabled)
-// The residual stream (o_prev, o*, o) may be fp32 or the activation type; the
-// expert rows, S and u' are in the activation type.  One warp per token, 8
+// The residual stream (o_prev, o*, o) may be fp32 or the activation type; S is
+// fp32; the expert rows and u' are in the activation type.  One warp per token, 8
 // columns per lane step: each lane loads the k expert rows of its columns
 // together (k loads in flight), sums in fp32, rounds once per output.
 #include "common.cuh"
@@ -84,7 +84,7 @@ __device__ __forceinline__ void fma_raw8(float w, const Raw8<BF16>& r, float (&a
     }
 }
 
-template <bool BF16, int KMAX>   // BF16: activation type of y_perm, shared_out and u_next
+template <bool BF16, int KMAX>   // BF16: activation type of y_perm and u_next
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos, const float* __restrict__ topk_w,
                const void* __restrict__ o_prev, bool prev_bf16, const void* __restrict__ shared_out,
@@ -115,7 +115,7 @@ combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos,
         float base[8], sv[8], acc[8];
         load8(o_prev, row + c8, prev_bf16, base);
         if (shared_out) {
-            load8(shared_out, row + c8, BF16, sv);
+            load8(shared_out, row + c8, false, sv);     // S is fp32
 #pragma unroll
             for (int j = 0; j < 8; ++j) base[j] += sv[j];
         }

@@ -33,9 +33,10 @@
  *   - Storage: the configurations store activations in bf16 (or fp32) between
  *     steps.  With storage != ORACLE_EXACT the oracle rounds (RNE) exactly the
  *     tensors the layer writes out: the expert hidden h, each routed expert
- *     output y, the shared output S and every block input u_k (k >= 2; the
- *     operand of the block's GEMMs).  The residual stream o_k, o_k* is carried
- *     in fp32, and the stack outputs o_L, o_L* are returned at that precision:
+ *     output y and every block input u_k (k >= 2; the operand of the block's
+ *     GEMMs).  The residual stream o_k, o_k* and the shared output S, which is
+ *     only ever added into it, are carried in fp32, and the stack outputs
+ *     o_L, o_L* are returned at that precision:
  *     storing them in bf16 is the layer's own output rounding, which the
  *     comparison tolerance covers.  All sums stay fp64.
  */
@@ -203,7 +204,7 @@ int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_d
  *   o_prev : o_{k-1}                     [n_tok, d] fp64
  * Computes, per token (§2.1 MoE and shared expert; §3 FarSkip, eq. 8b):
  *   R    = sum_s w_s * y_{e_s}(u)       (y_e stored, so rounded per storage)
- *   S    = sum_i MLP_shared_i(u)        (rounded once)
+ *   S    = sum_i MLP_shared_i(u)        (rounded once, at residual precision)
  *   o*   = o_prev + S                   (rounded per out_storage)
  *   o    = o_prev + S + R               (rounded per out_storage)
  */
@@ -214,6 +215,8 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
                  double* R_out, double* S_out) {
     const int d = cfg->d, E = cfg->E, k = cfg->k, c = cfg->c;
     const int ns = cfg->n_shared, cs = cfg->c_shared;
+    /* S only feeds the residual stream, which is carried in fp32 */
+    const int resid = cfg->storage == ORACLE_STORE_BF16 ? ORACLE_STORE_F32 : cfg->storage;
     double* z = logits;
     double* zbuf = NULL;
     if (!z) {
@@ -249,7 +252,7 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
             for (int i = 0; i < d; ++i) S[i] += y[i];
         }
         for (int i = 0; i < d; ++i) {
-            double sv = oracle_round(S[i], cfg->storage);
+            double sv = oracle_round(S[i], resid);
             double op = o_prev[(size_t)t * d + i];
             o_star[(size_t)t * d + i] = oracle_round(op + sv, out_storage);
             o_full[(size_t)t * d + i] = oracle_round(op + sv + R[i], out_storage);

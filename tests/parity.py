@@ -90,7 +90,7 @@ def gpu_stack_stepwise(cfg, packed_blocks, x, wiring, DEV="cuda"):
     pos, perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
     x_perm = torch.empty((T * k, d), dtype=dt, device=DEV)
     y_perm = torch.empty((T * k, d), dtype=dt, device=DEV)
-    s = torch.empty((T, d), dtype=dt, device=DEV) if cfg.n_shared else None
+    s = torch.empty((T, d), dtype=torch.float32, device=DEV) if cfg.n_shared else None
     u, o_prev = x, x
     routing = []
     o_k = o_star = None

@@ -171,7 +171,7 @@ def test_shared_expert(fs, dtype, ns, cs, T):
     packed = fs.pack_block(cfg, w)
     desc = fs.make_desc(cfg)
     ws = fs.alloc_workspace(desc, 0)
-    s = torch.empty((T, cfg.d), dtype=x.dtype, device=DEV)
+    s = torch.empty((T, cfg.d), dtype=torch.float32, device=DEV)
     fs.fs_shared_expert(desc, x, packed["w13_shared"], packed["w3_shared"], s, ws)
     _no_dev_error()
     out = oracle.stack(oracle_cfg(cfg), oracle_weights([w]), "partial", synth.to_numpy(x), want_rs=True)
@@ -200,7 +200,7 @@ def test_combine(fs, dtype, T, k, d, shared, partial, resid):
     pdt = sdt if resid == "act" else torch.float32
     odt = torch.float32 if resid == "f32" else sdt
     op = torch.randn((T, d), generator=g, device=DEV).to(pdt)
-    s = torch.randn((T, d), generator=g, device=DEV).to(sdt) if shared else None
+    s = torch.randn((T, d), generator=g, device=DEV) if shared else None     # fp32
     o_star = torch.empty((T, d), dtype=odt, device=DEV) if partial else None
     o = torch.empty((T, d), dtype=odt, device=DEV)
     u_next = {wi: torch.empty((T, d), dtype=sdt, device=DEV) for wi in ("partial", "outdated", "disabled")}
@@ -208,9 +208,10 @@ def test_combine(fs, dtype, T, k, d, shared, partial, resid):
         fs.fs_combine(fs.make_desc(cfg), y, torch.from_numpy(pos).to(DEV), w, op, s, o_star, o, un, wi)
     _no_dev_error()
     ost = oracle.STORE_BF16 if odt == torch.bfloat16 else oracle.STORE_F32
-    sn = None if s is None else synth.to_numpy(s.to(pdt)) if pdt == torch.float32 else synth.to_numpy(s)
-    y_in = synth.to_numpy(y.to(pdt)) if pdt == torch.float32 else synth.to_numpy(y)
-    r_star, r = oracle.combine(T, k, d, y_in, pos, w.cpu().numpy(), synth.to_numpy(op), sn, storage=ost)
+    # the oracle combine takes one element type: widen everything to fp64 (exact)
+    f64 = lambda t: None if t is None else t.double().cpu().numpy()
+    y_in, sn, opn = f64(y), f64(s), f64(op)
+    r_star, r = oracle.combine(T, k, d, y_in, pos, w.cpu().numpy(), opn, sn, storage=ost)
     # fp32 sums vs fp64 sums, each rounded once: equal but for 1-ulp rounding flips
     # plus the fp32 accumulation error, bounded by a few fp32 ulps of the term magnitudes
     ulp = 2.0 ** -7 if odt == torch.bfloat16 else 2.0 ** -23
@@ -223,7 +224,7 @@ def test_combine(fs, dtype, T, k, d, shared, partial, resid):
         assert np.all(d_star <= ulp * np.abs(r_star) + 2.0 ** -23 * mag + 1e-30), d_star.max()
     # next-block inputs: the chosen residual rounded to the activation type
     act = oracle.STORE_BF16 if dtype == "bf16" else oracle.STORE_F32
-    r_star_u, r_u = oracle.combine(T, k, d, y_in, pos, w.cpu().numpy(), synth.to_numpy(op), sn, storage=act)
+    r_star_u, r_u = oracle.combine(T, k, d, y_in, pos, w.cpu().numpy(), opn, sn, storage=act)
     ulp_u = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -23
     for wi, want in (("partial", r_star_u), ("disabled", r_u)):
         du = np.abs(to64(u_next[wi]) - want)

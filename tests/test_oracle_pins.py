@@ -403,9 +403,9 @@ def test_bf16_storage_outputs_are_fp32_and_close():
         np.testing.assert_array_equal(v, v.astype(np.float32).astype(np.float64))   # fp32 values
         rel = np.linalg.norm(v - ex[key]) / np.linalg.norm(ex[key])
         assert rel < 1e-2, rel
-    # S is a stored tensor: bf16 values
+    # S feeds only the fp32 residual: fp32 values
     s1 = bf["S"][0]
-    np.testing.assert_array_equal(s1, torch.from_numpy(s1.astype(np.float32)).to(torch.bfloat16).double().numpy())
+    np.testing.assert_array_equal(s1, s1.astype(np.float32).astype(np.float64))
     # block 2 sees u_2 = bf16(o_1*) with o_1* = fp32(x + S_1)
     o1s = (x + s1).astype(np.float32)
     u2 = torch.from_numpy(o1s).to(torch.bfloat16).double().numpy()
