@@ -154,11 +154,12 @@ class Weights:
 
 
 def stack(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, want_rs: bool = False,
-          want_logits: bool = True):
+          want_logits: bool = True, want_inputs: bool = False):
     """Run L = len(weights) FarSkip blocks on the rows of x.
 
     Returns a dict with o (= o_L), o_star (= o_L*), topk_idx [L,n,k], topk_w [L,n,k],
-    logits [L,n,E] and, with want_rs, R and S [L,n,d]."""
+    logits [L,n,E], with want_rs R and S [L,n,d], and with want_inputs the
+    block inputs U (u_k) and P (o_{k-1}) and block outputs O (o_k), OS (o_k*) [L,n,d]."""
     x = np.ascontiguousarray(x)
     L = len(weights)
     n = x.shape[0]
@@ -171,11 +172,17 @@ def stack(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, want_rs: bool = 
         "logits": np.zeros((L, n, cfg.E), np.float64) if want_logits else None,
         "R": np.zeros((L, n, cfg.d), np.float64) if want_rs else None,
         "S": np.zeros((L, n, cfg.d), np.float64) if want_rs else None,
+        "U": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
+        "P": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
+        "O": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
+        "OS": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
     }
     _check(lib().oracle_stack(ctypes.byref(cfg), arr, ctypes.c_int(L), ctypes.c_int(WIRINGS[wiring]),
                               ctypes.c_int(n), _p(x), ctypes.c_int(_dt(x)),
                               _p(out["o"]), _p(out["o_star"]), _p(out["topk_idx"]), _p(out["topk_w"]),
-                              _p(out["logits"]), _p(out["R"]), _p(out["S"])), "stack")
+                              _p(out["logits"]), _p(out["R"]), _p(out["S"]), _p(out["U"]), _p(out["P"]),
+                              _p(out["O"]), _p(out["OS"])),
+           "stack")
     return out
 
 

@@ -276,14 +276,16 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
  * Storage (when not exact): o_k, o_k* are rounded to fp32 (the residual
  * stream) and u_{k+1} to the storage type; the fp32-storage configuration
  * rounds everything to fp32.
- * Outputs o_L and o_L*; per-block routing and R/S when the pointers are set
- * ([L, n_tok, ...], block-major).  Token rows are independent, so any subset
- * of the rows of x can be passed. */
+ * Outputs o_L and o_L*; per-block routing, R/S, the block inputs u_k (U_all)
+ * and o_{k-1} (P_all) and the block outputs o_k (O_all) and o_k* (OS_all) when
+ * the pointers are set ([L, n_tok, ...], block-major).
+ * Token rows are independent, so any subset of the rows of x can be passed. */
 int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wiring,
                  int n_tok, const void* x, int x_dtype,
                  double* o_last, double* o_last_star,
                  int32_t* topk_idx_all, double* topk_w_all, double* logits_all,
-                 double* R_all, double* S_all) {
+                 double* R_all, double* S_all, double* U_all, double* P_all,
+                 double* O_all, double* OS_all) {
     const int d = cfg->d, E = cfg->E, k = cfg->k;
     const size_t n = (size_t)n_tok * d;
     if (L < 1 || n_tok < 0) return -1;
@@ -306,12 +308,16 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
             double* o_k = ring[b % 3];
             double* os_k = star[b % 2];
             const oracle_weights* wb = wts + (b - 1);
+            if (U_all) memcpy(U_all + (size_t)(b - 1) * n, u, sizeof(double) * n);
+            if (P_all) memcpy(P_all + (size_t)(b - 1) * n, o_km1, sizeof(double) * n);
             rc = oracle_block(cfg, wb, n_tok, u, o_km1, resid, os_k, o_k, idx, w,
                               logits_all ? logits_all + (size_t)(b - 1) * n_tok * E : NULL,
                               R_all ? R_all + (size_t)(b - 1) * n : NULL,
                               S_all ? S_all + (size_t)(b - 1) * n : NULL);
             if (topk_idx_all) memcpy(topk_idx_all + (size_t)(b - 1) * n_tok * k, idx, sizeof(int32_t) * (size_t)n_tok * k);
             if (topk_w_all) memcpy(topk_w_all + (size_t)(b - 1) * n_tok * k, w, sizeof(double) * (size_t)n_tok * k);
+            if (O_all) memcpy(O_all + (size_t)(b - 1) * n, o_k, sizeof(double) * n);
+            if (OS_all) memcpy(OS_all + (size_t)(b - 1) * n, os_k, sizeof(double) * n);
             if (b == L) {
                 memcpy(o_last, o_k, sizeof(double) * n);
                 memcpy(o_last_star, os_k, sizeof(double) * n);

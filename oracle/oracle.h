@@ -55,7 +55,8 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
                  int n_tok, const void* x, int x_dtype,
                  double* o_last, double* o_last_star,
                  int32_t* topk_idx_all, double* topk_w_all, double* logits_all,
-                 double* R_all, double* S_all);
+                 double* R_all, double* S_all, double* U_all, double* P_all,
+                 double* O_all, double* OS_all);
 int oracle_dispatch(int T, int k, int E, const int32_t* topk_idx,
                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src);
 int oracle_combine(int T, int k, int d, int in_dtype, int storage,

@@ -74,44 +74,61 @@ def topk_mismatch(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_logits: np.ndarr
     return bad
 
 
-def gpu_stack_stepwise(cfg, packed_blocks, x, wiring, DEV="cuda"):
-    """The FarSkip stack driven from Python through the single-step C-ABI
-    entry points (router, dispatch, routed experts, shared expert, combine),
-    keeping each block's routing.  Returns (o_L, o_L*, [topk_idx per block])."""
-    from mixture_experts_layer_expert_gb300 import fs
-    T, d, k, E = x.shape[0], cfg.d, cfg.k, cfg.E
-    desc = fs.make_desc(cfg, T)
-    ws = fs.alloc_workspace(desc, 0)
-    dt = x.dtype
-    i32 = dict(dtype=torch.int32, device=DEV)
-    idx = torch.empty((T, k), **i32)
-    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
-    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
-    pos, perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
-    x_perm = torch.empty((T * k, d), dtype=dt, device=DEV)
-    y_perm = torch.empty((T * k, d), dtype=dt, device=DEV)
-    s = torch.empty((T, d), dtype=torch.float32, device=DEV) if cfg.n_shared else None
+class GpuBlockRunner:
+    """One FarSkip block driven through the single-step C-ABI entry points
+    (router, dispatch, routed experts, shared expert, combine) with buffers
+    for T tokens; the same launch sequence fs_farskip_stack issues."""
+
+    def __init__(self, cfg, T, DEV="cuda"):
+        from mixture_experts_layer_expert_gb300 import fs
+        self.fs, self.cfg, self.T, self.dev = fs, cfg, T, DEV
+        d, k, E = cfg.d, cfg.k, cfg.E
+        self.desc = fs.make_desc(cfg, T)
+        self.ws = fs.alloc_workspace(self.desc, 0)
+        self.dt = synth.storage_dtype(cfg)
+        i32 = dict(dtype=torch.int32, device=DEV)
+        self.idx = torch.empty((T, k), **i32)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+        self.counts, self.offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+        self.pos, self.perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
+        self.x_perm = torch.empty((T * k, d), dtype=self.dt, device=DEV)
+        self.y_perm = torch.empty((T * k, d), dtype=self.dt, device=DEV)
+        self.s = torch.empty((T, d), dtype=torch.float32, device=DEV) if cfg.n_shared else None
+
+    def run(self, pw, u, o_prev, last, wiring):
+        """Returns (o_k, o_k*, u_next or None, topk_idx numpy)."""
+        fs, T, d = self.fs, self.T, self.cfg.d
+        fs.fs_router_topk(self.desc, u, pw["w_r"], pw["bias"], self.idx, self.w, None, self.ws)
+        idx = self.idx.cpu().numpy().copy()
+        fs.fs_dispatch(self.desc, self.idx, u, self.counts, self.offsets, self.pos, self.perm, self.x_perm, self.ws)
+        fs.fs_grouped_swiglu(self.desc, self.x_perm, self.offsets, pw["w13"], pw["w3"], self.y_perm, self.ws)
+        if self.s is not None:
+            fs.fs_shared_expert(self.desc, u, pw["w13_shared"], pw["w3_shared"], self.s, self.ws)
+        rdt = self.dt if last else torch.float32          # fp32 residual stream between blocks
+        o_k = torch.empty((T, d), dtype=rdt, device=self.dev)
+        o_star = torch.empty((T, d), dtype=rdt, device=self.dev)
+        u_next = None if last else torch.empty((T, d), dtype=self.dt, device=self.dev)
+        fs.fs_combine(self.desc, self.y_perm, self.pos, self.w, o_prev, self.s, o_star, o_k, u_next, wiring)
+        torch.cuda.synchronize()
+        return o_k, o_star, u_next, idx
+
+
+def gpu_stack_stepwise(cfg, packed_blocks, x, wiring, DEV="cuda", keep_inputs=False):
+    """The FarSkip stack driven from Python through the single-step entry
+    points, keeping each block's routing (and, with keep_inputs, its inputs
+    u_k and o_{k-1}).  Returns (o_L, o_L*, [topk_idx per block], [(u, o_prev)])."""
+    run = GpuBlockRunner(cfg, x.shape[0], DEV)
     u, o_prev = x, x
-    routing = []
+    routing, inputs = [], []
     o_k = o_star = None
     L = len(packed_blocks)
     for b, pw in enumerate(packed_blocks):
-        last = b == L - 1
-        fs.fs_router_topk(desc, u, pw["w_r"], pw["bias"], idx, w, None, ws)
-        routing.append(idx.cpu().numpy().copy())
-        fs.fs_dispatch(desc, idx, u, counts, offsets, pos, perm, x_perm, ws)
-        fs.fs_grouped_swiglu(desc, x_perm, offsets, pw["w13"], pw["w3"], y_perm, ws)
-        if s is not None:
-            fs.fs_shared_expert(desc, u, pw["w13_shared"], pw["w3_shared"], s, ws)
-        rdt = dt if last else torch.float32          # fp32 residual stream between blocks
-        o_k = torch.empty((T, d), dtype=rdt, device=DEV)
-        o_star = torch.empty((T, d), dtype=rdt, device=DEV)
-        u_next = None if last else torch.empty((T, d), dtype=dt, device=DEV)
-        fs.fs_combine(desc, y_perm, pos, w, o_prev, s, o_star, o_k, u_next, wiring)
-        u = u_next
-        o_prev = o_k
-    torch.cuda.synchronize()
-    return o_k, o_star, routing
+        if keep_inputs:
+            inputs.append((u, o_prev))
+        o_k, o_star, u_next, idx = run.run(pw, u, o_prev, b == L - 1, wiring)
+        routing.append(idx)
+        u, o_prev = u_next, o_k
+    return o_k, o_star, routing, inputs
 
 
 def routing_mismatch_all_blocks(cfg, gpu_routing, ref, blocks, strict_blocks=1):

@@ -1,8 +1,24 @@
-"""GPU parity of the whole FarSkip stack (fs_farskip_stack through the C ABI)
-against the CPU oracle: small multi-tile shapes for every wiring and gate, the
-fp32 workload in full, and the full-size bf16 workloads on sampled tokens
-(token rows are independent through the whole stack, so the oracle can follow
-any subset of tokens through all L blocks)."""
+"""GPU parity of the FarSkip stack against the CPU oracle.
+
+Two kinds of check, for small multi-tile shapes (every token) and for the
+full-size workloads (in the launch configuration the benchmark times, on a
+seeded sample of tokens; token rows are independent through the whole stack):
+
+blockwise   every block k is run on the GPU on the oracle's own inputs u_k
+            (bf16) and o_{k-1} (fp32), spliced into the sampled rows of a
+            full-size GPU input, so both sides route identical inputs: the
+            routing rule (top-k sets equal unless the k-th/(k+1)-th gap
+            < 1e-4, such tokens < 0.1%) and the output tolerance (relative
+            Frobenius <= 5e-3, max-abs <= 2e-2 rms) hold per block.
+end-to-end  fs_farskip_stack as a whole vs the oracle stack.  After block 1
+            the two sides' bf16 block inputs differ by rounding flips of the
+            residual, so later-block routing may differ near ties: such
+            tokens are counted (bounded) and left out; outputs must meet the
+            relative Frobenius bound, and a max-abs bound that sums the
+            per-block bound over the blocks (errors add through the residual).
+The stack driver is also checked bit-for-bit against the same stack driven
+step by step through the single-step entry points.
+"""
 import os
 
 import numpy as np
@@ -11,11 +27,12 @@ import torch
 
 import oracle
 from mixture_experts_layer_expert_gb300 import configs, fs, synth
-from parity import (compare, gpu_stack_stepwise, oracle_cfg, oracle_weights, routing_mismatch_all_blocks,
-                    to64, topk_mismatch)
+from parity import (GpuBlockRunner, TOL, compare, gpu_stack_stepwise, kth_gap, oracle_cfg, oracle_weights, to64,
+                    topk_mismatch)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+DRIFT_FRAC = 0.05      # end-to-end: tokens whose later-block routing may differ
 
 
 def _run_gpu(cfg, prob, wiring):
@@ -27,31 +44,79 @@ def _run_gpu(cfg, prob, wiring):
     return stack, o, o_star
 
 
-def _gpu_routing(cfg, stack, u):
-    """Top-k indices the GPU picks for input u with block 0's router."""
-    T = u.shape[0]
-    desc = fs.make_desc(cfg, T)
-    ws = fs.alloc_workspace(desc, 0)
-    idx = torch.empty((T, cfg.k), dtype=torch.int32, device=DEV)
-    w = torch.empty((T, cfg.k), dtype=torch.float32, device=DEV)
-    fs.fs_router_topk(desc, u, stack.blocks[0]["w_r"], stack.blocks[0]["bias"], idx, w, None, ws)
-    torch.cuda.synchronize()
-    return idx.cpu().numpy()
+def blockwise(cfg, prob, stack, wiring, rows=None):
+    """Per-block parity on identical inputs (see module docstring)."""
+    T = cfg.T
+    x = prob["x"]
+    rows = np.arange(T) if rows is None else rows
+    rows_t = torch.as_tensor(rows, device=DEV)
+    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x[rows_t]),
+                       want_inputs=True)
+    _, _, _, gpu_inputs = gpu_stack_stepwise(cfg, stack.blocks, x, wiring, keep_inputs=True)
+    run = GpuBlockRunner(cfg, T)
+    for b, pw in enumerate(stack.blocks):
+        u, o_prev = gpu_inputs[b]
+        u = u.clone()
+        o_prev = o_prev.clone()
+        if b > 0:   # splice the oracle's inputs into the sampled rows
+            u[rows_t] = torch.from_numpy(ref["U"][b]).to(DEV, u.dtype)
+            o_prev[rows_t] = torch.from_numpy(ref["P"][b]).to(DEV, o_prev.dtype)
+        o_k, o_star, _, idx = run.run(pw, u, o_prev, b == cfg.L - 1, wiring)
+        bias = pw["bias"]
+        bnp = None if bias is None else bias.cpu().numpy()
+        z = ref["logits"][b] - (0 if bnp is None else bnp.astype(np.float64)[None, :])
+        bad = topk_mismatch(idx[rows], ref["topk_idx"][b], z, cfg.k, bnp)
+        keep = ~bad
+        compare(to64(o_k[rows_t])[keep], ref["O"][b][keep], cfg.dtype, "block %d o_k" % (b + 1))
+        compare(to64(o_star[rows_t])[keep], ref["OS"][b][keep], cfg.dtype, "block %d o_k*" % (b + 1))
+    return ref
+
+
+def end_to_end(cfg, prob, stack, o, o_star, wiring, rows=None):
+    T = cfg.T
+    rows = np.arange(T) if rows is None else rows
+    rows_t = torch.as_tensor(rows, device=DEV)
+    x_s = prob["x"][rows_t]
+    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x_s),
+                       want_inputs=True)
+    _, _, routing, _ = gpu_stack_stepwise(cfg, stack.blocks, x_s, wiring)
+    bad_any = np.zeros(len(rows), bool)
+    drift = []
+    for b in range(cfg.L):
+        bias = prob["blocks"][b]["bias"]
+        bnp = None if bias is None else synth.to_numpy(bias)
+        z = ref["logits"][b] - (0 if bnp is None else bnp.astype(np.float64)[None, :])
+        if b == 0:       # identical inputs: the strict rule
+            bad = topk_mismatch(routing[0], ref["topk_idx"][0], z, cfg.k, bnp)
+        else:
+            bad = np.any(np.sort(routing[b], 1) != np.sort(ref["topk_idx"][b], 1), axis=1)
+            zz = ref["logits"][b]
+            drift.append((b + 1, int(bad.sum()), float(kth_gap(zz[bad], cfg.k).max()) if bad.any() else 0.0))
+        bad_any |= bad
+    assert bad_any.sum() <= max(1, int(DRIFT_FRAC * len(rows))), "routing drift %s" % drift
+    keep = ~bad_any
+    got, got_s = to64(o[rows_t])[keep], to64(o_star[rows_t])[keep]
+    if cfg.L == 1:
+        compare(got, ref["o"][keep], cfg.dtype, "o_L")
+        compare(got_s, ref["o_star"][keep], cfg.dtype, "o_L*")
+        return drift
+    tol = TOL[cfg.dtype]
+    rms_sum = sum(np.sqrt(np.mean(ref["O"][b] ** 2)) for b in range(cfg.L))
+    for g, r, what in ((got, ref["o"][keep], "o_L"), (got_s, ref["o_star"][keep], "o_L*")):
+        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+        assert rel <= tol["rel_fro"], "%s: relative Frobenius %.3e" % (what, rel)
+        mx = np.abs(g - r).max()
+        assert mx <= tol["max_abs_rms"] * rms_sum, "%s: max-abs %.3e > %.1e * sum_k rms(o_k) (%.3e)" % (
+            what, mx, tol["max_abs_rms"], rms_sum)
+    return drift
 
 
 def _check_stack(cfg, prob, wiring):
-    """fs_farskip_stack vs the oracle on every token; the same stack driven
-    step by step through the single-step entry points must give identical
-    bits and supplies each block's routing for the mismatch rule."""
     stack, o, o_star = _run_gpu(cfg, prob, wiring)
-    so, so_star, routing = gpu_stack_stepwise(cfg, stack.blocks, prob["x"], wiring)
+    so, so_star, _, _ = gpu_stack_stepwise(cfg, stack.blocks, prob["x"], wiring)
     assert torch.equal(so, o) and torch.equal(so_star, o_star), "stack driver != single-step calls"
-    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(prob["x"]))
-    bad, stats = routing_mismatch_all_blocks(cfg, routing, ref, prob["blocks"])
-    keep = ~bad
-    compare(to64(o)[keep], ref["o"][keep], cfg.dtype, "o_L")
-    compare(to64(o_star)[keep], ref["o_star"][keep], cfg.dtype, "o_L*")
-    return ref
+    blockwise(cfg, prob, stack, wiring)
+    end_to_end(cfg, prob, stack, o, o_star, wiring)
 
 
 @pytest.mark.parametrize("wiring", ["partial", "outdated", "disabled"])
@@ -103,20 +168,33 @@ SAMPLE = int(os.environ.get("FS_PARITY_SAMPLE", "128"))
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(fs, name):
-    """Full-size workload, in the launch configuration the benchmark times
-    (one fs_farskip_stack call over all T tokens); the oracle follows a seeded
-    sample of tokens through all L blocks, and block-1 routing of every token
-    is checked against the oracle's router."""
+    """Full-size workload, one fs_farskip_stack call over all T tokens (the
+    benchmark's launch configuration); the oracle follows a seeded sample of
+    tokens through all L blocks, blockwise and end to end."""
     cfg = configs.CONFIGS[name]
     prob = synth.make_problem(cfg, DEV)
     stack, o, o_star = _run_gpu(cfg, prob, cfg.wiring)
     g = np.random.default_rng(0)
     rows = np.sort(g.choice(cfg.T, size=min(SAMPLE, cfg.T), replace=False))
-    x_s = prob["x"][torch.as_tensor(rows, device=DEV)]
-    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), cfg.wiring, synth.to_numpy(x_s))
-    _, _, routing = gpu_stack_stepwise(cfg, stack.blocks, x_s, cfg.wiring)
-    bad, stats = routing_mismatch_all_blocks(cfg, routing, ref, prob["blocks"])
-    keep = ~bad
-    rows_t = torch.as_tensor(rows, device=DEV)
-    compare(to64(o[rows_t])[keep], ref["o"][keep], cfg.dtype, name + " o_L")
-    compare(to64(o_star[rows_t])[keep], ref["o_star"][keep], cfg.dtype, name + " o_L*")
+    blockwise(cfg, prob, stack, cfg.wiring, rows)
+    end_to_end(cfg, prob, stack, o, o_star, cfg.wiring, rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["v3", "qwen3"])
+def test_full_size_routing_all_tokens(fs, name):
+    """Block-1 routing of EVERY token at full size against the oracle's router:
+    top-k sets equal except near-ties (< 1e-4), and those are < 0.1% of tokens."""
+    cfg = configs.CONFIGS[name]
+    x = synth.make_x(cfg, DEV)
+    w = synth.make_block_weights(cfg, 0, DEV)
+    desc = fs.make_desc(cfg)
+    ws = fs.alloc_workspace(desc, 0)
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    tw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+    fs.fs_router_topk(desc, x, w["w_r"], w["bias"], idx, tw, None, ws)
+    torch.cuda.synchronize()
+    bias = synth.to_numpy(w["bias"])
+    z, ridx, _ = oracle.router(oracle_cfg(cfg), synth.to_numpy(x), synth.to_numpy(w["w_r"]), bias)
+    zref = z - (0 if bias is None else bias.astype(np.float64)[None, :])
+    topk_mismatch(idx.cpu().numpy(), ridx, zref, cfg.k, bias)
