@@ -387,7 +387,7 @@ def main():
     ap.add_argument("--config", default="v3", choices=sorted(configs.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
     args = ap.parse_args()
     rank, world, local = dist_env()
