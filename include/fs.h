@@ -133,6 +133,26 @@ fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const 
                       int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
                       void* x_perm, void* ws, size_t ws_bytes, void* stream);
 
+/* fs_dispatch without a workspace.  The paper has no counterpart: this exists
+ * for callers that cannot hand the library device scratch memory -- for example
+ * a plugin or custom-op interface that passes only input and output buffers,
+ * or code that must not call cudaMalloc/cudaFree (which can synchronise the
+ * device) on its execution path.  Same arguments and results as fs_dispatch,
+ * minus ws/ws_bytes.  Its scratch (the per-chunk expert histogram) is a fixed
+ * 256 KiB device array inside the library, present on every GPU that loads the
+ * library until the process exits; it holds ceil(T / 1024) * E <= 65536 ints
+ * (e.g. T <= 65536 tokens with E <= 1024 experts, T <= 262144 with E <= 256).
+ * Larger shapes return FS_ERR_WORKSPACE before any launch (fs_last_cuda_error
+ * gives the sizes).  Nothing in the scratch needs to start at zero: each call
+ * overwrites every entry it reads.  All calls share the one array, so calls
+ * that overlap on the GPU (several streams, or several host threads) race and
+ * must be serialised by the caller.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  Allocates nothing. */
+fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u,
+                              int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
+                              void* x_perm, void* stream);
+
 /* Routed experts (§2.1 MLP and MoE equations), grouped by expert: for every
  * expert e and every row p in [offsets[e], offsets[e+1]):
  *   h = SiLU(x W2_e^T) * (x W1_e^T)  (fp32 accumulate, stored bf16/fp32 in ws)

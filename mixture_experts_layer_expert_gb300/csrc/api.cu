@@ -285,6 +285,27 @@ fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const 
                          static_cast<cudaStream_t>(stream));
 }
 
+fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u, int32_t* counts,
+                              int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm, void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(topk_idx));
+    FS_CHECK(need(u));
+    FS_CHECK(need(counts));
+    FS_CHECK(need(offsets));
+    FS_CHECK(need(pos));
+    FS_CHECK(need(perm_src));
+    FS_CHECK(need(x_perm));
+    if (dispatch_ws_bytes(desc->T, desc->E) > static_cast<size_t>(kStaticDispatchScratchInts) * sizeof(int32_t)) {
+        std::snprintf(g_last_cuda, sizeof g_last_cuda,
+                      "fs_dispatch_noalloc: ceil(T/1024) * E = %zu scratch ints exceed the static maximum %d",
+                      dispatch_ws_bytes(desc->T, desc->E) / sizeof(int32_t), kStaticDispatchScratchInts);
+        return FS_ERR_WORKSPACE;
+    }
+    FS_TRY(launch_dispatch_noalloc(topk_idx, u, desc->T, desc->d, desc->E, desc->k, elem_bytes(desc), counts, offsets,
+                                   pos, perm_src, x_perm, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
 fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets, const void* w13,
                             const void* w3, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
     FS_CHECK(check_desc(desc));

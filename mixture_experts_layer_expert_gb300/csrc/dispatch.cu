@@ -15,6 +15,8 @@
 //             rank inside the chunk -> pos[t k + s], perm_src[p]
 //   4 copy    one warp per token: read the row of u once (16-byte vectors),
 //             write it to its k permuted rows
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -215,6 +217,43 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d
         reinterpret_cast<const uint4*>(u), T, row_vecs, k, pos, reinterpret_cast<uint4*>(x_perm));
     count_launch();
     return cudaGetLastError();
+}
+
+// ------------------------------------------------ dispatch without allocation
+// Scratch of fs_dispatch_noalloc: the per-chunk expert histogram lives in this
+// file-scope device array instead of a caller-provided workspace.  It is loaded
+// with the library on every GPU that loads it and stays until the process exits.
+static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticDispatchScratchInts];
+
+static int32_t* g_dispatch_scratch_ptr[64] = {nullptr};
+static std::mutex g_dispatch_scratch_mu;
+
+// Device address of g_dispatch_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+static cudaError_t dispatch_scratch_address(int32_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dispatch_scratch_mu);
+    if (!g_dispatch_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess) return e;
+        g_dispatch_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_dispatch_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_dispatch_noalloc(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
+                                    int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
+                                    void* x_perm, cudaStream_t st) {
+    int32_t* scratch = nullptr;
+    cudaError_t e = dispatch_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    return launch_dispatch(topk_idx, u, T, d, E, k, elem_bytes, counts, offsets, pos, perm_src, x_perm, scratch, st);
 }
 
 }  // namespace fs

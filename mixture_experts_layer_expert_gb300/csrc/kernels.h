@@ -32,7 +32,11 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         int32_t* topk_idx, float* topk_w, cudaStream_t st);
 
 // dispatch.cu
+constexpr int kStaticDispatchScratchInts = 65536;   // 256 KiB: fs_dispatch_noalloc's scratch
 size_t dispatch_ws_bytes(int T, int E);
+cudaError_t launch_dispatch_noalloc(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
+                                    int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
+                                    void* x_perm, cudaStream_t st);
 cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
                             int32_t* scratch, cudaStream_t st);

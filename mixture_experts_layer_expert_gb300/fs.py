@@ -47,6 +47,7 @@ _SIGS = {
     "fs_pack_w3_shared": (_I32, [_I32, _I32, _I32, _I32, _VP, _VP, _VP]),
     "fs_router_topk": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_dispatch": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_dispatch_noalloc": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fs_grouped_swiglu": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_shared_expert": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32,
@@ -78,7 +79,7 @@ def lib():
 def _check(status: int, what: str):
     if status != 0:
         detail = ""
-        if status == 4:
+        if status in (3, 4):
             detail = (lib().fs_last_cuda_error() or b"").decode()
         raise FsError(status, what, detail)
 
@@ -127,6 +128,13 @@ def fs_router_topk(desc, u, w_r, bias, topk_idx, topk_w, logits, ws, stream=None
 def fs_dispatch(desc, topk_idx, u, counts, offsets, pos, perm_src, x_perm, ws, stream=None):
     _check(lib().fs_dispatch(ctypes.byref(desc), _p(topk_idx), _p(u), _p(counts), _p(offsets), _p(pos),
                              _p(perm_src), _p(x_perm), _p(ws), _nbytes(ws), _stream(stream)), "fs_dispatch")
+
+
+def fs_dispatch_noalloc(desc, topk_idx, u, counts, offsets, pos, perm_src, x_perm, stream=None):
+    """fs_dispatch with the library's fixed static scratch instead of a workspace
+    (for callers that cannot provide device scratch memory)."""
+    _check(lib().fs_dispatch_noalloc(ctypes.byref(desc), _p(topk_idx), _p(u), _p(counts), _p(offsets), _p(pos),
+                                     _p(perm_src), _p(x_perm), _stream(stream)), "fs_dispatch_noalloc")
 
 
 def fs_grouped_swiglu(desc, x_perm, offsets, w13, w3, y_perm, ws, stream=None):
