@@ -12,12 +12,16 @@
 // host never reads them).  Each group's rows [row_start[g], row_start[g+1]) are
 // multiplied by the group's own B = W[g] ([N, K], K-major).
 //
-// CTA = 6 warps, one CTA per SM, persistent over a static tile order:
+// CTA = 10 warps, one CTA per SM, persistent over a static tile order:
 //   warp 0      TMA producer (one lane): A tile 128 x 64 and B tile 256 x 64 per stage
 //   warp 1      TMEM owner + MMA issuer (one lane): 4 x (128 x 256 x 16) MMAs per stage
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, activation, stores
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the
+//               tile's columns: tcgen05.ld of the accumulator, activation, stores
 // TMEM holds two 128 x 256 fp32 accumulators (512 columns) so the epilogue of
 // tile i overlaps the MMAs of tile i + 1.  Every wait is bounded in time.
+// Tile order inside a group: blocks of kGroupM M-tiles, N-tiles outer inside a
+// block, so the ~152 tiles in flight share a few MB of A and B in L2 instead of
+// streaming a tall A operand from HBM once per N-tile.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -35,7 +39,9 @@ constexpr int B_STAGE = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int NACC = 2;
 constexpr int TMEM_COLS = NACC * BN;   // 512
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;   // 320
+constexpr int kGroupM = 16;                    // M-tiles per rasterisation block
 constexpr int BAR_BYTES = 256;
 constexpr size_t SMEM_BYTES =
     1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * sizeof(int);
@@ -69,8 +75,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const in
     r.g = lo;
     const int mtiles = mt_start[lo + 1] - mt_start[lo];
     const int local = t - mt_start[lo] * n_tiles;
-    r.n = local / mtiles;
-    r.m = local - r.n * mtiles;
+    const int blk = local / (kGroupM * n_tiles);            // block of kGroupM M-tiles
+    const int gm = min(kGroupM, mtiles - blk * kGroupM);     // M-tiles in this block
+    const int rr = local - blk * kGroupM * n_tiles;
+    r.n = rr / gm;
+    r.m = blk * kGroupM + (rr - r.n * gm);
     r.a_row = row_start[lo] + r.m * BM;
     const int rem = row_start[lo + 1] - r.a_row;
     r.rows_valid = rem < BM ? rem : BM;
@@ -107,7 +116,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(smem_u32(&tfull[a]), 1);
-            mbar_init(smem_u32(&tempty[a]), 4);
+            mbar_init(smem_u32(&tempty[a]), EPI_WARPS);
         }
         mbar_init(smem_u32(fin), 1);
         *abort_flag = 0;
@@ -208,6 +217,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;          // TMEM lanes [32 quarter, 32 quarter + 32)
+        const int half = (warp - 2) >> 2;      // which half of the tile's columns
         const int r = quarter * 32 + lane;     // row of the tile owned by this thread
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -225,7 +235,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int rem = args.N - tl.n * BN;
                 const int npk = (rem >= BN ? BN : rem) / 128;
                 __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
-                for (int g2 = 0; g2 < npk; ++g2) {
+                for (int g2 = half; g2 < npk; g2 += 2) {
 #pragma unroll 1
                     for (int j0 = 0; j0 < 64; j0 += 32) {
                         uint32_t gv[32], uv[32];
@@ -251,8 +261,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int rem = args.out_cols - tl.n * BN;
                 const int ncols = rem >= BN ? BN : rem;
                 __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(args.out);
+                const int cend = min(ncols, (half + 1) * (BN / 2));
 #pragma unroll 1
-                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c0, v);
                     tmem_ld_wait();
@@ -272,8 +283,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int ncols = rem >= BN ? BN : rem;
                 float* Z = reinterpret_cast<float*>(args.out);
                 const bool vec = (args.ldo & 3) == 0;
+                const int cend = min(ncols, (half + 1) * (BN / 2));
 #pragma unroll 1
-                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c0, v);
                     tmem_ld_wait();
