@@ -23,6 +23,8 @@
 // block, so the ~152 tiles in flight share a few MB of A and B in L2 instead of
 // streaming a tall A operand from HBM once per N-tile.
 #include <cudaTypedefs.h>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -64,7 +66,7 @@ struct Tile {
 };
 
 __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const int* row_start, int G,
-                                            int n_tiles, int BNrows, int N) {
+                                            int n_tiles, int BNrows, int N, int bm = BM) {
     const int q = t / n_tiles;
     int lo = 0, hi = G;            // last g with mt_start[g] <= q
     while (hi - lo > 1) {
@@ -80,11 +82,93 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const in
     const int rr = local - blk * kGroupM * n_tiles;
     r.n = rr / gm;
     r.m = blk * kGroupM + (rr - r.n * gm);
-    r.a_row = row_start[lo] + r.m * BM;
+    r.a_row = row_start[lo] + r.m * bm;
     const int rem = row_start[lo + 1] - r.a_row;
-    r.rows_valid = rem < BM ? rem : BM;
+    r.rows_valid = rem < bm ? rem : bm;
     r.b_row = lo * N + r.n * BNrows;
     return r;
+}
+
+// Epilogue of one accumulator tile for the thread owning TMEM lane `r` of its
+// CTA (row a_row + r of the output), columns of half `half` of the tile.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(uint32_t tbase, int a_row, int rows_valid, int n, int r, int half,
+                                              const Args& args) {
+    const Tile tl{0, 0, n, a_row, rows_valid, 0};
+    const bool row_ok = r < tl.rows_valid;
+    const long long orow = static_cast<long long>(tl.a_row + r);
+    if constexpr (EPI == EPI_SWIGLU) {
+        // packed tile columns: [gate 64 | up 64] x 2 -> 128 expert columns
+        const int rem = args.N - tl.n * BN;
+        const int npk = (rem >= BN ? BN : rem) / 128;
+        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
+        for (int g2 = half; g2 < npk; g2 += 2) {
+#pragma unroll 1
+            for (int j0 = 0; j0 < 64; j0 += 32) {
+                uint32_t gv[32], uv[32];
+                tmem_ld32(tbase + g2 * 128 + j0, gv);
+                tmem_ld32(tbase + g2 * 128 + 64 + j0, uv);
+                tmem_ld_wait();
+                if (row_ok) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float h0 = silu_f(__uint_as_float(gv[2 * q])) * __uint_as_float(uv[2 * q]);
+                        const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
+                        pk[q] = pack_bf16x2(h0, h1);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(H + orow * args.ldo + tl.n * 128 + g2 * 64 + j0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_BF16) {
+        const int rem = args.out_cols - tl.n * BN;
+        const int ncols = rem >= BN ? BN : rem;
+        __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(args.out);
+        const int cend = min(ncols, (half + 1) * (BN / 2));
+#pragma unroll 1
+        for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c0, v);
+            tmem_ld_wait();
+            if (row_ok) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                uint4* dst = reinterpret_cast<uint4*>(Y + orow * args.ldo + tl.n * BN + c0);
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+            }
+        }
+    } else {  // EPI_F32
+        const int rem = args.out_cols - tl.n * BN;
+        const int ncols = rem >= BN ? BN : rem;
+        float* Z = reinterpret_cast<float*>(args.out);
+        const bool vec = (args.ldo & 3) == 0;
+        const int cend = min(ncols, (half + 1) * (BN / 2));
+#pragma unroll 1
+        for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c0, v);
+            tmem_ld_wait();
+            if (row_ok) {
+                float* dst = Z + orow * args.ldo + tl.n * BN + c0;
+                const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
+                if (vec && nv == 32) {
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        reinterpret_cast<uint4*>(dst)[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+                } else {
+                    for (int j = 0; j < nv; ++j) dst[j] = __uint_as_float(v[j]);
+                }
+            }
+        }
+    }
 }
 
 template <int EPI>
@@ -228,80 +312,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            const bool row_ok = r < tl.rows_valid;
-            const long long orow = static_cast<long long>(tl.a_row + r);
-            if constexpr (EPI == EPI_SWIGLU) {
-                // packed tile columns: [gate 64 | up 64] x 2 -> 128 expert columns
-                const int rem = args.N - tl.n * BN;
-                const int npk = (rem >= BN ? BN : rem) / 128;
-                __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
-                for (int g2 = half; g2 < npk; g2 += 2) {
-#pragma unroll 1
-                    for (int j0 = 0; j0 < 64; j0 += 32) {
-                        uint32_t gv[32], uv[32];
-                        tmem_ld32(tbase + g2 * 128 + j0, gv);
-                        tmem_ld32(tbase + g2 * 128 + 64 + j0, uv);
-                        tmem_ld_wait();
-                        if (row_ok) {
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const float h0 = silu_f(__uint_as_float(gv[2 * q])) * __uint_as_float(uv[2 * q]);
-                                const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
-                                pk[q] = pack_bf16x2(h0, h1);
-                            }
-                            uint4* dst = reinterpret_cast<uint4*>(H + orow * args.ldo + tl.n * 128 + g2 * 64 + j0);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                        }
-                    }
-                }
-            } else if constexpr (EPI == EPI_BF16) {
-                const int rem = args.out_cols - tl.n * BN;
-                const int ncols = rem >= BN ? BN : rem;
-                __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(args.out);
-                const int cend = min(ncols, (half + 1) * (BN / 2));
-#pragma unroll 1
-                for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c0, v);
-                    tmem_ld_wait();
-                    if (row_ok) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-                        uint4* dst = reinterpret_cast<uint4*>(Y + orow * args.ldo + tl.n * BN + c0);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-                    }
-                }
-            } else {  // EPI_F32
-                const int rem = args.out_cols - tl.n * BN;
-                const int ncols = rem >= BN ? BN : rem;
-                float* Z = reinterpret_cast<float*>(args.out);
-                const bool vec = (args.ldo & 3) == 0;
-                const int cend = min(ncols, (half + 1) * (BN / 2));
-#pragma unroll 1
-                for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c0, v);
-                    tmem_ld_wait();
-                    if (row_ok) {
-                        float* dst = Z + orow * args.ldo + tl.n * BN + c0;
-                        const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
-                        if (vec && nv == 32) {
-#pragma unroll
-                            for (int w = 0; w < 8; ++w)
-                                reinterpret_cast<uint4*>(dst)[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
-                        } else {
-                            for (int j = 0; j < nv; ++j) dst[j] = __uint_as_float(v[j]);
-                        }
-                    }
-                }
-            }
+            epilogue_tile<EPI>(tbase, tl.a_row, tl.rows_valid, tl.n, r, half, args);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
@@ -313,6 +324,195 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------- CTA pairs
+// The same GEMM on 256 x 256 tiles computed by a pair of CTAs on the two SMs of
+// a TPC with the 2-SM MMA (tcgen05.mma.cta_group::2): each CTA stages its own
+// 128 rows of A and its half (128 rows) of B per k-block (32 KB, 6 stages), the
+// even CTA issues the MMAs, and each CTA's TMEM holds its 128 rows x 256
+// columns of the accumulator (two buffers).  Per SM this halves the operand
+// bytes per FLOP against the single-CTA 128 x 256 tile.
+//   full[s]   (even CTA)  both CTAs' TMA loads complete on it (64 KB expected)
+//   empty[s]  (each CTA)  2-SM commit multicast to both CTAs frees stage s
+//   tfull[a]  (each CTA)  2-SM commit multicast: accumulator a is ready
+//   tempty[a] (even CTA)  16 epilogue warps of the pair release accumulator a
+constexpr int P_STAGES = 6;
+constexpr int P_A_STAGE = 128 * BK * 2;       // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_STAGE = 128 * BK * 2;       // 16 KB: this CTA's half of B
+constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
+constexpr int P_BM = 256;                     // rows per pair tile
+constexpr size_t P_SMEM_BYTES =
+    1024 + static_cast<size_t>(P_STAGES) * P_STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * sizeof(int);
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const Args args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint64_t* full = bars;                   // [P_STAGES]
+    uint64_t* empty = bars + P_STAGES;       // [P_STAGES]
+    uint64_t* tfull = bars + 2 * P_STAGES;   // [NACC]
+    uint64_t* tempty = tfull + NACC;         // [NACC]
+    uint64_t* fin = tempty + NACC;           // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* mt_start = reinterpret_cast<int*>(smem + P_STAGES * P_STAGE_BYTES + BAR_BYTES);
+    int* row_start = mt_start + (args.G + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = args.G;
+    const uint32_t rank = cluster_ctarank();      // 0 = the CTA that issues the MMAs
+    const bool leader = rank == 0;
+
+    for (int i = threadIdx.x; i < 2 * (G + 1); i += THREADS) mt_start[i] = args.plan[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 2 * EPI_WARPS);
+        }
+        mbar_init(smem_u32(fin), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();          // the even CTA's barriers exist before the odd CTA signals them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int total_mtiles = mt_start[G];
+    if (total_mtiles < 0 || total_mtiles > args.max_mtiles) {
+        if (threadIdx.x == 0) set_dev_error(args.err, DEV_ERR_OFFSETS);
+        total_mtiles = 0;
+    }
+    const int total = total_mtiles * args.n_tiles;
+    const int num_kb = args.K / BK;
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(nclusters_x());
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = cid; t < total && ok; t += ncl) {
+                const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N, P_BM);
+                const int a_row = tl.a_row + static_cast<int>(rank) * 128;
+                const int b_row = tl.b_row + static_cast<int>(rank) * 128;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                    const uint32_t fb_local = smem_u32(&full[stage]);
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
+                    const uint32_t fb = map_to_cta(fb_local, 0);
+                    uint8_t* sa = smem + stage * P_STAGE_BYTES;
+                    tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, a_row);
+                    tma_load_2d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, kb * BK, b_row);
+                    ++issued;
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (leader) {   // the loads of both CTAs complete on the even CTA's barriers
+                const int pending = issued < P_STAGES ? issued : P_STAGES;
+                for (int j = 1; j <= pending; ++j) {
+                    int s = stage - j;
+                    uint32_t ph = phase;
+                    if (s < 0) { s += P_STAGES; ph ^= 1u; }
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(smem_u32(&full[s]), ph)) {
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            if (leader) {
+                constexpr uint32_t idesc = idesc_bf16_f32(P_BM, BN);
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                int it = 0;
+                for (int t = cid; t < total && ok; t += ncl, ++it) {
+                    const int acc = it & 1;
+                    const uint32_t use = static_cast<uint32_t>(it >> 1);
+                    if (!mbar_wait(smem_u32(&tempty[acc]), (use & 1u) ^ 1u, abort_flag, args.err)) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                    for (int kb = 0; kb < num_kb; ++kb) {
+                        if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err)) { ok = false; break; }
+                        tc_fence_after();
+                        uint8_t* sa = smem + stage * P_STAGE_BYTES;
+                        const uint64_t adesc = smem_desc_sw128(smem_u32(sa));
+                        const uint64_t bdesc = smem_desc_sw128(smem_u32(sa + P_A_STAGE));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
+                                             (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
+                        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
+                }
+                tc_commit_pair_multicast(smem_u32(fin), 0x3);
+            }
+            // both CTAs: every MMA writing this CTA's TMEM has completed
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(fin), 0)) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane;
+        int it = 0;
+        for (int t = cid; t < total; t += ncl, ++it) {
+            const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N, P_BM);
+            const int a_row = tl.a_row + static_cast<int>(rank) * 128;
+            // this CTA's rows of the pair tile, clipped to the group (may be none)
+            int rows_valid = row_start[tl.g + 1] - a_row;
+            rows_valid = rows_valid < 0 ? 0 : (rows_valid > 128 ? 128 : rows_valid);
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            epilogue_tile<EPI>(tbase, a_row, rows_valid, tl.n, r, half, args);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(map_to_cta(smem_u32(&tempty[acc]), 0));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();          // neither CTA releases TMEM or exits while the pair still works
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -425,22 +625,38 @@ cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan
     return cudaGetLastError();
 }
 
+// Kernel variant: the single-CTA kernel, or the CTA-pair kernel when the
+// environment sets FS_TC_VARIANT=pair.
+static bool use_pair() {
+    static int mode = -1;
+    if (mode < 0) {
+        const char* e = getenv("FS_TC_VARIANT");
+        mode = (e && std::strcmp(e, "pair") == 0) ? 1 : 0;
+    }
+    return mode == 1;
+}
+
 template <int EPI>
 static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,
                                   const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
                                   cudaStream_t st) {
-    static bool attr_set = false;
+    const bool pair = use_pair();
+    static bool attr_set[2] = {false, false};
     cudaError_t e;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tc::SMEM_BYTES));
+    if (!attr_set[pair]) {
+        if (pair)
+            e = cudaFuncSetAttribute(tc::pair_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(tc::P_SMEM_BYTES));
+        else
+            e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(tc::SMEM_BYTES));
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[pair] = true;
     }
     CUtensorMap ta, tb;
-    e = make_map(&ta, A, a_rows, K, tc::BM);
+    e = make_map(&ta, A, a_rows, K, 128);
     if (e != cudaSuccess) return e;
-    e = make_map(&tb, B, static_cast<long long>(G) * N, K, tc::BN);
+    e = make_map(&tb, B, static_cast<long long>(G) * N, K, pair ? 128 : tc::BN);
     if (e != cudaSuccess) return e;
     tc::Args args;
     args.plan = plan;
@@ -456,10 +672,17 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
-    long long max_tiles = static_cast<long long>(max_mtiles) * args.n_tiles;
-    int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
-    if (grid < 1) grid = 1;
-    tc::grouped_gemm_kernel<EPI><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    const long long max_tiles = static_cast<long long>(max_mtiles) * args.n_tiles;
+    if (pair) {
+        long long clusters = sms / 2;
+        if (max_tiles < clusters) clusters = max_tiles;
+        if (clusters < 1) clusters = 1;
+        tc::pair_gemm_kernel<EPI><<<static_cast<int>(2 * clusters), tc::THREADS, tc::P_SMEM_BYTES, st>>>(ta, tb, args);
+    } else {
+        int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+        if (grid < 1) grid = 1;
+        tc::grouped_gemm_kernel<EPI><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    }
     count_launch();
     return cudaGetLastError();
 }
@@ -479,6 +702,6 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
     }
 }
 
-int tc_block_m() { return tc::BM; }
+int tc_block_m() { return use_pair() ? tc::P_BM : tc::BM; }
 
 }  // namespace fs
