@@ -119,6 +119,15 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def reduce_max(values, world, device="cpu"):
+    """Max over ranks of per-rank timings (the only collective; not on the data path)."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def cuda_events(n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
@@ -194,10 +203,7 @@ def run_ours(args, cfg, rank, world, local):
     if st != 0:
         raise RuntimeError("device error word after timing: %d" % code)
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+    ms, e2e_ms = reduce_max([ms, e2e_ms], world, dev)
 
     if rank != 0:
         return None
