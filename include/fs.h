@@ -126,7 +126,8 @@ fs_status fs_router_topk(const fs_layer_desc* desc, const void* u, const void* w
  *   -> counts [E], offsets [E+1] (exclusive prefix, offsets[E] = T k),
  *      pos [T k] (pos[t k + s] = permuted row of (t, s)),
  *      perm_src [T k] (perm_src[p] = token of permuted row p),
- *      x_perm [T k, d] (x_perm[p] = u[perm_src[p]]).
+ *      x_perm [T k, d] (x_perm[p] = u[perm_src[p]]); x_perm NULL = no row copy
+ *      (for fs_grouped_swiglu_gather, which gathers the rows itself).
  * An index outside [0, E) sets the device error word (reported by
  * fs_get_error) and that pair is dropped. */
 fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u,
@@ -163,6 +164,17 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
 fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets,
                             const void* w13, const void* w3, void* y_perm,
                             void* ws, size_t ws_bytes, void* stream);
+
+/* fs_grouped_swiglu with the Dispatch row copy fused into the first GEMM: row
+ * p of the routed-expert input is read straight from u[perm_src[p]] by the
+ * GEMM's operand loads (TMA tile::gather4 on the tensor cores), so x_perm is
+ * never written or read.  u [T, d], perm_src [T k] (fs_dispatch's output),
+ * offsets [E+1] -> y_perm [T k, d].  Results are bit-identical to
+ * fs_dispatch + fs_grouped_swiglu.  FS_ERR_UNSUPPORTED with the CTA-pair GEMM
+ * variant. */
+fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, const int32_t* perm_src,
+                                   const int32_t* offsets, const void* w13, const void* w3,
+                                   void* y_perm, void* ws, size_t ws_bytes, void* stream);
 
 /* Shared expert(s) (§2.1): S = sum_i MLP_shared_i(u) over all T tokens, as one
  * MLP of width n_shared c_shared.  u [T, d] -> s_out [T, d] in fp32 (S is only

@@ -144,12 +144,12 @@ static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* 
         const int bm = tc_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
         FS_TRY(launch_tc_gemm(EPI_F32, u, d->T, w_r, 1, d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E,
-                              st));
+                              nullptr, 0, st));
     } else {
         const int bm = simt_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
-        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(u), static_cast<const float*>(w_r), 1, d->E,
-                                d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E, st));
+        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(u), d->T, static_cast<const float*>(w_r), 1,
+                                d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E, nullptr, 0, st));
     }
     FS_TRY(launch_topk(z, bias, d->T, d->E, d->k, d->gate, idx, w, st));
     return FS_OK;
@@ -166,25 +166,27 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 
 // Two grouped GEMMs over `rows` rows split into G groups by `offsets`
 // (nullptr = one group): h = SiLU(x W2^T) * (x W1^T), then y = h W3^T, with
-// y stored in the activation type (y_f32 = false) or in fp32.
-static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, int rows, const int32_t* offsets, int G,
-                             int cw, const void* w13, const void* w3, void* y, bool y_f32, int* plan, void* h,
-                             cudaStream_t st) {
+// y stored in the activation type (y_f32 = false) or in fp32.  With gather
+// non-null, GEMM row p reads row gather[p] of x (x has x_rows rows): the
+// Dispatch permutation applied inside the first GEMM's operand loads.
+static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_rows, const int32_t* gather, int rows,
+                             const int32_t* offsets, int G, int cw, const void* w13, const void* w3, void* y,
+                             bool y_f32, int* plan, void* h, cudaStream_t st) {
     if (d->dtype == FS_BF16) {
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
-        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, st));
+        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, gather, rows, st));
         FS_TRY(launch_tc_gemm(y_f32 ? EPI_F32 : EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d,
-                              st));
+                              nullptr, 0, st));
     } else {
         const int bm = simt_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
-        FS_TRY(launch_simt_gemm(EPI_SWIGLU, static_cast<const float*>(x), static_cast<const float*>(w13), G, 2 * cw,
-                                d->d, plan, max_mt, static_cast<float*>(h), cw, cw, st));
-        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(h), static_cast<const float*>(w3), G, d->d, cw,
-                                plan, max_mt, static_cast<float*>(y), d->d, d->d, st));
+        FS_TRY(launch_simt_gemm(EPI_SWIGLU, static_cast<const float*>(x), x_rows, static_cast<const float*>(w13), G,
+                                2 * cw, d->d, plan, max_mt, static_cast<float*>(h), cw, cw, gather, rows, st));
+        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(h), rows, static_cast<const float*>(w3), G, d->d,
+                                cw, plan, max_mt, static_cast<float*>(y), d->d, d->d, nullptr, 0, st));
     }
     return FS_OK;
 }
@@ -192,14 +194,23 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, int rows, co
 static fs_status routed_impl(const fs_layer_desc* d, const void* x_perm, const int32_t* offsets, const void* w13,
                              const void* w3, void* y_perm, void* ws, cudaStream_t st) {
     const Layout l = layout(d, 0);
-    return swiglu_impl(d, x_perm, d->T * d->k, offsets, d->E, d->c, w13, w3, y_perm, false, at<int>(ws, l.plan_r),
-                       at<void>(ws, l.h_r), st);
+    const int rows = d->T * d->k;
+    return swiglu_impl(d, x_perm, rows, nullptr, rows, offsets, d->E, d->c, w13, w3, y_perm, false,
+                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), st);
+}
+
+static fs_status routed_gather_impl(const fs_layer_desc* d, const void* u, const int32_t* perm_src,
+                                    const int32_t* offsets, const void* w13, const void* w3, void* y_perm, void* ws,
+                                    cudaStream_t st) {
+    const Layout l = layout(d, 0);
+    return swiglu_impl(d, u, d->T, perm_src, d->T * d->k, offsets, d->E, d->c, w13, w3, y_perm, false,
+                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), st);
 }
 
 static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* w13s, const void* w3s, void* s_out,
                              void* ws, cudaStream_t st) {
     const Layout l = layout(d, 0);
-    return swiglu_impl(d, u, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
+    return swiglu_impl(d, u, d->T, nullptr, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
                        at<int>(ws, l.plan_s), at<void>(ws, l.h_s), st);
 }
 
@@ -279,7 +290,7 @@ fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const 
     FS_CHECK(need(offsets));
     FS_CHECK(need(pos));
     FS_CHECK(need(perm_src));
-    FS_CHECK(need(x_perm));
+    if (x_perm && !aligned16(x_perm)) return FS_ERR_UNSUPPORTED;
     FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
     return dispatch_impl(desc, topk_idx, u, counts, offsets, pos, perm_src, x_perm, ws,
                          static_cast<cudaStream_t>(stream));
@@ -316,6 +327,21 @@ fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const
     FS_CHECK(need(y_perm));
     FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
     return routed_impl(desc, x_perm, offsets, w13, w3, y_perm, ws, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, const int32_t* perm_src,
+                                   const int32_t* offsets, const void* w13, const void* w3, void* y_perm, void* ws,
+                                   size_t ws_bytes, void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(u));
+    FS_CHECK(need(perm_src));
+    FS_CHECK(need(offsets));
+    FS_CHECK(need(w13));
+    FS_CHECK(need(w3));
+    FS_CHECK(need(y_perm));
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    if (desc->dtype == FS_BF16 && !tc_gather_supported()) return FS_ERR_UNSUPPORTED;
+    return routed_gather_impl(desc, u, perm_src, offsets, w13, w3, y_perm, ws, static_cast<cudaStream_t>(stream));
 }
 
 fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void* w13_shared, const void* w3_shared,
@@ -380,6 +406,9 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
     void* y_perm = at<void>(ws, l.y_perm);
     void* s_out = desc->n_shared > 0 ? at<void>(ws, l.s_out) : nullptr;
 
+    // Row gathering inside the gate/up GEMM (tile::gather4 moves 512 B per TMA op)
+    // is issue-bound on the tensor-core path; the separate copy runs near HBM peak.
+    const bool gather = false;
     const void* u = x;        // u_k   (= o_{k-1}* in the page's notation), activation type
     const void* o_prev = x;   // o_{k-1}: the caller's x for k = 1, then the fp32 residual stream
     int prev_dtype = desc->dtype;
@@ -391,8 +420,13 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
         void* u_next = last ? nullptr : at<void>(ws, l.ubuf[(b - 1) % l.nu]);
         const int out_dtype = last ? desc->dtype : FS_F32;
         FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
-        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
-        FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
+        if (gather) {   // the permuted copy happens inside the gate/up GEMM's operand loads
+            FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, nullptr, ws, st));
+            FS_CHECK(routed_gather_impl(desc, u, perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
+        } else {
+            FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
+            FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
+        }
         if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st));
         FS_CHECK(combine_impl(desc, y_perm, pos, w, o_prev, prev_dtype, s_out, os_k, o_k, out_dtype, u_next, wiring,
                               st));

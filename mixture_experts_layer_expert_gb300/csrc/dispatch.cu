@@ -212,6 +212,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d
     count_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (!x_perm) return cudaSuccess;     // the caller gathers rows itself (no permuted copy)
     const int row_vecs = d * elem_bytes / 16;
     dispatch_copy_kernel<<<(T + kCopyWarps - 1) / kCopyWarps, kCopyWarps * 32, 0, st>>>(
         reinterpret_cast<const uint4*>(u), T, row_vecs, k, pos, reinterpret_cast<uint4*>(x_perm));

@@ -24,6 +24,9 @@ struct Args {
     long long ldo;
     int out_cols;
     int* err;
+    const int* gather_rows;   // A row of GEMM row p = gather_rows[p], or nullptr
+    int gather_limit;
+    long long a_rows;         // rows of A (bound of a gathered row)
 };
 
 template <int EPI>
@@ -67,8 +70,17 @@ simt_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B, const
         {   // A: 64 rows x 16 -> one float4 per thread
             const int r = tid >> 2, kq = (tid & 3) * 4;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (a_row + r < row_end)
-                v = *reinterpret_cast<const float4*>(A + static_cast<long long>(a_row + r) * args.K + k0 + kq);
+            if (a_row + r < row_end) {
+                long long src = a_row + r;
+                if (args.gather_rows) {
+                    src = a_row + r < args.gather_limit ? args.gather_rows[a_row + r] : 0;
+                    if (src < 0 || src >= args.a_rows) {      // corrupt permutation: record, read nothing
+                        set_dev_error(args.err, DEV_ERR_OFFSETS);
+                        src = -1;
+                    }
+                }
+                if (src >= 0) v = *reinterpret_cast<const float4*>(A + src * args.K + k0 + kq);
+            }
             As[kq + 0][r] = v.x; As[kq + 1][r] = v.y; As[kq + 2][r] = v.z; As[kq + 3][r] = v.w;
         }
         for (int i = tid; i < BNT * 4; i += THREADS) {   // B: BNT rows x 16
@@ -124,8 +136,9 @@ simt_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B, const
 
 int simt_block_m() { return simt::BM; }
 
-cudaError_t launch_simt_gemm(int epi, const float* A, const float* B, int G, int N, int K, const int* plan,
-                             int max_mtiles, float* out, long long ldo, int out_cols, cudaStream_t st) {
+cudaError_t launch_simt_gemm(int epi, const float* A, long long a_rows, const float* B, int G, int N, int K,
+                             const int* plan, int max_mtiles, float* out, long long ldo, int out_cols,
+                             const int* gather_rows, int gather_limit, cudaStream_t st) {
     simt::Args args;
     args.plan = plan;
     args.G = G;
@@ -137,6 +150,9 @@ cudaError_t launch_simt_gemm(int epi, const float* A, const float* B, int G, int
     args.ldo = ldo;
     args.out_cols = out_cols;
     args.err = dev_error_ptr();
+    args.gather_rows = gather_rows;
+    args.gather_limit = gather_limit;
+    args.a_rows = a_rows;
     long long grid = static_cast<long long>(max_mtiles) * args.n_tiles;
     if (grid < 1) grid = 1;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -59,6 +59,8 @@ struct Args {
     long long ldo;     // output row stride in elements
     int out_cols;      // valid output columns (EPI_F32 / EPI_BF16), c for EPI_SWIGLU
     int* err;          // device error word
+    const int* gather_rows;  // A row of GEMM row p = gather_rows[p] (tile::gather4), or nullptr
+    int gather_limit;        // entries of gather_rows
 };
 
 struct Tile {
@@ -223,7 +225,54 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int total = total_mtiles * args.n_tiles;
     const int num_kb = args.K / BK;
 
-    if (warp == 0) {
+    if (warp == 0 && args.gather_rows != nullptr) {
+        // ----------------------------------------------- producer, gathered A
+        // The whole warp: lane l fetches rows 4l .. 4l+3 of each A tile with one
+        // tile::gather4 per k-block (rows of the token matrix named by
+        // gather_rows, i.e. the Dispatch permutation), lane 0 arms the stage and
+        // loads B.
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N);
+            int rr[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int p = tl.a_row + 4 * lane + j;
+                rr[j] = p < args.gather_limit ? __ldg(args.gather_rows + p) : 0;
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const bool got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                const uint32_t fb = smem_u32(&full[stage]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                uint8_t* sa = smem + stage * STAGE_BYTES;
+                tma_gather4(smem_u32(sa) + 512u * lane, &tmA, fb, kb * BK, rr[0], rr[1], rr[2], rr[3]);
+                if (lane == 0) tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (lane == 0) {   // drain: the last loads must land before the CTA exits
+            const int pending = issued < STAGES ? issued : STAGES;
+            for (int j = 1; j <= pending; ++j) {
+                int s = stage - j;
+                uint32_t ph = phase;
+                if (s < 0) { s += STAGES; ph ^= 1u; }
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(&full[s]), ph)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
@@ -639,8 +688,9 @@ static bool use_pair() {
 template <int EPI>
 static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,
                                   const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                                  cudaStream_t st) {
+                                  const int* gather_rows, int gather_limit, cudaStream_t st) {
     const bool pair = use_pair();
+    if (pair && gather_rows) return cudaErrorNotSupported;
     static bool attr_set[2] = {false, false};
     cudaError_t e;
     if (!attr_set[pair]) {
@@ -654,7 +704,7 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
         attr_set[pair] = true;
     }
     CUtensorMap ta, tb;
-    e = make_map(&ta, A, a_rows, K, 128);
+    e = make_map(&ta, A, a_rows, K, gather_rows ? 1 : 128);
     if (e != cudaSuccess) return e;
     e = make_map(&tb, B, static_cast<long long>(G) * N, K, pair ? 128 : tc::BN);
     if (e != cudaSuccess) return e;
@@ -669,6 +719,8 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.ldo = ldo;
     args.out_cols = out_cols;
     args.err = dev_error_ptr();
+    args.gather_rows = gather_rows;
+    args.gather_limit = gather_limit;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -687,16 +739,21 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     return cudaGetLastError();
 }
 
+bool tc_gather_supported() { return !use_pair(); }
+
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                           cudaStream_t st) {
+                           const int* gather_rows, int gather_limit, cudaStream_t st) {
     switch (epi) {
         case EPI_SWIGLU:
-            return launch_tc_impl<EPI_SWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols, st);
+            return launch_tc_impl<EPI_SWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
+                                              gather_rows, gather_limit, st);
         case EPI_BF16:
-            return launch_tc_impl<EPI_BF16>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols, st);
+            return launch_tc_impl<EPI_BF16>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
+                                            gather_rows, gather_limit, st);
         case EPI_F32:
-            return launch_tc_impl<EPI_F32>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols, st);
+            return launch_tc_impl<EPI_F32>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
+                                           gather_rows, gather_limit, st);
         default:
             return cudaErrorInvalidValue;
     }

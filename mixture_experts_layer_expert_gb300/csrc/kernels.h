@@ -18,14 +18,17 @@ int* dev_error_ptr();
 // gemm_tc.cu (bf16 operands, tcgen05)
 int tc_block_m();
 cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st);
+// gather_rows (nullable): GEMM row p reads row gather_rows[p] of A (p < gather_limit)
+bool tc_gather_supported();
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                           cudaStream_t st);
+                           const int* gather_rows, int gather_limit, cudaStream_t st);
 
 // gemm_simt.cu (fp32 operands, fp32 FMA)
 int simt_block_m();
-cudaError_t launch_simt_gemm(int epi, const float* A, const float* B, int G, int N, int K, const int* plan,
-                             int max_mtiles, float* out, long long ldo, int out_cols, cudaStream_t st);
+cudaError_t launch_simt_gemm(int epi, const float* A, long long a_rows, const float* B, int G, int N, int K,
+                             const int* plan, int max_mtiles, float* out, long long ldo, int out_cols,
+                             const int* gather_rows, int gather_limit, cudaStream_t st);
 
 // router.cu
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int gate,

@@ -49,6 +49,7 @@ _SIGS = {
     "fs_dispatch": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_dispatch_noalloc": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fs_grouped_swiglu": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_grouped_swiglu_gather": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_shared_expert": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32,
                           _VP]),
@@ -140,6 +141,12 @@ def fs_dispatch_noalloc(desc, topk_idx, u, counts, offsets, pos, perm_src, x_per
 def fs_grouped_swiglu(desc, x_perm, offsets, w13, w3, y_perm, ws, stream=None):
     _check(lib().fs_grouped_swiglu(ctypes.byref(desc), _p(x_perm), _p(offsets), _p(w13), _p(w3), _p(y_perm),
                                    _p(ws), _nbytes(ws), _stream(stream)), "fs_grouped_swiglu")
+
+
+def fs_grouped_swiglu_gather(desc, u, perm_src, offsets, w13, w3, y_perm, ws, stream=None):
+    _check(lib().fs_grouped_swiglu_gather(ctypes.byref(desc), _p(u), _p(perm_src), _p(offsets), _p(w13), _p(w3),
+                                          _p(y_perm), _p(ws), _nbytes(ws), _stream(stream)),
+           "fs_grouped_swiglu_gather")
 
 
 def fs_shared_expert(desc, u, w13_shared, w3_shared, s_out, ws, stream=None):

@@ -163,6 +163,38 @@ def test_grouped_swiglu(fs, dtype, counts, d, c):
     compare(to64(y), ry, dtype, "y_perm")
 
 
+@pytest.mark.parametrize("dtype,T,E,k,d,c,skew", [
+    ("bf16", 300, 8, 2, 256, 128, False), ("bf16", 1000, 64, 6, 128, 192, True), ("bf16", 1, 8, 2, 64, 64, False),
+    ("bf16", 4097, 16, 4, 192, 128, False), ("f32", 257, 8, 2, 128, 128, False),
+])
+def test_grouped_swiglu_gather(fs, dtype, T, E, k, d, c, skew):
+    """Routed experts reading their rows straight from u through the Dispatch
+    permutation: equal to the oracle on u[perm_src], and bit-identical to the
+    copy-then-GEMM path."""
+    cfg = small(dtype, T=T, E=E, k=k, d=d, c=c)
+    idx = _rand_topk(T, E, k, seed=T + 7, skew=skew)
+    counts, offs, pos, perm = oracle.dispatch(T, k, E, idx.numpy())
+    u = synth.make_x(cfg, DEV)
+    w = synth.make_block_weights(cfg, 0, DEV)
+    packed = fs.pack_block(cfg, w)
+    desc = fs.make_desc(cfg)
+    ws = fs.alloc_workspace(desc, 0)
+    y = torch.full((T * k, d), float("nan"), dtype=u.dtype, device=DEV)
+    perm_t = torch.from_numpy(perm).to(DEV)
+    offs_t = torch.from_numpy(offs).to(DEV)
+    fs.fs_grouped_swiglu_gather(desc, u, perm_t, offs_t, packed["w13"], packed["w3"], y, ws)
+    _no_dev_error()
+    x_perm = u[perm_t.long()].contiguous()
+    y2 = torch.empty_like(y)
+    fs.fs_grouped_swiglu(desc, x_perm, offs_t, packed["w13"], packed["w3"], y2, ws)
+    _no_dev_error()
+    assert torch.equal(y, y2)
+    expert = np.repeat(np.arange(E, dtype=np.int32), counts)
+    _, ry = oracle.expert_rows(oracle_cfg(cfg), synth.to_numpy(u)[perm], expert, synth.to_numpy(w["w1"]),
+                               synth.to_numpy(w["w2"]), synth.to_numpy(w["w3"]))
+    compare(to64(y), ry, dtype, "y_perm (gathered)")
+
+
 @pytest.mark.parametrize("dtype,ns,cs,T", [("bf16", 1, 128, 300), ("bf16", 2, 192, 129), ("f32", 1, 256, 100)])
 def test_shared_expert(fs, dtype, ns, cs, T):
     cfg = small(dtype, T=T, n_shared=ns, c_shared=cs, d=256)
