@@ -172,8 +172,9 @@ def run_ours(args, cfg, rank, world, local):
             torch.distributed.barrier()
 
     # ------------------------------------------------ timed region 1: the stack
+    fwd = stack.forward_overlap if args.overlap else stack.forward
     for _ in range(args.warmup):
-        stack.forward(x)
+        fwd(x)
     torch.cuda.synchronize()
     st, code = fs.fs_get_error()
     if st != 0:
@@ -186,7 +187,7 @@ def run_ours(args, cfg, rank, world, local):
     e0, e1 = cuda_events(2)
     e0.record(stream)
     for _ in range(args.steps):
-        stack.forward(x)
+        fwd(x)
     e1.record(stream)
     torch.cuda.synchronize()
     launches = (fs.fs_launch_count() - l0) // args.steps
@@ -232,7 +233,8 @@ def run_ours(args, cfg, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), uniform router",
-        "config": {"workload": configs.describe(cfg), "T_per_gpu": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+        "config": {"workload": configs.describe(cfg), "schedule": "two-stream overlap" if args.overlap else "one stream",
+                   "T_per_gpu": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
                    "c": cfg.c, "n_shared": cfg.n_shared, "c_shared": cfg.c_shared, "L": L, "gate": cfg.gate,
                    "wiring": cfg.wiring,
                    "l2": "inputs larger than L2 (x %.2f GB, weights %.1f GB per block)" % (
@@ -395,6 +397,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
+    ap.add_argument("--overlap", action="store_true",
+                    help="two-stream FarSkip schedule (router/dispatch/shared of block k+1 beside block k's routed GEMMs)")
     args = ap.parse_args()
     rank, world, local = dist_env()
     cfg = configs.CONFIGS[args.config]

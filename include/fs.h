@@ -214,6 +214,25 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
                            void* o_full, void* o_partial, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* fs_farskip_stack on two streams, the single-GPU form of the overlap the
+ * FarSkip wiring enables (§3, §4): with the partial (or outdated) wiring the
+ * input of block k+1 is u_{k+1} = o_{k-1} + S_k (or o_{k-1}), which does not
+ * depend on block k's routed experts.  So `stream2` runs, for every block, the
+ * router, dispatch and shared expert and forms o_k* = o_{k-1} + S_k and
+ * u_{k+1}, while `stream` runs the routed experts and the final
+ * o_k = o_k* + R_k; block k+1's router/dispatch/shared thus run concurrently
+ * with block k's routed grouped GEMMs.  Bit-identical to fs_farskip_stack.
+ * wiring must be FS_WIRE_PARTIAL or FS_WIRE_OUTDATED; stream2 != stream.
+ * Work queued on `stream` before the call is complete before stream2 starts,
+ * and work queued on `stream` after the call sees all of the stack's results.
+ * Needs ws of fs_workspace_bytes_overlap(desc, L) bytes.  The library keeps
+ * three CUDA events per device for the hand-over (created on first use). */
+fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t wiring,
+                                   const fs_block_weights* blocks, const void* x,
+                                   void* o_full, void* o_partial, void* ws, size_t ws_bytes,
+                                   void* stream, void* stream2);
+size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L);
+
 /* Read and clear the device error word (synchronises the device).  FS_OK when
  * no kernel recorded a fault; FS_ERR_DEVICE_STATE otherwise, with the raw code
  * in *code when code != NULL (1 = expert index out of range, 2 = inconsistent

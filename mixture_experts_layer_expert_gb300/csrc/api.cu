@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/fs.h"
 #include "common.cuh"
@@ -34,6 +35,29 @@ int* dev_error_ptr() {
         g_err_ptr[dev] = static_cast<int*>(p);
     }
     return g_err_ptr[dev];
+}
+
+// Three events per device for the two-stream stack, created on first use and
+// reused (cudaStreamWaitEvent waits for the most recent record).
+static cudaEvent_t g_events[64][3];
+static bool g_events_ready[64] = {false};
+static std::mutex g_events_mu;
+
+static cudaError_t stack_events(cudaEvent_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_events_mu);
+    if (!g_events_ready[dev]) {
+        for (int i = 0; i < 3; ++i) {
+            e = cudaEventCreateWithFlags(&g_events[dev][i], cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        g_events_ready[dev] = true;
+    }
+    *out = g_events[dev];
+    return cudaSuccess;
 }
 
 static fs_status cuda_status(cudaError_t e) {
@@ -115,6 +139,43 @@ static Layout layout(const fs_layer_desc* d, int L) {
     for (int i = 0; i < 3; ++i) l.ring[i] = i < nring ? take(T * dm * 4) : 0;
     for (int i = 0; i < 2; ++i) l.star[i] = i < nstar ? take(T * dm * 4) : 0;
     for (int i = 0; i < 2; ++i) l.ubuf[i] = i < nstar ? take(T * dm * es) : 0;
+    l.end = o;
+    return l;
+}
+
+// Workspace of the two-stream stack: the single-step regions, then two slots
+// (blocks alternate) of every per-block buffer the two streams hand over.
+struct OverlapLayout {
+    size_t end0;
+    size_t idx[2], w[2], counts[2], offsets[2], pos[2], perm[2], x_perm[2], s_out[2], ostar[2], oring[2], ubuf[2];
+    size_t y_perm, end;
+};
+
+static OverlapLayout layout_overlap(const fs_layer_desc* d, int L) {
+    const size_t A = 256;
+    const size_t es = elem_bytes(d);
+    const size_t T = d->T, E = d->E, k = d->k, dm = d->d;
+    const size_t rows = T * k;
+    OverlapLayout l;
+    size_t o = layout(d, 0).end0;
+    l.end0 = o;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, A); return at; };
+    const int slots = L < 2 ? 1 : 2;
+    for (int i = 0; i < 2; ++i) {
+        const bool on = i < slots;
+        l.idx[i] = on ? take(rows * 4) : 0;
+        l.w[i] = on ? take(rows * 4) : 0;
+        l.counts[i] = on ? take(E * 4) : 0;
+        l.offsets[i] = on ? take((E + 1) * 4) : 0;
+        l.pos[i] = on ? take(rows * 4) : 0;
+        l.perm[i] = on ? take(rows * 4) : 0;
+        l.x_perm[i] = on ? take(rows * dm * es) : 0;
+        l.s_out[i] = on ? take(T * dm * 4) : 0;
+        l.ostar[i] = on ? take(T * dm * 4) : 0;
+        l.oring[i] = on ? take(T * dm * 4) : 0;
+        l.ubuf[i] = on ? take(T * dm * es) : 0;
+    }
+    l.y_perm = take(rows * dm * es);
     l.end = o;
     return l;
 }
@@ -243,6 +304,11 @@ size_t fs_workspace_bytes(const fs_layer_desc* desc, int L) {
     if (check_desc(desc) != FS_OK || L < 0) return 0;
     const Layout l = layout(desc, L);
     return L >= 1 ? l.end : l.end0;
+}
+
+size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L) {
+    if (check_desc(desc) != FS_OK || L < 1) return 0;
+    return layout_overlap(desc, L).end;
 }
 
 fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype, const void* w1, const void* w2, void* w13,
@@ -434,6 +500,86 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
         o_prev = o_k;
         prev_dtype = out_dtype;
     }
+    return FS_OK;
+}
+
+fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t wiring,
+                                   const fs_block_weights* blocks, const void* x, void* o_full, void* o_partial,
+                                   void* ws, size_t ws_bytes, void* stream, void* stream2) {
+    FS_CHECK(check_desc(desc));
+    if (L < 1 || !blocks) return FS_ERR_INVALID_ARG;
+    if (wiring != FS_WIRE_PARTIAL && wiring != FS_WIRE_OUTDATED) return FS_ERR_INVALID_ARG;
+    if (!stream2 || stream2 == stream) return FS_ERR_INVALID_ARG;
+    FS_CHECK(need(x));
+    FS_CHECK(need(o_full));
+    if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
+    for (int b = 0; b < L; ++b) {
+        FS_CHECK(need(blocks[b].w_r));
+        FS_CHECK(need(blocks[b].w13));
+        FS_CHECK(need(blocks[b].w3));
+        if (blocks[b].bias && !aligned16(blocks[b].bias)) return FS_ERR_UNSUPPORTED;
+        if (desc->n_shared > 0) {
+            FS_CHECK(need(blocks[b].w13_shared));
+            FS_CHECK(need(blocks[b].w3_shared));
+        }
+    }
+    if (!ws) return FS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return FS_ERR_WORKSPACE;
+    const OverlapLayout l = layout_overlap(desc, L);
+    if (ws_bytes < l.end) return FS_ERR_WORKSPACE;
+    cudaEvent_t* ev = nullptr;
+    FS_TRY(stack_events(&ev));
+    cudaEvent_t evD = ev[0], evU = ev[1], evA = ev[2];
+    cudaStream_t sa = static_cast<cudaStream_t>(stream);     // routed experts + combine
+    cudaStream_t sb = static_cast<cudaStream_t>(stream2);    // router, dispatch, shared expert, o_k*
+    const int act = desc->dtype;
+    void* y_perm = at<void>(ws, l.y_perm);
+
+    // fork: stream2 starts after everything already queued on stream (x ready)
+    FS_TRY(cudaEventRecord(evA, sa));
+    FS_TRY(cudaStreamWaitEvent(sb, evA, 0));
+    const void* u = x;          // u_k, activation type
+    const void* o_prev = x;     // o_{k-1}
+    int prev_dtype = act;
+    for (int b = 1; b <= L; ++b) {
+        const fs_block_weights& bw = blocks[b - 1];
+        const int sl = (b - 1) & 1;
+        const bool last = (b == L);
+        int32_t* idx = at<int32_t>(ws, l.idx[sl]);
+        float* w = at<float>(ws, l.w[sl]);
+        int32_t* counts = at<int32_t>(ws, l.counts[sl]);
+        int32_t* offsets = at<int32_t>(ws, l.offsets[sl]);
+        int32_t* pos = at<int32_t>(ws, l.pos[sl]);
+        int32_t* perm = at<int32_t>(ws, l.perm[sl]);
+        void* x_perm = at<void>(ws, l.x_perm[sl]);
+        float* s_out = desc->n_shared > 0 ? at<float>(ws, l.s_out[sl]) : nullptr;
+        float* ostar = at<float>(ws, l.ostar[sl]);
+        void* o_k = last ? o_full : at<void>(ws, l.oring[sl]);
+        void* u_next = last ? nullptr : at<void>(ws, l.ubuf[sl]);
+        // ---- stream2: everything of block b that does not need the routed experts
+        FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, sb));
+        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, sb));
+        FS_TRY(cudaEventRecord(evD, sb));
+        if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, sb));
+        if (b > 1) FS_TRY(cudaStreamWaitEvent(sb, evA, 0));       // o_{b-1} from block b-1's combine
+        // o_b* = o_{b-1} + S_b (fp32) and the next input (partial: o_b*, outdated: o_{b-1})
+        FS_TRY(launch_combine(nullptr, nullptr, nullptr, o_prev, prev_dtype == FS_BF16, s_out, nullptr, ostar, 0,
+                              u_next, wiring, desc->T, desc->d, 0, act == FS_BF16, sb));
+        FS_TRY(cudaEventRecord(evU, sb));
+        // ---- stream: the routed experts, then o_b = o_b* + R_b
+        FS_TRY(cudaStreamWaitEvent(sa, evD, 0));
+        FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, sa));
+        FS_TRY(cudaStreamWaitEvent(sa, evU, 0));
+        FS_CHECK(combine_impl(desc, y_perm, pos, w, ostar, FS_F32, nullptr, last ? o_partial : nullptr, o_k,
+                              last ? act : FS_F32, nullptr, wiring, sa));
+        FS_TRY(cudaEventRecord(evA, sa));
+        u = u_next;
+        o_prev = o_k;
+        prev_dtype = FS_F32;
+    }
+    // join: stream waits for stream2's last work
+    FS_TRY(cudaEventRecord(evU, sb));
+    FS_TRY(cudaStreamWaitEvent(sa, evU, 0));
     return FS_OK;
 }
 

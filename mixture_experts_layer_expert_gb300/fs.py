@@ -55,6 +55,9 @@ _SIGS = {
                           _VP]),
     "fs_farskip_stack": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP, _VP,
                                 _VP, _VP, _SZ, _VP]),
+    "fs_farskip_stack_overlap": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP,
+                                        _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "fs_workspace_bytes_overlap": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "fs_launch_count": (ctypes.c_uint64, []),
     "fs_last_cuda_error": (ctypes.c_char_p, []),
@@ -182,6 +185,19 @@ def fs_farskip_stack(desc, L, wiring, blocks, x, o_full, o_partial, ws, stream=N
                                   _nbytes(ws), _stream(stream)), "fs_farskip_stack")
 
 
+def fs_workspace_bytes_overlap(desc: LayerDesc, L: int) -> int:
+    return int(lib().fs_workspace_bytes_overlap(ctypes.byref(desc), L))
+
+
+def fs_farskip_stack_overlap(desc, L, wiring, blocks, x, o_full, o_partial, ws, stream=None, stream2=None):
+    """Two-stream stack: `stream2` (a torch.cuda.Stream) runs router/dispatch/shared."""
+    arr = (BlockWeights * L)(*[block_struct(b) for b in blocks])
+    w = WIRINGS[wiring] if isinstance(wiring, str) else int(wiring)
+    _check(lib().fs_farskip_stack_overlap(ctypes.byref(desc), L, w, arr, _p(x), _p(o_full), _p(o_partial), _p(ws),
+                                          _nbytes(ws), _stream(stream), _stream(stream2)),
+           "fs_farskip_stack_overlap")
+
+
 def fs_get_error():
     code = ctypes.c_int32(0)
     st = lib().fs_get_error(ctypes.byref(code))
@@ -237,4 +253,14 @@ class FarSkipStack:
     def forward(self, x: torch.Tensor, stream=None):
         fs_farskip_stack(self.desc, len(self.blocks), self.wiring, self.blocks, x, self.o_full, self.o_partial,
                          self.ws, stream)
+        return self.o_full, self.o_partial
+
+    def forward_overlap(self, x: torch.Tensor, stream=None):
+        """Two-stream FarSkip schedule (partial/outdated wiring)."""
+        if not hasattr(self, "ws_overlap"):
+            n = fs_workspace_bytes_overlap(self.desc, len(self.blocks))
+            self.ws_overlap = torch.empty(n, dtype=torch.uint8, device=self.o_full.device)
+            self.stream2 = torch.cuda.Stream(device=self.o_full.device)
+        fs_farskip_stack_overlap(self.desc, len(self.blocks), self.wiring, self.blocks, x, self.o_full,
+                                 self.o_partial, self.ws_overlap, stream, self.stream2)
         return self.o_full, self.o_partial

@@ -201,3 +201,29 @@ def test_full_size_routing_all_tokens(fs, name):
     z, ridx, _ = oracle.router(oracle_cfg(cfg), synth.to_numpy(x), synth.to_numpy(w["w_r"]), bias)
     zref = z - (0 if bias is None else bias.astype(np.float64)[None, :])
     topk_mismatch(idx.cpu().numpy(), ridx, zref, cfg.k, bias)
+
+
+@pytest.mark.parametrize("wiring,L,dtype", [("partial", 1, "bf16"), ("partial", 3, "bf16"), ("outdated", 3, "bf16"),
+                                           ("partial", 2, "f32"), ("outdated", 4, "bf16")])
+def test_overlap_stack_matches_sequential(fs, wiring, L, dtype):
+    """The two-stream FarSkip schedule gives the same bits as the one-stream stack."""
+    cfg = configs.LayerConfig("ov", T=700, d=256, E=16, k=4, c=192, n_shared=1, c_shared=128, L=L,
+                              gate="sigmoid_norm", dtype=dtype)
+    prob = synth.make_problem(cfg, DEV)
+    stack = fs.FarSkipStack(cfg, prob["blocks"], wiring=wiring)
+    o, o_star = stack.forward(prob["x"])
+    o, o_star = o.clone(), o_star.clone()
+    for _ in range(2):       # twice: the second call reuses the library's events and slots
+        o2, o2_star = stack.forward_overlap(prob["x"])
+        torch.cuda.synchronize()
+        assert fs.fs_get_error() == (0, 0)
+        assert torch.equal(o2, o) and torch.equal(o2_star, o_star)
+
+
+def test_overlap_stack_rejects_disabled_wiring(fs):
+    cfg = configs.LayerConfig("ov", T=64, d=64, E=4, k=1, c=64, n_shared=0, c_shared=0, L=1, gate="sigmoid",
+                              dtype="bf16")
+    prob = synth.make_problem(cfg, DEV)
+    stack = fs.FarSkipStack(cfg, prob["blocks"], wiring="disabled")
+    with pytest.raises(fs.FsError):
+        stack.forward_overlap(prob["x"])
