@@ -36,7 +36,7 @@ _lib = None
 F32, BF16, F64 = 0, 1, 2
 EXACT, STORE_BF16, STORE_F32 = 0, 1, 2
 GATES = {"softmax": 0, "softmax_renorm": 1, "sigmoid": 2, "sigmoid_norm": 3}
-WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2}
+WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2, "attn_farskip": 3, "attn_plain": 4}
 
 
 def build(force: bool = False) -> str:
@@ -60,7 +60,8 @@ class _Cfg(ctypes.Structure):
 class _W(ctypes.Structure):
     _fields_ = [("w_r", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("w1", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w3", ctypes.c_void_p),
-                ("w1s", ctypes.c_void_p), ("w2s", ctypes.c_void_p), ("w3s", ctypes.c_void_p)]
+                ("w1s", ctypes.c_void_p), ("w2s", ctypes.c_void_p), ("w3s", ctypes.c_void_p),
+                ("w_att", ctypes.c_void_p)]
 
 
 def lib():
@@ -140,17 +141,18 @@ def expert_rows(cfg: _Cfg, a: np.ndarray, expert: np.ndarray, w1, w2, w3):
 class Weights:
     """One block's weights in the page's layout (numpy; bf16 as uint16)."""
 
-    def __init__(self, w_r, w1, w2, w3, bias=None, w1s=None, w2s=None, w3s=None):
+    def __init__(self, w_r, w1, w2, w3, bias=None, w1s=None, w2s=None, w3s=None, w_att=None):
         c = np.ascontiguousarray
         self.w_r, self.w1, self.w2, self.w3 = c(w_r), c(w1), c(w2), c(w3)
         self.bias = None if bias is None else c(bias, dtype=np.float32)
         self.w1s = None if w1s is None else c(w1s)
         self.w2s = None if w2s is None else c(w2s)
         self.w3s = None if w3s is None else c(w3s)
+        self.w_att = None if w_att is None else c(w_att)
 
     def struct(self) -> _W:
         return _W(_p(self.w_r), _p(self.bias), _p(self.w1), _p(self.w2), _p(self.w3),
-                  _p(self.w1s), _p(self.w2s), _p(self.w3s))
+                  _p(self.w1s), _p(self.w2s), _p(self.w3s), _p(self.w_att))
 
 
 def stack(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, want_rs: bool = False,
@@ -159,7 +161,8 @@ def stack(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, want_rs: bool = 
 
     Returns a dict with o (= o_L), o_star (= o_L*), topk_idx [L,n,k], topk_w [L,n,k],
     logits [L,n,E], with want_rs R and S [L,n,d], and with want_inputs the
-    block inputs U (u_k) and P (o_{k-1}) and block outputs O (o_k), OS (o_k*) [L,n,d]."""
+    block inputs U (u_k, the MoE input) and P (o_{k-1}), the attention inputs
+    A (attention wirings), and block outputs O (o_k), OS (o_k*) [L,n,d]."""
     x = np.ascontiguousarray(x)
     L = len(weights)
     n = x.shape[0]
@@ -176,13 +179,23 @@ def stack(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, want_rs: bool = 
         "P": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
         "O": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
         "OS": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
+        "A": np.zeros((L, n, cfg.d), np.float64) if want_inputs else None,
     }
     _check(lib().oracle_stack(ctypes.byref(cfg), arr, ctypes.c_int(L), ctypes.c_int(WIRINGS[wiring]),
                               ctypes.c_int(n), _p(x), ctypes.c_int(_dt(x)),
                               _p(out["o"]), _p(out["o_star"]), _p(out["topk_idx"]), _p(out["topk_w"]),
                               _p(out["logits"]), _p(out["R"]), _p(out["S"]), _p(out["U"]), _p(out["P"]),
-                              _p(out["O"]), _p(out["OS"])),
+                              _p(out["O"]), _p(out["OS"]), _p(out["A"])),
            "stack")
+    return out
+
+
+def attn_standin(cfg: _Cfg, a: np.ndarray, w_att: np.ndarray):
+    """Stand-in attention A(a) = a W_att^T (fp64)."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    out = np.zeros_like(a)
+    _check(lib().oracle_attn_standin(ctypes.byref(cfg), ctypes.c_int(a.shape[0]), _p(a),
+                                     _p(np.ascontiguousarray(w_att)), _p(out)), "attn_standin")
     return out
 
 

@@ -199,17 +199,36 @@ int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_d
 
 /* ------------------------------------------------------------------- block */
 
+/* Stand-in attention sub-block: a per-token dense map A(a) = a W_att^T,
+ * W_att [d, d] (one GEMM, keeping token rows independent).  It stands in for
+ * the attention of the attention/MoE wiring of §3; it is not attention. */
+int oracle_attn_standin(const oracle_cfg* cfg, int n_tok, const double* a, const void* w_att, double* out) {
+    const int d = cfg->d;
+    if (!w_att) return -1;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int t = 0; t < n_tok; ++t) {
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j) acc += a[(size_t)t * d + j] * elem(w_att, (size_t)i * d + j, cfg->in_dtype);
+            out[(size_t)t * d + i] = acc;
+        }
+    }
+    return 0;
+}
+
 /* One FarSkip MoE block for n_tok independent token rows.
  *   u      : block input u_k = o_{k-1}*  [n_tok, d] fp64
  *   o_prev : o_{k-1}                     [n_tok, d] fp64
+ *   extra  : a further term added into the residual (the attention output
+ *            of the attention wirings), or NULL
  * Computes, per token (§2.1 MoE and shared expert; §3 FarSkip, eq. 8b):
  *   R    = sum_s w_s * y_{e_s}(u)       (y_e stored, so rounded per storage)
  *   S    = sum_i MLP_shared_i(u)        (rounded once, at residual precision)
- *   o*   = o_prev + S                   (rounded per out_storage)
- *   o    = o_prev + S + R               (rounded per out_storage)
+ *   o*   = o_prev + extra + S           (rounded per out_storage)
+ *   o    = o_prev + extra + S + R       (rounded per out_storage)
  */
 int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
-                 const double* u, const double* o_prev, int out_storage,
+                 const double* u, const double* o_prev, const double* extra, int out_storage,
                  double* o_star, double* o_full,
                  int32_t* topk_idx, double* topk_w, double* logits,
                  double* R_out, double* S_out) {
@@ -253,7 +272,7 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
         }
         for (int i = 0; i < d; ++i) {
             double sv = oracle_round(S[i], resid);
-            double op = o_prev[(size_t)t * d + i];
+            double op = o_prev[(size_t)t * d + i] + (extra ? extra[(size_t)t * d + i] : 0.0);
             o_star[(size_t)t * d + i] = oracle_round(op + sv, out_storage);
             o_full[(size_t)t * d + i] = oracle_round(op + sv + R[i], out_storage);
             if (R_out) R_out[(size_t)t * d + i] = R[i];
@@ -273,24 +292,40 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
  *     ORACLE_WIRE_PARTIAL  : u_{k+1} = o_k*          (eq. 8b, f* = shared expert)
  *     ORACLE_WIRE_OUTDATED : u_{k+1} = o_{k-1}       (eq. 8a)
  *     ORACLE_WIRE_DISABLED : u_{k+1} = o_k           (the plain residual recurrence)
+ * Layers with a stand-in attention sub-block A_k (w_att) before the MoE:
+ *     ORACLE_WIRE_ATTN_FARSKIP (§3, attention/MoE wiring):
+ *         attn-in_k = o_{k-2} + attn-out_{k-1} + shared-out_{k-1}   (partial, 8b)
+ *         mlp-in_k  = attn-in_k + routed-out_{k-1} = o_{k-1}         (outdated, 8a)
+ *         o_k = o_{k-1} + A_k(attn-in_k) + S_k(mlp-in_k) + R_k(mlp-in_k);
+ *         o_k* = o_k - R_k is the next attention input, o_k the next MoE input
+ *     ORACLE_WIRE_ATTN_PLAIN (the ordinary layer): h_k = o_{k-1} + A_k(o_{k-1}),
+ *         o_k = h_k + S_k(h_k) + R_k(h_k), o_k* = h_k + S_k
  * Storage (when not exact): o_k, o_k* are rounded to fp32 (the residual
  * stream) and u_{k+1} to the storage type; the fp32-storage configuration
  * rounds everything to fp32.
  * Outputs o_L and o_L*; per-block routing, R/S, the block inputs u_k (U_all)
  * and o_{k-1} (P_all) and the block outputs o_k (O_all) and o_k* (OS_all) when
- * the pointers are set ([L, n_tok, ...], block-major).
+ * the pointers are set ([L, n_tok, ...], block-major); with the attention
+ * wirings U_all holds the MoE inputs, A_all the attention inputs, and P_all the
+ * residual o_{k-1} entering the layer.  The attention output is carried at
+ * residual precision; its input, like every block input, is rounded to the
+ * storage type.
  * Token rows are independent, so any subset of the rows of x can be passed. */
 int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wiring,
                  int n_tok, const void* x, int x_dtype,
                  double* o_last, double* o_last_star,
                  int32_t* topk_idx_all, double* topk_w_all, double* logits_all,
                  double* R_all, double* S_all, double* U_all, double* P_all,
-                 double* O_all, double* OS_all) {
+                 double* O_all, double* OS_all, double* A_all) {
     const int d = cfg->d, E = cfg->E, k = cfg->k;
     const size_t n = (size_t)n_tok * d;
     if (L < 1 || n_tok < 0) return -1;
+    const int attn = wiring == ORACLE_WIRE_ATTN_FARSKIP || wiring == ORACLE_WIRE_ATTN_PLAIN;
     double* x64 = (double*)malloc(sizeof(double) * (n ? n : 1));
     double* ubuf = (double*)malloc(sizeof(double) * (n ? n : 1));
+    double* abuf = (double*)malloc(sizeof(double) * (n ? n : 1));   /* attention input */
+    double* att = (double*)malloc(sizeof(double) * (n ? n : 1));    /* attention output */
+    double* hbuf = (double*)malloc(sizeof(double) * (n ? n : 1));   /* h_k (plain attention layer) */
     double* ring[3];
     double* star[2];
     for (int i = 0; i < 3; ++i) ring[i] = (double*)malloc(sizeof(double) * (n ? n : 1));
@@ -298,19 +333,44 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
     int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_tok ? n_tok : 1) * k);
     double* w = (double*)malloc(sizeof(double) * (size_t)(n_tok ? n_tok : 1) * k);
     int rc = 0;
-    if (!x64 || !ubuf || !ring[0] || !ring[1] || !ring[2] || !star[0] || !star[1] || !idx || !w) rc = -2;
+    if (!x64 || !ubuf || !abuf || !att || !hbuf || !ring[0] || !ring[1] || !ring[2] || !star[0] || !star[1] ||
+        !idx || !w)
+        rc = -2;
     const int resid = cfg->storage == ORACLE_STORE_BF16 ? ORACLE_STORE_F32 : cfg->storage;
     if (!rc) {
         for (size_t i = 0; i < n; ++i) x64[i] = elem(x, i, x_dtype);
         const double* o_km1 = x64;  /* o_{k-1} */
-        const double* u = x64;      /* u_k */
+        const double* u = x64;      /* u_k (the MoE input) */
+        const double* a_in = x64;   /* attention input (attention wirings) */
         for (int b = 1; b <= L && !rc; ++b) {
             double* o_k = ring[b % 3];
             double* os_k = star[b % 2];
             const oracle_weights* wb = wts + (b - 1);
+            const double* extra = NULL;
+            const double* base = o_km1;
+            if (attn) {
+                if (wiring == ORACLE_WIRE_ATTN_PLAIN) {
+                    if (b > 1) {
+                        for (size_t i = 0; i < n; ++i) abuf[i] = oracle_round(o_km1[i], cfg->storage);
+                        a_in = abuf;
+                    }
+                }
+                rc = oracle_attn_standin(cfg, n_tok, a_in, wb->w_att, att);
+                if (rc) break;
+                for (size_t i = 0; i < n; ++i) att[i] = oracle_round(att[i], resid);
+                if (wiring == ORACLE_WIRE_ATTN_PLAIN) {
+                    for (size_t i = 0; i < n; ++i) hbuf[i] = oracle_round(o_km1[i] + att[i], resid);
+                    for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(hbuf[i], cfg->storage);
+                    u = ubuf;
+                    base = hbuf;
+                } else {
+                    extra = att;
+                }
+                if (A_all) memcpy(A_all + (size_t)(b - 1) * n, a_in, sizeof(double) * n);
+            }
             if (U_all) memcpy(U_all + (size_t)(b - 1) * n, u, sizeof(double) * n);
             if (P_all) memcpy(P_all + (size_t)(b - 1) * n, o_km1, sizeof(double) * n);
-            rc = oracle_block(cfg, wb, n_tok, u, o_km1, resid, os_k, o_k, idx, w,
+            rc = oracle_block(cfg, wb, n_tok, u, base, extra, resid, os_k, o_k, idx, w,
                               logits_all ? logits_all + (size_t)(b - 1) * n_tok * E : NULL,
                               R_all ? R_all + (size_t)(b - 1) * n : NULL,
                               S_all ? S_all + (size_t)(b - 1) * n : NULL);
@@ -322,17 +382,28 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
                 memcpy(o_last, o_k, sizeof(double) * n);
                 memcpy(o_last_star, os_k, sizeof(double) * n);
             }
-            const double* nxt;
-            if (wiring == ORACLE_WIRE_PARTIAL) nxt = os_k;
-            else if (wiring == ORACLE_WIRE_OUTDATED) nxt = o_km1;
-            else nxt = o_k;
-            for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(nxt[i], cfg->storage);
-            u = ubuf;
+            if (wiring == ORACLE_WIRE_ATTN_FARSKIP) {
+                /* next attention input o_k* = o_k - R_k, next MoE input o_k */
+                for (size_t i = 0; i < n; ++i) abuf[i] = oracle_round(os_k[i], cfg->storage);
+                for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(o_k[i], cfg->storage);
+                a_in = abuf;
+                u = ubuf;
+            } else if (wiring != ORACLE_WIRE_ATTN_PLAIN) {
+                const double* nxt;
+                if (wiring == ORACLE_WIRE_PARTIAL) nxt = os_k;
+                else if (wiring == ORACLE_WIRE_OUTDATED) nxt = o_km1;
+                else nxt = o_k;
+                for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(nxt[i], cfg->storage);
+                u = ubuf;
+            }
             o_km1 = o_k;
         }
     }
     free(x64);
     free(ubuf);
+    free(abuf);
+    free(att);
+    free(hbuf);
     for (int i = 0; i < 3; ++i) free(ring[i]);
     for (int i = 0; i < 2; ++i) free(star[i]);
     free(idx);

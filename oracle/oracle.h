@@ -18,7 +18,8 @@ enum { ORACLE_EXACT = 0, ORACLE_STORE_BF16 = 1, ORACLE_STORE_F32 = 2 };
 enum { ORACLE_GATE_SOFTMAX = 0, ORACLE_GATE_SOFTMAX_RENORM = 1,
        ORACLE_GATE_SIGMOID = 2, ORACLE_GATE_SIGMOID_NORM = 3 };
 /* input wiring of block k+1 */
-enum { ORACLE_WIRE_PARTIAL = 0, ORACLE_WIRE_OUTDATED = 1, ORACLE_WIRE_DISABLED = 2 };
+enum { ORACLE_WIRE_PARTIAL = 0, ORACLE_WIRE_OUTDATED = 1, ORACLE_WIRE_DISABLED = 2,
+       ORACLE_WIRE_ATTN_FARSKIP = 3, ORACLE_WIRE_ATTN_PLAIN = 4 };
 
 typedef struct {
     int d, E, k, c;          /* model dim, routed experts, top-k, expert width */
@@ -37,6 +38,7 @@ typedef struct {
     const void* w1s;   /* [n_shared, c_shared, d] */
     const void* w2s;   /* [n_shared, c_shared, d] */
     const void* w3s;   /* [n_shared, d, c_shared] */
+    const void* w_att; /* [d, d] stand-in attention A(a) = a W_att^T (attention wirings), or NULL */
 } oracle_weights;
 
 double oracle_round(double x, int storage);
@@ -47,7 +49,7 @@ int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_d
                        const int32_t* expert, const void* w1, const void* w2, const void* w3,
                        double* h_out, double* y_out);
 int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
-                 const double* u, const double* o_prev, int out_storage,
+                 const double* u, const double* o_prev, const double* extra, int out_storage,
                  double* o_star, double* o_full,
                  int32_t* topk_idx, double* topk_w, double* logits,
                  double* R_out, double* S_out);
@@ -56,7 +58,8 @@ int oracle_stack(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wi
                  double* o_last, double* o_last_star,
                  int32_t* topk_idx_all, double* topk_w_all, double* logits_all,
                  double* R_all, double* S_all, double* U_all, double* P_all,
-                 double* O_all, double* OS_all);
+                 double* O_all, double* OS_all, double* A_all);
+int oracle_attn_standin(const oracle_cfg* cfg, int n_tok, const double* a, const void* w_att, double* out);
 int oracle_dispatch(int T, int k, int E, const int32_t* topk_idx,
                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src);
 int oracle_combine(int T, int k, int d, int in_dtype, int storage,

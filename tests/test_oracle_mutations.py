@@ -36,6 +36,10 @@ MUTANTS = {
     "combine_weight_dropped": ("r += (double)topk_w[(size_t)t * k + s] * elem(y_perm, p * d + i, in_dtype);",
                                "r += elem(y_perm, p * d + i, in_dtype);"),
     "rounding_ties_away": ("double r = nearbyint(x / q) * q;", "double r = round(x / q) * q;"),
+    "attn_mlp_input_misses_routed": ("for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(o_k[i], cfg->storage);\n                a_in = abuf;",
+                                     "for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(os_k[i], cfg->storage);\n                a_in = abuf;"),
+    "attn_output_dropped": ("double op = o_prev[(size_t)t * d + i] + (extra ? extra[(size_t)t * d + i] : 0.0);",
+                            "double op = o_prev[(size_t)t * d + i];"),
     "shared_sum_rounded_per_expert": ("for (int i = 0; i < d; ++i) S[i] += y[i];",
                                       "for (int i = 0; i < d; ++i) S[i] += (sh == 0 ? y[i] : 0.0);"),
 }
@@ -53,6 +57,8 @@ PIN_TESTS = [
     lambda: [pins.test_telescoping_and_wiring(w) for w in ("partial", "outdated", "disabled")],
     pins.test_disabled_is_plain_recurrence_and_L1_agrees,
     lambda: [pins.test_dispatch_combine_round_trip(k, w) for k, w in ((1, 1.0), (2, 0.5), (4, 0.25))],
+    pins.test_attn_farskip_wiring_identities,
+    pins.test_attn_plain_is_the_ordinary_layer,
 ]
 
 

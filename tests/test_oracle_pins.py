@@ -426,3 +426,72 @@ def test_bf16_inputs_widen_exactly():
     z64, i64, w64 = oracle.router(cfg_of(d, E, k, 8), u.double().numpy(), w_r.double().numpy())
     np.testing.assert_array_equal(z16, z64)
     np.testing.assert_array_equal(i16, i64)
+
+
+# ---------------------------------------------- attention/MoE wiring (FarSkip §3)
+
+def _attn_problem(seed, L, zero_att=False, **kw):
+    cfg, ws, x = _stack_problem(seed, L, **kw)
+    r = rng(seed + 100)
+    d = x.shape[1]
+    for w in ws:
+        w["w_att"] = np.zeros((d, d)) if zero_att else r.standard_normal((d, d)) / math.sqrt(d)
+    return cfg, ws, x
+
+
+def test_attn_farskip_wiring_identities():
+    """FarSkip §3 attention/MoE wiring: mlp-in_k = attn-in_k + routed-out_{k-1} (the page's
+    decomposition), attn-in_k = o_{k-2} + attn-out_{k-1} + shared-out_{k-1}, and
+    o_k = o_{k-1} + attn-out_k + shared-out_k + routed-out_k (telescoping)."""
+    L = 4
+    cfg, ws, x = _attn_problem(21, L)
+    out = oracle.stack(cfg, [W(w) for w in ws], "attn_farskip", x, want_rs=True, want_inputs=True)
+    A, U, P, O, R, S = out["A"], out["U"], out["P"], out["O"], out["R"], out["S"]
+    att = [A[b] @ ws[b]["w_att"].T for b in range(L)]                # library matmul
+    np.testing.assert_array_equal(A[0], x)
+    np.testing.assert_array_equal(U[0], x)
+    for b in range(1, L):
+        np.testing.assert_allclose(U[b], A[b] + R[b - 1], rtol=1e-12, atol=1e-12)
+        o_km2 = x if b == 1 else O[b - 2]
+        np.testing.assert_allclose(A[b], o_km2 + att[b - 1] + S[b - 1], rtol=1e-12, atol=1e-12)
+    o = x
+    for b in range(L):
+        np.testing.assert_allclose(P[b], o, rtol=1e-12, atol=1e-12)
+        o = o + att[b] + S[b] + R[b]
+        np.testing.assert_allclose(O[b], o, rtol=1e-11, atol=1e-11)
+    # the MoE sees o_{k-1}: its routing is the router of mlp-in
+    for b in range(L):
+        z = U[b] @ ws[b]["w_r"].T + ws[b]["bias"].astype(np.float64)
+        np.testing.assert_allclose(out["logits"][b], z, rtol=1e-10, atol=1e-10)
+
+
+def test_attn_plain_is_the_ordinary_layer():
+    """h_k = o_{k-1} + A_k(o_{k-1}); o_k = h_k + S_k(h_k) + R_k(h_k)."""
+    L = 3
+    cfg, ws, x = _attn_problem(22, L)
+    out = oracle.stack(cfg, [W(w) for w in ws], "attn_plain", x, want_rs=True, want_inputs=True)
+    o = x
+    for b in range(L):
+        np.testing.assert_allclose(out["A"][b], o, rtol=1e-12, atol=1e-12)
+        h = o + o @ ws[b]["w_att"].T
+        np.testing.assert_allclose(out["U"][b], h, rtol=1e-12, atol=1e-12)
+        o = h + out["S"][b] + out["R"][b]
+        np.testing.assert_allclose(out["O"][b], o, rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(out["OS"][b], h + out["S"][b], rtol=1e-11, atol=1e-11)
+
+
+@pytest.mark.parametrize("wiring", ["attn_farskip", "attn_plain"])
+def test_zero_attention_reduces_to_the_moe_recurrence(wiring):
+    """With A = 0 both attention wirings feed the MoE o_{k-1}: the disabled (plain) MoE stack."""
+    cfg, ws, x = _attn_problem(23, 3, zero_att=True)
+    a = oracle.stack(cfg, [W(w) for w in ws], wiring, x)
+    ref = oracle.stack(cfg, [W({k: v for k, v in w.items() if k != "w_att"}) for w in ws], "disabled", x)
+    np.testing.assert_allclose(a["o"], ref["o"], rtol=1e-13, atol=1e-13)
+
+
+def test_attn_standin_is_a_matmul():
+    r = rng(24)
+    a = r.standard_normal((5, 16))
+    w = r.standard_normal((16, 16))
+    cfg = cfg_of(16, 2, 1, 8)
+    np.testing.assert_allclose(oracle.attn_standin(cfg, a, w), a @ w.T, rtol=1e-13, atol=1e-13)
