@@ -67,7 +67,20 @@ typedef enum {
 
 /* Input of block k+1 (§3, eq. 8a/8b): PARTIAL u = o_k* = o_{k-1} + S_k,
  * OUTDATED u = o_{k-1}, DISABLED u = o_k (plain residual recurrence). */
-typedef enum { FS_WIRE_PARTIAL = 0, FS_WIRE_OUTDATED = 1, FS_WIRE_DISABLED = 2 } fs_wiring;
+typedef enum {
+    FS_WIRE_PARTIAL = 0,
+    FS_WIRE_OUTDATED = 1,
+    FS_WIRE_DISABLED = 2,
+    /* Layers with a stand-in attention sub-block A_k(a) = a W_att^T before the MoE
+     * (fs_block_weights.w_att), wired as in §3's attention/MoE wiring:
+     *   attn-in_k = o_{k-2} + attn-out_{k-1} + shared-out_{k-1}
+     *   mlp-in_k  = attn-in_k + routed-out_{k-1} = o_{k-1}
+     *   o_k = o_{k-1} + A_k(attn-in_k) + S_k(mlp-in_k) + R_k(mlp-in_k), o_k* = o_k - R_k */
+    FS_WIRE_ATTN_FARSKIP = 3,
+    /* the ordinary layer: h_k = o_{k-1} + A_k(o_{k-1}), o_k = h_k + S_k(h_k) + R_k(h_k),
+     * o_k* = h_k + S_k */
+    FS_WIRE_ATTN_PLAIN = 4
+} fs_wiring;
 
 /* One MoE layer: T tokens of width d, E routed experts of width c, top-k,
  * n_shared shared experts of width c_shared (0 = none), activation dtype, gate. */
@@ -86,11 +99,17 @@ typedef struct {
     const void* w3;         /* [E, d, c] down (W3) */
     const void* w13_shared; /* [2 n_shared c_shared, d] packed, NULL when n_shared = 0 */
     const void* w3_shared;  /* [d, n_shared c_shared] (fs_pack_w3_shared) */
+    const void* w_att;      /* [d, d] stand-in attention weight (attention wirings only), or NULL */
 } fs_block_weights;
 
 /* Bytes of workspace needed by the single-step calls (L = 0) or by
- * fs_farskip_stack with L blocks (L >= 1).  Returns 0 for an invalid desc. */
+ * fs_farskip_stack with L blocks (L >= 1) and the MoE wirings (PARTIAL,
+ * OUTDATED, DISABLED).  Returns 0 for an invalid desc. */
 size_t fs_workspace_bytes(const fs_layer_desc* desc, int L);
+
+/* Workspace of fs_farskip_stack with the attention wirings (FS_WIRE_ATTN_*):
+ * fs_workspace_bytes(desc, L) plus the attention buffers.  0 if invalid. */
+size_t fs_workspace_bytes_attn(const fs_layer_desc* desc, int L);
 
 /* Repack the page's W1 (up) and W2 (gate), each [G, c, d], into w13 [G, 2c, d]:
  * for each group of 64 expert columns b, rows [128b, 128b+64) of w13 are W2
@@ -185,26 +204,38 @@ fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void*
 
 /* Combine (§2.1, local form) fused with the FarSkip update (§3, eq. 8a/8b):
  *   R[t]  = sum_{s<k} topk_w[t, s] * y_perm[pos[t k + s]]   (fp32, slot order)
- *   o_partial[t] = o_prev[t] + S[t]                          (o_k*)
- *   o_full[t]    = o_prev[t] + S[t] + R[t]                   (o_k)
+ *   o_partial[t] = o_prev[t] + S[t] + extra[t]               (o_k*)
+ *   o_full[t]    = o_prev[t] + S[t] + extra[t] + R[t]        (o_k)
  *   u_next[t]    = the next block's input per `wiring`: o_k* (PARTIAL),
  *                  o_prev (OUTDATED) or o_k (DISABLED)
- * All sums in fp32, each output rounded once.  y_perm and u_next have the
- * activation type desc->dtype, shared_out is fp32 (fs_shared_expert's output);
- * the residual stream o_prev (prev_dtype)
- * and o_partial / o_full (out_dtype) are FS_BF16 or FS_F32 each, so a stack can
- * carry its residual in fp32.  shared_out NULL = no shared expert (S = 0);
- * o_partial NULL and u_next NULL = not written (wiring is then ignored). */
+ *   u_full[t]    = o_k
+ * All sums in fp32, each output rounded once.  y_perm, u_next and u_full have
+ * the activation type desc->dtype; shared_out (fs_shared_expert's output) and
+ * extra (e.g. fs_attn_standin's output) are fp32; the residual stream o_prev
+ * (prev_dtype) and o_partial / o_full (out_dtype) are FS_BF16 or FS_F32 each,
+ * so a stack can carry its residual in fp32.  shared_out NULL = no shared
+ * expert; extra NULL = no extra term; o_partial, u_next, u_full NULL = not
+ * written (wiring is then ignored). */
 fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_t* pos,
                      const float* topk_w, const void* o_prev, int32_t prev_dtype,
-                     const void* shared_out, void* o_partial, void* o_full, int32_t out_dtype,
-                     void* u_next, int32_t wiring, void* stream);
+                     const void* shared_out, const float* extra, void* o_partial, void* o_full,
+                     int32_t out_dtype, void* u_next, int32_t wiring, void* u_full, void* stream);
+
+/* Stand-in attention sub-block for the attention wirings: out = a W_att^T
+ * (a per-token dense GEMM on the tensor cores for bf16, fp32 FMA for fp32).
+ * It stands in for attention (which mixes tokens) so the §3 attention/MoE
+ * wiring can be run; it is not attention.  a [T, d] (activation type),
+ * w_att [d, d] -> out [T, d] fp32.  Needs ws of fs_workspace_bytes(desc, 0). */
+fs_status fs_attn_standin(const fs_layer_desc* desc, const void* a, const void* w_att, float* out,
+                          void* ws, size_t ws_bytes, void* stream);
 
 /* L FarSkip blocks (§3): o_0 = u_1 = x; block k runs router, dispatch, routed
  * experts, shared expert and combine on u_k and o_{k-1}, producing
  * o_k* = o_{k-1} + S_k and o_k = o_k* + R_k; u_{k+1} follows `wiring`.
  * Between blocks the residual stream o_k, o_k* is kept in fp32 (in ws) and
- * u_{k+1} is its rounding to the activation type (the GEMM operand).
+ * u_{k+1} is its rounding to the activation type (the GEMM operand).  The
+ * attention wirings (FS_WIRE_ATTN_*) run A_k from blocks[k].w_att first and
+ * need fs_workspace_bytes_attn(desc, L) bytes of ws.
  *   blocks [L] (host array of device pointers), x [T, d]
  *   -> o_full = o_L, o_partial = o_L* (NULL = not written), activation type.
  * Needs ws of fs_workspace_bytes(desc, L) bytes.  Everything is enqueued on

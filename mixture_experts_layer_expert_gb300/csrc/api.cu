@@ -96,9 +96,10 @@ static inline int elem_bytes(const fs_layer_desc* d) { return d->dtype == FS_BF1
 // ------------------------------------------------------------- workspace
 struct Layout {
     // single-step regions (L = 0)
-    size_t logits, disp, plan_z, plan_r, h_r, plan_s, h_s, end0;
+    size_t logits, disp, plan_z, plan_r, h_r, plan_s, h_s, plan_a, end0;
     // stack regions (L >= 1)
     size_t topk_idx, topk_w, counts, offsets, pos, perm, x_perm, y_perm, s_out, ring[3], star[2], ubuf[2], end;
+    size_t att, hbuf, abuf[2], end_attn;   // attention wirings only: A_k output, h_k, attention inputs
     int nring, nstar, nu;   // fp32 o_k / o_k* and activation-type u_{k+1} buffers of blocks 1..L-1
 };
 
@@ -118,6 +119,7 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.h_r = take(rows * d->c * es);
     l.plan_s = take(4 * sizeof(int));
     l.h_s = take(T * cw * es);
+    l.plan_a = take(4 * sizeof(int));
     l.end0 = o;
     l.topk_idx = take(rows * 4);
     l.topk_w = take(rows * 4);
@@ -140,6 +142,10 @@ static Layout layout(const fs_layer_desc* d, int L) {
     for (int i = 0; i < 2; ++i) l.star[i] = i < nstar ? take(T * dm * 4) : 0;
     for (int i = 0; i < 2; ++i) l.ubuf[i] = i < nstar ? take(T * dm * es) : 0;
     l.end = o;
+    l.att = take(T * dm * 4);
+    l.hbuf = take(T * dm * 4);
+    for (int i = 0; i < 2; ++i) l.abuf[i] = take(T * dm * es);
+    l.end_attn = o;
     return l;
 }
 
@@ -276,10 +282,31 @@ static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* 
 }
 
 static fs_status combine_impl(const fs_layer_desc* d, const void* y_perm, const int32_t* pos, const float* w,
-                              const void* o_prev, int prev_dtype, const void* s, void* o_partial, void* o_full,
-                              int out_dtype, void* u_next, int wiring, cudaStream_t st) {
-    FS_TRY(launch_combine(y_perm, pos, w, o_prev, prev_dtype == FS_BF16, s, o_partial, o_full, out_dtype == FS_BF16,
-                          u_next, wiring, d->T, d->d, d->k, d->dtype == FS_BF16, st));
+                              const void* o_prev, int prev_dtype, const void* s, const float* extra, void* o_partial,
+                              void* o_full, int out_dtype, void* u_next, int u_src, void* u_full, cudaStream_t st,
+                              int k_override = -1) {
+    FS_TRY(launch_combine(y_perm, pos, w, o_prev, prev_dtype == FS_BF16, s, extra, o_partial, o_full,
+                          out_dtype == FS_BF16, u_next, u_src, u_full, d->T, d->d, k_override >= 0 ? k_override : d->k,
+                          d->dtype == FS_BF16, st));
+    return FS_OK;
+}
+
+// Stand-in attention sub-block: out (fp32) = a W_att^T, a per-token dense GEMM.
+static fs_status attn_impl(const fs_layer_desc* d, const void* a, const void* w_att, float* out, void* ws,
+                           cudaStream_t st) {
+    const Layout l = layout(d, 0);
+    int* plan = at<int>(ws, l.plan_a);
+    if (d->dtype == FS_BF16) {
+        const int bm = tc_block_m();
+        FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
+        FS_TRY(launch_tc_gemm(EPI_F32, a, d->T, w_att, 1, d->d, d->d, plan, ceil_div(d->T, bm) + 1, out, d->d, d->d,
+                              nullptr, 0, st));
+    } else {
+        const int bm = simt_block_m();
+        FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
+        FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(a), d->T, static_cast<const float*>(w_att), 1,
+                                d->d, d->d, plan, ceil_div(d->T, bm) + 1, out, d->d, d->d, nullptr, 0, st));
+    }
     return FS_OK;
 }
 
@@ -304,6 +331,11 @@ size_t fs_workspace_bytes(const fs_layer_desc* desc, int L) {
     if (check_desc(desc) != FS_OK || L < 0) return 0;
     const Layout l = layout(desc, L);
     return L >= 1 ? l.end : l.end0;
+}
+
+size_t fs_workspace_bytes_attn(const fs_layer_desc* desc, int L) {
+    if (check_desc(desc) != FS_OK || L < 1) return 0;
+    return layout(desc, L).end_attn;
 }
 
 size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L) {
@@ -423,8 +455,9 @@ fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void*
 }
 
 fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_t* pos, const float* topk_w,
-                     const void* o_prev, int32_t prev_dtype, const void* shared_out, void* o_partial, void* o_full,
-                     int32_t out_dtype, void* u_next, int32_t wiring, void* stream) {
+                     const void* o_prev, int32_t prev_dtype, const void* shared_out, const float* extra,
+                     void* o_partial, void* o_full, int32_t out_dtype, void* u_next, int32_t wiring, void* u_full,
+                     void* stream) {
     FS_CHECK(check_desc(desc));
     FS_CHECK(need(y_perm));
     FS_CHECK(need(pos));
@@ -437,15 +470,28 @@ fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_
     if (shared_out && !aligned16(shared_out)) return FS_ERR_UNSUPPORTED;
     if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
     if (u_next && !aligned16(u_next)) return FS_ERR_UNSUPPORTED;
-    return combine_impl(desc, y_perm, pos, topk_w, o_prev, prev_dtype, shared_out, o_partial, o_full, out_dtype,
-                        u_next, wiring, static_cast<cudaStream_t>(stream));
+    if (u_full && !aligned16(u_full)) return FS_ERR_UNSUPPORTED;
+    if (extra && !aligned16(extra)) return FS_ERR_UNSUPPORTED;
+    return combine_impl(desc, y_perm, pos, topk_w, o_prev, prev_dtype, shared_out, extra, o_partial, o_full,
+                        out_dtype, u_next, wiring, u_full, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_attn_standin(const fs_layer_desc* desc, const void* a, const void* w_att, float* out, void* ws,
+                          size_t ws_bytes, void* stream) {
+    FS_CHECK(check_desc(desc));
+    FS_CHECK(need(a));
+    FS_CHECK(need(w_att));
+    FS_CHECK(need(out));
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    return attn_impl(desc, a, w_att, out, ws, static_cast<cudaStream_t>(stream));
 }
 
 fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring, const fs_block_weights* blocks,
                            const void* x, void* o_full, void* o_partial, void* ws, size_t ws_bytes, void* stream) {
     FS_CHECK(check_desc(desc));
     if (L < 1 || !blocks) return FS_ERR_INVALID_ARG;
-    if (wiring < FS_WIRE_PARTIAL || wiring > FS_WIRE_DISABLED) return FS_ERR_INVALID_ARG;
+    if (wiring < FS_WIRE_PARTIAL || wiring > FS_WIRE_ATTN_PLAIN) return FS_ERR_INVALID_ARG;
+    const bool attn = wiring == FS_WIRE_ATTN_FARSKIP || wiring == FS_WIRE_ATTN_PLAIN;
     FS_CHECK(need(x));
     FS_CHECK(need(o_full));
     if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
@@ -458,10 +504,12 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
             FS_CHECK(need(blocks[b].w13_shared));
             FS_CHECK(need(blocks[b].w3_shared));
         }
+        if (attn) FS_CHECK(need(blocks[b].w_att));
     }
     FS_CHECK(check_ws(desc, L, ws, ws_bytes));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const Layout l = layout(desc, L);
+    if (attn && ws_bytes < l.end_attn) return FS_ERR_WORKSPACE;
     int32_t* idx = at<int32_t>(ws, l.topk_idx);
     float* w = at<float>(ws, l.topk_w);
     int32_t* counts = at<int32_t>(ws, l.counts);
@@ -477,26 +525,55 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
     const bool gather = false;
     const void* u = x;        // u_k   (= o_{k-1}* in the page's notation), activation type
     const void* o_prev = x;   // o_{k-1}: the caller's x for k = 1, then the fp32 residual stream
+    const void* a_in = x;     // attention input (attention wirings), activation type
     int prev_dtype = desc->dtype;
+    float* att = at<float>(ws, l.att);
     for (int b = 1; b <= L; ++b) {
         const fs_block_weights& bw = blocks[b - 1];
         const bool last = (b == L);
         void* o_k = last ? o_full : at<void>(ws, l.ring[(b - 1) % l.nring]);
         void* os_k = last ? o_partial : at<void>(ws, l.star[(b - 1) % l.nstar]);
         void* u_next = last ? nullptr : at<void>(ws, l.ubuf[(b - 1) % l.nu]);
+        void* a_next = last ? nullptr : at<void>(ws, l.abuf[(b - 1) & 1]);
         const int out_dtype = last ? desc->dtype : FS_F32;
-        FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
-        if (gather) {   // the permuted copy happens inside the gate/up GEMM's operand loads
-            FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, nullptr, ws, st));
-            FS_CHECK(routed_gather_impl(desc, u, perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
-        } else {
-            FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
-            FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
+        const void* base = o_prev;          // residual the MoE outputs are added to
+        int base_dtype = prev_dtype;
+        const float* extra = nullptr;
+        if (attn) {
+            FS_CHECK(attn_impl(desc, a_in, bw.w_att, att, ws, st));
+            if (wiring == FS_WIRE_ATTN_PLAIN) {
+                // h_k = o_{k-1} + A_k(o_{k-1}) (fp32) and the MoE input bf16(h_k)
+                float* h = at<float>(ws, l.hbuf);
+                void* m_in = at<void>(ws, l.abuf[b & 1]);
+                FS_CHECK(combine_impl(desc, nullptr, nullptr, nullptr, o_prev, prev_dtype, nullptr, att, nullptr, h,
+                                      FS_F32, m_in, FS_WIRE_PARTIAL, nullptr, st, 0));
+                u = m_in;
+                base = h;
+                base_dtype = FS_F32;
+            } else {
+                extra = att;                // o_k = o_{k-1} + A_k(attn-in_k) + S_k + R_k
+            }
         }
+        FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
+        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
+        FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
         if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st));
-        FS_CHECK(combine_impl(desc, y_perm, pos, w, o_prev, prev_dtype, s_out, os_k, o_k, out_dtype, u_next, wiring,
-                              st));
-        u = u_next;
+        if (wiring == FS_WIRE_ATTN_FARSKIP) {
+            // next attention input bf16(o_k*) = bf16(o_k - R_k), next MoE input bf16(o_k)
+            FS_CHECK(combine_impl(desc, y_perm, pos, w, base, base_dtype, s_out, extra, os_k, o_k, out_dtype, a_next,
+                                  FS_WIRE_PARTIAL, u_next, st));
+            a_in = a_next;
+            u = u_next;
+        } else if (wiring == FS_WIRE_ATTN_PLAIN) {
+            // o_k = h_k + S_k + R_k; next attention input bf16(o_k)
+            FS_CHECK(combine_impl(desc, y_perm, pos, w, base, base_dtype, s_out, nullptr, os_k, o_k, out_dtype,
+                                  nullptr, FS_WIRE_PARTIAL, a_next, st));
+            a_in = a_next;
+        } else {
+            FS_CHECK(combine_impl(desc, y_perm, pos, w, o_prev, prev_dtype, s_out, nullptr, os_k, o_k, out_dtype,
+                                  u_next, wiring, nullptr, st));
+            u = u_next;
+        }
         o_prev = o_k;
         prev_dtype = out_dtype;
     }
@@ -563,15 +640,15 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
         if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, sb));
         if (b > 1) FS_TRY(cudaStreamWaitEvent(sb, evA, 0));       // o_{b-1} from block b-1's combine
         // o_b* = o_{b-1} + S_b (fp32) and the next input (partial: o_b*, outdated: o_{b-1})
-        FS_TRY(launch_combine(nullptr, nullptr, nullptr, o_prev, prev_dtype == FS_BF16, s_out, nullptr, ostar, 0,
-                              u_next, wiring, desc->T, desc->d, 0, act == FS_BF16, sb));
+        FS_TRY(launch_combine(nullptr, nullptr, nullptr, o_prev, prev_dtype == FS_BF16, s_out, nullptr, nullptr, ostar,
+                              0, u_next, wiring, nullptr, desc->T, desc->d, 0, act == FS_BF16, sb));
         FS_TRY(cudaEventRecord(evU, sb));
         // ---- stream: the routed experts, then o_b = o_b* + R_b
         FS_TRY(cudaStreamWaitEvent(sa, evD, 0));
         FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, sa));
         FS_TRY(cudaStreamWaitEvent(sa, evU, 0));
-        FS_CHECK(combine_impl(desc, y_perm, pos, w, ostar, FS_F32, nullptr, last ? o_partial : nullptr, o_k,
-                              last ? act : FS_F32, nullptr, wiring, sa));
+        FS_CHECK(combine_impl(desc, y_perm, pos, w, ostar, FS_F32, nullptr, nullptr, last ? o_partial : nullptr, o_k,
+                              last ? act : FS_F32, nullptr, wiring, nullptr, sa));
         FS_TRY(cudaEventRecord(evA, sa));
         u = u_next;
         o_prev = o_k;

@@ -10,6 +10,9 @@
 //   o[t]   = o_prev[t] + S[t] + R[t]
 //   u'[t]  = the next block's input, rounded to the activation type:
 //            o*[t] (partial), o_prev[t] (outdated) or o[t] (disabled)
+// An optional fp32 term (the stand-in attention output of the attention
+// wirings) is added into o* and o, and o may also be written rounded to the
+// activation type (the next MoE input of the attention/MoE wiring).
 // The residual stream (o_prev, o*, o) may be fp32 or the activation type; S is
 // fp32; the expert rows and u' are in the activation type.  One warp per token, 8
 // columns per lane step: each lane loads the k expert rows of its columns
@@ -88,8 +91,8 @@ template <bool BF16, int KMAX>   // BF16: activation type of y_perm and u_next
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos, const float* __restrict__ topk_w,
                const void* __restrict__ o_prev, bool prev_bf16, const void* __restrict__ shared_out,
-               void* __restrict__ o_partial, void* __restrict__ o_full, bool out_bf16, void* __restrict__ u_next,
-               int u_src, int T, int d, int k) {
+               const float* __restrict__ extra, void* __restrict__ o_partial, void* __restrict__ o_full, bool out_bf16,
+               void* __restrict__ u_next, int u_src, void* __restrict__ u_full, int T, int d, int k) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -119,6 +122,11 @@ combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos,
 #pragma unroll
             for (int j = 0; j < 8; ++j) base[j] += sv[j];
         }
+        if (extra) {                                    // e.g. the attention output (fp32)
+            load8(extra, row + c8, false, sv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) base[j] += sv[j];
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll
@@ -140,17 +148,20 @@ combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos,
                 store8(u_next, row + c8, BF16, full);
             }
         }
+        if (u_full) store8(u_full, row + c8, BF16, full);
     }
 }
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* topk_w, const void* o_prev,
-                           int prev_bf16, const void* shared_out, void* o_partial, void* o_full, int out_bf16,
-                           void* u_next, int u_src, int T, int d, int k, int is_bf16, cudaStream_t st) {
+                           int prev_bf16, const void* shared_out, const float* extra, void* o_partial, void* o_full,
+                           int out_bf16, void* u_next, int u_src, void* u_full, int T, int d, int k, int is_bf16,
+                           cudaStream_t st) {
     const int grid = (T + kCombineWarps - 1) / kCombineWarps;
     const int threads = kCombineWarps * 32;
 #define FS_COMBINE(BF, KM)                                                                                  \
-    combine_kernel<BF, KM><<<grid, threads, 0, st>>>(y_perm, pos, topk_w, o_prev, prev_bf16 != 0, shared_out, \
-                                                     o_partial, o_full, out_bf16 != 0, u_next, u_src, T, d, k)
+    combine_kernel<BF, KM><<<grid, threads, 0, st>>>(y_perm, pos, topk_w, o_prev, prev_bf16 != 0, shared_out,   \
+                                                     extra, o_partial, o_full, out_bf16 != 0, u_next, u_src, u_full, \
+                                                     T, d, k)
     if (is_bf16) {
         if (k <= 8) FS_COMBINE(true, 8); else FS_COMBINE(true, 16);
     } else {

@@ -46,8 +46,9 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d
 
 // combine.cu
 cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* topk_w, const void* o_prev,
-                           int prev_bf16, const void* shared_out, void* o_partial, void* o_full, int out_bf16,
-                           void* u_next, int u_src, int T, int d, int k, int is_bf16, cudaStream_t st);
+                           int prev_bf16, const void* shared_out, const float* extra, void* o_partial, void* o_full,
+                           int out_bf16, void* u_next, int u_src, void* u_full, int T, int d, int k, int is_bf16,
+                           cudaStream_t st);
 
 // pack.cu
 cudaError_t launch_pack_w13(int G, int c, int d, int elem_bytes, const void* w1, const void* w2, void* w13,

@@ -20,7 +20,7 @@ _lib = None
 
 FS_BF16, FS_F32 = 0, 1
 GATES = {"softmax": 0, "softmax_renorm": 1, "sigmoid": 2, "sigmoid_norm": 3}
-WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2}
+WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2, "attn_farskip": 3, "attn_plain": 4}
 STATUS = {0: "FS_OK", 1: "FS_ERR_INVALID_ARG", 2: "FS_ERR_UNSUPPORTED", 3: "FS_ERR_WORKSPACE",
           4: "FS_ERR_CUDA", 5: "FS_ERR_DEVICE_STATE"}
 
@@ -37,7 +37,8 @@ class LayerDesc(ctypes.Structure):
 
 class BlockWeights(ctypes.Structure):
     _fields_ = [("w_r", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("w13", ctypes.c_void_p),
-                ("w3", ctypes.c_void_p), ("w13_shared", ctypes.c_void_p), ("w3_shared", ctypes.c_void_p)]
+                ("w3", ctypes.c_void_p), ("w13_shared", ctypes.c_void_p), ("w3_shared", ctypes.c_void_p),
+                ("w_att", ctypes.c_void_p)]
 
 
 _VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
@@ -51,13 +52,15 @@ _SIGS = {
     "fs_grouped_swiglu": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_grouped_swiglu_gather": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_shared_expert": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
-    "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _I32, _VP, _I32,
-                          _VP]),
+    "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _I32, _VP, _I32,
+                          _VP, _VP]),
+    "fs_attn_standin": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_farskip_stack": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP, _VP,
                                 _VP, _VP, _SZ, _VP]),
     "fs_farskip_stack_overlap": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP,
                                         _VP, _VP, _VP, _SZ, _VP, _VP]),
     "fs_workspace_bytes_overlap": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
+    "fs_workspace_bytes_attn": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "fs_launch_count": (ctypes.c_uint64, []),
     "fs_last_cuda_error": (ctypes.c_char_p, []),
@@ -162,19 +165,24 @@ def _dtype_code(t):
 
 
 def fs_combine(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full, u_next=None, wiring="partial",
-               stream=None):
+               extra=None, u_full=None, stream=None):
     """Residual dtypes (bf16 or fp32) are taken from the o_prev and o_full tensors."""
     if o_partial is not None:
         assert o_partial.dtype == o_full.dtype
     w = WIRINGS[wiring] if isinstance(wiring, str) else int(wiring)
     _check(lib().fs_combine(ctypes.byref(desc), _p(y_perm), _p(pos), _p(topk_w), _p(o_prev), _dtype_code(o_prev),
-                            _p(shared_out), _p(o_partial), _p(o_full), _dtype_code(o_full), _p(u_next), w,
-                            _stream(stream)), "fs_combine")
+                            _p(shared_out), _p(extra), _p(o_partial), _p(o_full), _dtype_code(o_full), _p(u_next), w,
+                            _p(u_full), _stream(stream)), "fs_combine")
+
+
+def fs_attn_standin(desc, a, w_att, out, ws, stream=None):
+    _check(lib().fs_attn_standin(ctypes.byref(desc), _p(a), _p(w_att), _p(out), _p(ws), _nbytes(ws),
+                                 _stream(stream)), "fs_attn_standin")
 
 
 def block_struct(packed: dict) -> BlockWeights:
     return BlockWeights(_p(packed["w_r"]), _p(packed.get("bias")), _p(packed["w13"]), _p(packed["w3"]),
-                        _p(packed.get("w13_shared")), _p(packed.get("w3_shared")))
+                        _p(packed.get("w13_shared")), _p(packed.get("w3_shared")), _p(packed.get("w_att")))
 
 
 def fs_farskip_stack(desc, L, wiring, blocks, x, o_full, o_partial, ws, stream=None):
@@ -210,8 +218,12 @@ def fs_launch_count() -> int:
 
 # -------------------------------------------------------------- conveniences
 
-def alloc_workspace(desc: LayerDesc, L: int, device="cuda") -> torch.Tensor:
-    n = fs_workspace_bytes(desc, L)
+def fs_workspace_bytes_attn(desc: LayerDesc, L: int) -> int:
+    return int(lib().fs_workspace_bytes_attn(ctypes.byref(desc), L))
+
+
+def alloc_workspace(desc: LayerDesc, L: int, device="cuda", attn: bool = False) -> torch.Tensor:
+    n = fs_workspace_bytes_attn(desc, L) if attn else fs_workspace_bytes(desc, L)
     if n == 0:
         raise FsError(1, "fs_workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -225,6 +237,8 @@ def pack_block(cfg: LayerConfig, w: dict, stream=None) -> dict:
     out["w13"] = torch.empty((E, 2 * c, d), dtype=w["w1"].dtype, device=w["w1"].device)
     fs_pack_w13(E, c, d, dt, w["w1"].contiguous(), w["w2"].contiguous(), out["w13"], stream)
     out["w3"] = w["w3"].contiguous()
+    if w.get("w_att") is not None:
+        out["w_att"] = w["w_att"].contiguous()
     if cfg.n_shared:
         cw = cfg.n_shared * cfg.c_shared
         out["w13_shared"] = torch.empty((2 * cw, d), dtype=w["w1s"].dtype, device=w["w1s"].device)
@@ -245,7 +259,7 @@ class FarSkipStack:
         self.wiring = wiring or cfg.wiring
         self.desc = make_desc(cfg, self.T)
         self.blocks = [pack_block(cfg, b) for b in raw_blocks]
-        self.ws = alloc_workspace(self.desc, len(self.blocks), device)
+        self.ws = alloc_workspace(self.desc, len(self.blocks), device, attn=self.wiring.startswith("attn"))
         dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
         self.o_full = torch.empty((self.T, cfg.d), dtype=dt, device=device)
         self.o_partial = torch.empty((self.T, cfg.d), dtype=dt, device=device)

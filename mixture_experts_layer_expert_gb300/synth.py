@@ -79,6 +79,14 @@ def make_block_weights(cfg: LayerConfig, block: int, device="cpu") -> dict:
     return w
 
 
+def add_attention_standin(blocks: list, cfg: LayerConfig, device="cpu") -> list:
+    """Stand-in attention weights W_att [d, d] ~ N(0, 1/d) per block (attention wirings)."""
+    dt = storage_dtype(cfg)
+    for b, w in enumerate(blocks):
+        w["w_att"] = _randn((cfg.d, cfg.d), cfg.seed * 1000 + _ids(b)["bias"] + 8, device, 1.0 / math.sqrt(cfg.d), dt)
+    return blocks
+
+
 def make_problem(cfg: LayerConfig, device="cpu", T: int | None = None) -> dict:
     return {"x": make_x(cfg, device, T),
             "blocks": [make_block_weights(cfg, b, device) for b in range(cfg.L)]}

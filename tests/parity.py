@@ -32,6 +32,7 @@ def oracle_weights(blocks):
     return [oracle.Weights(**{k: synth.to_numpy(v) for k, v in b.items()}) for b in blocks]
 
 
+
 def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 

@@ -102,14 +102,21 @@ def test_other_entry_points_reject_bad_args(L):
                          _vp(FAKE * 256), 1 << 40, None) == 1
     assert L.fs_grouped_swiglu(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE),
                                _vp(FAKE * 256), 16, None) == 3
-    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, None, None, 0, None,
-                        0, None) == 1                                       # null o_full
-    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, _vp(MIS), None, _vp(FAKE),
-                        0, None, 0, None) == 2                              # misaligned S
-    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 3, None, None, _vp(FAKE),
-                        0, None, 0, None) == 1                              # bad residual dtype
-    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, None, _vp(FAKE),
-                        0, _vp(FAKE), 9, None) == 1                         # bad wiring for u_next
+    # fs_combine(desc, y, pos, w, o_prev, prev_dtype, S, extra, o_partial, o_full, out_dtype, u_next, wiring, u_full, st)
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, None, None, None, 0,
+                        None, 0, None, None) == 1                           # null o_full
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, _vp(MIS), None, None,
+                        _vp(FAKE), 0, None, 0, None, None) == 2             # misaligned S
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 3, None, None, None,
+                        _vp(FAKE), 0, None, 0, None, None) == 1             # bad residual dtype
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, None, None,
+                        _vp(FAKE), 0, _vp(FAKE), 9, None, None) == 1        # bad wiring for u_next
+    assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, _vp(MIS), None,
+                        _vp(FAKE), 0, None, 0, None, None) == 2             # misaligned extra
+    assert L.fs_attn_standin(ctypes.byref(d), None, _vp(FAKE), _vp(FAKE), _vp(FAKE * 256), 1 << 40, None) == 1
+    blocks1 = (fs.BlockWeights * 1)(fs.BlockWeights(FAKE, None, FAKE, FAKE, FAKE, FAKE, None))
+    assert L.fs_farskip_stack(ctypes.byref(d), 1, 3, blocks1, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256),
+                              1 << 40, None) == 1              # attention wiring without w_att
     nd = desc(n_shared=0)
     assert L.fs_shared_expert(ctypes.byref(nd), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE * 256),
                               1 << 40, None) == 1
