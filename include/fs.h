@@ -90,16 +90,16 @@ typedef struct {
     int32_t gate;    /* fs_gate */
 } fs_layer_desc;
 
-/* One block's weights in the library's packed layout (see fs_pack_w13 /
+/* One block's weights in the library's packed layouts (fs_pack_w13, fs_pack_w3,
  * fs_pack_w3_shared).  Element type = desc->dtype. */
 typedef struct {
-    const void* w_r;        /* [E, d] router (W_R) */
+    const void* w_r;        /* [E, d] router (W_R), row-major */
     const float* bias;      /* [E] router bias added to the logits, or NULL */
-    const void* w13;        /* [E, 2c, d] packed gate/up (fs_pack_w13) */
-    const void* w3;         /* [E, d, c] down (W3) */
-    const void* w13_shared; /* [2 n_shared c_shared, d] packed, NULL when n_shared = 0 */
-    const void* w3_shared;  /* [d, n_shared c_shared] (fs_pack_w3_shared) */
-    const void* w_att;      /* [d, d] stand-in attention weight (attention wirings only), or NULL */
+    const void* w13;        /* packed gate/up: fs_pack_w13(E, c, d) */
+    const void* w3;         /* packed down: fs_pack_w3(E, d, c) */
+    const void* w13_shared; /* fs_pack_w13(1, n_shared c_shared, d) of the shared experts, NULL when n_shared = 0 */
+    const void* w3_shared;  /* fs_pack_w3_shared(n_shared, c_shared, d) */
+    const void* w_att;      /* [d, d] stand-in attention weight, row-major (attention wirings only), or NULL */
 } fs_block_weights;
 
 /* Bytes of workspace needed by the single-step calls (L = 0) or by
@@ -111,20 +111,37 @@ size_t fs_workspace_bytes(const fs_layer_desc* desc, int L);
  * fs_workspace_bytes(desc, L) plus the attention buffers.  0 if invalid. */
 size_t fs_workspace_bytes_attn(const fs_layer_desc* desc, int L);
 
-/* Repack the page's W1 (up) and W2 (gate), each [G, c, d], into w13 [G, 2c, d]:
- * for each group of 64 expert columns b, rows [128b, 128b+64) of w13 are W2
- * rows [64b, 64b+64) (gate) and rows [128b+64, 128b+128) are W1 rows (up).
- * The SwiGLU epilogue then finds gate and up of one column in the same tile.
- * c must be a multiple of 64.  Element type = dtype. */
+/* Packed weight layouts.  A weight matrix [G, N, K] (N output rows, K the
+ * contracted dimension, K-contiguous as the page writes W1, W2 [c, d] and
+ * W3 [d, c]) is stored
+ *   bf16: tiled, [G][ceil(N/256)][K/64][256][64]: every 256-row x 64-column
+ *         tile the tensor-core GEMM loads is one contiguous 32 KB block
+ *         (rows past N are zero), so weight streaming reads HBM sequentially;
+ *   fp32: row-major [G, N, K].
+ * fs_packed_bytes gives the size (0 for invalid arguments; K % 64 == 0). */
+size_t fs_packed_bytes(int32_t G, int32_t N, int32_t K, int32_t dtype);
+
+/* Gate/up: the page's W1 (up) and W2 (gate), each [G, c, d], as one packed
+ * [G, N = 2c, K = d] matrix whose rows interleave gate and up: for each block
+ * of 64 expert columns b, packed rows [128b, 128b+64) are W2 rows [64b, 64b+64)
+ * and rows [128b+64, 128b+128) are W1 rows, so the SwiGLU epilogue finds gate
+ * and up of one column in the same tile.  c % 64 == 0, d % 64 == 0.  w13 holds
+ * fs_packed_bytes(G, 2c, d, dtype) bytes. */
 fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype,
                       const void* w1, const void* w2, void* w13, void* stream);
 
-/* Concatenate n_shared shared-expert down projections, each [d, c_shared],
- * along the expert width: w3cat[i, s c_shared + j] = w3s[s, i, j], giving
- * [d, n_shared c_shared].  By the TP-slicing identity of §2.1 the sum of the
+/* Down: the page's W3 [G, d, c] as a packed [G, N = d, K = c] matrix
+ * (fs_packed_bytes(G, d, c, dtype) bytes). */
+fs_status fs_pack_w3(int32_t G, int32_t d, int32_t c, int32_t dtype, const void* w3, void* w3p,
+                     void* stream);
+
+/* Shared experts: n_shared down projections, each [d, c_shared], side by side
+ * along the expert width, w3cat[i, s c_shared + j] = w3s[s, i, j], packed as a
+ * [1, N = d, K = n_shared c_shared] matrix (fs_packed_bytes(1, d, n_shared
+ * c_shared, dtype) bytes).  By the TP-slicing identity of §2.1 the sum of the
  * shared experts equals one MLP over the concatenated width; their gate/up
  * weights [n_shared, c_shared, d] are already concatenated in memory and are
- * packed with fs_pack_w13(G = 1, c = n_shared c_shared). */
+ * packed with fs_pack_w13(G = 1, c = n_shared c_shared).  c_shared % 64 == 0. */
 fs_status fs_pack_w3_shared(int32_t n_shared, int32_t c_shared, int32_t d, int32_t dtype,
                             const void* w3s, void* w3cat, void* stream);
 
@@ -178,7 +195,7 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
  *   h = SiLU(x W2_e^T) * (x W1_e^T)  (fp32 accumulate, stored bf16/fp32 in ws)
  *   y_perm[p] = h W3_e^T             (fp32 accumulate, stored in desc->dtype)
  *   x_perm [T k, d], offsets [E+1] (device; the host never reads them),
- *   w13 [E, 2c, d] packed, w3 [E, d, c] -> y_perm [T k, d].
+ *   w13 = fs_pack_w13(E, c, d), w3 = fs_pack_w3(E, d, c) -> y_perm [T k, d].
  * bf16: persistent tcgen05/TMEM grouped GEMMs fed by TMA; fp32: fp32 FMA. */
 fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets,
                             const void* w13, const void* w3, void* y_perm,

@@ -211,7 +211,7 @@ static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* 
         const int bm = tc_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
         FS_TRY(launch_tc_gemm(EPI_F32, u, d->T, w_r, 1, d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E,
-                              nullptr, 0, st));
+                              nullptr, 0, false, st));
     } else {
         const int bm = simt_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
@@ -243,9 +243,10 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
-        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, gather, rows, st));
+        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, gather, rows,
+                              true, st));
         FS_TRY(launch_tc_gemm(y_f32 ? EPI_F32 : EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d,
-                              nullptr, 0, st));
+                              nullptr, 0, true, st));
     } else {
         const int bm = simt_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -300,7 +301,7 @@ static fs_status attn_impl(const fs_layer_desc* d, const void* a, const void* w_
         const int bm = tc_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
         FS_TRY(launch_tc_gemm(EPI_F32, a, d->T, w_att, 1, d->d, d->d, plan, ceil_div(d->T, bm) + 1, out, d->d, d->d,
-                              nullptr, 0, st));
+                              nullptr, 0, false, st));
     } else {
         const int bm = simt_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
@@ -351,6 +352,20 @@ fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype, const void
     FS_CHECK(need(w2));
     FS_CHECK(need(w13));
     FS_TRY(launch_pack_w13(G, c, d, dtype == FS_BF16 ? 2 : 4, w1, w2, w13, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+size_t fs_packed_bytes(int32_t G, int32_t N, int32_t K, int32_t dtype) {
+    if (G < 1 || N < 1 || K < 1 || K % 64 || (dtype != FS_BF16 && dtype != FS_F32)) return 0;
+    return packed_bytes(G, N, K, dtype == FS_BF16 ? 2 : 4);
+}
+
+fs_status fs_pack_w3(int32_t G, int32_t d, int32_t c, int32_t dtype, const void* w3, void* w3p, void* stream) {
+    if (G < 1 || c < 1 || d < 1 || (dtype != FS_BF16 && dtype != FS_F32)) return FS_ERR_INVALID_ARG;
+    if (c % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w3));
+    FS_CHECK(need(w3p));
+    FS_TRY(launch_pack_w3(G, d, c, dtype == FS_BF16 ? 2 : 4, w3, w3p, static_cast<cudaStream_t>(stream)));
     return FS_OK;
 }
 

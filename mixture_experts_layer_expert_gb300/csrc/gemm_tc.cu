@@ -19,9 +19,10 @@
 //               tile's columns: tcgen05.ld of the accumulator, activation, stores
 // TMEM holds two 128 x 256 fp32 accumulators (512 columns) so the epilogue of
 // tile i overlaps the MMAs of tile i + 1.  Every wait is bounded in time.
-// Tile order inside a group: blocks of kGroupM M-tiles, N-tiles outer inside a
-// block, so the ~152 tiles in flight share a few MB of A and B in L2 instead of
-// streaming a tall A operand from HBM once per N-tile.
+// Tile order inside a group: blocks of M-tiles (the whole group up to 32
+// M-tiles, else 16), N-tiles outer inside a block, so the ~152 tiles in flight
+// share a few MB of A and B in L2 and each B slab is read from HBM once,
+// instead of streaming a tall A operand once per N-tile.
 #include <cudaTypedefs.h>
 #include <cstdlib>
 #include <cstring>
@@ -61,6 +62,7 @@ struct Args {
     int* err;          // device error word
     const int* gather_rows;  // A row of GEMM row p = gather_rows[p] (tile::gather4), or nullptr
     int gather_limit;        // entries of gather_rows
+    int b_blocked;           // B in the tiled weight layout [G][n_tiles][K/64][256][64] (3D map)
 };
 
 struct Tile {
@@ -79,11 +81,15 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const in
     r.g = lo;
     const int mtiles = mt_start[lo + 1] - mt_start[lo];
     const int local = t - mt_start[lo] * n_tiles;
-    const int blk = local / (kGroupM * n_tiles);            // block of kGroupM M-tiles
-    const int gm = min(kGroupM, mtiles - blk * kGroupM);     // M-tiles in this block
-    const int rr = local - blk * kGroupM * n_tiles;
+    // groups of up to 2 kGroupM M-tiles form one block, so every B slab of the
+    // group is used by all its M-tiles back to back; taller groups use blocks
+    // of kGroupM M-tiles
+    const int GM = mtiles <= 2 * kGroupM ? mtiles : kGroupM;
+    const int blk = local / (GM * n_tiles);                 // block of GM M-tiles
+    const int gm = min(GM, mtiles - blk * GM);              // M-tiles in this block
+    const int rr = local - blk * GM * n_tiles;
     r.n = rr / gm;
-    r.m = blk * kGroupM + (rr - r.n * gm);
+    r.m = blk * GM + (rr - r.n * gm);
     r.a_row = row_start[lo] + r.m * bm;
     const int rem = row_start[lo + 1] - r.a_row;
     r.rows_valid = rem < bm ? rem : bm;
@@ -254,7 +260,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
                 uint8_t* sa = smem + stage * STAGE_BYTES;
                 tma_gather4(smem_u32(sa) + 512u * lane, &tmA, fb, kb * BK, rr[0], rr[1], rr[2], rr[3]);
-                if (lane == 0) tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
+                if (lane == 0) {
+                    if (args.b_blocked)
+                        tma_load_3d(smem_u32(sa + A_STAGE), &tmB, fb, 0, 0, (tl.g * args.n_tiles + tl.n) * num_kb + kb);
+                    else
+                        tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
+                }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -289,7 +300,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     uint8_t* sa = smem + stage * STAGE_BYTES;
                     tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, tl.a_row);
-                    tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
+                    if (args.b_blocked)
+                        tma_load_3d(smem_u32(sa + A_STAGE), &tmB, fb, 0, 0, (tl.g * args.n_tiles + tl.n) * num_kb + kb);
+                    else
+                        tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -472,7 +486,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t fb = map_to_cta(fb_local, 0);
                     uint8_t* sa = smem + stage * P_STAGE_BYTES;
                     tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, a_row);
-                    tma_load_2d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, kb * BK, b_row);
+                    if (args.b_blocked)
+                        tma_load_3d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, 0, static_cast<int>(rank) * 128,
+                                         (tl.g * args.n_tiles + tl.n) * num_kb + kb);
+                    else
+                        tma_load_2d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, kb * BK, b_row);
                     ++issued;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -654,6 +672,21 @@ static cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, lo
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3D bf16 tensor map over the tiled weight layout [nblocks][256][64] (each
+// block a contiguous 32 KB [256 rows x 64 K] tile) with a box of box_rows x 64.
+static cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows) {
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    cuuint64_t gdim[3] = {64, 256, static_cast<cuuint64_t>(nblocks)};
+    cuuint64_t gstride[2] = {128, 256 * 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static int g_num_sms = 0;
 
 static cudaError_t num_sms(int* out) {
@@ -688,7 +721,7 @@ static bool use_pair() {
 template <int EPI>
 static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,
                                   const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                                  const int* gather_rows, int gather_limit, cudaStream_t st) {
+                                  const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st) {
     const bool pair = use_pair();
     if (pair && gather_rows) return cudaErrorNotSupported;
     static bool attr_set[2] = {false, false};
@@ -706,7 +739,11 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     CUtensorMap ta, tb;
     e = make_map(&ta, A, a_rows, K, gather_rows ? 1 : 128);
     if (e != cudaSuccess) return e;
-    e = make_map(&tb, B, static_cast<long long>(G) * N, K, pair ? 128 : tc::BN);
+    const int n_tiles = (N + tc::BN - 1) / tc::BN;
+    if (b_blocked)
+        e = make_map_blocked(&tb, B, static_cast<long long>(G) * n_tiles * (K / tc::BK), pair ? 128 : tc::BN);
+    else
+        e = make_map(&tb, B, static_cast<long long>(G) * N, K, pair ? 128 : tc::BN);
     if (e != cudaSuccess) return e;
     tc::Args args;
     args.plan = plan;
@@ -721,6 +758,7 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.err = dev_error_ptr();
     args.gather_rows = gather_rows;
     args.gather_limit = gather_limit;
+    args.b_blocked = b_blocked ? 1 : 0;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -743,17 +781,17 @@ bool tc_gather_supported() { return !use_pair(); }
 
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                           const int* gather_rows, int gather_limit, cudaStream_t st) {
+                           const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st) {
     switch (epi) {
         case EPI_SWIGLU:
             return launch_tc_impl<EPI_SWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
-                                              gather_rows, gather_limit, st);
+                                              gather_rows, gather_limit, b_blocked, st);
         case EPI_BF16:
             return launch_tc_impl<EPI_BF16>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
-                                            gather_rows, gather_limit, st);
+                                            gather_rows, gather_limit, b_blocked, st);
         case EPI_F32:
             return launch_tc_impl<EPI_F32>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
-                                           gather_rows, gather_limit, st);
+                                           gather_rows, gather_limit, b_blocked, st);
         default:
             return cudaErrorInvalidValue;
     }

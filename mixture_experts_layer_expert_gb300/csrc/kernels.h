@@ -20,9 +20,10 @@ int tc_block_m();
 cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st);
 // gather_rows (nullable): GEMM row p reads row gather_rows[p] of A (p < gather_limit)
 bool tc_gather_supported();
+// b_blocked: B is in the tiled weight layout of pack.cu ([G][ceil(N/256)][K/64][256][64])
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                           const int* gather_rows, int gather_limit, cudaStream_t st);
+                           const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st);
 
 // gemm_simt.cu (fp32 operands, fp32 FMA)
 int simt_block_m();
@@ -50,9 +51,12 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* 
                            int out_bf16, void* u_next, int u_src, void* u_full, int T, int d, int k, int is_bf16,
                            cudaStream_t st);
 
-// pack.cu
+// pack.cu -- bf16 weights are packed into the tiled layout [G][ceil(N/256)][K/64][256][64]
+// (rows past N are zero); fp32 weights keep row-major layouts.
+size_t packed_bytes(int G, int N, int K, int elem_bytes);
 cudaError_t launch_pack_w13(int G, int c, int d, int elem_bytes, const void* w1, const void* w2, void* w13,
                             cudaStream_t st);
+cudaError_t launch_pack_w3(int G, int d, int c, int elem_bytes, const void* w3, void* w3p, cudaStream_t st);
 cudaError_t launch_pack_w3_shared(int ns, int cs, int d, int elem_bytes, const void* w3s, void* w3cat,
                                   cudaStream_t st);
 

@@ -46,6 +46,8 @@ _SIGS = {
     "fs_workspace_bytes": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
     "fs_pack_w13": (_I32, [_I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP]),
     "fs_pack_w3_shared": (_I32, [_I32, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "fs_pack_w3": (_I32, [_I32, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "fs_packed_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
     "fs_router_topk": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_dispatch": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "fs_dispatch_noalloc": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -120,6 +122,14 @@ def fs_workspace_bytes(desc: LayerDesc, L: int = 0) -> int:
 
 def fs_pack_w13(G, c, d, dtype, w1, w2, w13, stream=None):
     _check(lib().fs_pack_w13(G, c, d, dtype, _p(w1), _p(w2), _p(w13), _stream(stream)), "fs_pack_w13")
+
+
+def fs_packed_bytes(G, N, K, dtype) -> int:
+    return int(lib().fs_packed_bytes(G, N, K, dtype))
+
+
+def fs_pack_w3(G, d, c, dtype, w3, w3p, stream=None):
+    _check(lib().fs_pack_w3(G, d, c, dtype, _p(w3), _p(w3p), _stream(stream)), "fs_pack_w3")
 
 
 def fs_pack_w3_shared(n_shared, c_shared, d, dtype, w3s, w3cat, stream=None):
@@ -229,21 +239,29 @@ def alloc_workspace(desc: LayerDesc, L: int, device="cuda", attn: bool = False) 
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def _packed(G, N, K, dt, like):
+    n = fs_packed_bytes(G, N, K, dt)
+    if n == 0:
+        raise FsError(1, "fs_packed_bytes")
+    return torch.empty(n // like.element_size(), dtype=like.dtype, device=like.device)
+
+
 def pack_block(cfg: LayerConfig, w: dict, stream=None) -> dict:
     """Repack one block's page-layout weights (on the GPU) into the library layout."""
     dt = FS_BF16 if cfg.dtype == "bf16" else FS_F32
     E, c, d = cfg.E, cfg.c, cfg.d
     out = {"w_r": w["w_r"].contiguous(), "bias": None if w.get("bias") is None else w["bias"].contiguous().float()}
-    out["w13"] = torch.empty((E, 2 * c, d), dtype=w["w1"].dtype, device=w["w1"].device)
+    out["w13"] = _packed(E, 2 * c, d, dt, w["w1"])
     fs_pack_w13(E, c, d, dt, w["w1"].contiguous(), w["w2"].contiguous(), out["w13"], stream)
-    out["w3"] = w["w3"].contiguous()
+    out["w3"] = _packed(E, d, c, dt, w["w3"])
+    fs_pack_w3(E, d, c, dt, w["w3"].contiguous(), out["w3"], stream)
     if w.get("w_att") is not None:
         out["w_att"] = w["w_att"].contiguous()
     if cfg.n_shared:
         cw = cfg.n_shared * cfg.c_shared
-        out["w13_shared"] = torch.empty((2 * cw, d), dtype=w["w1s"].dtype, device=w["w1s"].device)
+        out["w13_shared"] = _packed(1, 2 * cw, d, dt, w["w1s"])
         fs_pack_w13(1, cw, d, dt, w["w1s"].contiguous(), w["w2s"].contiguous(), out["w13_shared"], stream)
-        out["w3_shared"] = torch.empty((d, cw), dtype=w["w3s"].dtype, device=w["w3s"].device)
+        out["w3_shared"] = _packed(1, d, cw, dt, w["w3s"])
         fs_pack_w3_shared(cfg.n_shared, cfg.c_shared, d, dt, w["w3s"].contiguous(), out["w3_shared"], stream)
     return out
 
