@@ -54,7 +54,7 @@ def build(force: bool = False) -> str:
 
 class _Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("d", "E", "k", "c", "n_shared", "c_shared", "gate", "in_dtype", "storage")]
+                ("d", "E", "k", "c", "n_shared", "c_shared", "gate", "in_dtype", "storage", "fp8")]
 
 
 class _W(ctypes.Structure):
@@ -101,14 +101,38 @@ def round_storage(x: float, storage: int) -> float:
 
 
 def make_cfg(d, E, k, c, n_shared=0, c_shared=0, gate="softmax_renorm", in_dtype=F32,
-             storage=EXACT) -> _Cfg:
+             storage=EXACT, fp8=False) -> _Cfg:
+    """fp8=True: expert GEMM operands in FP8 E4M3 with one power-of-two scale per
+    row along the contraction (tokens, hidden rows, weight output channels)."""
     g = GATES[gate] if isinstance(gate, str) else int(gate)
-    return _Cfg(d, E, k, c, n_shared, c_shared, g, in_dtype, storage)
+    return _Cfg(d, E, k, c, n_shared, c_shared, g, in_dtype, storage, int(bool(fp8)))
 
 
 def _check(rc, what):
     if rc != 0:
         raise RuntimeError("oracle %s failed (rc=%d)" % (what, rc))
+
+
+def e4m3(x: np.ndarray):
+    """Nearest FP8 E4M3 values (ties to even, saturating at +-448) and their codes."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    codes = np.zeros(x.shape, np.uint8)
+    _check(lib().oracle_e4m3_array(ctypes.c_int64(x.size), _p(x), _p(out), _p(codes)), "e4m3")
+    return out, codes
+
+
+def quant_rows(x: np.ndarray, dtype: str | None = None):
+    """Per-row FP8 quantisation of x [rows, cols]: codes [rows, cols] uint8, the row
+    exponents e [rows] (scale 2^e) and the dequantised values e4m3(x 2^-e) 2^e."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), np.uint8)
+    exps = np.zeros(rows, np.int32)
+    deq = np.zeros((rows, cols), np.float64)
+    _check(lib().oracle_quant_rows(ctypes.c_int(rows), ctypes.c_int(cols), _p(x), ctypes.c_int(_dt(x, dtype)),
+                                   _p(codes), _p(exps), _p(deq)), "quant_rows")
+    return codes, exps, deq
 
 
 def router(cfg: _Cfg, u: np.ndarray, w_r: np.ndarray, bias: np.ndarray | None = None):
@@ -126,7 +150,9 @@ def router(cfg: _Cfg, u: np.ndarray, w_r: np.ndarray, bias: np.ndarray | None = 
 
 
 def expert_rows(cfg: _Cfg, a: np.ndarray, expert: np.ndarray, w1, w2, w3):
-    """Per row r: h = SiLU(a W2[e]^T) * (a W1[e]^T) and y = h W3[e]^T (rounded per storage)."""
+    """Per row r: h = SiLU(a W2[e]^T) * (a W1[e]^T) and y = h W3[e]^T (rounded per storage).
+    With cfg.fp8 the FP8 form: a, the weight rows and h quantised per row (h is
+    returned before its quantisation)."""
     a = np.ascontiguousarray(a)
     n = a.shape[0]
     h = np.zeros((n, cfg.c), np.float64)

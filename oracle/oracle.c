@@ -39,6 +39,17 @@
  *     o_L, o_L* are returned at that precision:
  *     storing them in bf16 is the layer's own output rounding, which the
  *     comparison tolerance covers.  All sums stay fp64.
+ *   - FP8 experts (cfg->fp8; the pages run inference with FP8 quantisation
+ *     and fused MoE kernels but give no format): the operands of the expert
+ *     GEMMs are FP8 E4M3 values times one power-of-two scale per row along
+ *     the contraction -- per token for the activations (the block input u,
+ *     quantised once per token; the stored hidden h, quantised per row after
+ *     its storage rounding), per output channel for the weights (rows of W1,
+ *     W2 along d, rows of W3 along c).  Because each scale multiplies a whole
+ *     row of the contraction it factors out of the sum, so the GEMM is the
+ *     plain sum over the dequantised values.  The router, Combine and the
+ *     residual stream are unchanged.  The shared experts are quantised as the
+ *     one MLP over their concatenated width that they sum to (§2.1).
  */
 #include <math.h>
 #include <stdint.h>
@@ -81,6 +92,114 @@ double oracle_round(double x, int storage) {
     if (storage == ORACLE_STORE_BF16) return round_sig(x, 8);
     if (storage == ORACLE_STORE_F32) return round_sig(x, 24);
     return x;
+}
+
+/* ---------------------------------------------------------------- FP8 E4M3 */
+
+/* FP8 E4M3, the "e4m3fn" format of the OCP 8-bit floating-point formats: a
+ * sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities, and
+ * the code S.1111.111 is NaN.  Finite magnitudes: normals (1 + m/8) 2^(E-7)
+ * for exponent fields E = 1..15 (m = 0..7, except m = 7 at E = 15), the
+ * largest 1.75 * 2^8 = 448; subnormals m 2^-9 for m = 1..7 (E = 0).
+ * oracle_e4m3(x): the value of that set nearest to x, ties to the even
+ * mantissa; magnitudes above 448 saturate to 448 (a "satfinite" conversion). */
+double oracle_e4m3(double x) {
+    if (isnan(x)) return x;
+    if (isinf(x)) return x < 0 ? -448.0 : 448.0;
+    double a = fabs(x);
+    if (a == 0.0) return x;
+    int e;
+    (void)frexp(a, &e);             /* a in [2^(e-1), 2^e) */
+    int lead = e - 1;               /* exponent of the leading bit */
+    if (lead < -6) lead = -6;       /* below the smallest normal 2^-6 the quantum stays 2^-9 */
+    double q = ldexp(1.0, lead - 3);
+    double r = nearbyint(a / q) * q; /* ties to even */
+    if (r > 448.0) r = 448.0;
+    return x < 0 ? -r : r;
+}
+
+/* The E4M3 code of a value v from oracle_e4m3. */
+static uint8_t e4m3_code(double v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sgn = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    if (a < ldexp(1.0, -6)) return sgn | (uint8_t)(a / ldexp(1.0, -9));   /* subnormal or zero */
+    int e;
+    (void)frexp(a, &e);
+    int lead = e - 1;
+    int m = (int)((a / ldexp(1.0, lead) - 1.0) * 8.0);
+    return sgn | (uint8_t)((lead + 7) << 3) | (uint8_t)m;
+}
+
+int oracle_e4m3_array(int64_t n, const double* x, double* out, uint8_t* codes) {
+    for (int64_t i = 0; i < n; ++i) {
+        double v = oracle_e4m3(x[i]);
+        if (out) out[i] = v;
+        if (codes) codes[i] = e4m3_code(v);
+    }
+    return 0;
+}
+
+/* Scale of one FP8 operand row: the power of two 2^e with the smallest integer
+ * e such that max_i |x_i| 2^-e <= 448, so the row's largest element lands in
+ * (224, 448]; e = 0 for a row of zeros. */
+static int fp8_row_exp(double amax) {
+    if (!(amax > 0.0)) return 0;
+    int e;
+    (void)frexp(amax, &e);          /* 2^(e-1) <= amax < 2^e, so the answer is e-9 or e-8 */
+    int s = e - 10;
+    while (amax > ldexp(448.0, s)) ++s;
+    return s;
+}
+
+/* Quantise one row in place: x_i <- e4m3(x_i 2^-e) 2^e with e = fp8_row_exp(max |x|);
+ * returns e and, when codes is set, the E4M3 codes of e4m3(x_i 2^-e). */
+static int quant_row(double* x, int n, uint8_t* codes) {
+    double amax = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (fabs(x[i]) > amax) amax = fabs(x[i]);
+    int e = fp8_row_exp(amax);
+    for (int i = 0; i < n; ++i) {
+        double v = oracle_e4m3(ldexp(x[i], -e));
+        if (codes) codes[i] = e4m3_code(v);
+        x[i] = ldexp(v, e);
+    }
+    return e;
+}
+
+int oracle_quant_rows(int rows, int cols, const void* x, int x_dtype,
+                      uint8_t* codes, int32_t* exps, double* deq) {
+    if (rows < 0 || cols <= 0) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        double* row = (double*)malloc(sizeof(double) * (size_t)cols);
+        if (!row) { bad = 1; continue; }
+        for (int i = 0; i < cols; ++i) row[i] = elem(x, (size_t)r * cols + i, x_dtype);
+        int e = quant_row(row, cols, codes ? codes + (size_t)r * cols : NULL);
+        if (exps) exps[r] = e;
+        if (deq) memcpy(deq + (size_t)r * cols, row, sizeof(double) * (size_t)cols);
+        free(row);
+    }
+    return bad ? -2 : 0;
+}
+
+/* Exponents of `rows` weight rows of length K starting at element `base`. */
+static void weight_row_exps(const void* w, int dt, size_t rows, int K, int32_t* out) {
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < (long long)rows; ++r) {
+        double amax = 0.0;
+        for (int i = 0; i < K; ++i) {
+            double v = fabs(elem(w, (size_t)r * K + i, dt));
+            if (v > amax) amax = v;
+        }
+        out[r] = fp8_row_exp(amax);
+    }
+}
+
+/* One weight element quantised with its row's exponent e. */
+static double wq(const void* w, size_t i, int dt, int e) {
+    return ldexp(oracle_e4m3(ldexp(elem(w, i, dt), -e)), e);
 }
 
 static double silu(double v) { return v / (1.0 + exp(-v)); }
@@ -175,25 +294,118 @@ static void mlp_row(int d, int c, const double* a,
     }
 }
 
+/* The FP8 form of one expert (cfg->fp8 = 1).  aq[d] is the token row already
+ * quantised (quant_row; once per token, shared by all its experts).  The
+ * expert has width c made of sub-experts of width cw side by side (cw = c for
+ * a routed expert; the shared experts form one MLP over their concatenated
+ * width, the TP-slicing identity of §2.1).  W1, W2 are [c, d] from element
+ * base12, row j quantised with exponent e1[j] / e2[j]; W3 element (i, jj) sits
+ * at base3 + (jj / cw) d cw + i cw + jj % cw and row i (over all c) uses e3[i].
+ *   gate_j = sum_i aq[i] Wq2[j, i],  up_j = sum_i aq[i] Wq1[j, i]
+ *   h_j    = SiLU(gate_j) up_j, rounded per storage (the stored hidden)
+ *   hq     = h quantised as one row (quant_row over its c elements)
+ *   y_i    = sum_jj hq[jj] Wq3[i, jj]
+ * h returns the stored hidden before its quantisation. */
+static void mlp_row_fp8(int d, int c, int cw, const double* aq,
+                        const void* w1, const void* w2, size_t base12, const int32_t* e1, const int32_t* e2,
+                        const void* w3, size_t base3, const int32_t* e3, int wdt, int storage,
+                        double* h, double* hq, double* y) {
+    for (int j = 0; j < c; ++j) {
+        double gate = 0.0, up = 0.0;
+        for (int i = 0; i < d; ++i) {
+            gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[j]);
+            up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[j]);
+        }
+        h[j] = oracle_round(silu(gate) * up, storage);
+        hq[j] = h[j];
+    }
+    quant_row(hq, c, NULL);
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int jj = 0; jj < c; ++jj) {
+            size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);
+            acc += hq[jj] * wq(w3, off, wdt, e3[i]);
+        }
+        y[i] = acc;
+    }
+}
+
+/* Row exponents of one block's FP8 expert weights: routed W1, W2 rows [E c]
+ * (along d) and W3 rows [E d] (along c); the shared experts' gate/up rows
+ * [n_s c_s] and the rows of their concatenated down projection [d] (along the
+ * n_s c_s concatenated columns). */
+typedef struct { int32_t *e1, *e2, *e3, *e1s, *e2s, *e3s; } fp8_exps;
+
+static void fp8_exps_free(fp8_exps* x) {
+    free(x->e1); free(x->e2); free(x->e3); free(x->e1s); free(x->e2s); free(x->e3s);
+}
+
+static int fp8_exps_make(const oracle_cfg* cfg, const void* w1, const void* w2, const void* w3,
+                         const void* w1s, const void* w2s, const void* w3s, fp8_exps* x) {
+    const int d = cfg->d, E = cfg->E, c = cfg->c, ns = cfg->n_shared, cs = cfg->c_shared;
+    const int wdt = cfg->in_dtype;
+    memset(x, 0, sizeof *x);
+    x->e1 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * c);
+    x->e2 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * c);
+    x->e3 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * d);
+    if (!x->e1 || !x->e2 || !x->e3) return -2;
+    weight_row_exps(w1, wdt, (size_t)E * c, d, x->e1);
+    weight_row_exps(w2, wdt, (size_t)E * c, d, x->e2);
+    weight_row_exps(w3, wdt, (size_t)E * d, c, x->e3);
+    if (ns > 0 && w1s) {
+        x->e1s = (int32_t*)malloc(sizeof(int32_t) * (size_t)ns * cs);
+        x->e2s = (int32_t*)malloc(sizeof(int32_t) * (size_t)ns * cs);
+        x->e3s = (int32_t*)malloc(sizeof(int32_t) * (size_t)d);
+        if (!x->e1s || !x->e2s || !x->e3s) return -2;
+        weight_row_exps(w1s, wdt, (size_t)ns * cs, d, x->e1s);
+        weight_row_exps(w2s, wdt, (size_t)ns * cs, d, x->e2s);
+        for (int i = 0; i < d; ++i) {
+            double amax = 0.0;
+            for (int sh = 0; sh < ns; ++sh)
+                for (int j = 0; j < cs; ++j) {
+                    double v = fabs(elem(w3s, (size_t)sh * d * cs + (size_t)i * cs + j, wdt));
+                    if (v > amax) amax = v;
+                }
+            x->e3s[i] = fp8_row_exp(amax);
+        }
+    }
+    return 0;
+}
+
 int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_dtype,
                        const int32_t* expert, const void* w1, const void* w2, const void* w3,
                        double* h_out, double* y_out) {
     const int d = cfg->d, c = cfg->c;
     int bad = 0;
+    fp8_exps fx;
+    memset(&fx, 0, sizeof fx);
+    if (cfg->fp8 && fp8_exps_make(cfg, w1, w2, w3, NULL, NULL, NULL, &fx)) {
+        fp8_exps_free(&fx);
+        return -2;
+    }
 #pragma omp parallel for schedule(dynamic, 4)
     for (int r = 0; r < n_rows; ++r) {
         double* arow = (double*)malloc(sizeof(double) * (size_t)d);
         double* h = (double*)malloc(sizeof(double) * (size_t)c);
-        if (!arow || !h) { bad = 1; free(arow); free(h); continue; }
+        double* hq = (double*)malloc(sizeof(double) * (size_t)c);
+        if (!arow || !h || !hq) { bad = 1; free(arow); free(h); free(hq); continue; }
         for (int i = 0; i < d; ++i) arow[i] = elem(a, (size_t)r * d + i, a_dtype);
         size_t e = (size_t)expert[r];
-        mlp_row(d, c, arow, w1, e * c * d, w2, e * c * d, w3, e * d * c, cfg->in_dtype,
-                cfg->storage, h, y_out + (size_t)r * d);
+        if (cfg->fp8) {
+            quant_row(arow, d, NULL);
+            mlp_row_fp8(d, c, c, arow, w1, w2, e * c * d, fx.e1 + e * c, fx.e2 + e * c,
+                        w3, e * d * c, fx.e3 + e * d, cfg->in_dtype, cfg->storage, h, hq, y_out + (size_t)r * d);
+        } else {
+            mlp_row(d, c, arow, w1, e * c * d, w2, e * c * d, w3, e * d * c, cfg->in_dtype,
+                    cfg->storage, h, y_out + (size_t)r * d);
+        }
+        free(hq);
         for (int i = 0; i < d; ++i) y_out[(size_t)r * d + i] = oracle_round(y_out[(size_t)r * d + i], cfg->storage);
         if (h_out) memcpy(h_out + (size_t)r * c, h, sizeof(double) * (size_t)c);
         free(arow);
         free(h);
     }
+    fp8_exps_free(&fx);
     return bad ? -2 : 0;
 }
 
@@ -247,28 +459,53 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
     free(zbuf);
     if (rc) return rc;
     int bad = 0;
-    const int cmax = c > cs ? c : cs;
+    fp8_exps fx;
+    memset(&fx, 0, sizeof fx);
+    if (cfg->fp8 && fp8_exps_make(cfg, wts->w1, wts->w2, wts->w3, wts->w1s, wts->w2s, wts->w3s, &fx)) {
+        fp8_exps_free(&fx);
+        return -2;
+    }
+    int cmax = c > cs ? c : cs;
+    if (cfg->fp8 && ns * cs > cmax) cmax = ns * cs;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < n_tok; ++t) {
         double* h = (double*)malloc(sizeof(double) * (size_t)(cmax > 0 ? cmax : 1));
+        double* hq = (double*)malloc(sizeof(double) * (size_t)(cmax > 0 ? cmax : 1));
+        double* aq = (double*)malloc(sizeof(double) * (size_t)d);
         double* y = (double*)malloc(sizeof(double) * (size_t)d);
         double* R = (double*)calloc((size_t)d, sizeof(double));
         double* S = (double*)calloc((size_t)d, sizeof(double));
-        if (!h || !y || !R || !S) { bad = 1; free(h); free(y); free(R); free(S); continue; }
+        if (!h || !hq || !aq || !y || !R || !S) {
+            bad = 1; free(h); free(hq); free(aq); free(y); free(R); free(S); continue;
+        }
         const double* a = u + (size_t)t * d;
+        if (cfg->fp8) {     /* the token row quantised once for all of its experts */
+            memcpy(aq, a, sizeof(double) * (size_t)d);
+            quant_row(aq, d, NULL);
+        }
         /* routed experts: Combine = gate-weighted sum of the k expert outputs */
         for (int s = 0; s < k; ++s) {
             size_t e = (size_t)topk_idx[(size_t)t * k + s];
             double w = topk_w[(size_t)t * k + s];
-            mlp_row(d, c, a, wts->w1, e * c * d, wts->w2, e * c * d, wts->w3, e * d * c,
-                    cfg->in_dtype, cfg->storage, h, y);
+            if (cfg->fp8)
+                mlp_row_fp8(d, c, c, aq, wts->w1, wts->w2, e * c * d, fx.e1 + e * c, fx.e2 + e * c,
+                            wts->w3, e * d * c, fx.e3 + e * d, cfg->in_dtype, cfg->storage, h, hq, y);
+            else
+                mlp_row(d, c, a, wts->w1, e * c * d, wts->w2, e * c * d, wts->w3, e * d * c,
+                        cfg->in_dtype, cfg->storage, h, y);
             for (int i = 0; i < d; ++i) R[i] += w * oracle_round(y[i], cfg->storage);
         }
         /* shared experts: every token, gate weight 1 */
-        for (int sh = 0; sh < ns; ++sh) {
-            mlp_row(d, cs, a, wts->w1s, (size_t)sh * cs * d, wts->w2s, (size_t)sh * cs * d,
-                    wts->w3s, (size_t)sh * d * cs, cfg->in_dtype, cfg->storage, h, y);
-            for (int i = 0; i < d; ++i) S[i] += y[i];
+        if (cfg->fp8 && ns > 0) {
+            mlp_row_fp8(d, ns * cs, cs, aq, wts->w1s, wts->w2s, 0, fx.e1s, fx.e2s,
+                        wts->w3s, 0, fx.e3s, cfg->in_dtype, cfg->storage, h, hq, y);
+            for (int i = 0; i < d; ++i) S[i] = y[i];    /* one MLP over the concatenated width */
+        } else {
+            for (int sh = 0; sh < ns; ++sh) {
+                mlp_row(d, cs, a, wts->w1s, (size_t)sh * cs * d, wts->w2s, (size_t)sh * cs * d,
+                        wts->w3s, (size_t)sh * d * cs, cfg->in_dtype, cfg->storage, h, y);
+                for (int i = 0; i < d; ++i) S[i] += y[i];
+            }
         }
         for (int i = 0; i < d; ++i) {
             double sv = oracle_round(S[i], resid);
@@ -278,8 +515,9 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
             if (R_out) R_out[(size_t)t * d + i] = R[i];
             if (S_out) S_out[(size_t)t * d + i] = sv;
         }
-        free(h); free(y); free(R); free(S);
+        free(h); free(hq); free(aq); free(y); free(R); free(S);
     }
+    fp8_exps_free(&fx);
     return bad ? -2 : 0;
 }
 

@@ -12,6 +12,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_fp8_pins as fp8
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -42,6 +43,20 @@ MUTANTS = {
                             "double op = o_prev[(size_t)t * d + i];"),
     "shared_sum_rounded_per_expert": ("for (int i = 0; i < d; ++i) S[i] += y[i];",
                                       "for (int i = 0; i < d; ++i) S[i] += (sh == 0 ? y[i] : 0.0);"),
+    # FP8 expert path
+    "e4m3_without_subnormal_floor": ("    if (lead < -6) lead = -6;       /* below the smallest normal 2^-6 the quantum stays 2^-9 */\n", ""),
+    "e4m3_ties_away": ("double r = nearbyint(a / q) * q; /* ties to even */", "double r = round(a / q) * q;"),
+    "fp8_scale_search_starts_high": ("int s = e - 10;", "int s = e - 8;"),
+    "fp8_scale_boundary_exclusive": ("while (amax > ldexp(448.0, s)) ++s;", "while (amax >= ldexp(448.0, s)) ++s;"),
+    "fp8_hidden_not_quantised": ("    quant_row(hq, c, NULL);\n", ""),
+    "fp8_gate_uses_up_row_exponent": ("gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[j]);",
+                                      "gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e1[j]);"),
+    "fp8_down_exponent_by_column": ("acc += hq[jj] * wq(w3, off, wdt, e3[i]);", "acc += hq[jj] * wq(w3, off, wdt, e3[jj % d]);"),
+    "fp8_token_row_not_quantised_in_block": ("            quant_row(aq, d, NULL);\n", ""),
+    "fp8_shared_down_read_as_one_matrix": ("size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);",
+                                           "size_t off = base3 + (size_t)i * c + (size_t)jj;"),
+    "fp8_shared_down_exponent_first_expert": ("            for (int sh = 0; sh < ns; ++sh)\n                for (int j = 0; j < cs; ++j) {",
+                                              "            for (int sh = 0; sh < 1; ++sh)\n                for (int j = 0; j < cs; ++j) {"),
 }
 
 PIN_TESTS = [
@@ -59,6 +74,13 @@ PIN_TESTS = [
     lambda: [pins.test_dispatch_combine_round_trip(k, w) for k, w in ((1, 1.0), (2, 0.5), (4, 0.25))],
     pins.test_attn_farskip_wiring_identities,
     pins.test_attn_plain_is_the_ordinary_layer,
+    fp8.test_every_e4m3_code_is_a_fixed_point,
+    fp8.test_e4m3_rounding_matches_the_library,
+    fp8.test_row_scales_brute_force,
+    fp8.test_gate_up_reduces_to_exact_on_representable_operands,
+    fp8.test_down_projection_reduces_to_the_quantised_hidden,
+    fp8.test_down_projection_with_representable_weights_is_a_matmul_of_the_quantised_hidden,
+    fp8.test_block_sums_are_the_per_row_fp8_experts,
 ]
 
 
