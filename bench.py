@@ -38,6 +38,8 @@ import torch  # noqa: E402
 from mixture_experts_layer_expert_gb300 import configs, synth  # noqa: E402
 
 METRIC = "MoE layer tokens/s, DeepSeek-V3 shape, 64K tokens; % of roofline (BF16/HBM)"
+METRIC_FP8 = "MoE layer tokens/s, FP8 E4M3 expert GEMMs; % of roofline (FP8/HBM)"
+FP8_PER_BF16 = 2.0     # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -219,9 +221,17 @@ def run_ours(args, cfg, rank, world, local):
     routed_flops = 6.0 * T * cfg.k * cfg.d * cfg.c
     routed_ms = stage_ms["routed"] / L
     achieved = routed_flops / (routed_ms / 1e3) / 1e12
-    peak = pk["bf16_tflops_sustained"]
+    fp8 = cfg.dtype == "fp8"
+    peak = pk["bf16_tflops_sustained"] * (FP8_PER_BF16 if fp8 else 1.0)
+    if fp8:   # expert GEMMs at the FP8 rate, the router at the bf16 rate
+        expert_flops = cfg.gemm_flops_per_block() * L
+        t_flops = (expert_flops / (FP8_PER_BF16 * pk["bf16_tflops"] * 1e12)
+                   + (flops - expert_flops) / (pk["bf16_tflops"] * 1e12))
+        t_roof = max(t_flops, bytes_ / (pk["hbm_gbs"] * 1e9))
+    else:
+        t_flops = flops / (pk["bf16_tflops"] * 1e12)
     line = {
-        "metric": METRIC,
+        "metric": METRIC_FP8 if fp8 else METRIC,
         "value": round(value, 1),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -231,7 +241,7 @@ def run_ours(args, cfg, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "dtype": {"bf16": "bf16", "f32": "f32", "fp8": "e4m3"}[cfg.dtype],
         "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), uniform router",
         "config": {"workload": configs.describe(cfg), "schedule": "two-stream overlap" if args.overlap else "one stream",
                    "T_per_gpu": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
@@ -241,10 +251,12 @@ def run_ours(args, cfg, rank, world, local):
                        T * cfg.d * 2 / 1e9, cfg.alg_bytes_per_block() / 1e9)},
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (routed gate/up + down, tcgen05)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": "bf16 sustained, %s" % pk_src,
+                     "frac": round(achieved / peak, 4),
+                     "peak_kind": ("fp8 = %.0f x bf16 sustained (nominal ratio), %s" % (FP8_PER_BF16, pk_src)) if fp8
+                     else "bf16 sustained, %s" % pk_src,
                      "traffic": gemm_traffic(cfg.name),
                      "flops_per_launch_pair": routed_flops, "ms_per_launch_pair": round(routed_ms, 4)},
-        "layer_roofline": {"bound": "tensor" if flops / (pk["bf16_tflops"] * 1e12) >= bytes_ / (pk["hbm_gbs"] * 1e9)
+        "layer_roofline": {"bound": "tensor" if t_flops >= bytes_ / (pk["hbm_gbs"] * 1e9)
                            else "hbm", "tokens_per_s_at_roofline": round(T / t_roof, 1),
                            "frac": round((T / (ms / 1e3)) / (T / t_roof), 4),
                            "tflops": round(flops / (ms / 1e3) / 1e12, 1),
@@ -273,7 +285,8 @@ def per_stage_timing(cfg, stack, x, steps, stream):
     idx, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
     counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
     pos, perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
-    x_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
+    x_perm = (fs.fp8_rows_empty(T * k, d, dev) if cfg.dtype == "fp8"
+              else torch.empty((T * k, d), dtype=x.dtype, device=dev))
     y_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
     s = torch.empty((T, d), dtype=torch.float32, device=dev) if cfg.n_shared else None
     L = len(stack.blocks)
@@ -335,14 +348,20 @@ def e2e_timing(cfg, stack, x, steps, stream):
 
 # ------------------------------------------------------------ CPU oracle
 
+def oracle_cfg_for(cfg):
+    import oracle
+    dt = oracle.F32 if cfg.dtype == "f32" else oracle.BF16
+    st = oracle.STORE_F32 if cfg.dtype == "f32" else oracle.STORE_BF16
+    return oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st,
+                           fp8=cfg.dtype == "fp8")
+
+
 def cpu_baseline(cfg, host_blocks, x, sample):
     import oracle
     oracle.build()
     rows = np.arange(sample)
     xs = synth.to_numpy(x[:sample])
-    dt = oracle.BF16 if cfg.dtype == "bf16" else oracle.F32
-    st = oracle.STORE_BF16 if cfg.dtype == "bf16" else oracle.STORE_F32
-    oc = oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st)
+    oc = oracle_cfg_for(cfg)
     ws = [oracle.Weights(**b) for b in host_blocks]
     t0 = time.perf_counter()
     oracle.stack(oc, ws, cfg.wiring, xs, want_logits=False)
@@ -366,9 +385,7 @@ def run_reference(args, cfg, rank, world):
     hb = [oracle.Weights(**{k: synth.to_numpy(v) for k, v in b.items()}) for b in blocks]
     del blocks
     xs = synth.to_numpy(x)
-    dt = oracle.BF16 if cfg.dtype == "bf16" else oracle.F32
-    st = oracle.STORE_BF16 if cfg.dtype == "bf16" else oracle.STORE_F32
-    oc = oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st)
+    oc = oracle_cfg_for(cfg)
     for _ in range(args.warmup):
         oracle.stack(oc, hb, cfg.wiring, xs[: max(1, T // 8)], want_logits=False)
     t0 = time.perf_counter()
@@ -377,7 +394,7 @@ def run_reference(args, cfg, rank, world):
     sec = (time.perf_counter() - t0) / args.steps
     value = T / sec
     sample = "%d of the %d tokens per step, all L=%d blocks" % (T, cfg.T, cfg.L)
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+    return {"impl": "reference", "metric": METRIC_FP8 if cfg.dtype == "fp8" else METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in)",

@@ -26,7 +26,8 @@
  *   - Row-major layouts throughout.  Activations are [rows, d] with dtype
  *     desc->dtype (bf16 or fp32); gate weights and logits are fp32; indices int32.
  *   - Pointers must be 16-byte aligned; d and c must be multiples of 64;
- *     n_shared * c_shared must be a multiple of 64.  Otherwise FS_ERR_UNSUPPORTED.
+ *     n_shared * c_shared must be a multiple of 64 (FS_FP8: d, c and c_shared
+ *     multiples of 128).  Otherwise FS_ERR_UNSUPPORTED.
  *   - Workspace: `ws` is caller-owned device scratch of at least
  *     fs_workspace_bytes(desc, L) bytes (L = 0 for the single-step calls),
  *     256-byte aligned.  Contents need not be initialised.
@@ -50,7 +51,18 @@ typedef enum {
     FS_ERR_DEVICE_STATE = 5   /* fs_get_error: a kernel recorded a device-side fault */
 } fs_status;
 
-typedef enum { FS_BF16 = 0, FS_F32 = 1 } fs_dtype;
+/* FS_FP8: the FP8 expert path (the pages run inference with FP8 quantisation
+ * and fused MoE forward kernels; experimental setup, software configuration).
+ * Activations, the router, Combine and the residual stream are as for FS_BF16;
+ * the operands of the expert GEMMs (routed and shared) are FP8 E4M3 with one
+ * power-of-two scale per row along the contraction: per token for the block
+ * input (quantised once by Dispatch), per row of the stored bf16 hidden h, per
+ * output channel for the weights.  The scale of a row x is 2^e with e the
+ * smallest integer such that max |x_i| 2^-e <= 448; the code of x_i is
+ * x_i 2^-e rounded to E4M3 (nearest, ties to even, saturating at 448).  The
+ * tensor cores take the E4M3 codes (kind::f8f6f4, fp32 accumulate) and the
+ * GEMM epilogue multiplies by the two row scales. */
+typedef enum { FS_BF16 = 0, FS_F32 = 1, FS_FP8 = 2 } fs_dtype;
 
 /* Gate rule s() applied to the top-k logits z (after the optional bias):
  *   SOFTMAX         w_s = exp(z_s) / sum over ALL experts of exp(z_j)
@@ -117,8 +129,13 @@ size_t fs_workspace_bytes_attn(const fs_layer_desc* desc, int L);
  *   bf16: tiled, [G][ceil(N/256)][K/64][256][64]: every 256-row x 64-column
  *         tile the tensor-core GEMM loads is one contiguous 32 KB block
  *         (rows past N are zero), so weight streaming reads HBM sequentially;
- *   fp32: row-major [G, N, K].
- * fs_packed_bytes gives the size (0 for invalid arguments; K % 64 == 0). */
+ *   fp32: row-major [G, N, K];
+ *   FP8:  E4M3 codes tiled as [G][ceil(N/256)][K/128][256][128] (32 KB blocks,
+ *         rows past N zero), then the G N fp32 row scales (output channel n of
+ *         group g at index g N + n).  The pack functions take the bf16 weights
+ *         and quantise each output-channel row (FS_FP8 in fs_dtype).
+ * fs_packed_bytes gives the size (0 for invalid arguments; K % 64 == 0, FP8:
+ * K % 128 == 0). */
 size_t fs_packed_bytes(int32_t G, int32_t N, int32_t K, int32_t dtype);
 
 /* Gate/up: the page's W1 (up) and W2 (gate), each [G, c, d], as one packed
@@ -145,6 +162,18 @@ fs_status fs_pack_w3(int32_t G, int32_t d, int32_t c, int32_t dtype, const void*
 fs_status fs_pack_w3_shared(int32_t n_shared, int32_t c_shared, int32_t d, int32_t dtype,
                             const void* w3s, void* w3cat, void* stream);
 
+/* FP8 row-scaled matrix [rows, cols] (the FS_FP8 activations x_perm and the
+ * output of fs_quantize_rows_fp8): rows * cols E4M3 codes, row-major, then
+ * from byte offset rows * cols rounded up to a multiple of 256 the rows fp32
+ * scales; element (r, i) = value(code[r, i]) * scale[r].  Its size in bytes,
+ * or 0 for rows < 1 or cols < 1. */
+size_t fs_fp8_rows_bytes(int64_t rows, int32_t cols);
+
+/* Quantise bf16 rows x [rows, cols] to the FP8 row-scaled matrix q (see
+ * FS_FP8): the quantisation of the hidden between the two expert GEMMs.
+ * cols % 128 == 0. */
+fs_status fs_quantize_rows_fp8(int64_t rows, int32_t cols, const void* x, void* q, void* stream);
+
 /* Router (§2.1, G(A) = s(A W_R^T)): logits z = u W_R^T + bias (fp32 accumulate;
  * bf16 operands on the tensor cores for FS_BF16, fp32 FMA for FS_F32), then the
  * top-k selection and gate weights of desc->gate.
@@ -165,7 +194,9 @@ fs_status fs_router_topk(const fs_layer_desc* desc, const void* u, const void* w
  *      x_perm [T k, d] (x_perm[p] = u[perm_src[p]]); x_perm NULL = no row copy
  *      (for fs_grouped_swiglu_gather, which gathers the rows itself).
  * An index outside [0, E) sets the device error word (reported by
- * fs_get_error) and that pair is dropped. */
+ * fs_get_error) and that pair is dropped.  FS_FP8: u is bf16 and x_perm is an
+ * FP8 row-scaled matrix [T k, d] (fs_fp8_rows_bytes(T k, d) bytes): each token
+ * row is quantised once and its codes and scale go to all of its k rows. */
 fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u,
                       int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
                       void* x_perm, void* ws, size_t ws_bytes, void* stream);
@@ -196,7 +227,10 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
  *   y_perm[p] = h W3_e^T             (fp32 accumulate, stored in desc->dtype)
  *   x_perm [T k, d], offsets [E+1] (device; the host never reads them),
  *   w13 = fs_pack_w13(E, c, d), w3 = fs_pack_w3(E, d, c) -> y_perm [T k, d].
- * bf16: persistent tcgen05/TMEM grouped GEMMs fed by TMA; fp32: fp32 FMA. */
+ * bf16: persistent tcgen05/TMEM grouped GEMMs fed by TMA; fp32: fp32 FMA.
+ * FS_FP8: x_perm is fs_dispatch's FP8 row-scaled matrix, the weights are the
+ * FP8 packs; h is stored bf16, quantised per row (fs_quantize_rows_fp8) and
+ * fed to the down GEMM as E4M3; y_perm is bf16. */
 fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets,
                             const void* w13, const void* w3, void* y_perm,
                             void* ws, size_t ws_bytes, void* stream);
@@ -207,14 +241,15 @@ fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const
  * never written or read.  u [T, d], perm_src [T k] (fs_dispatch's output),
  * offsets [E+1] -> y_perm [T k, d].  Results are bit-identical to
  * fs_dispatch + fs_grouped_swiglu.  FS_ERR_UNSUPPORTED with the CTA-pair GEMM
- * variant. */
+ * variant and for FS_FP8. */
 fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, const int32_t* perm_src,
                                    const int32_t* offsets, const void* w13, const void* w3,
                                    void* y_perm, void* ws, size_t ws_bytes, void* stream);
 
 /* Shared expert(s) (§2.1): S = sum_i MLP_shared_i(u) over all T tokens, as one
  * MLP of width n_shared c_shared.  u [T, d] -> s_out [T, d] in fp32 (S is only
- * ever added into the residual stream, so it keeps fp32 accumulator precision). */
+ * ever added into the residual stream, so it keeps fp32 accumulator precision).
+ * FS_FP8: u is bf16 and is quantised per token in ws; the weights are FP8 packs. */
 fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void* w13_shared,
                            const void* w3_shared, void* s_out, void* ws, size_t ws_bytes,
                            void* stream);

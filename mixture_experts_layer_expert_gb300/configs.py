@@ -24,7 +24,8 @@ class LayerConfig:
     c_shared: int        # shared expert width
     L: int               # FarSkip blocks
     gate: str            # softmax | softmax_renorm | sigmoid | sigmoid_norm
-    dtype: str           # "bf16" (bf16 storage, fp32 accumulate) or "f32"
+    dtype: str           # "bf16" (bf16 storage, fp32 accumulate), "f32", or "fp8"
+                         # (bf16 storage, FP8 E4M3 expert GEMM operands with row scales)
     zipf_s: float | None = None   # router-bias skew (Zipf exponent) or None
     wiring: str = "partial"
     seed: int = 0
@@ -46,11 +47,11 @@ class LayerConfig:
     def alg_bytes_per_block(self) -> float:
         """Algorithmic HBM bytes of one block: read u and o_prev, write o* and o,
         read every expert's, the shared experts' and the router's weights once."""
-        es = 2 if self.dtype == "bf16" else 4
+        es = 4 if self.dtype == "f32" else 2
+        wes = 1 if self.dtype == "fp8" else es        # FP8 expert weights: one byte per element
         T, d = self.T, self.d
         act = 4.0 * T * d * es
-        w = (3.0 * self.E * d * self.c + 3.0 * self.n_shared * d * self.c_shared
-             + self.E * d) * es
+        w = (3.0 * self.E * d * self.c + 3.0 * self.n_shared * d * self.c_shared) * wes + self.E * d * es
         return act + w
 
 
@@ -68,6 +69,9 @@ CONFIGS = {
     "v3_decode": LayerConfig("v3_decode", T=1024, d=7168, E=256, k=8, c=2048, n_shared=1,
                              c_shared=2048, L=1, gate="sigmoid_norm", dtype="bf16"),
 }
+# The FP8 expert path on the same shapes (the pages' inference precision).
+for _name in ("v2lite", "qwen3", "scout", "v3", "v3_decode"):
+    CONFIGS[_name + "_fp8"] = CONFIGS[_name].with_(name=_name + "_fp8", dtype="fp8")
 
 
 def describe(cfg: LayerConfig) -> str:

@@ -13,6 +13,7 @@
 
 #include "../../include/fs.h"
 #include "common.cuh"
+#include "fp8.cuh"
 #include "kernels.h"
 
 namespace fs {
@@ -80,23 +81,29 @@ static fs_status check_desc(const fs_layer_desc* d) {
     if (!d) return FS_ERR_INVALID_ARG;
     if (d->T < 1 || d->d < 1 || d->E < 1 || d->k < 1 || d->c < 1 || d->n_shared < 0) return FS_ERR_INVALID_ARG;
     if (d->k > d->E) return FS_ERR_INVALID_ARG;
-    if (d->dtype != FS_BF16 && d->dtype != FS_F32) return FS_ERR_INVALID_ARG;
+    if (d->dtype != FS_BF16 && d->dtype != FS_F32 && d->dtype != FS_FP8) return FS_ERR_INVALID_ARG;
     if (d->gate < FS_GATE_SOFTMAX || d->gate > FS_GATE_SIGMOID_NORM) return FS_ERR_INVALID_ARG;
     if (d->n_shared > 0 && d->c_shared < 1) return FS_ERR_INVALID_ARG;
     if (d->d % 64 || d->c % 64) return FS_ERR_UNSUPPORTED;
     if (d->n_shared > 0 && d->c_shared % 64) return FS_ERR_UNSUPPORTED;
+    if (d->dtype == FS_FP8 && (d->d % 128 || d->c % 128 || (d->n_shared > 0 && d->c_shared % 128)))
+        return FS_ERR_UNSUPPORTED;
     if (d->E > kMaxExperts || d->k > kMaxTopK) return FS_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(d->T) * d->k;
     if (rows > 0x7fffffffLL - 1024) return FS_ERR_UNSUPPORTED;
     return FS_OK;
 }
 
-static inline int elem_bytes(const fs_layer_desc* d) { return d->dtype == FS_BF16 ? 2 : 4; }
+// Activations (GEMM inputs u_k, y_perm, u_next) are bf16 for FS_BF16 and FS_FP8
+// (whose expert operands are quantised inside the path), fp32 for FS_F32.
+static inline int elem_bytes(const fs_layer_desc* d) { return d->dtype == FS_F32 ? 4 : 2; }
+static inline int act_dtype(const fs_layer_desc* d) { return d->dtype == FS_F32 ? FS_F32 : FS_BF16; }
+static inline bool is_fp8(const fs_layer_desc* d) { return d->dtype == FS_FP8; }
 
 // ------------------------------------------------------------- workspace
 struct Layout {
     // single-step regions (L = 0)
-    size_t logits, disp, plan_z, plan_r, h_r, plan_s, h_s, plan_a, end0;
+    size_t logits, disp, plan_z, plan_r, h_r, hq_r, plan_s, h_s, hq_s, uq, plan_a, end0;
     // stack regions (L >= 1)
     size_t topk_idx, topk_w, counts, offsets, pos, perm, x_perm, y_perm, s_out, ring[3], star[2], ubuf[2], end;
     size_t att, hbuf, abuf[2], end_attn;   // attention wirings only: A_k output, h_k, attention inputs
@@ -116,9 +123,13 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.disp = take(dispatch_ws_bytes(d->T, d->E));
     l.plan_z = take(4 * sizeof(int));
     l.plan_r = take(2 * (E + 1) * sizeof(int));
+    const bool f8 = is_fp8(d);
     l.h_r = take(rows * d->c * es);
+    l.hq_r = take(f8 ? fp8_rows_bytes(static_cast<long long>(rows), d->c) : 0);   // FP8: quantised h
     l.plan_s = take(4 * sizeof(int));
     l.h_s = take(T * cw * es);
+    l.hq_s = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), static_cast<int>(cw)) : 0);
+    l.uq = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), d->d) : 0);    // FP8: quantised u_k
     l.plan_a = take(4 * sizeof(int));
     l.end0 = o;
     l.topk_idx = take(rows * 4);
@@ -127,7 +138,7 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.offsets = take((E + 1) * 4);
     l.pos = take(rows * 4);
     l.perm = take(rows * 4);
-    l.x_perm = take(rows * dm * es);
+    l.x_perm = take(f8 ? fp8_rows_bytes(static_cast<long long>(rows), d->d) : rows * dm * es);
     l.y_perm = take(rows * dm * es);
     l.s_out = take(cw ? T * dm * 4 : 0);     // S in fp32
     // The residual stream between blocks is fp32; the last block writes the
@@ -175,7 +186,7 @@ static OverlapLayout layout_overlap(const fs_layer_desc* d, int L) {
         l.offsets[i] = on ? take((E + 1) * 4) : 0;
         l.pos[i] = on ? take(rows * 4) : 0;
         l.perm[i] = on ? take(rows * 4) : 0;
-        l.x_perm[i] = on ? take(rows * dm * es) : 0;
+        l.x_perm[i] = on ? take(is_fp8(d) ? fp8_rows_bytes(static_cast<long long>(rows), d->d) : rows * dm * es) : 0;
         l.s_out[i] = on ? take(T * dm * 4) : 0;
         l.ostar[i] = on ? take(T * dm * 4) : 0;
         l.oring[i] = on ? take(T * dm * 4) : 0;
@@ -207,7 +218,7 @@ static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* 
     const Layout l = layout(d, 0);
     float* z = logits ? logits : at<float>(ws, l.logits);
     int* plan = at<int>(ws, l.plan_z);
-    if (d->dtype == FS_BF16) {
+    if (d->dtype != FS_F32) {
         const int bm = tc_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
         FS_TRY(launch_tc_gemm(EPI_F32, u, d->T, w_r, 1, d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E,
@@ -222,12 +233,14 @@ static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* 
     return FS_OK;
 }
 
+// FS_FP8: x_perm is an FP8 row-scaled matrix; with u_q set the quantised u_k
+// is also written there (the shared experts' operand).
 static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const void* u, int32_t* counts,
                                int32_t* offsets, int32_t* pos, int32_t* perm, void* x_perm, void* ws,
-                               cudaStream_t st) {
+                               cudaStream_t st, void* u_q = nullptr) {
     const Layout l = layout(d, 0);
     FS_TRY(launch_dispatch(idx, u, d->T, d->d, d->E, d->k, elem_bytes(d), counts, offsets, pos, perm, x_perm,
-                           at<int32_t>(ws, l.disp), st));
+                           at<int32_t>(ws, l.disp), st, is_fp8(d), is_fp8(d) ? u_q : nullptr));
     return FS_OK;
 }
 
@@ -236,10 +249,23 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 // y stored in the activation type (y_f32 = false) or in fp32.  With gather
 // non-null, GEMM row p reads row gather[p] of x (x has x_rows rows): the
 // Dispatch permutation applied inside the first GEMM's operand loads.
+// FS_FP8: x is an FP8 row-scaled matrix [x_rows, d], the weights FP8 packs; h
+// (bf16) is quantised per row into hq before the down GEMM.
 static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_rows, const int32_t* gather, int rows,
                              const int32_t* offsets, int G, int cw, const void* w13, const void* w3, void* y,
-                             bool y_f32, int* plan, void* h, cudaStream_t st) {
-    if (d->dtype == FS_BF16) {
+                             bool y_f32, int* plan, void* h, void* hq, cudaStream_t st) {
+    if (is_fp8(d)) {
+        const int bm = tc_block_m_f8();
+        const int max_mt = ceil_div(rows, bm) + G;
+        const float* xs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x) + fp8_scale_offset(x_rows, d->d));
+        const float* hs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(hq) + fp8_scale_offset(rows, cw));
+        FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
+        FS_TRY(launch_tc_gemm_f8(EPI_SWIGLU, x, x_rows, xs, w13, packed_scales_fp8(w13, G, 2 * cw, d->d), G, 2 * cw,
+                                 d->d, plan, max_mt, h, cw, cw, st));
+        FS_TRY(launch_quant_rows(h, rows, cw, hq, st));
+        FS_TRY(launch_tc_gemm_f8(y_f32 ? EPI_F32 : EPI_BF16, hq, rows, hs, w3, packed_scales_fp8(w3, G, d->d, cw), G,
+                                 d->d, cw, plan, max_mt, y, d->d, d->d, st));
+    } else if (d->dtype == FS_BF16) {
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
@@ -264,7 +290,7 @@ static fs_status routed_impl(const fs_layer_desc* d, const void* x_perm, const i
     const Layout l = layout(d, 0);
     const int rows = d->T * d->k;
     return swiglu_impl(d, x_perm, rows, nullptr, rows, offsets, d->E, d->c, w13, w3, y_perm, false,
-                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), st);
+                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), at<void>(ws, l.hq_r), st);
 }
 
 static fs_status routed_gather_impl(const fs_layer_desc* d, const void* u, const int32_t* perm_src,
@@ -272,14 +298,21 @@ static fs_status routed_gather_impl(const fs_layer_desc* d, const void* u, const
                                     cudaStream_t st) {
     const Layout l = layout(d, 0);
     return swiglu_impl(d, u, d->T, perm_src, d->T * d->k, offsets, d->E, d->c, w13, w3, y_perm, false,
-                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), st);
+                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), nullptr, st);
 }
 
+// FS_FP8: the GEMMs read the quantised u_k in ws (written by the stack's
+// Dispatch when u_q_ready, else quantised here from u).
 static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* w13s, const void* w3s, void* s_out,
-                             void* ws, cudaStream_t st) {
+                             void* ws, cudaStream_t st, bool u_q_ready = false) {
     const Layout l = layout(d, 0);
-    return swiglu_impl(d, u, d->T, nullptr, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
-                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), st);
+    const void* x = u;
+    if (is_fp8(d)) {
+        x = at<void>(ws, l.uq);
+        if (!u_q_ready) FS_TRY(launch_quant_rows(u, d->T, d->d, at<void>(ws, l.uq), st));
+    }
+    return swiglu_impl(d, x, d->T, nullptr, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
+                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), at<void>(ws, l.hq_s), st);
 }
 
 static fs_status combine_impl(const fs_layer_desc* d, const void* y_perm, const int32_t* pos, const float* w,
@@ -288,7 +321,7 @@ static fs_status combine_impl(const fs_layer_desc* d, const void* y_perm, const 
                               int k_override = -1) {
     FS_TRY(launch_combine(y_perm, pos, w, o_prev, prev_dtype == FS_BF16, s, extra, o_partial, o_full,
                           out_dtype == FS_BF16, u_next, u_src, u_full, d->T, d->d, k_override >= 0 ? k_override : d->k,
-                          d->dtype == FS_BF16, st));
+                          d->dtype != FS_F32, st));
     return FS_OK;
 }
 
@@ -297,7 +330,7 @@ static fs_status attn_impl(const fs_layer_desc* d, const void* a, const void* w_
                            cudaStream_t st) {
     const Layout l = layout(d, 0);
     int* plan = at<int>(ws, l.plan_a);
-    if (d->dtype == FS_BF16) {
+    if (d->dtype != FS_F32) {
         const int bm = tc_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
         FS_TRY(launch_tc_gemm(EPI_F32, a, d->T, w_att, 1, d->d, d->d, plan, ceil_div(d->T, bm) + 1, out, d->d, d->d,
@@ -344,39 +377,70 @@ size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L) {
     return layout_overlap(desc, L).end;
 }
 
+static inline bool valid_dtype(int32_t t) { return t == FS_BF16 || t == FS_F32 || t == FS_FP8; }
+
 fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype, const void* w1, const void* w2, void* w13,
                       void* stream) {
-    if (G < 1 || c < 1 || d < 1 || (dtype != FS_BF16 && dtype != FS_F32)) return FS_ERR_INVALID_ARG;
-    if (c % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    if (G < 1 || c < 1 || d < 1 || !valid_dtype(dtype)) return FS_ERR_INVALID_ARG;
+    const int q = dtype == FS_FP8 ? 128 : 64;
+    if (c % q || d % q) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(w1));
     FS_CHECK(need(w2));
     FS_CHECK(need(w13));
-    FS_TRY(launch_pack_w13(G, c, d, dtype == FS_BF16 ? 2 : 4, w1, w2, w13, static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == FS_FP8)
+        FS_TRY(launch_pack_w13_fp8(G, c, d, w1, w2, w13, st));
+    else
+        FS_TRY(launch_pack_w13(G, c, d, dtype == FS_BF16 ? 2 : 4, w1, w2, w13, st));
     return FS_OK;
 }
 
 size_t fs_packed_bytes(int32_t G, int32_t N, int32_t K, int32_t dtype) {
-    if (G < 1 || N < 1 || K < 1 || K % 64 || (dtype != FS_BF16 && dtype != FS_F32)) return 0;
+    if (G < 1 || N < 1 || K < 1 || K % 64 || !valid_dtype(dtype)) return 0;
+    if (dtype == FS_FP8) return K % 128 ? 0 : packed_bytes_fp8(G, N, K);
     return packed_bytes(G, N, K, dtype == FS_BF16 ? 2 : 4);
 }
 
 fs_status fs_pack_w3(int32_t G, int32_t d, int32_t c, int32_t dtype, const void* w3, void* w3p, void* stream) {
-    if (G < 1 || c < 1 || d < 1 || (dtype != FS_BF16 && dtype != FS_F32)) return FS_ERR_INVALID_ARG;
-    if (c % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    if (G < 1 || c < 1 || d < 1 || !valid_dtype(dtype)) return FS_ERR_INVALID_ARG;
+    const int q = dtype == FS_FP8 ? 128 : 64;
+    if (c % q || d % q) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(w3));
     FS_CHECK(need(w3p));
-    FS_TRY(launch_pack_w3(G, d, c, dtype == FS_BF16 ? 2 : 4, w3, w3p, static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == FS_FP8)
+        FS_TRY(launch_pack_w3_fp8(G, d, c, w3, w3p, st));
+    else
+        FS_TRY(launch_pack_w3(G, d, c, dtype == FS_BF16 ? 2 : 4, w3, w3p, st));
     return FS_OK;
 }
 
 fs_status fs_pack_w3_shared(int32_t n_shared, int32_t c_shared, int32_t d, int32_t dtype, const void* w3s,
                             void* w3cat, void* stream) {
-    if (n_shared < 1 || c_shared < 1 || d < 1 || (dtype != FS_BF16 && dtype != FS_F32)) return FS_ERR_INVALID_ARG;
-    if (c_shared % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    if (n_shared < 1 || c_shared < 1 || d < 1 || !valid_dtype(dtype)) return FS_ERR_INVALID_ARG;
+    const int q = dtype == FS_FP8 ? 128 : 64;
+    if (c_shared % q || d % q) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(w3s));
     FS_CHECK(need(w3cat));
-    FS_TRY(launch_pack_w3_shared(n_shared, c_shared, d, dtype == FS_BF16 ? 2 : 4, w3s, w3cat,
-                                 static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == FS_FP8)
+        FS_TRY(launch_pack_w3_shared_fp8(n_shared, c_shared, d, w3s, w3cat, st));
+    else
+        FS_TRY(launch_pack_w3_shared(n_shared, c_shared, d, dtype == FS_BF16 ? 2 : 4, w3s, w3cat, st));
+    return FS_OK;
+}
+
+size_t fs_fp8_rows_bytes(int64_t rows, int32_t cols) {
+    if (rows < 1 || cols < 1) return 0;
+    return fp8_rows_bytes(rows, cols);
+}
+
+fs_status fs_quantize_rows_fp8(int64_t rows, int32_t cols, const void* x, void* q, void* stream) {
+    if (rows < 1 || cols < 1) return FS_ERR_INVALID_ARG;
+    if (cols % 128 || rows > 0x7fffffffLL) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(x));
+    FS_CHECK(need(q));
+    FS_TRY(launch_quant_rows(x, rows, cols, q, static_cast<cudaStream_t>(stream)));
     return FS_OK;
 }
 
@@ -426,7 +490,7 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
         return FS_ERR_WORKSPACE;
     }
     FS_TRY(launch_dispatch_noalloc(topk_idx, u, desc->T, desc->d, desc->E, desc->k, elem_bytes(desc), counts, offsets,
-                                   pos, perm_src, x_perm, static_cast<cudaStream_t>(stream)));
+                                   pos, perm_src, x_perm, static_cast<cudaStream_t>(stream), is_fp8(desc)));
     return FS_OK;
 }
 
@@ -453,6 +517,7 @@ fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, con
     FS_CHECK(need(w3));
     FS_CHECK(need(y_perm));
     FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    if (is_fp8(desc)) return FS_ERR_UNSUPPORTED;
     if (desc->dtype == FS_BF16 && !tc_gather_supported()) return FS_ERR_UNSUPPORTED;
     return routed_gather_impl(desc, u, perm_src, offsets, w13, w3, y_perm, ws, static_cast<cudaStream_t>(stream));
 }
@@ -535,14 +600,15 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
     void* y_perm = at<void>(ws, l.y_perm);
     void* s_out = desc->n_shared > 0 ? at<void>(ws, l.s_out) : nullptr;
 
-    // Row gathering inside the gate/up GEMM (tile::gather4 moves 512 B per TMA op)
-    // is issue-bound on the tensor-core path; the separate copy runs near HBM peak.
-    const bool gather = false;
+    // The stack copies rows in Dispatch: gathering them inside the gate/up GEMM
+    // (tile::gather4 moves 512 B per TMA op) is issue-bound on the tensor-core
+    // path, and the separate copy runs near HBM peak.
     const void* u = x;        // u_k   (= o_{k-1}* in the page's notation), activation type
     const void* o_prev = x;   // o_{k-1}: the caller's x for k = 1, then the fp32 residual stream
     const void* a_in = x;     // attention input (attention wirings), activation type
-    int prev_dtype = desc->dtype;
+    int prev_dtype = act_dtype(desc);
     float* att = at<float>(ws, l.att);
+    void* u_q = is_fp8(desc) && desc->n_shared > 0 ? at<void>(ws, layout(desc, 0).uq) : nullptr;
     for (int b = 1; b <= L; ++b) {
         const fs_block_weights& bw = blocks[b - 1];
         const bool last = (b == L);
@@ -550,7 +616,7 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
         void* os_k = last ? o_partial : at<void>(ws, l.star[(b - 1) % l.nstar]);
         void* u_next = last ? nullptr : at<void>(ws, l.ubuf[(b - 1) % l.nu]);
         void* a_next = last ? nullptr : at<void>(ws, l.abuf[(b - 1) & 1]);
-        const int out_dtype = last ? desc->dtype : FS_F32;
+        const int out_dtype = last ? act_dtype(desc) : FS_F32;
         const void* base = o_prev;          // residual the MoE outputs are added to
         int base_dtype = prev_dtype;
         const float* extra = nullptr;
@@ -570,9 +636,9 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
             }
         }
         FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
-        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st));
+        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st, u_q));
         FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
-        if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st));
+        if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st, u_q != nullptr));
         if (wiring == FS_WIRE_ATTN_FARSKIP) {
             // next attention input bf16(o_k*) = bf16(o_k - R_k), next MoE input bf16(o_k)
             FS_CHECK(combine_impl(desc, y_perm, pos, w, base, base_dtype, s_out, extra, os_k, o_k, out_dtype, a_next,
@@ -624,8 +690,9 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
     cudaEvent_t evD = ev[0], evU = ev[1], evA = ev[2];
     cudaStream_t sa = static_cast<cudaStream_t>(stream);     // routed experts + combine
     cudaStream_t sb = static_cast<cudaStream_t>(stream2);    // router, dispatch, shared expert, o_k*
-    const int act = desc->dtype;
+    const int act = act_dtype(desc);
     void* y_perm = at<void>(ws, l.y_perm);
+    void* u_q = is_fp8(desc) && desc->n_shared > 0 ? at<void>(ws, layout(desc, 0).uq) : nullptr;
 
     // fork: stream2 starts after everything already queued on stream (x ready)
     FS_TRY(cudaEventRecord(evA, sa));
@@ -650,9 +717,9 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
         void* u_next = last ? nullptr : at<void>(ws, l.ubuf[sl]);
         // ---- stream2: everything of block b that does not need the routed experts
         FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, sb));
-        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, sb));
+        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, sb, u_q));
         FS_TRY(cudaEventRecord(evD, sb));
-        if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, sb));
+        if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, sb, u_q != nullptr));
         if (b > 1) FS_TRY(cudaStreamWaitEvent(sb, evA, 0));       // o_{b-1} from block b-1's combine
         // o_b* = o_{b-1} + S_b (fp32) and the next input (partial: o_b*, outdated: o_{b-1})
         FS_TRY(launch_combine(nullptr, nullptr, nullptr, o_prev, prev_dtype == FS_BF16, s_out, nullptr, nullptr, ostar,

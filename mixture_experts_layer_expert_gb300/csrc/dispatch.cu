@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "fp8.cuh"
 #include "kernels.h"
 
 namespace fs {
@@ -187,6 +188,53 @@ dispatch_copy_kernel(const uint4* __restrict__ u, int T, int row_vecs, int k, co
     }
 }
 
+// FP8 expert path: one warp per token quantises u[t] once (one power-of-two
+// scale for the row) and writes its E4M3 codes to every slot's row of x_q and,
+// when u_q is set, to row t of u_q (the shared experts' operand); each row's
+// scale goes with it.
+__global__ void __launch_bounds__(kCopyWarps * 32)
+dispatch_copy_fp8_kernel(const uint4* __restrict__ u, int T, int d, int k, const int32_t* __restrict__ pos,
+                         uint8_t* __restrict__ x_q, float* __restrict__ x_scale, uint8_t* __restrict__ u_q,
+                         float* __restrict__ u_scale) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kCopyWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int nv = d / 8;
+    const int my_p = lane < k ? pos[static_cast<long long>(t) * k + lane] : -1;
+    const uint4* src = u + static_cast<long long>(t) * nv;
+    float amax = 0.0f;
+    for (int v = lane; v < nv; v += 32) amax = fmaxf(amax, absmax_bf16x8(__ldg(src + v)));
+    const RowQuant rq = row_quant(warp_max(amax));
+    for (int v0 = 0; v0 < nv; v0 += 4 * 32) {
+        uint2 c[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int v = v0 + j * 32 + lane;
+            if (v < nv) c[j] = quant_bf16x8(__ldg(src + v), rq);
+        }
+        for (int s = 0; s < k; ++s) {
+            const int p = __shfl_sync(0xffffffffu, my_p, s);
+            if (p < 0) continue;
+            uint2* dst = reinterpret_cast<uint2*>(x_q + static_cast<long long>(p) * d);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int v = v0 + j * 32 + lane;
+                if (v < nv) dst[v] = c[j];
+            }
+        }
+        if (u_q) {
+            uint2* dst = reinterpret_cast<uint2*>(u_q + static_cast<long long>(t) * d);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int v = v0 + j * 32 + lane;
+                if (v < nv) dst[v] = c[j];
+            }
+        }
+    }
+    if (my_p >= 0) x_scale[my_p] = rq.scale;
+    if (u_q && lane == 0) u_scale[t] = rq.scale;
+}
+
 static cudaError_t set_smem_attr(const void* fn, size_t bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
@@ -194,7 +242,7 @@ static cudaError_t set_smem_attr(const void* fn, size_t bytes) {
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
-                            int32_t* scratch, cudaStream_t st) {
+                            int32_t* scratch, cudaStream_t st, bool fp8, void* u_q) {
     const int nc = n_chunks(T);
     int* err = dev_error_ptr();
     dispatch_count_kernel<<<nc, kChunk, E * sizeof(int32_t), st>>>(topk_idx, T, E, k, scratch, err);
@@ -213,6 +261,16 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (!x_perm) return cudaSuccess;     // the caller gathers rows itself (no permuted copy)
+    if (fp8) {
+        const long long rows = static_cast<long long>(T) * k;
+        uint8_t* xq = static_cast<uint8_t*>(x_perm);
+        uint8_t* uq = static_cast<uint8_t*>(u_q);
+        dispatch_copy_fp8_kernel<<<(T + kCopyWarps - 1) / kCopyWarps, kCopyWarps * 32, 0, st>>>(
+            reinterpret_cast<const uint4*>(u), T, d, k, pos, xq, reinterpret_cast<float*>(xq + fp8_scale_offset(rows, d)),
+            uq, uq ? reinterpret_cast<float*>(uq + fp8_scale_offset(T, d)) : nullptr);
+        count_launch();
+        return cudaGetLastError();
+    }
     const int row_vecs = d * elem_bytes / 16;
     dispatch_copy_kernel<<<(T + kCopyWarps - 1) / kCopyWarps, kCopyWarps * 32, 0, st>>>(
         reinterpret_cast<const uint4*>(u), T, row_vecs, k, pos, reinterpret_cast<uint4*>(x_perm));
@@ -250,11 +308,12 @@ static cudaError_t dispatch_scratch_address(int32_t** out) {
 
 cudaError_t launch_dispatch_noalloc(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
-                                    void* x_perm, cudaStream_t st) {
+                                    void* x_perm, cudaStream_t st, bool fp8) {
     int32_t* scratch = nullptr;
     cudaError_t e = dispatch_scratch_address(&scratch);
     if (e != cudaSuccess) return e;
-    return launch_dispatch(topk_idx, u, T, d, E, k, elem_bytes, counts, offsets, pos, perm_src, x_perm, scratch, st);
+    return launch_dispatch(topk_idx, u, T, d, E, k, elem_bytes, counts, offsets, pos, perm_src, x_perm, scratch, st,
+                           fp8, nullptr);
 }
 
 }  // namespace fs

@@ -1,6 +1,9 @@
 // gemm_tc.cu -- persistent grouped GEMM on the 5th-generation tensor cores
-// (tcgen05.mma kind::f16, bf16 operands, fp32 accumulators in TMEM), operands
-// staged in shared memory by TMA with the 128-byte swizzle.
+// (tcgen05.mma kind::f16 with bf16 operands, or kind::f8f6f4 with FP8 E4M3
+// operands; fp32 accumulators in TMEM), operands staged in shared memory by TMA
+// with the 128-byte swizzle.  A stage is 128 bytes of K per row either way (64
+// bf16 or 128 E4M3 elements); FP8 rows carry power-of-two scales (one per A row,
+// one per B row) that the epilogue applies to the fp32 accumulator.
 //
 // One GEMM shape serves every dense contraction of the MoE layer
 // ("FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
@@ -62,7 +65,9 @@ struct Args {
     int* err;          // device error word
     const int* gather_rows;  // A row of GEMM row p = gather_rows[p] (tile::gather4), or nullptr
     int gather_limit;        // entries of gather_rows
-    int b_blocked;           // B in the tiled weight layout [G][n_tiles][K/64][256][64] (3D map)
+    int b_blocked;           // B in the tiled weight layout [G][n_tiles][K/BK][256][128 bytes] (3D map)
+    const float* a_scale;    // FP8: scale of A row p (a_scale[p])
+    const float* b_scale;    // FP8: scale of B row n of group g (b_scale[g N + n])
 };
 
 struct Tile {
@@ -99,12 +104,31 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const in
 
 // Epilogue of one accumulator tile for the thread owning TMEM lane `r` of its
 // CTA (row a_row + r of the output), columns of half `half` of the tile.
-template <int EPI>
-__device__ __forceinline__ void epilogue_tile(uint32_t tbase, int a_row, int rows_valid, int n, int r, int half,
+// v[j] <- (v[j] * sa) * sb[j] for 32 fp32 accumulator columns.
+__device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float* sb) {
+    const float4* s4 = reinterpret_cast<const float4*>(sb);
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 b = __ldg(s4 + q4);
+        const float f[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[4 * q4 + i] = __float_as_uint((__uint_as_float(v[4 * q4 + i]) * sa) * f[i]);
+    }
+}
+
+// With F8 the accumulator is scaled by the A row's and the B rows' scales:
+// (acc * a_scale[row]) * b_scale[g N + col].
+template <int EPI, bool F8 = false>
+__device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, int rows_valid, int n, int r, int half,
                                               const Args& args) {
-    const Tile tl{0, 0, n, a_row, rows_valid, 0};
+    const Tile tl{g, 0, n, a_row, rows_valid, 0};
     const bool row_ok = r < tl.rows_valid;
     const long long orow = static_cast<long long>(tl.a_row + r);
+    float sa = 1.0f;
+    if constexpr (F8) {
+        if (row_ok) sa = __ldg(args.a_scale + orow);
+    }
+    const float* sb = F8 ? args.b_scale + static_cast<long long>(g) * args.N + tl.n * BN : nullptr;
     if constexpr (EPI == EPI_SWIGLU) {
         // packed tile columns: [gate 64 | up 64] x 2 -> 128 expert columns
         const int rem = args.N - tl.n * BN;
@@ -118,6 +142,20 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int a_row, int row
                 tmem_ld32(tbase + g2 * 128 + 64 + j0, uv);
                 tmem_ld_wait();
                 if (row_ok) {
+                    if constexpr (F8) {
+                        const float4* sg4 = reinterpret_cast<const float4*>(sb + g2 * 128 + j0);
+                        const float4* su4 = reinterpret_cast<const float4*>(sb + g2 * 128 + 64 + j0);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            const float4 a = __ldg(sg4 + q4), b = __ldg(su4 + q4);
+                            const float fg[4] = {a.x, a.y, a.z, a.w}, fu[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                gv[4 * q4 + i] = __float_as_uint((__uint_as_float(gv[4 * q4 + i]) * sa) * fg[i]);
+                                uv[4 * q4 + i] = __float_as_uint((__uint_as_float(uv[4 * q4 + i]) * sa) * fu[i]);
+                            }
+                        }
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -143,6 +181,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int a_row, int row
             tmem_ld32(tbase + c0, v);
             tmem_ld_wait();
             if (row_ok) {
+                if constexpr (F8) scale_cols32(v, sa, sb + c0);
                 uint32_t pk[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
@@ -165,6 +204,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int a_row, int row
             tmem_ld32(tbase + c0, v);
             tmem_ld_wait();
             if (row_ok) {
+                if constexpr (F8) scale_cols32(v, sa, sb + c0);
                 float* dst = Z + orow * args.ldo + tl.n * BN + c0;
                 const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
                 if (vec && nv == 32) {
@@ -179,10 +219,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int a_row, int row
     }
 }
 
-template <int EPI>
+template <int EPI, bool F8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const Args args) {
+    constexpr int BKE = F8 ? 128 : BK;     // K elements per stage (128 bytes per row)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -229,9 +270,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         total_mtiles = 0;
     }
     const int total = total_mtiles * args.n_tiles;
-    const int num_kb = args.K / BK;
+    const int num_kb = args.K / BKE;
 
-    if (warp == 0 && args.gather_rows != nullptr) {
+    if (!F8 && warp == 0 && args.gather_rows != nullptr) {
         // ----------------------------------------------- producer, gathered A
         // The whole warp: lane l fetches rows 4l .. 4l+3 of each A tile with one
         // tile::gather4 per k-block (rows of the token matrix named by
@@ -299,11 +340,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     uint8_t* sa = smem + stage * STAGE_BYTES;
-                    tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, tl.a_row);
+                    tma_load_2d(smem_u32(sa), &tmA, fb, kb * BKE, tl.a_row);
                     if (args.b_blocked)
                         tma_load_3d(smem_u32(sa + A_STAGE), &tmB, fb, 0, 0, (tl.g * args.n_tiles + tl.n) * num_kb + kb);
                     else
-                        tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, tl.b_row);
+                        tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BKE, tl.b_row);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -324,7 +365,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -342,10 +383,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint64_t adesc = smem_desc_sw128(smem_u32(sa));
                     const uint64_t bdesc = smem_desc_sw128(smem_u32(sa + A_STAGE));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // +32 bytes along K inside the 128-byte swizzle row = +2 in the >>4 address field
-                        tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
-                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // one MMA takes 32 bytes of K (16 bf16 or 32 E4M3): +32 bytes inside the
+                        // 128-byte swizzle row = +2 in the >>4 address field
+                        if constexpr (F8)
+                            tc_mma_f8(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
+                                        (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -375,7 +420,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            epilogue_tile<EPI>(tbase, tl.a_row, tl.rows_valid, tl.n, r, half, args);
+            epilogue_tile<EPI, F8>(tbase, tl.g, tl.a_row, tl.rows_valid, tl.n, r, half, args);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
@@ -567,7 +612,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            epilogue_tile<EPI>(tbase, a_row, rows_valid, tl.n, r, half, args);
+            epilogue_tile<EPI>(tbase, tl.g, a_row, rows_valid, tl.n, r, half, args);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(map_to_cta(smem_u32(&tempty[acc]), 0));
@@ -657,32 +702,39 @@ static cudaError_t get_encode() {
     return cudaSuccess;
 }
 
-// 2D bf16 tensor map over a [rows, cols] row-major matrix with a box of
-// box_rows x 64 elements and the 128-byte swizzle.
-static cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+// 2D tensor map over a [rows, cols] row-major matrix of bf16 (f8 = false) or
+// 8-bit codes (f8 = true) with a box of box_rows x 128 bytes and the 128-byte
+// swizzle.
+static cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows,
+                            bool f8 = false) {
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
+    const int es = f8 ? 1 : 2;
     cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * es};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 3D bf16 tensor map over the tiled weight layout [nblocks][256][64] (each
-// block a contiguous 32 KB [256 rows x 64 K] tile) with a box of box_rows x 64.
-static cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows) {
+// 3D tensor map over the tiled weight layout [nblocks][256][128 bytes] (each
+// block a contiguous 32 KB tile of 256 rows) with a box of box_rows x 128 bytes.
+static cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows,
+                                   bool f8 = false) {
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
-    cuuint64_t gdim[3] = {64, 256, static_cast<cuuint64_t>(nblocks)};
+    const int es = f8 ? 1 : 2;
+    cuuint64_t gdim[3] = {static_cast<cuuint64_t>(128 / es), 256, static_cast<cuuint64_t>(nblocks)};
     cuuint64_t gstride[2] = {128, 256 * 128};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = g_encode(m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -759,6 +811,8 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.gather_rows = gather_rows;
     args.gather_limit = gather_limit;
     args.b_blocked = b_blocked ? 1 : 0;
+    args.a_scale = nullptr;
+    args.b_scale = nullptr;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -775,6 +829,70 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     }
     count_launch();
     return cudaGetLastError();
+}
+
+template <int EPI>
+static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const float* a_scale, const void* B,
+                                     const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles,
+                                     void* out, long long ldo, int out_cols, cudaStream_t st) {
+    static bool attr_set = false;
+    cudaError_t e;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    if (K % 128 || N % 128) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    e = make_map(&ta, A, a_rows, K, tc::BM, true);
+    if (e != cudaSuccess) return e;
+    const int n_tiles = (N + tc::BN - 1) / tc::BN;
+    e = make_map_blocked(&tb, B, static_cast<long long>(G) * n_tiles * (K / 128), tc::BN, true);
+    if (e != cudaSuccess) return e;
+    tc::Args args;
+    args.plan = plan;
+    args.G = G;
+    args.N = N;
+    args.K = K;
+    args.n_tiles = n_tiles;
+    args.max_mtiles = max_mtiles;
+    args.out = out;
+    args.ldo = ldo;
+    args.out_cols = out_cols;
+    args.err = dev_error_ptr();
+    args.gather_rows = nullptr;
+    args.gather_limit = 0;
+    args.b_blocked = 1;
+    args.a_scale = a_scale;
+    args.b_scale = b_scale;
+    int sms = 0;
+    e = num_sms(&sms);
+    if (e != cudaSuccess) return e;
+    const long long max_tiles = static_cast<long long>(max_mtiles) * n_tiles;
+    int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+    if (grid < 1) grid = 1;
+    tc::grouped_gemm_kernel<EPI, true><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const float* a_scale, const void* B,
+                              const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles, void* out,
+                              long long ldo, int out_cols, cudaStream_t st) {
+    switch (epi) {
+        case EPI_SWIGLU:
+            return launch_tc_f8_impl<EPI_SWIGLU>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
+                                                 out_cols, st);
+        case EPI_BF16:
+            return launch_tc_f8_impl<EPI_BF16>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
+                                               out_cols, st);
+        case EPI_F32:
+            return launch_tc_f8_impl<EPI_F32>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
+                                              out_cols, st);
+        default:
+            return cudaErrorInvalidValue;
+    }
 }
 
 bool tc_gather_supported() { return !use_pair(); }
@@ -798,5 +916,6 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
 }
 
 int tc_block_m() { return use_pair() ? tc::P_BM : tc::BM; }
+int tc_block_m_f8() { return tc::BM; }
 
 }  // namespace fs

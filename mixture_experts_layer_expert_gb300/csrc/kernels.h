@@ -17,6 +17,7 @@ int* dev_error_ptr();
 
 // gemm_tc.cu (bf16 operands, tcgen05)
 int tc_block_m();
+int tc_block_m_f8();
 cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st);
 // gather_rows (nullable): GEMM row p reads row gather_rows[p] of A (p < gather_limit)
 bool tc_gather_supported();
@@ -24,6 +25,12 @@ bool tc_gather_supported();
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
                            const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st);
+// FP8 E4M3 operands (kind::f8f6f4): A codes [a_rows, K] with a_scale[a_rows],
+// B packed by quant.cu with b_scale[G N]; the epilogue multiplies the fp32
+// accumulator by a_scale[row] b_scale[g N + col].  Single-CTA kernel only.
+cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const float* a_scale, const void* B,
+                              const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles, void* out,
+                              long long ldo, int out_cols, cudaStream_t st);
 
 // gemm_simt.cu (fp32 operands, fp32 FMA)
 int simt_block_m();
@@ -38,12 +45,14 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 // dispatch.cu
 constexpr int kStaticDispatchScratchInts = 65536;   // 256 KiB: fs_dispatch_noalloc's scratch
 size_t dispatch_ws_bytes(int T, int E);
+// fp8: x_perm is an FP8 row-scaled matrix [T k, d] (fp8.cuh) and u (bf16) is
+// quantised per token on the way; u_q (nullable) receives the quantised u [T, d].
 cudaError_t launch_dispatch_noalloc(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
-                                    void* x_perm, cudaStream_t st);
+                                    void* x_perm, cudaStream_t st, bool fp8);
 cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
-                            int32_t* scratch, cudaStream_t st);
+                            int32_t* scratch, cudaStream_t st, bool fp8 = false, void* u_q = nullptr);
 
 // combine.cu
 cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* topk_w, const void* o_prev,
@@ -59,5 +68,14 @@ cudaError_t launch_pack_w13(int G, int c, int d, int elem_bytes, const void* w1,
 cudaError_t launch_pack_w3(int G, int d, int c, int elem_bytes, const void* w3, void* w3p, cudaStream_t st);
 cudaError_t launch_pack_w3_shared(int ns, int cs, int d, int elem_bytes, const void* w3s, void* w3cat,
                                   cudaStream_t st);
+
+// quant.cu -- FP8 E4M3: packed weights hold codes [G][ceil(N/256)][K/128][256][128]
+// then G N fp32 row scales; launch_quant_rows writes an FP8 row-scaled matrix.
+size_t packed_bytes_fp8(int G, int N, int K);
+const float* packed_scales_fp8(const void* packed, int G, int N, int K);
+cudaError_t launch_pack_w13_fp8(int G, int c, int d, const void* w1, const void* w2, void* w13, cudaStream_t st);
+cudaError_t launch_pack_w3_fp8(int G, int d, int c, const void* w3, void* w3p, cudaStream_t st);
+cudaError_t launch_pack_w3_shared_fp8(int ns, int cs, int d, const void* w3s, void* w3cat, cudaStream_t st);
+cudaError_t launch_quant_rows(const void* x, long long rows, int cols, void* q, cudaStream_t st);
 
 }  // namespace fs

@@ -18,7 +18,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfs.so")
 _lib = None
 
-FS_BF16, FS_F32 = 0, 1
+FS_BF16, FS_F32, FS_FP8 = 0, 1, 2
+DTYPES = {"bf16": FS_BF16, "f32": FS_F32, "fp8": FS_FP8}
 GATES = {"softmax": 0, "softmax_renorm": 1, "sigmoid": 2, "sigmoid_norm": 3}
 WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2, "attn_farskip": 3, "attn_plain": 4}
 STATUS = {0: "FS_OK", 1: "FS_ERR_INVALID_ARG", 2: "FS_ERR_UNSUPPORTED", 3: "FS_ERR_WORKSPACE",
@@ -63,6 +64,8 @@ _SIGS = {
                                         _VP, _VP, _VP, _SZ, _VP, _VP]),
     "fs_workspace_bytes_overlap": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
     "fs_workspace_bytes_attn": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
+    "fs_fp8_rows_bytes": (_SZ, [ctypes.c_int64, _I32]),
+    "fs_quantize_rows_fp8": (_I32, [ctypes.c_int64, _I32, _VP, _VP, _VP]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "fs_launch_count": (ctypes.c_uint64, []),
     "fs_last_cuda_error": (ctypes.c_char_p, []),
@@ -111,7 +114,7 @@ def _nbytes(t: torch.Tensor) -> int:
 
 def make_desc(cfg: LayerConfig, T: int | None = None) -> LayerDesc:
     return LayerDesc(cfg.T if T is None else T, cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared,
-                     FS_BF16 if cfg.dtype == "bf16" else FS_F32, GATES[cfg.gate])
+                     DTYPES[cfg.dtype], GATES[cfg.gate])
 
 
 # ----------------------------------------------------------------- entry points
@@ -135,6 +138,25 @@ def fs_pack_w3(G, d, c, dtype, w3, w3p, stream=None):
 def fs_pack_w3_shared(n_shared, c_shared, d, dtype, w3s, w3cat, stream=None):
     _check(lib().fs_pack_w3_shared(n_shared, c_shared, d, dtype, _p(w3s), _p(w3cat), _stream(stream)),
            "fs_pack_w3_shared")
+
+
+def fs_fp8_rows_bytes(rows: int, cols: int) -> int:
+    return int(lib().fs_fp8_rows_bytes(rows, cols))
+
+
+def fs_quantize_rows_fp8(rows, cols, x, q, stream=None):
+    _check(lib().fs_quantize_rows_fp8(rows, cols, _p(x), _p(q), _stream(stream)), "fs_quantize_rows_fp8")
+
+
+def fp8_rows_empty(rows: int, cols: int, device="cuda") -> torch.Tensor:
+    """A byte buffer for an FP8 row-scaled matrix [rows, cols] (codes, then scales)."""
+    return torch.empty(fs_fp8_rows_bytes(rows, cols), dtype=torch.uint8, device=device)
+
+
+def fp8_rows_split(buf: torch.Tensor, rows: int, cols: int):
+    """Views (codes [rows, cols] uint8, scales [rows] fp32) of an FP8 row-scaled matrix."""
+    off = (rows * cols + 255) // 256 * 256
+    return buf[:rows * cols].view(rows, cols), buf[off:off + 4 * rows].view(torch.float32)
 
 
 def fs_router_topk(desc, u, w_r, bias, topk_idx, topk_w, logits, ws, stream=None):
@@ -243,12 +265,15 @@ def _packed(G, N, K, dt, like):
     n = fs_packed_bytes(G, N, K, dt)
     if n == 0:
         raise FsError(1, "fs_packed_bytes")
+    if dt == FS_FP8:
+        return torch.empty(n, dtype=torch.uint8, device=like.device)
     return torch.empty(n // like.element_size(), dtype=like.dtype, device=like.device)
 
 
 def pack_block(cfg: LayerConfig, w: dict, stream=None) -> dict:
-    """Repack one block's page-layout weights (on the GPU) into the library layout."""
-    dt = FS_BF16 if cfg.dtype == "bf16" else FS_F32
+    """Repack one block's page-layout weights (on the GPU) into the library layout
+    (FP8: quantised from the bf16 weights)."""
+    dt = DTYPES[cfg.dtype]
     E, c, d = cfg.E, cfg.c, cfg.d
     out = {"w_r": w["w_r"].contiguous(), "bias": None if w.get("bias") is None else w["bias"].contiguous().float()}
     out["w13"] = _packed(E, 2 * c, d, dt, w["w1"])
@@ -278,7 +303,7 @@ class FarSkipStack:
         self.desc = make_desc(cfg, self.T)
         self.blocks = [pack_block(cfg, b) for b in raw_blocks]
         self.ws = alloc_workspace(self.desc, len(self.blocks), device, attn=self.wiring.startswith("attn"))
-        dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
         self.o_full = torch.empty((self.T, cfg.d), dtype=dt, device=device)
         self.o_partial = torch.empty((self.T, cfg.d), dtype=dt, device=device)
 

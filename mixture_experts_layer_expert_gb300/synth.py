@@ -40,7 +40,7 @@ def _randn(shape, seed: int, device, scale: float, dtype: torch.dtype) -> torch.
 
 
 def storage_dtype(cfg: LayerConfig) -> torch.dtype:
-    return torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    return torch.float32 if cfg.dtype == "f32" else torch.bfloat16
 
 
 def make_x(cfg: LayerConfig, device="cpu", T: int | None = None) -> torch.Tensor:

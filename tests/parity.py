@@ -4,6 +4,12 @@ of the workload definition:
   bf16 storage / fp32 accumulate : relative Frobenius <= 5e-3 and
                                    max-abs <= 2e-2 * rms(reference)
   fp32                           : relative Frobenius <= 1e-5
+  FP8 experts                    : the bf16 bounds.  Both sides quantise the same
+                                   bf16 values with the same rule, the E4M3
+                                   products are exact in fp32, so what is left
+                                   is accumulation order plus rare one-quantum
+                                   flips where the two sides' bf16 hidden values
+                                   straddle an E4M3 rounding boundary.
   routing                        : top-k sets equal except where the k-th and
                                    (k+1)-th oracle logits differ by < 1e-4;
                                    such tokens must be < 0.1% and are left
@@ -18,14 +24,16 @@ import oracle
 from mixture_experts_layer_expert_gb300 import synth
 
 TOL = {"bf16": dict(rel_fro=5e-3, max_abs_rms=2e-2), "f32": dict(rel_fro=1e-5, max_abs_rms=1e-4)}
+TOL["fp8"] = TOL["bf16"]
 GAP = 1e-4
 MISMATCH_FRAC = 1e-3
 
 
 def oracle_cfg(cfg, storage=True):
-    dt = oracle.BF16 if cfg.dtype == "bf16" else oracle.F32
-    st = (oracle.STORE_BF16 if cfg.dtype == "bf16" else oracle.STORE_F32) if storage else oracle.EXACT
-    return oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st)
+    dt = oracle.F32 if cfg.dtype == "f32" else oracle.BF16
+    st = (oracle.STORE_F32 if cfg.dtype == "f32" else oracle.STORE_BF16) if storage else oracle.EXACT
+    return oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st,
+                           fp8=cfg.dtype == "fp8")
 
 
 def oracle_weights(blocks):
@@ -48,6 +56,90 @@ def compare(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
     assert mx <= tol["max_abs_rms"] * rms + 1e-30, "%s: max-abs %.3e > %.1e * rms (%.3e)" % (
         what, mx, tol["max_abs_rms"], rms)
     return rel, mx / max(rms, 1e-300)
+
+
+# ---------------------------------------------------------------- FP8 flips
+# Both sides quantise the stored bf16 hidden h with the same rule, but the two
+# sides' h come from fp32 (tensor cores) and fp64 (oracle) sums, and a one-ulp
+# bf16 difference that straddles an E4M3 rounding boundary moves that hidden
+# code by one step -- the quantised analogue of a routing near-tie.  One step is
+# at most 2^-3 of the value (3 mantissa bits), so one flipped code j changes
+# output element i by at most w_s 2^-3 |h_j| |W3[i, j]|.  FP8 outputs therefore
+# meet: relative Frobenius <= 5e-3 overall, and per element max-abs <= 2e-2 rms
+# plus the largest such one-flip change feeding that element; elements beyond
+# that (several flips, or a row whose scale exponent flipped) are counted per
+# token and must be < 0.1% of tokens (one token allowed in small samples).
+FP8_STEP = 2.0 ** -3
+W3_Q = 1.0 + 2.0 ** -4          # |W3| dequantised is within one half-step of the bf16 weight
+
+
+def _bf16_to_f64(a: np.ndarray) -> np.ndarray:
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+class Fp8Flips:
+    """One-flip allowances of a block's outputs for its token rows u (bf16 as
+    uint16), routing (topk_idx, topk_w) and numpy weights `w` (page layout)."""
+
+    def __init__(self, cfg, w: dict, u: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray):
+        self.cfg, self.w, self.u, self.idx, self.tw = cfg, w, u, topk_idx, topk_w
+        self.oc = oracle_cfg(cfg)
+        self._w3 = _bf16_to_f64(w["w3"])
+        if cfg.n_shared:
+            ns, cs, d = cfg.n_shared, cfg.c_shared, cfg.d
+            self._w3cat_raw = np.ascontiguousarray(np.concatenate([w["w3s"][s] for s in range(ns)], axis=1))
+            self._w3cat = _bf16_to_f64(self._w3cat_raw)
+            self._w13s = (w["w1s"].reshape(1, ns * cs, d), w["w2s"].reshape(1, ns * cs, d))
+            self._oc1 = oracle.make_cfg(d, 1, 1, ns * cs, 0, 0, cfg.gate, self.oc.in_dtype, self.oc.storage, fp8=True)
+        self._cache = {}
+
+    def _token(self, t):
+        if t not in self._cache:
+            k = self.cfg.k
+            rows = np.ascontiguousarray(np.repeat(self.u[t:t + 1], k, axis=0))
+            h, _ = oracle.expert_rows(self.oc, rows, self.idx[t].astype(np.int32), self.w["w1"], self.w["w2"],
+                                      self.w["w3"])
+            hs = None
+            if self.cfg.n_shared:
+                hs, _ = oracle.expert_rows(self._oc1, np.ascontiguousarray(self.u[t:t + 1]), np.zeros(1, np.int32),
+                                           self._w13s[0], self._w13s[1], self._w3cat_raw[None])
+            self._cache[t] = (np.abs(h), None if hs is None else np.abs(hs[0]))
+        return self._cache[t]
+
+    def allowance(self, t: int, i: int) -> float:
+        h, hs = self._token(t)
+        a = 0.0
+        for s in range(self.cfg.k):
+            e = int(self.idx[t, s])
+            a = max(a, abs(float(self.tw[t, s])) * FP8_STEP * W3_Q * float(np.max(h[s] * np.abs(self._w3[e, i]))))
+        if hs is not None:
+            a = max(a, FP8_STEP * W3_Q * float(np.max(hs * np.abs(self._w3cat[i]))))
+        return a
+
+
+def compare_fp8(got: np.ndarray, ref: np.ndarray, flips: "Fp8Flips", tokens: np.ndarray, what: str = ""):
+    """FP8 outputs [n, d] against the oracle (see the FP8 flips note above);
+    tokens[r] = the token of row r in the Fp8Flips inputs."""
+    tol = TOL["fp8"]
+    err = got - ref
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(err) / max(nref, 1e-300)
+    rms = nref / np.sqrt(max(ref.size, 1))
+    assert rel <= tol["rel_fro"], "%s: relative Frobenius %.3e > %.1e" % (what, rel, tol["rel_fro"])
+    base = tol["max_abs_rms"] * rms
+    over = np.argwhere(np.abs(err) > base)
+    unexplained = set()
+    for r, i in over:
+        if r in unexplained:
+            continue
+        if abs(err[r, i]) > base + flips.allowance(int(tokens[r]), int(i)):
+            unexplained.add(int(r))
+    n = got.shape[0]
+    assert len(unexplained) <= max(1, int(MISMATCH_FRAC * n)), (
+        "%s: %d of %d tokens beyond max-abs + one-flip allowance" % (what, len(unexplained), n))
+    return rel, len(over), len(unexplained)
 
 
 def kth_gap(logits: np.ndarray, k: int) -> np.ndarray:
@@ -92,7 +184,8 @@ class GpuBlockRunner:
         self.w = torch.empty((T, k), dtype=torch.float32, device=DEV)
         self.counts, self.offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
         self.pos, self.perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
-        self.x_perm = torch.empty((T * k, d), dtype=self.dt, device=DEV)
+        self.x_perm = (fs.fp8_rows_empty(T * k, d, DEV) if cfg.dtype == "fp8"
+                       else torch.empty((T * k, d), dtype=self.dt, device=DEV))
         self.y_perm = torch.empty((T * k, d), dtype=self.dt, device=DEV)
         self.s = torch.empty((T, d), dtype=torch.float32, device=DEV) if cfg.n_shared else None
 

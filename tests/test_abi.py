@@ -132,5 +132,28 @@ def test_other_entry_points_reject_bad_args(L):
                               1 << 40, None) == 1              # bad wiring
 
 
+def test_fp8_argument_checks(L):
+    """FS_FP8 needs d, c, c_shared multiples of 128; rejected before any launch."""
+    ok = desc(dtype=2)
+    assert fs.fs_workspace_bytes(ok, 1) > 0
+    # FP8 x_perm (1 byte per element) is smaller than the bf16 one
+    assert fs.fs_workspace_bytes(ok, 1) < fs.fs_workspace_bytes(desc(), 1)
+    for bad in (dict(d=7168 + 64), dict(c=2048 + 64), dict(c_shared=2048 + 64)):
+        assert fs.fs_workspace_bytes(desc(dtype=2, **bad), 1) == 0, bad
+    assert fs.fs_packed_bytes(256, 4096, 7168, 2) == 256 * 4096 * 7168 + 256 * 4096 * 4
+    assert fs.fs_packed_bytes(1, 384, 256, 2) == 512 * 256 + 384 * 4      # rows padded to 256
+    assert fs.fs_packed_bytes(1, 256, 192, 2) == 0                        # K % 128
+    assert fs.fs_fp8_rows_bytes(3, 128) == 512 + 12
+    assert fs.fs_fp8_rows_bytes(0, 128) == 0
+    assert L.fs_pack_w13(1, 192, 256, 2, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_pack_w3(1, 256, 192, 2, _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_pack_w3_shared(2, 192, 256, 2, _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_quantize_rows_fp8(10, 100, _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_quantize_rows_fp8(0, 128, _vp(FAKE), _vp(FAKE), None) == 1
+    assert L.fs_quantize_rows_fp8(10, 128, _vp(MIS), _vp(FAKE), None) == 2
+    assert L.fs_pack_w13(1, 128, 128, 3, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 1      # unknown dtype
+    assert fs.fs_launch_count() == 0
+
+
 def test_no_launch_on_rejected_calls(L):
     assert fs.fs_launch_count() == 0

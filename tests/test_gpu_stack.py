@@ -30,8 +30,8 @@ import torch
 
 import oracle
 from mixture_experts_layer_expert_gb300 import configs, fs, synth
-from parity import (GpuBlockRunner, TOL, compare, gpu_stack_stepwise, kth_gap, oracle_cfg, oracle_weights, to64,
-                    topk_mismatch)
+from parity import (Fp8Flips, GpuBlockRunner, TOL, compare, compare_fp8, gpu_stack_stepwise, kth_gap, oracle_cfg,
+                    oracle_weights, to64, topk_mismatch)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -70,6 +70,14 @@ def blockwise(cfg, prob, stack, wiring, rows=None):
         z = ref["logits"][b] - (0 if bnp is None else bnp.astype(np.float64)[None, :])
         bad = topk_mismatch(idx[rows], ref["topk_idx"][b], z, cfg.k, bnp)
         keep = ~bad
+        if cfg.dtype == "fp8":
+            flips = Fp8Flips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][b].items()},
+                             synth.to_numpy(torch.from_numpy(ref["U"][b]).to(torch.bfloat16)),
+                             ref["topk_idx"][b], ref["topk_w"][b])
+            kept = np.nonzero(keep)[0]
+            compare_fp8(to64(o_k[rows_t])[keep], ref["O"][b][keep], flips, kept, "block %d o_k" % (b + 1))
+            compare_fp8(to64(o_star[rows_t])[keep], ref["OS"][b][keep], flips, kept, "block %d o_k*" % (b + 1))
+            continue
         compare(to64(o_k[rows_t])[keep], ref["O"][b][keep], cfg.dtype, "block %d o_k" % (b + 1))
         compare(to64(o_star[rows_t])[keep], ref["OS"][b][keep], cfg.dtype, "block %d o_k*" % (b + 1))
     return ref
@@ -100,6 +108,13 @@ def end_to_end(cfg, prob, stack, o, o_star, wiring, rows=None):
     keep = ~bad_any
     got, got_s = to64(o[rows_t])[keep], to64(o_star[rows_t])[keep]
     if cfg.L == 1:
+        if cfg.dtype == "fp8":
+            flips = Fp8Flips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][0].items()},
+                             synth.to_numpy(x_s), ref["topk_idx"][0], ref["topk_w"][0])
+            kept = np.nonzero(keep)[0]
+            compare_fp8(got, ref["o"][keep], flips, kept, "o_L")
+            compare_fp8(got_s, ref["o_star"][keep], flips, kept, "o_L*")
+            return drift
         compare(got, ref["o"][keep], cfg.dtype, "o_L")
         compare(got_s, ref["o_star"][keep], cfg.dtype, "o_L*")
         return drift

@@ -1,6 +1,7 @@
-"""Pins for the oracle's FP8 expert path (the pages' inference setting: "FP8
-quantisation and fused MoE forward kernels", FarSkip-Collective, experimental
-setup; format and scaling are this build's reading, stated in oracle.c).
+"""Pins for the oracle's FP8 expert path (the pages' inference setting: FP8
+quantisation with fused MoE forward kernels, "FarSkip-Collective" summary,
+experimental setup, software configuration; the format and the scaling are a
+reading of this build, stated in oracle.c).
 
 What fixes each function, and the mistake each pin catches:
   E4M3 values       -- every finite code of the library's float8_e4m3fn type is a
