@@ -454,10 +454,11 @@ constexpr int P_BM = 256;                     // rows per pair tile
 constexpr size_t P_SMEM_BYTES =
     1024 + static_cast<size_t>(P_STAGES) * P_STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * sizeof(int);
 
-template <int EPI>
+template <int EPI, bool F8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const Args args) {
+    constexpr int BKE = F8 ? 128 : BK;     // K elements per stage (128 bytes per row)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
@@ -507,7 +508,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         total_mtiles = 0;
     }
     const int total = total_mtiles * args.n_tiles;
-    const int num_kb = args.K / BK;
+    const int num_kb = args.K / BKE;
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(nclusters_x());
 
@@ -530,12 +531,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
                     const uint32_t fb = map_to_cta(fb_local, 0);
                     uint8_t* sa = smem + stage * P_STAGE_BYTES;
-                    tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, a_row);
+                    tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BKE, a_row);
                     if (args.b_blocked)
                         tma_load_3d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, 0, static_cast<int>(rank) * 128,
                                          (tl.g * args.n_tiles + tl.n) * num_kb + kb);
                     else
-                        tma_load_2d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, kb * BK, b_row);
+                        tma_load_2d_pair(smem_u32(sa + P_A_STAGE), &tmB, fb, kb * BKE, b_row);
                     ++issued;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -558,7 +559,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
             if (leader) {
-                constexpr uint32_t idesc = idesc_bf16_f32(P_BM, BN);
+                constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(P_BM, BN) : idesc_bf16_f32(P_BM, BN);
                 int stage = 0;
                 uint32_t phase = 0;
                 bool ok = true;
@@ -576,9 +577,14 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         const uint64_t adesc = smem_desc_sw128(smem_u32(sa));
                         const uint64_t bdesc = smem_desc_sw128(smem_u32(sa + P_A_STAGE));
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
-                                             (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {   // 32 bytes of K per MMA
+                            if constexpr (F8)
+                                tc_mma_f8_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
+                                               (kb > 0 || kk > 0) ? 1u : 0u);
+                            else
+                                tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
+                                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
                         tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
                         if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
                     }
@@ -612,7 +618,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            epilogue_tile<EPI>(tbase, tl.g, a_row, rows_valid, tl.n, r, half, args);
+            epilogue_tile<EPI, F8>(tbase, tl.g, a_row, rows_valid, tl.n, r, half, args);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(map_to_cta(smem_u32(&tempty[acc]), 0));
@@ -835,20 +841,25 @@ template <int EPI>
 static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const float* a_scale, const void* B,
                                      const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles,
                                      void* out, long long ldo, int out_cols, cudaStream_t st) {
-    static bool attr_set = false;
+    const bool pair = use_pair();
+    static bool attr_set[2] = {false, false};
     cudaError_t e;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tc::SMEM_BYTES));
+    if (!attr_set[pair]) {
+        if (pair)
+            e = cudaFuncSetAttribute(tc::pair_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(tc::P_SMEM_BYTES));
+        else
+            e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(tc::SMEM_BYTES));
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[pair] = true;
     }
     if (K % 128 || N % 128) return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
-    e = make_map(&ta, A, a_rows, K, tc::BM, true);
+    e = make_map(&ta, A, a_rows, K, 128, true);
     if (e != cudaSuccess) return e;
     const int n_tiles = (N + tc::BN - 1) / tc::BN;
-    e = make_map_blocked(&tb, B, static_cast<long long>(G) * n_tiles * (K / 128), tc::BN, true);
+    e = make_map_blocked(&tb, B, static_cast<long long>(G) * n_tiles * (K / 128), pair ? 128 : tc::BN, true);
     if (e != cudaSuccess) return e;
     tc::Args args;
     args.plan = plan;
@@ -870,9 +881,17 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
     const long long max_tiles = static_cast<long long>(max_mtiles) * n_tiles;
-    int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
-    if (grid < 1) grid = 1;
-    tc::grouped_gemm_kernel<EPI, true><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    if (pair) {
+        long long clusters = sms / 2;
+        if (max_tiles < clusters) clusters = max_tiles;
+        if (clusters < 1) clusters = 1;
+        tc::pair_gemm_kernel<EPI, true><<<static_cast<int>(2 * clusters), tc::THREADS, tc::P_SMEM_BYTES, st>>>(ta, tb,
+                                                                                                           args);
+    } else {
+        int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
+        if (grid < 1) grid = 1;
+        tc::grouped_gemm_kernel<EPI, true><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    }
     count_launch();
     return cudaGetLastError();
 }
@@ -916,6 +935,6 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
 }
 
 int tc_block_m() { return use_pair() ? tc::P_BM : tc::BM; }
-int tc_block_m_f8() { return tc::BM; }
+int tc_block_m_f8() { return use_pair() ? tc::P_BM : tc::BM; }
 
 }  // namespace fs
