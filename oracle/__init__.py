@@ -252,3 +252,51 @@ def combine(T, k, d, y_perm, pos, topk_w, o_prev, shared_out=None, storage=EXACT
                                 _p(None if shared_out is None else np.ascontiguousarray(shared_out)),
                                 _p(o_star), _p(o)), "combine")
     return o_star, o
+
+
+def _grad_arrays(cfg: _Cfg, L: int | None):
+    pre = () if L is None else (L,)
+    E, d, c, ns, cs = cfg.E, cfg.d, cfg.c, cfg.n_shared, cfg.c_shared
+    g = {"dW_R": np.zeros(pre + (E, d)), "dW1": np.zeros(pre + (E, c, d)), "dW2": np.zeros(pre + (E, c, d)),
+         "dW3": np.zeros(pre + (E, d, c))}
+    if ns:
+        g.update(dW1s=np.zeros(pre + (ns, cs, d)), dW2s=np.zeros(pre + (ns, cs, d)), dW3s=np.zeros(pre + (ns, d, cs)))
+    else:
+        g.update(dW1s=None, dW2s=None, dW3s=None)
+    return g
+
+
+def block_backward(cfg: _Cfg, weights: Weights, u: np.ndarray, dO: np.ndarray, dOs: np.ndarray | None = None):
+    """Backward of one block at its input rows u (fp64 values): du, do_prev, the
+    gate-weight gradients dw [n, k] and the weight gradients dW_R, dW1, dW2, dW3
+    (+ shared dW1s, dW2s, dW3s)."""
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    n = u.shape[0]
+    out = {"du": np.zeros((n, cfg.d)), "do_prev": np.zeros((n, cfg.d)), "dw": np.zeros((n, cfg.k))}
+    out.update(_grad_arrays(cfg, None))
+    dO = np.ascontiguousarray(dO, dtype=np.float64)
+    dOs = None if dOs is None else np.ascontiguousarray(dOs, dtype=np.float64)
+    _check(lib().oracle_block_backward(ctypes.byref(cfg), ctypes.byref(weights.struct()), ctypes.c_int(n), _p(u),
+                                       _p(dO), _p(dOs), _p(out["du"]), _p(out["do_prev"]), _p(out["dw"]),
+                                       _p(out["dW_R"]), _p(out["dW1"]), _p(out["dW2"]), _p(out["dW3"]),
+                                       _p(out["dW1s"]), _p(out["dW2s"]), _p(out["dW3s"])), "block_backward")
+    return out
+
+
+def stack_backward(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, dOL: np.ndarray,
+                   dOLs: np.ndarray | None = None):
+    """Backward of stack() for the MoE wirings: dx and per-block weight gradients [L, ...]."""
+    x = np.ascontiguousarray(x)
+    L = len(weights)
+    n = x.shape[0]
+    arr = (_W * L)(*[w.struct() for w in weights])
+    out = {"dx": np.zeros((n, cfg.d))}
+    out.update(_grad_arrays(cfg, L))
+    dOL = np.ascontiguousarray(dOL, dtype=np.float64)
+    dOLs = None if dOLs is None else np.ascontiguousarray(dOLs, dtype=np.float64)
+    _check(lib().oracle_stack_backward(ctypes.byref(cfg), arr, ctypes.c_int(L), ctypes.c_int(WIRINGS[wiring]),
+                                       ctypes.c_int(n), _p(x), ctypes.c_int(_dt(x)), _p(dOL), _p(dOLs),
+                                       _p(out["dx"]), _p(out["dW_R"]), _p(out["dW1"]), _p(out["dW2"]),
+                                       _p(out["dW3"]), _p(out["dW1s"]), _p(out["dW2s"]), _p(out["dW3s"])),
+           "stack_backward")
+    return out

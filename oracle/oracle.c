@@ -712,6 +712,302 @@ int oracle_combine(int T, int k, int d, int in_dtype, int storage,
     return 0;
 }
 
+/* ---------------------------------------------------------------- backward */
+
+/* Training form of one block (the pages train FarSkip models with Megatron-LM
+ * but print no gradient formulas; these are the derivatives of the forward
+ * definitions above).  With storage != ORACLE_EXACT the backward reads what the
+ * forward stored -- each expert row's gate/up pre-activations g, a, its hidden
+ * h and output y, rounded per storage -- and rounds its own stored operands the
+ * same way: the routed output gradient dy = w dR, the pre-activation gradients
+ * dg, da, each (token, slot)'s input gradient dx, the shared output gradient
+ * dS and the router logit gradient dz.  Sums are fp64.  Top-k selection is
+ * piecewise constant (no gradient); the router bias is not a parameter.
+ *
+ * Per token, with o = o_prev + S + R and o* = o_prev + S:
+ *   dR = dO,  dS = dO + dOs,  do_prev = dO + dOs
+ *   dw_s = <dR, y_s>,  dy_s = w_s dR
+ *   dh   = dy_s W3_e                 dh[j] = sum_i dy[i] W3[i, j]
+ *   dg   = dh a SiLU'(g),  da = dh SiLU(g),  SiLU'(g) = sig(g) (1 + g (1 - sig(g)))
+ *   dx_s = dg W2_e + da W1_e         dx[i] = sum_j dg[j] W2[j, i] + da[j] W1[j, i]
+ *   dW3_e += dy_s h^T,  dW2_e += dg u^T,  dW1_e += da u^T
+ *   shared experts: the same with dS for dy and gate weight 1
+ *   dz = gate-rule derivative of w applied to dw;  dW_R += dz u^T
+ *   du = sum_s dx_s + dx_shared + dz W_R
+ */
+
+/* dz[0..E) from dw[0..k) for the gate rules of oracle_router (z = the logits
+ * with the bias, e = the chosen experts, w = their gate weights). */
+static void gate_backward(int gate, int E, int k, const double* z, const int32_t* e, const double* w,
+                          const double* dw, double* dz) {
+    for (int j = 0; j < E; ++j) dz[j] = 0.0;
+    double c = 0.0;                       /* sum_s dw_s w_s */
+    for (int s = 0; s < k; ++s) c += dw[s] * w[s];
+    if (gate == ORACLE_GATE_SOFTMAX) {
+        /* w_s = p_{e_s}, p = softmax(z) over all E: dz_j = sum_s dw_s p_{e_s} (delta - p_j) */
+        double zmax = z[e[0]], den = 0.0;
+        for (int j = 0; j < E; ++j) den += exp(z[j] - zmax);
+        for (int j = 0; j < E; ++j) dz[j] = -c * exp(z[j] - zmax) / den;
+        for (int s = 0; s < k; ++s) dz[e[s]] += dw[s] * w[s];
+    } else if (gate == ORACLE_GATE_SOFTMAX_RENORM) {
+        /* w_s = softmax over the chosen: dz_{e_r} = w_r (dw_r - c) */
+        for (int r = 0; r < k; ++r) dz[e[r]] = w[r] * (dw[r] - c);
+    } else if (gate == ORACLE_GATE_SIGMOID) {
+        for (int s = 0; s < k; ++s) {
+            double sg = sigmoid(z[e[s]]);
+            dz[e[s]] = dw[s] * sg * (1.0 - sg);
+        }
+    } else {
+        /* w_s = sig_s / sum_r sig_r: dsig_r = (dw_r - c) / sum, dz_{e_r} = dsig_r sig_r (1 - sig_r) */
+        double den = 0.0;
+        for (int s = 0; s < k; ++s) den += sigmoid(z[e[s]]);
+        for (int r = 0; r < k; ++r) {
+            double sg = sigmoid(z[e[r]]);
+            dz[e[r]] = (dw[r] - c) / den * sg * (1.0 - sg);
+        }
+    }
+}
+
+static double silu_grad(double g) {
+    double sg = sigmoid(g);
+    return sg * (1.0 + g * (1.0 - sg));
+}
+
+/* One expert row forward and its backward for the row's output gradient dy
+ * (already the stored, rounded one): fills g, a (stored), h (stored), y
+ * (stored) when fwd, then dh, dg, da (stored) and dx (unrounded).  W1, W2
+ * [c, d] from element base12 and W3 element (i, jj) at
+ * base3 + (jj / cw) d cw + i cw + jj % cw (cw = c for a routed expert; the
+ * shared experts side by side). */
+static void mlp_row_fwd(int d, int c, int cw, const double* x, const void* w1, const void* w2, size_t base12,
+                        const void* w3, size_t base3, int wdt, int storage, double* g, double* a, double* h,
+                        double* y) {
+    for (int j = 0; j < c; ++j) {
+        double gate = 0.0, up = 0.0;
+        for (int i = 0; i < d; ++i) {
+            gate += x[i] * elem(w2, base12 + (size_t)j * d + i, wdt);
+            up += x[i] * elem(w1, base12 + (size_t)j * d + i, wdt);
+        }
+        h[j] = oracle_round(silu(gate) * up, storage);
+        g[j] = oracle_round(gate, storage);
+        a[j] = oracle_round(up, storage);
+    }
+    if (y) {
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int jj = 0; jj < c; ++jj)
+                acc += h[jj] * elem(w3, base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw), wdt);
+            y[i] = oracle_round(acc, storage);
+        }
+    }
+}
+
+static void mlp_row_bwd(int d, int c, int cw, const double* dy, const double* g, const double* a,
+                        const void* w1, const void* w2, size_t base12, const void* w3, size_t base3, int wdt,
+                        int storage, double* dg, double* da, double* dx) {
+    for (int jj = 0; jj < c; ++jj) {
+        double dh = 0.0;
+        for (int i = 0; i < d; ++i)
+            dh += dy[i] * elem(w3, base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw), wdt);
+        dg[jj] = oracle_round(dh * a[jj] * silu_grad(g[jj]), storage);
+        da[jj] = oracle_round(dh * silu(g[jj]), storage);
+    }
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < c; ++j)
+            acc += dg[j] * elem(w2, base12 + (size_t)j * d + i, wdt) + da[j] * elem(w1, base12 + (size_t)j * d + i, wdt);
+        dx[i] = acc;
+    }
+}
+
+int oracle_block_backward(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
+                          const double* u, const double* dO, const double* dOs,
+                          double* du, double* do_prev, double* dw_out,
+                          double* dW_R, double* dW1, double* dW2, double* dW3,
+                          double* dW1s, double* dW2s, double* dW3s) {
+    const int d = cfg->d, E = cfg->E, k = cfg->k, c = cfg->c;
+    const int ns = cfg->n_shared, cs = cfg->c_shared, cw = ns * cs;
+    const int st = cfg->storage;
+    const int wdt = cfg->in_dtype;
+    if (cfg->fp8 || n_tok < 0) return -1;
+    const size_t nk = (size_t)n_tok * k;
+    double* z = (double*)malloc(sizeof(double) * ((size_t)n_tok * E + 1));
+    int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (nk + 1));
+    double* w = (double*)malloc(sizeof(double) * (nk + 1));
+    /* per (token, slot): dy, h, dg, da; per token: dS, h_s, dg_s, da_s, dz */
+    double* r_dy = (double*)malloc(sizeof(double) * (nk * d + 1));
+    double* r_h = (double*)malloc(sizeof(double) * (nk * c + 1));
+    double* r_dg = (double*)malloc(sizeof(double) * (nk * c + 1));
+    double* r_da = (double*)malloc(sizeof(double) * (nk * c + 1));
+    double* s_dS = (double*)malloc(sizeof(double) * ((size_t)n_tok * d + 1));
+    double* s_h = (double*)malloc(sizeof(double) * ((size_t)n_tok * (cw ? cw : 1)));
+    double* s_dg = (double*)malloc(sizeof(double) * ((size_t)n_tok * (cw ? cw : 1)));
+    double* s_da = (double*)malloc(sizeof(double) * ((size_t)n_tok * (cw ? cw : 1)));
+    double* r_dz = (double*)malloc(sizeof(double) * ((size_t)n_tok * E + 1));
+    int rc = 0;
+    if (!z || !idx || !w || !r_dy || !r_h || !r_dg || !r_da || !s_dS || !s_h || !s_dg || !s_da || !r_dz) rc = -2;
+    if (!rc) rc = oracle_router(cfg, n_tok, u, ORACLE_F64, wts->w_r, wts->bias, z, idx, w);
+    int bad = 0;
+    if (!rc) {
+        const int cmax = c > cw ? c : cw;
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int t = 0; t < n_tok; ++t) {
+            double* g = (double*)malloc(sizeof(double) * (size_t)cmax);
+            double* a = (double*)malloc(sizeof(double) * (size_t)cmax);
+            double* y = (double*)malloc(sizeof(double) * (size_t)d);
+            double* dx = (double*)malloc(sizeof(double) * (size_t)d);
+            double* dw = (double*)malloc(sizeof(double) * (size_t)k);
+            if (!g || !a || !y || !dx || !dw) { bad = 1; free(g); free(a); free(y); free(dx); free(dw); continue; }
+            const double* x = u + (size_t)t * d;
+            const double* dR = dO + (size_t)t * d;
+            double* dut = du + (size_t)t * d;
+            for (int i = 0; i < d; ++i) {
+                double dsv = dO[(size_t)t * d + i] + (dOs ? dOs[(size_t)t * d + i] : 0.0);
+                do_prev[(size_t)t * d + i] = dsv;
+                s_dS[(size_t)t * d + i] = oracle_round(dsv, st);
+                dut[i] = 0.0;
+            }
+            /* routed experts */
+            for (int s = 0; s < k; ++s) {
+                const size_t ts = (size_t)t * k + s;
+                const size_t e = (size_t)idx[ts];
+                double* h = r_h + ts * c;
+                mlp_row_fwd(d, c, c, x, wts->w1, wts->w2, e * c * d, wts->w3, e * d * c, wdt, st, g, a, h, y);
+                double dws = 0.0;
+                for (int i = 0; i < d; ++i) dws += dR[i] * y[i];
+                dw[s] = dws;
+                double* dy = r_dy + ts * d;
+                for (int i = 0; i < d; ++i) dy[i] = oracle_round(w[ts] * dR[i], st);
+                mlp_row_bwd(d, c, c, dy, g, a, wts->w1, wts->w2, e * c * d, wts->w3, e * d * c, wdt, st,
+                            r_dg + ts * c, r_da + ts * c, dx);
+                for (int i = 0; i < d; ++i) dut[i] += oracle_round(dx[i], st);
+            }
+            if (dw_out) memcpy(dw_out + (size_t)t * k, dw, sizeof(double) * (size_t)k);
+            /* shared experts: one MLP over the concatenated width */
+            if (ns > 0) {
+                double* hs = s_h + (size_t)t * cw;
+                mlp_row_fwd(d, cw, cs, x, wts->w1s, wts->w2s, 0, wts->w3s, 0, wdt, st, g, a, hs, NULL);
+                mlp_row_bwd(d, cw, cs, s_dS + (size_t)t * d, g, a, wts->w1s, wts->w2s, 0, wts->w3s, 0, wdt, st,
+                            s_dg + (size_t)t * cw, s_da + (size_t)t * cw, dx);
+                for (int i = 0; i < d; ++i) dut[i] += dx[i];
+            }
+            /* router */
+            double* dz = r_dz + (size_t)t * E;
+            gate_backward(cfg->gate, E, k, z + (size_t)t * E, idx + (size_t)t * k, w + (size_t)t * k, dw, dz);
+            for (int j = 0; j < E; ++j) dz[j] = oracle_round(dz[j], st);
+            for (int i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < E; ++j) acc += dz[j] * elem(wts->w_r, (size_t)j * d + i, wdt);
+                dut[i] += acc;
+            }
+            free(g); free(a); free(y); free(dx); free(dw);
+        }
+    }
+    if (bad) rc = -2;
+    if (!rc) {
+        /* weight gradients: sums over the (token, slot) pairs routed to each expert */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int e = 0; e < E; ++e) {
+            for (size_t q = 0; q < (size_t)d * c; ++q) dW3[(size_t)e * d * c + q] = 0.0;
+            for (size_t q = 0; q < (size_t)c * d; ++q) {
+                dW1[(size_t)e * c * d + q] = 0.0;
+                dW2[(size_t)e * c * d + q] = 0.0;
+            }
+            for (size_t ts = 0; ts < nk; ++ts) {
+                if (idx[ts] != e) continue;
+                const double* x = u + (ts / k) * d;
+                const double* dy = r_dy + ts * d;
+                const double* h = r_h + ts * c;
+                const double* dg = r_dg + ts * c;
+                const double* da = r_da + ts * c;
+                for (int i = 0; i < d; ++i)
+                    for (int j = 0; j < c; ++j) dW3[((size_t)e * d + i) * c + j] += dy[i] * h[j];
+                for (int j = 0; j < c; ++j)
+                    for (int i = 0; i < d; ++i) {
+                        dW2[((size_t)e * c + j) * d + i] += dg[j] * x[i];
+                        dW1[((size_t)e * c + j) * d + i] += da[j] * x[i];
+                    }
+            }
+            for (int i = 0; i < d; ++i) {
+                double* row = dW_R + (size_t)e * d;
+                row[i] = 0.0;
+                for (int t = 0; t < n_tok; ++t) row[i] += r_dz[(size_t)t * E + e] * u[(size_t)t * d + i];
+            }
+        }
+        if (ns > 0) {
+#pragma omp parallel for schedule(static)
+            for (int jj = 0; jj < cw; ++jj) {
+                const int sh = jj / cs, j = jj % cs;
+                for (int i = 0; i < d; ++i) {
+                    double a3 = 0.0, a1 = 0.0, a2 = 0.0;
+                    for (int t = 0; t < n_tok; ++t) {
+                        a3 += s_dS[(size_t)t * d + i] * s_h[(size_t)t * cw + jj];
+                        a2 += s_dg[(size_t)t * cw + jj] * u[(size_t)t * d + i];
+                        a1 += s_da[(size_t)t * cw + jj] * u[(size_t)t * d + i];
+                    }
+                    dW3s[((size_t)sh * d + i) * cs + j] = a3;
+                    dW2s[((size_t)sh * cs + j) * d + i] = a2;
+                    dW1s[((size_t)sh * cs + j) * d + i] = a1;
+                }
+            }
+        }
+    }
+    free(z); free(idx); free(w); free(r_dy); free(r_h); free(r_dg); free(r_da);
+    free(s_dS); free(s_h); free(s_dg); free(s_da); free(r_dz);
+    return rc;
+}
+
+/* Backward of oracle_stack for the MoE wirings (PARTIAL, OUTDATED, DISABLED):
+ * dOL, dOLs are the gradients of o_L and o_L* (dOLs may be NULL).  Blocks are
+ * visited from L down to 1; block k's do_prev flows to o_{k-1}, and its du to
+ * where u_k came from -- o_{k-1}* (partial), o_{k-2} (outdated) or o_{k-1}
+ * (disabled), x for k = 1 -- through the storage rounding of u_k as the
+ * identity.  Weight gradients are [L, ...] block-major. */
+int oracle_stack_backward(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wiring,
+                          int n_tok, const void* x, int x_dtype, const double* dOL, const double* dOLs,
+                          double* dx, double* dW_R, double* dW1, double* dW2, double* dW3,
+                          double* dW1s, double* dW2s, double* dW3s) {
+    const int d = cfg->d, E = cfg->E, k = cfg->k, c = cfg->c, ns = cfg->n_shared, cs = cfg->c_shared;
+    if (L < 1 || n_tok < 0) return -1;
+    if (wiring != ORACLE_WIRE_PARTIAL && wiring != ORACLE_WIRE_OUTDATED && wiring != ORACLE_WIRE_DISABLED) return -1;
+    const size_t n = (size_t)n_tok * d;
+    double* U = (double*)malloc(sizeof(double) * (n * L + 1));
+    double* oL = (double*)malloc(sizeof(double) * (n + 1));
+    double* oLs = (double*)malloc(sizeof(double) * (n + 1));
+    double* go = (double*)calloc(n * (L + 1) + 1, sizeof(double));    /* gradients of o_0 .. o_L */
+    double* gos = (double*)calloc(n * (L + 1) + 1, sizeof(double));   /* gradients of o_0* .. o_L* */
+    double* du = (double*)malloc(sizeof(double) * (n + 1));
+    double* dp = (double*)malloc(sizeof(double) * (n + 1));
+    int rc = (!U || !oL || !oLs || !go || !gos || !du || !dp) ? -2 : 0;
+    if (!rc)
+        rc = oracle_stack(cfg, wts, L, wiring, n_tok, x, x_dtype, oL, oLs, NULL, NULL, NULL, NULL, NULL, U, NULL,
+                          NULL, NULL, NULL);
+    if (!rc) {
+        memcpy(go + n * L, dOL, sizeof(double) * n);
+        if (dOLs) memcpy(gos + n * L, dOLs, sizeof(double) * n);
+        for (size_t i = 0; i < n; ++i) dx[i] = 0.0;
+        for (int b = L; b >= 1 && !rc; --b) {
+            const size_t wo = (size_t)(b - 1);
+            rc = oracle_block_backward(cfg, wts + (b - 1), n_tok, U + (size_t)(b - 1) * n, go + n * b, gos + n * b,
+                                       du, dp, NULL, dW_R + wo * E * d, dW1 + wo * E * c * d, dW2 + wo * E * c * d,
+                                       dW3 + wo * E * d * c, ns ? dW1s + wo * ns * cs * d : NULL,
+                                       ns ? dW2s + wo * ns * cs * d : NULL, ns ? dW3s + wo * ns * d * cs : NULL);
+            if (rc) break;
+            double* g_prev = go + n * (b - 1);                     /* o_{b-1} */
+            for (size_t i = 0; i < n; ++i) g_prev[i] += dp[i];
+            double* target;
+            if (b == 1) target = dx;                               /* u_1 = x */
+            else if (wiring == ORACLE_WIRE_PARTIAL) target = gos + n * (b - 1);   /* u_b = o_{b-1}* */
+            else if (wiring == ORACLE_WIRE_OUTDATED) target = go + n * (b - 2);   /* u_b = o_{b-2} */
+            else target = go + n * (b - 1);                                       /* u_b = o_{b-1} */
+            for (size_t i = 0; i < n; ++i) target[i] += du[i];
+        }
+        for (size_t i = 0; i < n; ++i) dx[i] += go[i];             /* o_0 = x */
+    }
+    free(U); free(oL); free(oLs); free(go); free(gos); free(du); free(dp);
+    return rc;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

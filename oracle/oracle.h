@@ -71,6 +71,15 @@ int oracle_combine(int T, int k, int d, int in_dtype, int storage,
                    const void* y_perm, const int32_t* pos, const float* topk_w,
                    const void* o_prev, const void* shared_out,
                    double* o_star, double* o_full);
+int oracle_block_backward(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
+                          const double* u, const double* dO, const double* dOs,
+                          double* du, double* do_prev, double* dw_out,
+                          double* dW_R, double* dW1, double* dW2, double* dW3,
+                          double* dW1s, double* dW2s, double* dW3s);
+int oracle_stack_backward(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wiring,
+                          int n_tok, const void* x, int x_dtype, const double* dOL, const double* dOLs,
+                          double* dx, double* dW_R, double* dW1, double* dW2, double* dW3,
+                          double* dW1s, double* dW2s, double* dW3s);
 int oracle_num_threads(void);
 
 #ifdef __cplusplus

@@ -12,6 +12,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_backward_pins as bwd
 import test_oracle_fp8_pins as fp8
 import test_oracle_pins as pins
 
@@ -57,6 +58,31 @@ MUTANTS = {
                                            "size_t off = base3 + (size_t)i * c + (size_t)jj;"),
     "fp8_shared_down_exponent_first_expert": ("            for (int sh = 0; sh < ns; ++sh)\n                for (int j = 0; j < cs; ++j) {",
                                               "            for (int sh = 0; sh < 1; ++sh)\n                for (int j = 0; j < cs; ++j) {"),
+    # backward
+    "bwd_silu_grad_sign": ("return sg * (1.0 + g * (1.0 - sg));", "return sg * (1.0 - g * (1.0 - sg));"),
+    "bwd_dg_without_up": ("dg[jj] = oracle_round(dh * a[jj] * silu_grad(g[jj]), storage);",
+                          "dg[jj] = oracle_round(dh * silu_grad(g[jj]), storage);"),
+    "bwd_dy_without_gate_weight": ("for (int i = 0; i < d; ++i) dy[i] = oracle_round(w[ts] * dR[i], st);",
+                                   "for (int i = 0; i < d; ++i) dy[i] = oracle_round(dR[i], st);"),
+    "bwd_renorm_without_normaliser_term": ("for (int r = 0; r < k; ++r) dz[e[r]] = w[r] * (dw[r] - c);",
+                                           "for (int r = 0; r < k; ++r) dz[e[r]] = w[r] * dw[r];"),
+    "bwd_softmax_without_other_experts": ("for (int j = 0; j < E; ++j) dz[j] = -c * exp(z[j] - zmax) / den;",
+                                          "for (int j = 0; j < E; ++j) dz[j] = 0.0;"),
+    "bwd_sigmoid_norm_without_den": ("dz[e[r]] = (dw[r] - c) / den * sg * (1.0 - sg);",
+                                     "dz[e[r]] = (dw[r] - c) * sg * (1.0 - sg);"),
+    "bwd_gate_up_swapped_in_dx": (
+        "acc += dg[j] * elem(w2, base12 + (size_t)j * d + i, wdt) + da[j] * elem(w1, base12 + (size_t)j * d + i, wdt);",
+        "acc += dg[j] * elem(w1, base12 + (size_t)j * d + i, wdt) + da[j] * elem(w2, base12 + (size_t)j * d + i, wdt);"),
+    "bwd_partial_grad_to_o": ("else if (wiring == ORACLE_WIRE_PARTIAL) target = gos + n * (b - 1);",
+                              "else if (wiring == ORACLE_WIRE_PARTIAL) target = go + n * (b - 1);"),
+    "bwd_outdated_grad_one_block_late": ("else if (wiring == ORACLE_WIRE_OUTDATED) target = go + n * (b - 2);",
+                                         "else if (wiring == ORACLE_WIRE_OUTDATED) target = go + n * (b - 1);"),
+    "bwd_shared_without_dOs": ("double dsv = dO[(size_t)t * d + i] + (dOs ? dOs[(size_t)t * d + i] : 0.0);",
+                               "double dsv = dO[(size_t)t * d + i];"),
+    "bwd_router_input_grad_dropped": ("                dut[i] += acc;\n", ""),
+    "bwd_wgrad_wrong_token": ("const double* x = u + (ts / k) * d;", "const double* x = u + (ts % n_tok) * d;"),
+    "bwd_slots_not_summed": ("for (int i = 0; i < d; ++i) dut[i] += oracle_round(dx[i], st);",
+                             "for (int i = 0; i < d; ++i) dut[i] = oracle_round(dx[i], st);"),
 }
 
 PIN_TESTS = [
@@ -81,6 +107,10 @@ PIN_TESTS = [
     fp8.test_down_projection_reduces_to_the_quantised_hidden,
     fp8.test_down_projection_with_representable_weights_is_a_matmul_of_the_quantised_hidden,
     fp8.test_block_sums_are_the_per_row_fp8_experts,
+    lambda: [bwd.test_stack_backward_finite_differences_wirings(w) for w in ("partial", "outdated", "disabled")],
+    lambda: [bwd.test_stack_backward_finite_differences_gates(g) for g in ("softmax", "softmax_renorm", "sigmoid",
+                                                                          "sigmoid_norm")],
+    bwd.test_stack_backward_finite_differences_no_shared_top1,
 ]
 
 
