@@ -316,6 +316,82 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
                                    void* stream, void* stream2);
 size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L);
 
+/* ----------------------------------------------------------------- training
+ * The backward of the MoE stack for the MoE wirings (PARTIAL, OUTDATED,
+ * DISABLED), bf16 (FS_BF16) only.  The pages train FarSkip models but print no
+ * gradient formulas; these are the derivatives of the forward above:
+ *   per block, with o = o_prev + S + R and o* = o_prev + S:
+ *     dR = dO, dS = dO + dOs, do_prev = dO + dOs
+ *     routed: dw_s = <dR, y_s>, dy = w_s dR, dh = dy W3, dg = dh a SiLU'(g),
+ *             da = dh SiLU(g), dx = dg W2 + da W1, dW3 += dy h^T,
+ *             dW2 += dg u^T, dW1 += da u^T (u the block input)
+ *     shared experts: the same with dS and gate weight 1
+ *     router: dz = d(gate weights)/dz applied to dw (the gate rule of desc;
+ *             top-k selection has no gradient; the bias is not a parameter),
+ *             dW_R += dz u^T, du += dz W_R
+ *     du = sum_s dx_s (Dispatch backward) + dx_shared + dz W_R
+ *   the stack: block k's do_prev flows to o_{k-1}; its du to where u_k came
+ *   from (o_{k-1}* partial, o_{k-2} outdated, o_{k-1} disabled, x for k = 1).
+ * Stored backward operands are bf16 (dy, dg/da, dx per slot, dS, dz); every
+ * sum is fp32; the input gradient and the weight gradients are fp32 in the
+ * page's layouts.  fs_farskip_stack_train runs the forward and keeps what the
+ * backward reads (u_k, logits, routing, Dispatch permutation, pre-activations,
+ * hidden, y_perm) in `saved` (fs_train_saved_bytes(desc, L) bytes, 256-byte
+ * aligned); it needs ws of fs_workspace_bytes(desc, L).
+ * fs_farskip_stack_backward needs ws of fs_workspace_bytes_backward(desc, L). */
+
+/* Transposed weight packs of the input-gradient GEMMs, in the tiled bf16
+ * layout (sizes: fs_packed_bytes(G, N', K', FS_BF16) with the N', K' given):
+ *   fs_pack_w13t        [G, d, 2c]: element (i, q) = packed gate/up row q of W1/W2, column i
+ *   fs_pack_w3t         [G, c, d]:  element (j, i) = W3[i, j]
+ *   fs_pack_w3t_shared  [1, n_shared c_shared, d]: the transposed concatenated shared W3
+ *   fs_pack_wrt         [1, d, E rounded up to 64]: element (i, j) = W_R[j, i] (0 for j >= E) */
+fs_status fs_pack_w13t(int32_t G, int32_t c, int32_t d, const void* w1, const void* w2, void* out, void* stream);
+fs_status fs_pack_w3t(int32_t G, int32_t d, int32_t c, const void* w3, void* out, void* stream);
+fs_status fs_pack_w3t_shared(int32_t n_shared, int32_t c_shared, int32_t d, const void* w3s, void* out,
+                             void* stream);
+fs_status fs_pack_wrt(int32_t E, int32_t d, const void* w_r, void* out, void* stream);
+
+/* One block's transposed packs (device pointers; the shared ones NULL when n_shared = 0). */
+typedef struct {
+    const void* w13t;
+    const void* w3t;
+    const void* w13t_shared;   /* fs_pack_w13t(1, n_shared c_shared, d) of the shared gate/up */
+    const void* w3t_shared;
+    const void* w_rt;
+} fs_block_weights_t;
+
+/* One block's weight gradients (device, fp32, page layouts: dw_r [E, d],
+ * dw1, dw2 [E, c, d], dw3 [E, d, c], shared [n_shared, c_shared, d] and
+ * [n_shared, d, c_shared]).  Overwritten. */
+typedef struct {
+    float* dw_r;
+    float* dw1;
+    float* dw2;
+    float* dw3;
+    float* dw1_shared;
+    float* dw2_shared;
+    float* dw3_shared;
+} fs_block_grads;
+
+size_t fs_train_saved_bytes(const fs_layer_desc* desc, int L);
+size_t fs_workspace_bytes_backward(const fs_layer_desc* desc, int L);
+
+/* fs_farskip_stack for the MoE wirings, keeping the backward's inputs in `saved`. */
+fs_status fs_farskip_stack_train(const fs_layer_desc* desc, int32_t L, int32_t wiring,
+                                 const fs_block_weights* blocks, const void* x, void* o_full,
+                                 void* o_partial, void* saved, size_t saved_bytes, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* Backward of the stack run by fs_farskip_stack_train (same desc, L, wiring,
+ * blocks, saved): d_o, d_os [T, d] fp32 the gradients of o_L and o_L* (d_os
+ * NULL = zero) -> dx [T, d] fp32 and grads[L]. */
+fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_t wiring,
+                                    const fs_block_weights* blocks, const fs_block_weights_t* blocks_t,
+                                    const void* saved, size_t saved_bytes, const float* d_o,
+                                    const float* d_os, float* dx, const fs_block_grads* grads,
+                                    void* ws, size_t ws_bytes, void* stream);
+
 /* Read and clear the device error word (synchronises the device).  FS_OK when
  * no kernel recorded a fault; FS_ERR_DEVICE_STATE otherwise, with the raw code
  * in *code when code != NULL (1 = expert index out of range, 2 = inconsistent

@@ -253,7 +253,7 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 // (bf16) is quantised per row into hq before the down GEMM.
 static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_rows, const int32_t* gather, int rows,
                              const int32_t* offsets, int G, int cw, const void* w13, const void* w3, void* y,
-                             bool y_f32, int* plan, void* h, void* hq, cudaStream_t st) {
+                             bool y_f32, int* plan, void* h, void* hq, cudaStream_t st, void* gu_save = nullptr) {
     if (is_fp8(d)) {
         const int bm = tc_block_m_f8();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -269,8 +269,11 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
+        TcExtra ex;
+        ex.aux = gu_save;            // training forward: keep the pre-activations for the backward
+        ex.aux_ld = 2LL * cw;
         FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, gather, rows,
-                              true, st));
+                              true, st, &ex));
         FS_TRY(launch_tc_gemm(y_f32 ? EPI_F32 : EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d,
                               nullptr, 0, true, st));
     } else {
@@ -739,6 +742,351 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
     // join: stream waits for stream2's last work
     FS_TRY(cudaEventRecord(evU, sb));
     FS_TRY(cudaStreamWaitEvent(sa, evU, 0));
+    return FS_OK;
+}
+
+// ---------------------------------------------------------------- training
+// What the backward reads from the training forward, per block (bf16 unless
+// noted): the block input u_k, the router logits (fp32, without the bias), the
+// routing (top-k indices, gate weights), the Dispatch permutation (offsets,
+// pos, perm_src), the routed experts' pre-activations g, a (packed gate/up
+// column order) and hidden h, the routed outputs y_perm, and the shared
+// experts' pre-activations and hidden.
+struct SavedLayout {
+    size_t u, logits, idx, w, offsets, pos, perm, gu, h, y, gu_s, h_s, size;
+};
+
+static SavedLayout saved_layout(const fs_layer_desc* d) {
+    const size_t A = 256;
+    const size_t T = d->T, E = d->E, k = d->k, dm = d->d, c = d->c;
+    const size_t rows = T * k, cw = static_cast<size_t>(d->n_shared) * d->c_shared;
+    SavedLayout l;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at_ = o; o = align_up(o + bytes, A); return at_; };
+    l.u = take(T * dm * 2);
+    l.logits = take(T * E * 4);
+    l.idx = take(rows * 4);
+    l.w = take(rows * 4);
+    l.offsets = take((E + 1) * 4);
+    l.pos = take(rows * 4);
+    l.perm = take(rows * 4);
+    l.gu = take(rows * 2 * c * 2);
+    l.h = take(rows * c * 2);
+    l.y = take(rows * dm * 2);
+    l.gu_s = take(T * 2 * cw * 2);
+    l.h_s = take(T * cw * 2);
+    l.size = o;
+    return l;
+}
+
+// Workspace of the backward: gradients of o_0..o_L and o_0*..o_L* (fp32), the
+// per-block step buffers, the padded K-segment plan and two transposed-operand
+// buffers that the weight-gradient GEMMs reuse in turn.
+struct BwdLayout {
+    size_t go, gos, dy, dw, dS, dprev, dgu, dx, du, dgu_s, dz, plan_r, plan_s, kb, poff, src_row, kb1, ta, tb, end;
+    long long P, Tp;
+    int Epad;
+};
+
+static BwdLayout bwd_layout(const fs_layer_desc* d, int L) {
+    const size_t A = 256;
+    const size_t T = d->T, E = d->E, k = d->k, dm = d->d, c = d->c;
+    const size_t rows = T * k, cw = static_cast<size_t>(d->n_shared) * d->c_shared;
+    BwdLayout l;
+    l.Epad = static_cast<int>(align_up(E, 64));
+    l.Tp = static_cast<long long>(align_up(T, 64));
+    l.P = static_cast<long long>(align_up(rows + 64 * E, 64));
+    const size_t Pm = static_cast<size_t>(l.P > l.Tp ? l.P : l.Tp);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at_ = o; o = align_up(o + bytes, A); return at_; };
+    l.go = take(static_cast<size_t>(L + 1) * T * dm * 4);
+    l.gos = take(static_cast<size_t>(L + 1) * T * dm * 4);
+    l.dy = take(rows * dm * 2);
+    l.dw = take(rows * 4);
+    l.dS = take(T * dm * 2);
+    l.dprev = take(T * dm * 4);
+    l.dgu = take(rows * 2 * c * 2);
+    l.dx = take(rows * dm * 2);
+    l.du = take(T * dm * 4);
+    l.dgu_s = take(T * 2 * cw * 2);
+    l.dz = take(T * l.Epad * 2);
+    l.plan_r = take(2 * (E + 1) * sizeof(int));
+    l.plan_s = take(4 * sizeof(int));
+    l.kb = take(2 * E * sizeof(int));
+    l.poff = take((E + 1) * sizeof(int));
+    l.src_row = take(static_cast<size_t>(l.P) * sizeof(int));
+    l.kb1 = take(2 * sizeof(int));
+    size_t ra = dm > 2 * c ? dm : 2 * c;
+    if (2 * cw > ra) ra = 2 * cw;
+    if (static_cast<size_t>(l.Epad) > ra) ra = l.Epad;
+    size_t rb = c > dm ? c : dm;
+    if (cw > rb) rb = cw;
+    l.ta = take(ra * Pm * 2);
+    l.tb = take(rb * Pm * 2);
+    l.end = o;
+    return l;
+}
+
+static fs_status check_train(const fs_layer_desc* desc, int L, int wiring) {
+    FS_CHECK(check_desc(desc));
+    if (desc->dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+    if (L < 1) return FS_ERR_INVALID_ARG;
+    if (wiring < FS_WIRE_PARTIAL || wiring > FS_WIRE_DISABLED) return FS_ERR_INVALID_ARG;
+    return FS_OK;
+}
+
+size_t fs_train_saved_bytes(const fs_layer_desc* desc, int L) {
+    if (check_train(desc, L < 1 ? 1 : L, FS_WIRE_PARTIAL) != FS_OK || L < 1) return 0;
+    return static_cast<size_t>(L) * saved_layout(desc).size;
+}
+
+size_t fs_workspace_bytes_backward(const fs_layer_desc* desc, int L) {
+    if (check_train(desc, L < 1 ? 1 : L, FS_WIRE_PARTIAL) != FS_OK || L < 1) return 0;
+    return bwd_layout(desc, L).end;
+}
+
+fs_status fs_pack_w13t(int32_t G, int32_t c, int32_t d, const void* w1, const void* w2, void* out, void* stream) {
+    if (G < 1 || c < 1 || d < 1) return FS_ERR_INVALID_ARG;
+    if (c % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w1));
+    FS_CHECK(need(w2));
+    FS_CHECK(need(out));
+    FS_TRY(launch_pack_t(0, G, d, 2 * c, c, d, 0, 0, w1, w2, out, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+fs_status fs_pack_w3t(int32_t G, int32_t d, int32_t c, const void* w3, void* out, void* stream) {
+    if (G < 1 || c < 1 || d < 1) return FS_ERR_INVALID_ARG;
+    if (c % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w3));
+    FS_CHECK(need(out));
+    FS_TRY(launch_pack_t(1, G, c, d, c, d, 0, 0, w3, nullptr, out, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+fs_status fs_pack_w3t_shared(int32_t n_shared, int32_t c_shared, int32_t d, const void* w3s, void* out,
+                             void* stream) {
+    if (n_shared < 1 || c_shared < 1 || d < 1) return FS_ERR_INVALID_ARG;
+    if (c_shared % 64 || d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w3s));
+    FS_CHECK(need(out));
+    FS_TRY(launch_pack_t(2, 1, n_shared * c_shared, d, 0, d, c_shared, 0, w3s, nullptr, out,
+                         static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+fs_status fs_pack_wrt(int32_t E, int32_t d, const void* w_r, void* out, void* stream) {
+    if (E < 1 || d < 1) return FS_ERR_INVALID_ARG;
+    if (d % 64) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(w_r));
+    FS_CHECK(need(out));
+    FS_TRY(launch_pack_t(3, 1, d, static_cast<int>(align_up(E, 64)), 0, d, 0, E, w_r, nullptr, out,
+                         static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+fs_status fs_farskip_stack_train(const fs_layer_desc* desc, int32_t L, int32_t wiring, const fs_block_weights* blocks,
+                                 const void* x, void* o_full, void* o_partial, void* saved, size_t saved_bytes,
+                                 void* ws, size_t ws_bytes, void* stream) {
+    FS_CHECK(check_train(desc, L, wiring));
+    if (!blocks) return FS_ERR_INVALID_ARG;
+    FS_CHECK(need(x));
+    FS_CHECK(need(o_full));
+    if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
+    for (int b = 0; b < L; ++b) {
+        FS_CHECK(need(blocks[b].w_r));
+        FS_CHECK(need(blocks[b].w13));
+        FS_CHECK(need(blocks[b].w3));
+        if (blocks[b].bias && !aligned16(blocks[b].bias)) return FS_ERR_UNSUPPORTED;
+        if (desc->n_shared > 0) {
+            FS_CHECK(need(blocks[b].w13_shared));
+            FS_CHECK(need(blocks[b].w3_shared));
+        }
+    }
+    FS_CHECK(check_ws(desc, L, ws, ws_bytes));
+    if (!saved) return FS_ERR_INVALID_ARG;
+    const SavedLayout sl = saved_layout(desc);
+    if ((reinterpret_cast<uintptr_t>(saved) & 255u) || saved_bytes < static_cast<size_t>(L) * sl.size)
+        return FS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Layout l = layout(desc, L);
+    const Layout l0 = layout(desc, 0);
+    const int T = desc->T, rows = desc->T * desc->k, cw = desc->n_shared * desc->c_shared;
+    auto sv = [&](int blk, size_t off) { return static_cast<uint8_t*>(saved) + static_cast<size_t>(blk) * sl.size + off; };
+    int32_t* counts = at<int32_t>(ws, l.counts);
+    void* x_perm = at<void>(ws, l.x_perm);
+    void* s_out = cw > 0 ? at<void>(ws, l.s_out) : nullptr;
+    FS_TRY(launch_copy(sv(0, sl.u), x, static_cast<size_t>(T) * desc->d * 2, st));
+    const void* o_prev = x;
+    int prev_dtype = FS_BF16;
+    for (int b = 1; b <= L; ++b) {
+        const fs_block_weights& bw = blocks[b - 1];
+        const int blk = b - 1;
+        const bool last = (b == L);
+        const void* u = sv(blk, sl.u);
+        int32_t* idx = reinterpret_cast<int32_t*>(sv(blk, sl.idx));
+        float* w = reinterpret_cast<float*>(sv(blk, sl.w));
+        int32_t* offsets = reinterpret_cast<int32_t*>(sv(blk, sl.offsets));
+        int32_t* pos = reinterpret_cast<int32_t*>(sv(blk, sl.pos));
+        void* y = sv(blk, sl.y);
+        FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, reinterpret_cast<float*>(sv(blk, sl.logits)), ws, st));
+        FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, reinterpret_cast<int32_t*>(sv(blk, sl.perm)),
+                               x_perm, ws, st));
+        FS_CHECK(swiglu_impl(desc, x_perm, rows, nullptr, rows, offsets, desc->E, desc->c, bw.w13, bw.w3, y, false,
+                             at<int>(ws, l0.plan_r), sv(blk, sl.h), nullptr, st, sv(blk, sl.gu)));
+        if (s_out)
+            FS_CHECK(swiglu_impl(desc, u, T, nullptr, T, nullptr, 1, cw, bw.w13_shared, bw.w3_shared, s_out, true,
+                                 at<int>(ws, l0.plan_s), sv(blk, sl.h_s), nullptr, st, sv(blk, sl.gu_s)));
+        void* o_k = last ? o_full : at<void>(ws, l.ring[(b - 1) % l.nring]);
+        void* os_k = last ? o_partial : at<void>(ws, l.star[(b - 1) % l.nstar]);
+        void* u_next = last ? nullptr : sv(b, sl.u);
+        const int out_dtype = last ? FS_BF16 : FS_F32;
+        FS_CHECK(combine_impl(desc, y, pos, w, o_prev, prev_dtype, s_out, nullptr, os_k, o_k, out_dtype, u_next, wiring,
+                              nullptr, st));
+        o_prev = o_k;
+        prev_dtype = out_dtype;
+    }
+    return FS_OK;
+}
+
+fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_t wiring,
+                                    const fs_block_weights* blocks, const fs_block_weights_t* blocks_t,
+                                    const void* saved, size_t saved_bytes, const float* d_o, const float* d_os,
+                                    float* dx, const fs_block_grads* grads, void* ws, size_t ws_bytes, void* stream) {
+    FS_CHECK(check_train(desc, L, wiring));
+    if (!blocks || !blocks_t || !grads) return FS_ERR_INVALID_ARG;
+    FS_CHECK(need(d_o));
+    FS_CHECK(need(dx));
+    if (d_os && !aligned16(d_os)) return FS_ERR_UNSUPPORTED;
+    const bool sh = desc->n_shared > 0;
+    for (int b = 0; b < L; ++b) {
+        if (blocks[b].bias && !aligned16(blocks[b].bias)) return FS_ERR_UNSUPPORTED;
+        FS_CHECK(need(blocks_t[b].w13t));
+        FS_CHECK(need(blocks_t[b].w3t));
+        FS_CHECK(need(blocks_t[b].w_rt));
+        FS_CHECK(need(grads[b].dw_r));
+        FS_CHECK(need(grads[b].dw1));
+        FS_CHECK(need(grads[b].dw2));
+        FS_CHECK(need(grads[b].dw3));
+        if (sh) {
+            FS_CHECK(need(blocks_t[b].w13t_shared));
+            FS_CHECK(need(blocks_t[b].w3t_shared));
+            FS_CHECK(need(grads[b].dw1_shared));
+            FS_CHECK(need(grads[b].dw2_shared));
+            FS_CHECK(need(grads[b].dw3_shared));
+        }
+    }
+    if (!saved || !ws) return FS_ERR_INVALID_ARG;
+    const SavedLayout sl = saved_layout(desc);
+    const BwdLayout bl = bwd_layout(desc, L);
+    if ((reinterpret_cast<uintptr_t>(saved) & 255u) || saved_bytes < static_cast<size_t>(L) * sl.size)
+        return FS_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < bl.end) return FS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int T = desc->T, E = desc->E, k = desc->k, dm = desc->d, c = desc->c;
+    const int rows = T * k, cs = desc->c_shared, cw = desc->n_shared * cs;
+    const size_t n = static_cast<size_t>(T) * dm;
+    auto sv = [&](int blk, size_t off) {
+        return static_cast<const uint8_t*>(saved) + static_cast<size_t>(blk) * sl.size + off;
+    };
+    float* go = at<float>(ws, bl.go);
+    float* gos = at<float>(ws, bl.gos);
+    void* dy = at<void>(ws, bl.dy);
+    float* dw = at<float>(ws, bl.dw);
+    void* dS = at<void>(ws, bl.dS);
+    float* dprev = at<float>(ws, bl.dprev);
+    void* dgu = at<void>(ws, bl.dgu);
+    void* dxp = at<void>(ws, bl.dx);
+    float* du = at<float>(ws, bl.du);
+    void* dgu_s = at<void>(ws, bl.dgu_s);
+    void* dz = at<void>(ws, bl.dz);
+    int* plan_r = at<int>(ws, bl.plan_r);
+    int* plan_s = at<int>(ws, bl.plan_s);
+    int* kb = at<int>(ws, bl.kb);
+    int* poff = at<int>(ws, bl.poff);
+    int* src_row = at<int>(ws, bl.src_row);
+    int* kb1 = at<int>(ws, bl.kb1);
+    void* ta = at<void>(ws, bl.ta);
+    void* tb = at<void>(ws, bl.tb);
+    const int bm = tc_block_m();
+    const int max_mt = ceil_div(rows, bm) + E;
+    FS_TRY(launch_zero(go, static_cast<size_t>(L + 1) * n * 4, st));
+    FS_TRY(launch_zero(gos, static_cast<size_t>(L + 1) * n * 4, st));
+    FS_TRY(launch_copy(go + static_cast<size_t>(L) * n, d_o, n * 4, st));
+    if (d_os) FS_TRY(launch_copy(gos + static_cast<size_t>(L) * n, d_os, n * 4, st));
+    FS_TRY(launch_plan(nullptr, 1, T, bm, plan_s, st));
+    FS_TRY(launch_set_pair(kb1, 0, static_cast<int>(bl.Tp / 64), st));
+    for (int b = L; b >= 1; --b) {
+        const int blk = b - 1;
+        const fs_block_weights& bw = blocks[blk];
+        const fs_block_weights_t& bt = blocks_t[blk];
+        const fs_block_grads& gr = grads[blk];
+        const void* u = sv(blk, sl.u);
+        const int32_t* idx = reinterpret_cast<const int32_t*>(sv(blk, sl.idx));
+        const float* w = reinterpret_cast<const float*>(sv(blk, sl.w));
+        const int32_t* offsets = reinterpret_cast<const int32_t*>(sv(blk, sl.offsets));
+        const int32_t* pos = reinterpret_cast<const int32_t*>(sv(blk, sl.pos));
+        const int32_t* perm = reinterpret_cast<const int32_t*>(sv(blk, sl.perm));
+        // Combine backward: dy_perm, dw, dS = dO + dOs, do_prev
+        FS_TRY(launch_combine_backward(go + static_cast<size_t>(b) * n, gos + static_cast<size_t>(b) * n,
+                                       sv(blk, sl.y), pos, w, T, dm, k, dy, dw, sh ? dS : nullptr, dprev, st));
+        // routed experts: dh = dy W3 with the SwiGLU backward in the epilogue, then dx = dgu W13
+        FS_TRY(launch_plan(offsets, E, rows, bm, plan_r, st));
+        TcExtra exr;
+        exr.aux = const_cast<uint8_t*>(sv(blk, sl.gu));
+        exr.aux_ld = 2LL * c;
+        FS_TRY(launch_tc_gemm(EPI_DSWIGLU, dy, rows, bt.w3t, E, c, dm, plan_r, max_mt, dgu, 2LL * c, c, nullptr, 0, true,
+                              st, &exr));
+        FS_TRY(launch_tc_gemm(EPI_BF16, dgu, rows, bt.w13t, E, dm, 2 * c, plan_r, max_mt, dxp, dm, dm, nullptr, 0, true,
+                              st));
+        FS_TRY(launch_gather_sum(dxp, pos, T, dm, k, du, st));     // Dispatch backward
+        TcExtra acc;
+        acc.accumulate = 1;
+        if (sh) {
+            TcExtra exs;
+            exs.aux = const_cast<uint8_t*>(sv(blk, sl.gu_s));
+            exs.aux_ld = 2LL * cw;
+            FS_TRY(launch_tc_gemm(EPI_DSWIGLU, dS, T, bt.w3t_shared, 1, cw, dm, plan_s, ceil_div(T, bm) + 1, dgu_s,
+                                  2LL * cw, cw, nullptr, 0, true, st, &exs));
+            FS_TRY(launch_tc_gemm(EPI_F32, dgu_s, T, bt.w13t_shared, 1, dm, 2 * cw, plan_s, ceil_div(T, bm) + 1, du, dm,
+                                  dm, nullptr, 0, true, st, &acc));
+        }
+        // router: dz through the gate rule, du += dz W_R
+        FS_TRY(launch_gate_backward(reinterpret_cast<const float*>(sv(blk, sl.logits)), bw.bias, idx, w, dw, T, E,
+                                    bl.Epad, k, desc->gate, dz, st));
+        FS_TRY(launch_tc_gemm(EPI_F32, dz, T, bt.w_rt, 1, dm, bl.Epad, plan_s, ceil_div(T, bm) + 1, du, dm, dm, nullptr,
+                              0, true, st, &acc));
+        // weight gradients: contractions over each expert's padded row segment
+        FS_TRY(launch_pad_plan(offsets, E, rows, bl.P, kb, poff, src_row, st));
+        FS_TRY(launch_transpose_pad(dy, dm, src_row, 0, nullptr, bl.P, ta, st));
+        FS_TRY(launch_transpose_pad(sv(blk, sl.h), c, src_row, 0, nullptr, bl.P, tb, st));
+        FS_TRY(launch_wgrad_gemm(ta, bl.P, tb, kb, E, dm, c, gr.dw3, nullptr, 0, 0, st));
+        FS_TRY(launch_transpose_pad(dgu, 2 * c, src_row, 0, nullptr, bl.P, ta, st));
+        FS_TRY(launch_transpose_pad(u, dm, src_row, 0, perm, bl.P, tb, st));
+        FS_TRY(launch_wgrad_gemm(ta, bl.P, tb, kb, E, 2 * c, dm, gr.dw1, gr.dw2, 1, 0, st));
+        if (sh) {
+            FS_TRY(launch_transpose_pad(dS, dm, nullptr, T, nullptr, bl.Tp, ta, st));
+            FS_TRY(launch_transpose_pad(sv(blk, sl.h_s), cw, nullptr, T, nullptr, bl.Tp, tb, st));
+            FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, dm, cw, gr.dw3_shared, nullptr, 2, cs, st));
+            FS_TRY(launch_transpose_pad(dgu_s, 2 * cw, nullptr, T, nullptr, bl.Tp, ta, st));
+            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, tb, st));
+            FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, 2 * cw, dm, gr.dw1_shared, gr.dw2_shared, 1, 0, st));
+        } else {
+            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, tb, st));
+        }
+        FS_TRY(launch_transpose_pad(dz, bl.Epad, nullptr, T, nullptr, bl.Tp, ta, st));
+        FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, E, dm, gr.dw_r, nullptr, 0, 0, st));
+        // the wiring: o_{b-1} receives do_prev, u_b's source receives du (u_1 = o_0 = x)
+        float* g_prev = go + static_cast<size_t>(b - 1) * n;
+        FS_TRY(launch_add_f32(g_prev, dprev, static_cast<long long>(n), st));
+        float* target;
+        if (b == 1) target = go;
+        else if (wiring == FS_WIRE_PARTIAL) target = gos + static_cast<size_t>(b - 1) * n;
+        else if (wiring == FS_WIRE_OUTDATED) target = go + static_cast<size_t>(b - 2) * n;
+        else target = go + static_cast<size_t>(b - 1) * n;
+        FS_TRY(launch_add_f32(target, du, static_cast<long long>(n), st));
+    }
+    FS_TRY(launch_copy(dx, go, n * 4, st));
     return FS_OK;
 }
 

@@ -68,6 +68,9 @@ struct Args {
     int b_blocked;           // B in the tiled weight layout [G][n_tiles][K/BK][256][128 bytes] (3D map)
     const float* a_scale;    // FP8: scale of A row p (a_scale[p])
     const float* b_scale;    // FP8: scale of B row n of group g (b_scale[g N + n])
+    void* aux;               // TcExtra::aux (stored pre-activations out / in)
+    long long aux_ld;
+    int accumulate;          // EPI_F32: out += acc
 };
 
 struct Tile {
@@ -102,8 +105,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const in
     return r;
 }
 
-// Epilogue of one accumulator tile for the thread owning TMEM lane `r` of its
-// CTA (row a_row + r of the output), columns of half `half` of the tile.
 // v[j] <- (v[j] * sa) * sb[j] for 32 fp32 accumulator columns.
 __device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float* sb) {
     const float4* s4 = reinterpret_cast<const float4*>(sb);
@@ -116,6 +117,8 @@ __device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float*
     }
 }
 
+// Epilogue of one accumulator tile for the thread owning TMEM lane `r` of its
+// CTA (row a_row + r of the output), columns of half `half` of the tile.
 // With F8 the accumulator is scaled by the A row's and the B rows' scales:
 // (acc * a_scale[row]) * b_scale[g N + col].
 template <int EPI, bool F8 = false>
@@ -156,6 +159,23 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                             }
                         }
                     }
+                    if (args.aux) {   // training forward: keep g, a (bf16) for the backward
+                        uint32_t pg[16], pu[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            pg[q] = pack_bf16x2(__uint_as_float(gv[2 * q]), __uint_as_float(gv[2 * q + 1]));
+                            pu[q] = pack_bf16x2(__uint_as_float(uv[2 * q]), __uint_as_float(uv[2 * q + 1]));
+                        }
+                        __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(args.aux) + orow * args.aux_ld + tl.n * BN +
+                                            g2 * 128 + j0;
+                        uint4* gd = reinterpret_cast<uint4*>(gu);
+                        uint4* ud = reinterpret_cast<uint4*>(gu + 64);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            gd[v] = make_uint4(pg[4 * v], pg[4 * v + 1], pg[4 * v + 2], pg[4 * v + 3]);
+                            ud[v] = make_uint4(pu[4 * v], pu[4 * v + 1], pu[4 * v + 2], pu[4 * v + 3]);
+                        }
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -192,6 +212,52 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                     dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
             }
         }
+    } else if constexpr (EPI == EPI_DSWIGLU) {
+        // accumulator = dh of hidden columns j = 256 n + c; g_j, a_j sit at packed
+        // columns 128 (j / 64) + j % 64 and that + 64 of the aux row, and dg, da
+        // go to the same packed columns of out
+        const int rem = args.out_cols - tl.n * BN;
+        const int ncols = rem >= BN ? BN : rem;
+        const __nv_bfloat16* GU = static_cast<const __nv_bfloat16*>(args.aux);
+        __nv_bfloat16* D = static_cast<__nv_bfloat16*>(args.out);
+        const int cend = min(ncols, (half + 1) * (BN / 2));
+#pragma unroll 1
+        for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c0, v);
+            tmem_ld_wait();
+            if (row_ok) {
+                const int j0 = tl.n * BN + c0;
+                const long long pc = 128LL * (j0 >> 6) + (j0 & 63);
+                const uint4* gs = reinterpret_cast<const uint4*>(GU + orow * args.aux_ld + pc);
+                const uint4* as = reinterpret_cast<const uint4*>(GU + orow * args.aux_ld + pc + 64);
+                uint32_t gw[16], aw[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 x = __ldg(gs + q), y = __ldg(as + q);
+                    gw[4 * q] = x.x; gw[4 * q + 1] = x.y; gw[4 * q + 2] = x.z; gw[4 * q + 3] = x.w;
+                    aw[4 * q] = y.x; aw[4 * q + 1] = y.y; aw[4 * q + 2] = y.z; aw[4 * q + 3] = y.w;
+                }
+                uint32_t pg[16], pa[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float g0 = bf16lo(gw[q]), g1 = bf16hi(gw[q]);
+                    const float a0 = bf16lo(aw[q]), a1 = bf16hi(aw[q]);
+                    const float s0 = 1.0f / (1.0f + __expf(-g0)), s1 = 1.0f / (1.0f + __expf(-g1));
+                    const float dh0 = __uint_as_float(v[2 * q]), dh1 = __uint_as_float(v[2 * q + 1]);
+                    pg[q] = pack_bf16x2(dh0 * a0 * (s0 * (1.0f + g0 * (1.0f - s0))),
+                                        dh1 * a1 * (s1 * (1.0f + g1 * (1.0f - s1))));
+                    pa[q] = pack_bf16x2(dh0 * (g0 * s0), dh1 * (g1 * s1));
+                }
+                uint4* gd = reinterpret_cast<uint4*>(D + orow * args.ldo + pc);
+                uint4* ad = reinterpret_cast<uint4*>(D + orow * args.ldo + pc + 64);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    gd[w] = make_uint4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
+                    ad[w] = make_uint4(pa[4 * w], pa[4 * w + 1], pa[4 * w + 2], pa[4 * w + 3]);
+                }
+            }
+        }
     } else {  // EPI_F32
         const int rem = args.out_cols - tl.n * BN;
         const int ncols = rem >= BN ? BN : rem;
@@ -207,6 +273,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                 if constexpr (F8) scale_cols32(v, sa, sb + c0);
                 float* dst = Z + orow * args.ldo + tl.n * BN + c0;
                 const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
+                if (args.accumulate) {
+                    for (int j = 0; j < nv; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + dst[j]);
+                }
                 if (vec && nv == 32) {
 #pragma unroll
                     for (int w = 0; w < 8; ++w)
@@ -692,6 +761,208 @@ __global__ void plan_kernel(const int* __restrict__ offsets, int G, int n_rows, 
     }
 }
 
+// ------------------------------------------------------- weight gradients
+// out_g = A B^T over group g's padded K segment (launch_wgrad_gemm): the warp
+// roles, pipeline and bounded waits of grouped_gemm_kernel, with tiles (g, m,
+// n) of 128 x 256 (m inner, so consecutive tiles share the B slab) and the
+// K blocks [kb[2g], kb[2g+1]) of 64 columns.  A group with an empty segment
+// issues no MMAs and its epilogue writes zeros.
+struct WArgs {
+    const int* kb;
+    int G, M, N, m_tiles, n_tiles, max_kb;
+    float* out;
+    float* out2;
+    int remap, split;
+    int* err;
+};
+
+__device__ __forceinline__ float* wgrad_dst(const WArgs& a, int g, int row, int col) {
+    if (a.remap == 1) {      // packed gate/up row q -> W2 (gate) or W1 (up) row 64 (q / 128) + q % 64
+        const int blk = row >> 7, within = row & 127;
+        const long long drow = static_cast<long long>(g) * (a.M / 2) + blk * 64 + (within & 63);
+        return (within < 64 ? a.out2 : a.out) + drow * a.N + col;
+    }
+    if (a.remap == 2)        // concatenated shared columns jj -> [jj / split][row][jj % split]
+        return a.out + (static_cast<long long>(col / a.split) * a.M + row) * a.split + col % a.split;
+    return a.out + (static_cast<long long>(g) * a.M + row) * a.N + col;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const WArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + NACC;
+    uint64_t* fin = tempty + NACC;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* kbs = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);    // [2 G]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = args.G;
+    for (int i = threadIdx.x; i < G; i += THREADS) {
+        int a = args.kb[2 * i], b = args.kb[2 * i + 1];
+        if (a < 0 || b < a || b > args.max_kb) {     // corrupt plan: record it, treat as empty
+            set_dev_error(args.err, DEV_ERR_OFFSETS);
+            a = b = 0;
+        }
+        kbs[2 * i] = a;
+        kbs[2 * i + 1] = b;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), EPI_WARPS);
+        }
+        mbar_init(smem_u32(fin), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int per_g = args.m_tiles * args.n_tiles;
+    const int total = G * per_g;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const int g = t / per_g, rr = t - g * per_g;
+                const int m = rr % args.m_tiles, n = rr / args.m_tiles;
+                for (int kb = kbs[2 * g]; kb < kbs[2 * g + 1]; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m * BM);
+                    tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, n * BN);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            const int pending = issued < STAGES ? issued : STAGES;
+            for (int j = 1; j <= pending; ++j) {
+                int s = stage - j;
+                uint32_t ph = phase;
+                if (s < 0) { s += STAGES; ph ^= 1u; }
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(&full[s]), ph)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+                const int g = t / per_g;
+                const int acc = it & 1;
+                const uint32_t use = static_cast<uint32_t>(it >> 1);
+                if (!mbar_wait(smem_u32(&tempty[acc]), (use & 1u) ^ 1u, abort_flag, args.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const int kb0 = kbs[2 * g];
+                for (int kb = kb0; kb < kbs[2 * g + 1]; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err)) { ok = false; break; }
+                    tc_fence_after();
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sa));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sa + A_STAGE));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&tfull[acc]));
+            }
+            tc_commit(smem_u32(fin));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(fin), 0)) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) { set_dev_error(args.err, DEV_ERR_TIMEOUT); break; }
+            }
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const int g = t / per_g, rr = t - g * per_g;
+            const int m = rr % args.m_tiles, n = rr / args.m_tiles;
+            const bool any = kbs[2 * g + 1] > kbs[2 * g];
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            const int row = m * BM + r;
+            const int rem = args.N - n * BN;
+            const int ncols = rem >= BN ? BN : rem;
+            const int cend = min(ncols, (half + 1) * (BN / 2));
+#pragma unroll 1
+            for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
+                uint32_t v[32];
+                if (any) {
+                    tmem_ld32(tbase + c0, v);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0u;
+                }
+                if (row < args.M) {
+                    float* dst = wgrad_dst(args, g, row, n * BN + c0);
+                    const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
+                    if (nv == 32) {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+                            reinterpret_cast<uint4*>(dst)[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+                    } else {
+                        for (int j = 0; j < nv; ++j) dst[j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 }  // namespace tc
 
 // ------------------------------------------------------------------- host
@@ -779,7 +1050,8 @@ static bool use_pair() {
 template <int EPI>
 static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,
                                   const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                                  const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st) {
+                                  const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st,
+                                  const TcExtra* ex) {
     const bool pair = use_pair();
     if (pair && gather_rows) return cudaErrorNotSupported;
     static bool attr_set[2] = {false, false};
@@ -819,6 +1091,9 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.b_blocked = b_blocked ? 1 : 0;
     args.a_scale = nullptr;
     args.b_scale = nullptr;
+    args.aux = ex ? ex->aux : nullptr;
+    args.aux_ld = ex ? ex->aux_ld : 0;
+    args.accumulate = ex ? ex->accumulate : 0;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -877,6 +1152,9 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     args.b_blocked = 1;
     args.a_scale = a_scale;
     args.b_scale = b_scale;
+    args.aux = nullptr;
+    args.aux_ld = 0;
+    args.accumulate = 0;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -918,20 +1196,67 @@ bool tc_gather_supported() { return !use_pair(); }
 
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                           const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st) {
+                           const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st,
+                           const TcExtra* ex) {
     switch (epi) {
         case EPI_SWIGLU:
             return launch_tc_impl<EPI_SWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
-                                              gather_rows, gather_limit, b_blocked, st);
+                                              gather_rows, gather_limit, b_blocked, st, ex);
         case EPI_BF16:
             return launch_tc_impl<EPI_BF16>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
-                                            gather_rows, gather_limit, b_blocked, st);
+                                            gather_rows, gather_limit, b_blocked, st, ex);
         case EPI_F32:
             return launch_tc_impl<EPI_F32>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
-                                           gather_rows, gather_limit, b_blocked, st);
+                                           gather_rows, gather_limit, b_blocked, st, ex);
+        case EPI_DSWIGLU:
+            if (!ex || !ex->aux) return cudaErrorInvalidValue;
+            return launch_tc_impl<EPI_DSWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
+                                               gather_rows, gather_limit, b_blocked, st, ex);
         default:
             return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const int* kb, int G, int M, int N, float* out,
+                              float* out2, int remap, int split, cudaStream_t st) {
+    if (G < 1 || G > kMaxGroups || M < 1 || N < 1 || N % 32 || P % 64) return cudaErrorInvalidValue;
+    if (remap == 1 && (M % 128 || !out2)) return cudaErrorInvalidValue;
+    if (remap == 2 && (G != 1 || split < 32 || split % 32 || N % split)) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    cudaError_t e;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(tc::wgrad_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap ta, tb;
+    e = make_map(&ta, A, M, P, tc::BM);
+    if (e != cudaSuccess) return e;
+    e = make_map(&tb, B, N, P, tc::BN);
+    if (e != cudaSuccess) return e;
+    tc::WArgs args;
+    args.kb = kb;
+    args.G = G;
+    args.M = M;
+    args.N = N;
+    args.m_tiles = (M + tc::BM - 1) / tc::BM;
+    args.n_tiles = (N + tc::BN - 1) / tc::BN;
+    args.max_kb = static_cast<int>(P / 64);
+    args.out = out;
+    args.out2 = out2;
+    args.remap = remap;
+    args.split = split;
+    args.err = dev_error_ptr();
+    int sms = 0;
+    e = num_sms(&sms);
+    if (e != cudaSuccess) return e;
+    const long long total = static_cast<long long>(G) * args.m_tiles * args.n_tiles;
+    int grid = static_cast<int>(total < sms ? total : sms);
+    if (grid < 1) grid = 1;
+    tc::wgrad_gemm_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    count_launch();
+    return cudaGetLastError();
 }
 
 int tc_block_m() { return use_pair() ? tc::P_BM : tc::BM; }

@@ -10,7 +10,21 @@ constexpr int kMaxGroups = 1024;   // groups (experts) one grouped GEMM handles
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 512;   // router top-k kernel limit
 
-enum { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2 };
+// EPI_DSWIGLU: the accumulator is dh (hidden columns); with the stored
+// pre-activations g, a (TcExtra::aux, packed gate/up column order) it writes
+// dg = dh a SiLU'(g) and da = dh SiLU(g) (bf16) at the same packed columns.
+enum { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_DSWIGLU = 3 };
+
+// Optional epilogue inputs/outputs of launch_tc_gemm:
+//   aux          EPI_SWIGLU: also store the pre-activations g, a (bf16) here
+//                (training forward); EPI_DSWIGLU: read them from here
+//   aux_ld       row stride of aux in elements (2c)
+//   accumulate   EPI_F32: out += acc instead of out = acc
+struct TcExtra {
+    void* aux = nullptr;
+    long long aux_ld = 0;
+    int accumulate = 0;
+};
 
 void count_launch();
 int* dev_error_ptr();
@@ -24,7 +38,17 @@ bool tc_gather_supported();
 // b_blocked: B is in the tiled weight layout of pack.cu ([G][ceil(N/256)][K/64][256][64])
 cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void* B, int G, int N, int K,
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
-                           const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st);
+                           const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st,
+                           const TcExtra* ex = nullptr);
+// Weight-gradient GEMM: for each group g, out_g [M, N] = sum over the group's K
+// segment of A[m, k] B[n, k], with A [M, P] and B [N, P] bf16 (K = P
+// contiguous: transposed activations, every group's segment padded to a
+// multiple of 64 columns) and kb[2g], kb[2g+1] the segment's first and end
+// 64-column blocks (device).  fp32 out; remap 0: out [G][M][N]; remap 1 (packed
+// gate/up rows, M = 2c): rows to out2 (gate, W2) and out (up, W1), each
+// [G][c][N]; remap 2 (concatenated shared down columns): [N / split][M][split].
+cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const int* kb, int G, int M, int N, float* out,
+                              float* out2, int remap, int split, cudaStream_t st);
 // FP8 E4M3 operands (kind::f8f6f4): A codes [a_rows, K] with a_scale[a_rows],
 // B packed by quant.cu with b_scale[G N]; the epilogue multiplies the fp32
 // accumulator by a_scale[row] b_scale[g N + col].  Single-CTA kernel only.
@@ -77,5 +101,29 @@ cudaError_t launch_pack_w13_fp8(int G, int c, int d, const void* w1, const void*
 cudaError_t launch_pack_w3_fp8(int G, int d, int c, const void* w3, void* w3p, cudaStream_t st);
 cudaError_t launch_pack_w3_shared_fp8(int ns, int cs, int d, const void* w3s, void* w3cat, cudaStream_t st);
 cudaError_t launch_quant_rows(const void* x, long long rows, int cols, void* q, cudaStream_t st);
+
+// backward.cu -- memory-bound steps of the MoE block's backward
+cudaError_t launch_combine_backward(const float* dO, const float* dOs, const void* y_perm, const int32_t* pos,
+                                    const float* topk_w, int T, int d, int k, void* dy_perm, float* dw, void* dS,
+                                    float* do_prev, cudaStream_t st);
+cudaError_t launch_gather_sum(const void* dx_perm, const int32_t* pos, int T, int d, int k, float* du,
+                              cudaStream_t st);
+cudaError_t launch_gate_backward(const float* logits, const float* bias, const int32_t* idx, const float* w,
+                                 const float* dw, int T, int E, int E_pad, int k, int gate, void* dz,
+                                 cudaStream_t st);
+cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t st);
+cudaError_t launch_set_pair(int* dst, int a, int b, cudaStream_t st);
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);   // bytes % 16 == 0
+cudaError_t launch_zero(void* dst, size_t bytes, cudaStream_t st);                    // bytes % 16 == 0
+// padded K segments of the weight-gradient GEMMs: kb [2G], poff [G+1], src_row [P]
+cudaError_t launch_pad_plan(const int* offsets, int G, int n_rows, long long P, int* kb, int* poff, int* src_row,
+                            cudaStream_t st);
+// dst [cols, P] = transpose of src [rows, cols] bf16 through the padded column map
+// (src_row NULL: identity for pc < n_valid); gather: read row gather[r]
+cudaError_t launch_transpose_pad(const void* src, int cols, const int* src_row, int n_valid, const int* gather,
+                                 long long P, void* dst, cudaStream_t st);
+// transposed weight packs (mode 0 W13^T, 1 W3^T, 2 W3cat^T, 3 W_R^T) in the tiled layout [G][N'/256][K'/64][256][64]
+cudaError_t launch_pack_t(int mode, int G, int Np, int Kp, int c, int d, int cs, int E, const void* a, const void* b,
+                          void* out, cudaStream_t st);
 
 }  // namespace fs

@@ -42,6 +42,15 @@ class BlockWeights(ctypes.Structure):
                 ("w_att", ctypes.c_void_p)]
 
 
+class BlockWeightsT(ctypes.Structure):
+    _fields_ = [("w13t", ctypes.c_void_p), ("w3t", ctypes.c_void_p), ("w13t_shared", ctypes.c_void_p),
+                ("w3t_shared", ctypes.c_void_p), ("w_rt", ctypes.c_void_p)]
+
+
+class BlockGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dw_r", "dw1", "dw2", "dw3", "dw1_shared", "dw2_shared", "dw3_shared")]
+
+
 _VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 _SIGS = {
     "fs_workspace_bytes": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
@@ -65,6 +74,17 @@ _SIGS = {
     "fs_workspace_bytes_overlap": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
     "fs_workspace_bytes_attn": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
     "fs_fp8_rows_bytes": (_SZ, [ctypes.c_int64, _I32]),
+    "fs_pack_w13t": (_I32, [_I32, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "fs_pack_w3t": (_I32, [_I32, _I32, _I32, _VP, _VP, _VP]),
+    "fs_pack_w3t_shared": (_I32, [_I32, _I32, _I32, _VP, _VP, _VP]),
+    "fs_pack_wrt": (_I32, [_I32, _I32, _VP, _VP, _VP]),
+    "fs_train_saved_bytes": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
+    "fs_workspace_bytes_backward": (_SZ, [ctypes.POINTER(LayerDesc), ctypes.c_int]),
+    "fs_farskip_stack_train": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP, _VP,
+                                      _VP, _VP, _SZ, _VP, _SZ, _VP]),
+    "fs_farskip_stack_backward": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights),
+                                         ctypes.POINTER(BlockWeightsT), _VP, _SZ, _VP, _VP, _VP,
+                                         ctypes.POINTER(BlockGrads), _VP, _SZ, _VP]),
     "fs_quantize_rows_fp8": (_I32, [ctypes.c_int64, _I32, _VP, _VP, _VP]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "fs_launch_count": (ctypes.c_uint64, []),
@@ -321,3 +341,105 @@ class FarSkipStack:
         fs_farskip_stack_overlap(self.desc, len(self.blocks), self.wiring, self.blocks, x, self.o_full,
                                  self.o_partial, self.ws_overlap, stream, self.stream2)
         return self.o_full, self.o_partial
+
+
+# ------------------------------------------------------------------ training
+
+def fs_train_saved_bytes(desc: LayerDesc, L: int) -> int:
+    return int(lib().fs_train_saved_bytes(ctypes.byref(desc), L))
+
+
+def fs_workspace_bytes_backward(desc: LayerDesc, L: int) -> int:
+    return int(lib().fs_workspace_bytes_backward(ctypes.byref(desc), L))
+
+
+def fs_pack_w13t(G, c, d, w1, w2, out, stream=None):
+    _check(lib().fs_pack_w13t(G, c, d, _p(w1), _p(w2), _p(out), _stream(stream)), "fs_pack_w13t")
+
+
+def fs_pack_w3t(G, d, c, w3, out, stream=None):
+    _check(lib().fs_pack_w3t(G, d, c, _p(w3), _p(out), _stream(stream)), "fs_pack_w3t")
+
+
+def fs_pack_w3t_shared(n_shared, c_shared, d, w3s, out, stream=None):
+    _check(lib().fs_pack_w3t_shared(n_shared, c_shared, d, _p(w3s), _p(out), _stream(stream)), "fs_pack_w3t_shared")
+
+
+def fs_pack_wrt(E, d, w_r, out, stream=None):
+    _check(lib().fs_pack_wrt(E, d, _p(w_r), _p(out), _stream(stream)), "fs_pack_wrt")
+
+
+def pack_block_t(cfg: LayerConfig, w: dict, stream=None) -> dict:
+    """Transposed packs of one block's bf16 weights for the input-gradient GEMMs."""
+    E, c, d = cfg.E, cfg.c, cfg.d
+    epad = (E + 63) // 64 * 64
+    out = {"w13t": _packed(E, d, 2 * c, FS_BF16, w["w1"]), "w3t": _packed(E, c, d, FS_BF16, w["w3"]),
+           "w_rt": _packed(1, d, epad, FS_BF16, w["w_r"])}
+    fs_pack_w13t(E, c, d, w["w1"].contiguous(), w["w2"].contiguous(), out["w13t"], stream)
+    fs_pack_w3t(E, d, c, w["w3"].contiguous(), out["w3t"], stream)
+    fs_pack_wrt(E, d, w["w_r"].contiguous(), out["w_rt"], stream)
+    if cfg.n_shared:
+        cw = cfg.n_shared * cfg.c_shared
+        out["w13t_shared"] = _packed(1, d, 2 * cw, FS_BF16, w["w1s"])
+        out["w3t_shared"] = _packed(1, cw, d, FS_BF16, w["w3s"])
+        fs_pack_w13t(1, cw, d, w["w1s"].contiguous(), w["w2s"].contiguous(), out["w13t_shared"], stream)
+        fs_pack_w3t_shared(cfg.n_shared, cfg.c_shared, d, w["w3s"].contiguous(), out["w3t_shared"], stream)
+    return out
+
+
+def _block_t_struct(p: dict) -> BlockWeightsT:
+    return BlockWeightsT(_p(p["w13t"]), _p(p["w3t"]), _p(p.get("w13t_shared")), _p(p.get("w3t_shared")),
+                         _p(p["w_rt"]))
+
+
+def _grads_struct(g: dict) -> BlockGrads:
+    return BlockGrads(*[_p(g.get(k)) for k in ("dW_R", "dW1", "dW2", "dW3", "dW1s", "dW2s", "dW3s")])
+
+
+class FarSkipTrainer:
+    """Forward (keeping what the backward reads) and backward of an L-block
+    FarSkip MoE stack on one GPU (bf16, MoE wirings): two library calls."""
+
+    def __init__(self, cfg: LayerConfig, raw_blocks: list, wiring: str | None = None, T: int | None = None,
+                 device="cuda"):
+        self.cfg = cfg
+        self.T = cfg.T if T is None else T
+        self.wiring = wiring or cfg.wiring
+        self.desc = make_desc(cfg, self.T)
+        L = len(raw_blocks)
+        self.L = L
+        self.blocks = [pack_block(cfg, b) for b in raw_blocks]
+        self.blocks_t = [pack_block_t(cfg, b) for b in raw_blocks]
+        self.saved = torch.empty(fs_train_saved_bytes(self.desc, L), dtype=torch.uint8, device=device)
+        self.ws = alloc_workspace(self.desc, L, device)
+        self.ws_b = torch.empty(fs_workspace_bytes_backward(self.desc, L), dtype=torch.uint8, device=device)
+        E, c, d, ns, cs = cfg.E, cfg.c, cfg.d, cfg.n_shared, cfg.c_shared
+        f32 = dict(dtype=torch.float32, device=device)
+        self.grads = []
+        for _ in range(L):
+            g = {"dW_R": torch.empty((E, d), **f32), "dW1": torch.empty((E, c, d), **f32),
+                 "dW2": torch.empty((E, c, d), **f32), "dW3": torch.empty((E, d, c), **f32)}
+            if ns:
+                g.update(dW1s=torch.empty((ns, cs, d), **f32), dW2s=torch.empty((ns, cs, d), **f32),
+                         dW3s=torch.empty((ns, d, cs), **f32))
+            self.grads.append(g)
+        self.o_full = torch.empty((self.T, d), dtype=torch.bfloat16, device=device)
+        self.o_partial = torch.empty((self.T, d), dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty((self.T, d), **f32)
+
+    def forward(self, x: torch.Tensor, stream=None):
+        arr = (BlockWeights * self.L)(*[block_struct(b) for b in self.blocks])
+        _check(lib().fs_farskip_stack_train(ctypes.byref(self.desc), self.L, WIRINGS[self.wiring], arr, _p(x),
+                                            _p(self.o_full), _p(self.o_partial), _p(self.saved), _nbytes(self.saved),
+                                            _p(self.ws), _nbytes(self.ws), _stream(stream)), "fs_farskip_stack_train")
+        return self.o_full, self.o_partial
+
+    def backward(self, d_o: torch.Tensor, d_os: torch.Tensor | None = None, stream=None):
+        arr = (BlockWeights * self.L)(*[block_struct(b) for b in self.blocks])
+        arr_t = (BlockWeightsT * self.L)(*[_block_t_struct(b) for b in self.blocks_t])
+        gr = (BlockGrads * self.L)(*[_grads_struct(g) for g in self.grads])
+        _check(lib().fs_farskip_stack_backward(ctypes.byref(self.desc), self.L, WIRINGS[self.wiring], arr, arr_t,
+                                               _p(self.saved), _nbytes(self.saved), _p(d_o), _p(d_os), _p(self.dx),
+                                               gr, _p(self.ws_b), _nbytes(self.ws_b), _stream(stream)),
+               "fs_farskip_stack_backward")
+        return self.dx, self.grads

@@ -1,0 +1,96 @@
+"""GPU parity of the MoE stack's backward (fs_farskip_stack_train +
+fs_farskip_stack_backward) against the oracle's backward, on the same seeded
+inputs and output gradients.
+
+The backward's stored operands are bf16 on both sides at the same points (dy,
+dg/da, the per-slot dx, dS, dz) and every sum is fp32 (GPU) / fp64 (oracle),
+so the two sides differ by accumulation order and by bf16 rounding flips of
+stored values, compounded through the L blocks.  Bounds: relative Frobenius
+<= L x 5e-3 (the end-to-end forward bound) for the input gradient and for every weight gradient, computed
+over the tokens whose routing agrees in every block (near-ties are counted
+and bounded as in the forward); a weight gradient sums over all tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_expert_gb300 import configs, fs, synth
+from parity import gpu_stack_stepwise, oracle_cfg, oracle_weights, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+REL = 5e-3
+KEYS = ("dW_R", "dW1", "dW2", "dW3", "dW1s", "dW2s", "dW3s")
+
+
+def _run(cfg, wiring, seed=5):
+    prob = synth.make_problem(cfg, DEV)
+    x = prob["x"]
+    tr = fs.FarSkipTrainer(cfg, prob["blocks"], wiring=wiring)
+    o, o_star = tr.forward(x)
+    torch.cuda.synchronize()
+    assert fs.fs_get_error() == (0, 0)
+    ref_o, ref_os, routing, _ = gpu_stack_stepwise(cfg, tr.blocks, x, wiring)
+    assert torch.equal(o, ref_o) and torch.equal(o_star, ref_os), "training forward != inference forward"
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    dO = torch.randn((cfg.T, cfg.d), generator=g, device=DEV)
+    dOs = torch.randn((cfg.T, cfg.d), generator=g, device=DEV)
+    dx, grads = tr.backward(dO, dOs)
+    torch.cuda.synchronize()
+    assert fs.fs_get_error() == (0, 0)
+    ref = oracle.stack_backward(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x),
+                                to64(dO), to64(dOs))
+    fwd = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x))
+    same = np.ones(cfg.T, bool)
+    for b in range(cfg.L):
+        same &= np.all(np.sort(routing[b], 1) == np.sort(fwd["topk_idx"][b], 1), axis=1)
+    assert (~same).sum() <= max(1, int(1e-3 * cfg.T)), "routing differs on %d tokens" % int((~same).sum())
+    bound = REL * cfg.L
+    got = to64(dx)[same]
+    want = ref["dx"][same]
+    rel = np.linalg.norm(got - want) / np.linalg.norm(want)
+    stats = {"dx": rel}
+    assert rel <= bound, "dx: relative Frobenius %.3e > %.1e" % (rel, bound)
+    for b in range(cfg.L):
+        for key in KEYS:
+            if key not in grads[b]:
+                continue
+            gw = to64(grads[b][key])
+            rw = ref[key][b]
+            r = np.linalg.norm(gw - rw) / max(np.linalg.norm(rw), 1e-30)
+            stats["%s[%d]" % (key, b)] = r
+            assert r <= bound, "block %d %s: relative Frobenius %.3e > %.1e" % (b + 1, key, r, bound)
+    print("backward parity", cfg.name, wiring, {k: "%.2e" % v for k, v in stats.items()})
+    return stats
+
+
+@pytest.mark.parametrize("gate", ["sigmoid_norm", "softmax", "softmax_renorm", "sigmoid"])
+def test_block_backward_gates(fs, gate):
+    cfg = configs.LayerConfig("bw", T=300, d=256, E=8, k=2, c=128, n_shared=1, c_shared=128, L=1, gate=gate,
+                              dtype="bf16")
+    _run(cfg, "partial")
+
+
+@pytest.mark.parametrize("wiring", ["partial", "outdated", "disabled"])
+def test_stack_backward_wirings(fs, wiring):
+    L = 3 if wiring != "disabled" else 2
+    cfg = configs.LayerConfig("bws", T=333, d=256, E=8, k=2, c=192, n_shared=2, c_shared=128, L=L,
+                              gate="softmax_renorm", dtype="bf16")
+    _run(cfg, wiring)
+
+
+def test_backward_multi_tile_ragged(fs):
+    """Several M/N tiles, ragged expert segments (K of the weight-gradient GEMMs
+    padded per expert), 16 experts, top-4."""
+    cfg = configs.LayerConfig("bwm", T=1000, d=384, E=16, k=4, c=256, n_shared=1, c_shared=256, L=2,
+                              gate="sigmoid_norm", dtype="bf16")
+    _run(cfg, "partial")
+
+
+def test_backward_skewed_routing_and_small_E(fs):
+    """Zipf-skewed router bias (experts with few or no rows; empty segments
+    give zero gradients), E = 16 < 64 (padded router operands), top-1, no shared."""
+    cfg = configs.LayerConfig("bwz", T=520, d=192, E=16, k=1, c=128, n_shared=0, c_shared=0, L=2,
+                              gate="sigmoid", dtype="bf16", zipf_s=1.2)
+    _run(cfg, "outdated")
