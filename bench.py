@@ -39,6 +39,7 @@ from mixture_experts_layer_expert_gb300 import configs, synth  # noqa: E402
 
 METRIC = "MoE layer tokens/s, DeepSeek-V3 shape, 64K tokens; % of roofline (BF16/HBM)"
 METRIC_FP8 = "MoE layer tokens/s, FP8 E4M3 expert GEMMs; % of roofline (FP8/HBM)"
+METRIC_TRAIN = "MoE layer training tokens/s (forward keeping state + backward); % of bf16 tensor peak"
 FP8_PER_BF16 = 2.0     # nominal dense tensor rate ratio (4.5 / 2.25 PFLOP/s)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
@@ -346,6 +347,114 @@ def e2e_timing(cfg, stack, x, steps, stream):
     return e0.elapsed_time(e1) / steps, nb, stack.o_full.numel() * stack.o_full.element_size()
 
 
+# ------------------------------------------------------------ training step
+
+def run_train(args, cfg, rank, world, local):
+    """One step = fs_farskip_stack_train + fs_farskip_stack_backward over T tokens
+    (bf16), with a fixed output gradient dO resident on the device."""
+    from mixture_experts_layer_expert_gb300 import build, fs
+
+    build.build()
+    fs.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    prob = synth.make_problem(cfg, device=dev)
+    tr = fs.FarSkipTrainer(cfg, prob["blocks"], device=dev)
+    x = prob["x"]
+    del prob
+    torch.cuda.empty_cache()
+    T, L = cfg.T, cfg.L
+    g = torch.Generator(device=dev).manual_seed(3)
+    dO = torch.randn((T, cfg.d), generator=g, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        tr.forward(x)
+        tr.backward(dO)
+    torch.cuda.synchronize()
+    st, code = fs.fs_get_error()
+    if st != 0:
+        raise RuntimeError("device error word after warm-up: %d" % code)
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier()
+    torch.cuda.synchronize()
+    l0 = fs.fs_launch_count()
+    ev = [cuda_events(3) for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        tr.forward(x)
+        ev[i][1].record(stream)
+        tr.backward(dO)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    launches = (fs.fs_launch_count() - l0) // args.steps
+    barrier()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    ms = fwd_ms + bwd_ms
+    # end to end: x and dO from pinned host memory, dx back to the host
+    x_h, d_h = x.cpu().pin_memory(), dO.cpu().pin_memory()
+    dx_h = torch.empty(tr.dx.shape, dtype=tr.dx.dtype).pin_memory()
+    xd, dd = torch.empty_like(x), torch.empty_like(dO)
+    e0, e1 = cuda_events(2)
+    n_e2e = max(2, args.steps // 2)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        xd.copy_(x_h, non_blocking=True)
+        dd.copy_(d_h, non_blocking=True)
+        tr.forward(xd)
+        tr.backward(dd)
+        dx_h.copy_(tr.dx, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    clocks = sampler.stop() if sampler else None
+    st, code = fs.fs_get_error()
+    if st != 0:
+        raise RuntimeError("device error word after timing: %d" % code)
+    ms, e2e_ms = reduce_max([ms, e2e_ms], world, dev)
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    gemm = cfg.gemm_flops_per_block() * L
+    router = 2.0 * T * cfg.d * cfg.E * L
+    flops = 3.0 * gemm + 3.0 * router          # forward, input gradients, weight gradients
+    tflops = flops / (ms / 1e3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    return {
+        "metric": METRIC_TRAIN,
+        "value": round(T * world / (ms / 1e3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), output gradient dO~N(0,1)",
+        "config": {"workload": configs.describe(cfg) + ", training step", "T_per_gpu": T, "L": L,
+                   "wiring": cfg.wiring, "l2": "inputs larger than L2"},
+        "roofline": {"bound": "tensor", "kernel": "all GEMMs of the step (forward, input and weight gradients)",
+                     "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "peak_kind": "bf16 sustained, %s" % pk_src, "traffic": None,
+                     "flops_per_step": flops},
+        "breakdown_ms": {"forward_train": round(fwd_ms, 4), "backward": round(bwd_ms, 4)},
+        "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size() + dO.numel() * dO.element_size(),
+                "d2h_bytes_per_step": tr.dx.numel() * tr.dx.element_size(), "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": int(launches * args.steps),
+        "gpu_launches_per_step": int(launches),
+        "clocks": clocks,
+    }
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_cfg_for(cfg):
@@ -414,6 +523,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (forward keeping state + backward) instead of the forward")
     ap.add_argument("--overlap", action="store_true",
                     help="two-stream FarSkip schedule (router/dispatch/shared of block k+1 beside block k's routed GEMMs)")
     args = ap.parse_args()
@@ -426,6 +537,8 @@ def main():
         torch.distributed.init_process_group(backend=backend)
     if args.impl == "reference":
         line = run_reference(args, cfg, rank, world)
+    elif args.train:
+        line = run_train(args, cfg, rank, world, local)
     else:
         line = run_ours(args, cfg, rank, world, local)
     if line is not None:

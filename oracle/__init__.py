@@ -284,14 +284,18 @@ def block_backward(cfg: _Cfg, weights: Weights, u: np.ndarray, dO: np.ndarray, d
 
 
 def stack_backward(cfg: _Cfg, weights: list, wiring: str, x: np.ndarray, dOL: np.ndarray,
-                   dOLs: np.ndarray | None = None):
-    """Backward of stack() for the MoE wirings: dx and per-block weight gradients [L, ...]."""
+                   dOLs: np.ndarray | None = None, want_grads: bool = True):
+    """Backward of stack() for the MoE wirings: dx and (want_grads) the per-block
+    weight gradients [L, ...]."""
     x = np.ascontiguousarray(x)
     L = len(weights)
     n = x.shape[0]
     arr = (_W * L)(*[w.struct() for w in weights])
     out = {"dx": np.zeros((n, cfg.d))}
-    out.update(_grad_arrays(cfg, L))
+    if want_grads:
+        out.update(_grad_arrays(cfg, L))
+    else:
+        out.update({k: None for k in ("dW_R", "dW1", "dW2", "dW3", "dW1s", "dW2s", "dW3s")})
     dOL = np.ascontiguousarray(dOL, dtype=np.float64)
     dOLs = None if dOLs is None else np.ascontiguousarray(dOLs, dtype=np.float64)
     _check(lib().oracle_stack_backward(ctypes.byref(cfg), arr, ctypes.c_int(L), ctypes.c_int(WIRINGS[wiring]),

@@ -904,7 +904,7 @@ int oracle_block_backward(const oracle_cfg* cfg, const oracle_weights* wts, int 
         }
     }
     if (bad) rc = -2;
-    if (!rc) {
+    if (!rc && dW1 && dW2 && dW3 && dW_R) {
         /* weight gradients: sums over the (token, slot) pairs routed to each expert */
 #pragma omp parallel for schedule(dynamic, 1)
         for (int e = 0; e < E; ++e) {
@@ -934,7 +934,7 @@ int oracle_block_backward(const oracle_cfg* cfg, const oracle_weights* wts, int 
                 for (int t = 0; t < n_tok; ++t) row[i] += r_dz[(size_t)t * E + e] * u[(size_t)t * d + i];
             }
         }
-        if (ns > 0) {
+        if (ns > 0 && dW1s && dW2s && dW3s) {
 #pragma omp parallel for schedule(static)
             for (int jj = 0; jj < cw; ++jj) {
                 const int sh = jj / cs, j = jj % cs;
@@ -962,7 +962,8 @@ int oracle_block_backward(const oracle_cfg* cfg, const oracle_weights* wts, int 
  * visited from L down to 1; block k's do_prev flows to o_{k-1}, and its du to
  * where u_k came from -- o_{k-1}* (partial), o_{k-2} (outdated) or o_{k-1}
  * (disabled), x for k = 1 -- through the storage rounding of u_k as the
- * identity.  Weight gradients are [L, ...] block-major. */
+ * identity.  Weight gradients are [L, ...] block-major; with dW_R NULL none
+ * are computed (the input gradient alone). */
 int oracle_stack_backward(const oracle_cfg* cfg, const oracle_weights* wts, int L, int wiring,
                           int n_tok, const void* x, int x_dtype, const double* dOL, const double* dOLs,
                           double* dx, double* dW_R, double* dW1, double* dW2, double* dW3,
@@ -988,10 +989,13 @@ int oracle_stack_backward(const oracle_cfg* cfg, const oracle_weights* wts, int 
         for (size_t i = 0; i < n; ++i) dx[i] = 0.0;
         for (int b = L; b >= 1 && !rc; --b) {
             const size_t wo = (size_t)(b - 1);
+            const int gw = dW_R != NULL;    /* weight gradients wanted */
             rc = oracle_block_backward(cfg, wts + (b - 1), n_tok, U + (size_t)(b - 1) * n, go + n * b, gos + n * b,
-                                       du, dp, NULL, dW_R + wo * E * d, dW1 + wo * E * c * d, dW2 + wo * E * c * d,
-                                       dW3 + wo * E * d * c, ns ? dW1s + wo * ns * cs * d : NULL,
-                                       ns ? dW2s + wo * ns * cs * d : NULL, ns ? dW3s + wo * ns * d * cs : NULL);
+                                       du, dp, NULL, gw ? dW_R + wo * E * d : NULL, gw ? dW1 + wo * E * c * d : NULL,
+                                       gw ? dW2 + wo * E * c * d : NULL, gw ? dW3 + wo * E * d * c : NULL,
+                                       gw && ns ? dW1s + wo * ns * cs * d : NULL,
+                                       gw && ns ? dW2s + wo * ns * cs * d : NULL,
+                                       gw && ns ? dW3s + wo * ns * d * cs : NULL);
             if (rc) break;
             double* g_prev = go + n * (b - 1);                     /* o_{b-1} */
             for (size_t i = 0; i < n; ++i) g_prev[i] += dp[i];
