@@ -779,11 +779,12 @@ static SavedLayout saved_layout(const fs_layer_desc* d) {
     return l;
 }
 
-// Workspace of the backward: gradients of o_0..o_L and o_0*..o_L* (fp32), the
-// per-block step buffers, the padded K-segment plan and two transposed-operand
-// buffers that the weight-gradient GEMMs reuse in turn.
+// Workspace of the backward: the gradients of the inner residuals o_1..o_{L-1}
+// and o_1*..o_{L-1}* (fp32), the per-block step buffers, the padded K-segment
+// plan and two transposed-operand buffers that the weight-gradient GEMMs reuse
+// in turn.
 struct BwdLayout {
-    size_t go, gos, dy, dw, dS, dprev, dgu, dx, du, dgu_s, dz, plan_r, plan_s, kb, poff, src_row, kb1, ta, tb, end;
+    size_t go, gos, dy, dw, dS, dgu, dx, dgu_s, dz, plan_r, plan_s, kb, poff, src_row, kb1, ta, tb, end;
     long long P, Tp;
     int Epad;
 };
@@ -799,15 +800,13 @@ static BwdLayout bwd_layout(const fs_layer_desc* d, int L) {
     const size_t Pm = static_cast<size_t>(l.P > l.Tp ? l.P : l.Tp);
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at_ = o; o = align_up(o + bytes, A); return at_; };
-    l.go = take(static_cast<size_t>(L + 1) * T * dm * 4);
-    l.gos = take(static_cast<size_t>(L + 1) * T * dm * 4);
+    l.go = take(static_cast<size_t>(L) * T * dm * 4);      // gradients of o_1 .. o_{L-1} (slot b)
+    l.gos = take(static_cast<size_t>(L) * T * dm * 4);     // and of o_1* .. o_{L-1}*
     l.dy = take(rows * dm * 2);
     l.dw = take(rows * 4);
     l.dS = take(T * dm * 2);
-    l.dprev = take(T * dm * 4);
     l.dgu = take(rows * 2 * c * 2);
     l.dx = take(rows * dm * 2);
-    l.du = take(T * dm * 4);
     l.dgu_s = take(T * 2 * cw * 2);
     l.dz = take(T * l.Epad * 2);
     l.plan_r = take(2 * (E + 1) * sizeof(int));
@@ -816,11 +815,14 @@ static BwdLayout bwd_layout(const fs_layer_desc* d, int L) {
     l.poff = take((E + 1) * sizeof(int));
     l.src_row = take(static_cast<size_t>(l.P) * sizeof(int));
     l.kb1 = take(2 * sizeof(int));
+    // tiled transposed operands: A rows in blocks of 128, B rows in blocks of 256
     size_t ra = dm > 2 * c ? dm : 2 * c;
     if (2 * cw > ra) ra = 2 * cw;
     if (static_cast<size_t>(l.Epad) > ra) ra = l.Epad;
+    ra = align_up(ra, 128);
     size_t rb = c > dm ? c : dm;
     if (cw > rb) rb = cw;
+    rb = align_up(rb, 256);
     l.ta = take(ra * Pm * 2);
     l.tb = take(rb * Pm * 2);
     l.end = o;
@@ -994,10 +996,8 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
     void* dy = at<void>(ws, bl.dy);
     float* dw = at<float>(ws, bl.dw);
     void* dS = at<void>(ws, bl.dS);
-    float* dprev = at<float>(ws, bl.dprev);
     void* dgu = at<void>(ws, bl.dgu);
     void* dxp = at<void>(ws, bl.dx);
-    float* du = at<float>(ws, bl.du);
     void* dgu_s = at<void>(ws, bl.dgu_s);
     void* dz = at<void>(ws, bl.dz);
     int* plan_r = at<int>(ws, bl.plan_r);
@@ -1010,10 +1010,19 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
     void* tb = at<void>(ws, bl.tb);
     const int bm = tc_block_m();
     const int max_mt = ceil_div(rows, bm) + E;
-    FS_TRY(launch_zero(go, static_cast<size_t>(L + 1) * n * 4, st));
-    FS_TRY(launch_zero(gos, static_cast<size_t>(L + 1) * n * 4, st));
-    FS_TRY(launch_copy(go + static_cast<size_t>(L) * n, d_o, n * 4, st));
-    if (d_os) FS_TRY(launch_copy(gos + static_cast<size_t>(L) * n, d_os, n * 4, st));
+    // gradients of o_b (b = 0..L) and o_b* (b = 1..L): the caller's d_o, d_os for
+    // b = L, dx itself for o_0 = x, workspace in between; accumulated into
+    auto g_o = [&](int b) -> float* {
+        return b == L ? const_cast<float*>(d_o) : (b == 0 ? dx : go + static_cast<size_t>(b) * n);
+    };
+    auto g_os = [&](int b) -> float* {
+        return b == L ? const_cast<float*>(d_os) : gos + static_cast<size_t>(b) * n;
+    };
+    FS_TRY(launch_zero(dx, n * 4, st));
+    if (L > 1) {
+        FS_TRY(launch_zero(go + n, static_cast<size_t>(L - 1) * n * 4, st));
+        FS_TRY(launch_zero(gos + n, static_cast<size_t>(L - 1) * n * 4, st));
+    }
     FS_TRY(launch_plan(nullptr, 1, T, bm, plan_s, st));
     FS_TRY(launch_set_pair(kb1, 0, static_cast<int>(bl.Tp / 64), st));
     for (int b = L; b >= 1; --b) {
@@ -1027,9 +1036,16 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
         const int32_t* offsets = reinterpret_cast<const int32_t*>(sv(blk, sl.offsets));
         const int32_t* pos = reinterpret_cast<const int32_t*>(sv(blk, sl.pos));
         const int32_t* perm = reinterpret_cast<const int32_t*>(sv(blk, sl.perm));
-        // Combine backward: dy_perm, dw, dS = dO + dOs, do_prev
-        FS_TRY(launch_combine_backward(go + static_cast<size_t>(b) * n, gos + static_cast<size_t>(b) * n,
-                                       sv(blk, sl.y), pos, w, T, dm, k, dy, dw, sh ? dS : nullptr, dprev, st));
+        // the wiring: block b's do_prev goes to o_{b-1}; its du to where u_b came
+        // from (o_{b-1}* partial, o_{b-2} outdated, o_{b-1} disabled, x for b = 1)
+        float* target;
+        if (b == 1) target = g_o(0);
+        else if (wiring == FS_WIRE_PARTIAL) target = g_os(b - 1);
+        else if (wiring == FS_WIRE_OUTDATED) target = g_o(b - 2);
+        else target = g_o(b - 1);
+        // Combine backward: dy_perm, dw, dS = dO + dOs; do_prev accumulated into o_{b-1}'s gradient
+        FS_TRY(launch_combine_backward(g_o(b), g_os(b), sv(blk, sl.y), pos, w, T, dm, k, dy, dw, sh ? dS : nullptr,
+                                       g_o(b - 1), st));
         // routed experts: dh = dy W3 with the SwiGLU backward in the epilogue, then dx = dgu W13
         FS_TRY(launch_plan(offsets, E, rows, bm, plan_r, st));
         TcExtra exr;
@@ -1039,7 +1055,7 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
                               st, &exr));
         FS_TRY(launch_tc_gemm(EPI_BF16, dgu, rows, bt.w13t, E, dm, 2 * c, plan_r, max_mt, dxp, dm, dm, nullptr, 0, true,
                               st));
-        FS_TRY(launch_gather_sum(dxp, pos, T, dm, k, du, st));     // Dispatch backward
+        FS_TRY(launch_gather_sum(dxp, pos, T, dm, k, target, st));     // Dispatch backward
         TcExtra acc;
         acc.accumulate = 1;
         if (sh) {
@@ -1048,45 +1064,35 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
             exs.aux_ld = 2LL * cw;
             FS_TRY(launch_tc_gemm(EPI_DSWIGLU, dS, T, bt.w3t_shared, 1, cw, dm, plan_s, ceil_div(T, bm) + 1, dgu_s,
                                   2LL * cw, cw, nullptr, 0, true, st, &exs));
-            FS_TRY(launch_tc_gemm(EPI_F32, dgu_s, T, bt.w13t_shared, 1, dm, 2 * cw, plan_s, ceil_div(T, bm) + 1, du, dm,
-                                  dm, nullptr, 0, true, st, &acc));
+            FS_TRY(launch_tc_gemm(EPI_F32, dgu_s, T, bt.w13t_shared, 1, dm, 2 * cw, plan_s, ceil_div(T, bm) + 1, target,
+                                  dm, dm, nullptr, 0, true, st, &acc));
         }
         // router: dz through the gate rule, du += dz W_R
         FS_TRY(launch_gate_backward(reinterpret_cast<const float*>(sv(blk, sl.logits)), bw.bias, idx, w, dw, T, E,
                                     bl.Epad, k, desc->gate, dz, st));
-        FS_TRY(launch_tc_gemm(EPI_F32, dz, T, bt.w_rt, 1, dm, bl.Epad, plan_s, ceil_div(T, bm) + 1, du, dm, dm, nullptr,
-                              0, true, st, &acc));
+        FS_TRY(launch_tc_gemm(EPI_F32, dz, T, bt.w_rt, 1, dm, bl.Epad, plan_s, ceil_div(T, bm) + 1, target, dm, dm,
+                              nullptr, 0, true, st, &acc));
         // weight gradients: contractions over each expert's padded row segment
         FS_TRY(launch_pad_plan(offsets, E, rows, bl.P, kb, poff, src_row, st));
-        FS_TRY(launch_transpose_pad(dy, dm, src_row, 0, nullptr, bl.P, ta, st));
-        FS_TRY(launch_transpose_pad(sv(blk, sl.h), c, src_row, 0, nullptr, bl.P, tb, st));
+        FS_TRY(launch_transpose_pad(dy, dm, src_row, 0, nullptr, bl.P, 128, ta, st));
+        FS_TRY(launch_transpose_pad(sv(blk, sl.h), c, src_row, 0, nullptr, bl.P, 256, tb, st));
         FS_TRY(launch_wgrad_gemm(ta, bl.P, tb, kb, E, dm, c, gr.dw3, nullptr, 0, 0, st));
-        FS_TRY(launch_transpose_pad(dgu, 2 * c, src_row, 0, nullptr, bl.P, ta, st));
-        FS_TRY(launch_transpose_pad(u, dm, src_row, 0, perm, bl.P, tb, st));
+        FS_TRY(launch_transpose_pad(dgu, 2 * c, src_row, 0, nullptr, bl.P, 128, ta, st));
+        FS_TRY(launch_transpose_pad(u, dm, src_row, 0, perm, bl.P, 256, tb, st));
         FS_TRY(launch_wgrad_gemm(ta, bl.P, tb, kb, E, 2 * c, dm, gr.dw1, gr.dw2, 1, 0, st));
         if (sh) {
-            FS_TRY(launch_transpose_pad(dS, dm, nullptr, T, nullptr, bl.Tp, ta, st));
-            FS_TRY(launch_transpose_pad(sv(blk, sl.h_s), cw, nullptr, T, nullptr, bl.Tp, tb, st));
+            FS_TRY(launch_transpose_pad(dS, dm, nullptr, T, nullptr, bl.Tp, 128, ta, st));
+            FS_TRY(launch_transpose_pad(sv(blk, sl.h_s), cw, nullptr, T, nullptr, bl.Tp, 256, tb, st));
             FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, dm, cw, gr.dw3_shared, nullptr, 2, cs, st));
-            FS_TRY(launch_transpose_pad(dgu_s, 2 * cw, nullptr, T, nullptr, bl.Tp, ta, st));
-            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, tb, st));
+            FS_TRY(launch_transpose_pad(dgu_s, 2 * cw, nullptr, T, nullptr, bl.Tp, 128, ta, st));
+            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, 256, tb, st));
             FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, 2 * cw, dm, gr.dw1_shared, gr.dw2_shared, 1, 0, st));
         } else {
-            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, tb, st));
+            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, 256, tb, st));
         }
-        FS_TRY(launch_transpose_pad(dz, bl.Epad, nullptr, T, nullptr, bl.Tp, ta, st));
+        FS_TRY(launch_transpose_pad(dz, bl.Epad, nullptr, T, nullptr, bl.Tp, 128, ta, st));
         FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, E, dm, gr.dw_r, nullptr, 0, 0, st));
-        // the wiring: o_{b-1} receives do_prev, u_b's source receives du (u_1 = o_0 = x)
-        float* g_prev = go + static_cast<size_t>(b - 1) * n;
-        FS_TRY(launch_add_f32(g_prev, dprev, static_cast<long long>(n), st));
-        float* target;
-        if (b == 1) target = go;
-        else if (wiring == FS_WIRE_PARTIAL) target = gos + static_cast<size_t>(b - 1) * n;
-        else if (wiring == FS_WIRE_OUTDATED) target = go + static_cast<size_t>(b - 2) * n;
-        else target = go + static_cast<size_t>(b - 1) * n;
-        FS_TRY(launch_add_f32(target, du, static_cast<long long>(n), st));
     }
-    FS_TRY(launch_copy(dx, go, n * 4, st));
     return FS_OK;
 }
 

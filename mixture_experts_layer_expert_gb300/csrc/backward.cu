@@ -32,7 +32,7 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
 // Combine backward, one warp per token t, with dR = dO and dS = dO + dOs:
 //   dy_perm[pos[t, s]] = bf16(w[t, s] dO[t])       (the routed output gradient)
 //   dw[t, s]           = <dO[t], y_perm[pos[t, s]]> (fp32; lane partials, then a shuffle tree)
-//   dS[t] = bf16(dO + dOs), do_prev[t] = dO + dOs   (when the pointers are set)
+//   dS[t] = bf16(dO + dOs), do_prev[t] += dO + dOs  (when the pointers are set)
 template <int KMAX>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 combine_backward_kernel(const float* __restrict__ dO, const float* __restrict__ dOs, const uint4* __restrict__ y_perm,
@@ -81,8 +81,9 @@ combine_backward_kernel(const float* __restrict__ dO, const float* __restrict__ 
             if (dS) dS[static_cast<long long>(t) * nv + v] = pack8(sv);
             if (do_prev) {
                 float4* o = reinterpret_cast<float4*>(do_prev + static_cast<long long>(t) * d + 8 * v);
-                o[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-                o[1] = make_float4(sv[4], sv[5], sv[6], sv[7]);
+                const float4 a = o[0], b = o[1];
+                o[0] = make_float4(a.x + sv[0], a.y + sv[1], a.z + sv[2], a.w + sv[3]);
+                o[1] = make_float4(b.x + sv[4], b.y + sv[5], b.z + sv[6], b.w + sv[7]);
             }
         }
     }
@@ -95,7 +96,7 @@ combine_backward_kernel(const float* __restrict__ dO, const float* __restrict__ 
     }
 }
 
-// Dispatch backward, one warp per token: du[t] = sum_s dx_perm[pos[t, s]] (fp32, slot order).
+// Dispatch backward, one warp per token: du[t] += sum_s dx_perm[pos[t, s]] (fp32, slot order).
 __global__ void __launch_bounds__(kBwdWarps * 32)
 gather_sum_kernel(const uint4* __restrict__ dx_perm, const int32_t* __restrict__ pos, int T, int d, int k,
                   float* __restrict__ du) {
@@ -115,8 +116,9 @@ gather_sum_kernel(const uint4* __restrict__ dx_perm, const int32_t* __restrict__
             for (int i = 0; i < 8; ++i) sum[i] += x[i];
         }
         float4* o = reinterpret_cast<float4*>(du + static_cast<long long>(t) * d + 8 * v);
-        o[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
-        o[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
+        const float4 a = o[0], b = o[1];
+        o[0] = make_float4(a.x + sum[0], a.y + sum[1], a.z + sum[2], a.w + sum[3]);
+        o[1] = make_float4(b.x + sum[4], b.y + sum[5], b.z + sum[6], b.w + sum[7]);
     }
 }
 
@@ -268,39 +270,56 @@ __global__ void pad_map_kernel(const int* __restrict__ offsets, const int* __res
     }
 }
 
-// dst [cols, P] = the transpose of src [rows, cols] (bf16) with row r of src in
-// padded column pc (src_row[pc] = r; -1 = zeros).  With src_row NULL the map is
-// pc -> pc for pc < n_valid.  With gather set, the source row read is
-// gather[r].  64 x 64 tiles through shared memory.
+// The transpose of src [rows, cols] (bf16) as a [cols, P] operand of the
+// weight-gradient GEMM, stored TILED: element (c, pc) at
+// ((c / RB) (P / 64) + pc / 64) RB 64 + (c % RB) 64 + pc % 64, so every RB x 64
+// box the GEMM loads is one contiguous block (RB = 128 for A, 256 for B).
+// Row r of src goes to padded column pc with src_row[pc] = r (-1 = zeros);
+// with src_row NULL the map is pc -> pc for pc < n_valid.  With gather set,
+// the source row read is gather[r].  64 x 64 tiles through shared memory: each
+// CTA writes one contiguous 8 KB piece of a block.
 __global__ void __launch_bounds__(256)
 transpose_pad_kernel(const __nv_bfloat16* __restrict__ src, int cols, const int* __restrict__ src_row, int n_valid,
-                     const int* __restrict__ gather, long long P, __nv_bfloat16* __restrict__ dst) {
+                     const int* __restrict__ gather, long long P, int RB, __nv_bfloat16* __restrict__ dst) {
     __shared__ uint32_t tile[64][33];       // 64 padded columns x 64 source columns (bf16 pairs), +1 against conflicts
-    const long long pc0 = static_cast<long long>(blockIdx.x) * 64;
-    const int c0 = blockIdx.y * 64;
-    // load: 64 source rows (one per padded column) x 64 columns = 32 words each
-    for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x) {
-        const int rr = i >> 5, wd = i & 31;
-        const long long pc = pc0 + rr;
-        int r = -1;
-        if (pc < P) r = src_row ? src_row[pc] : (pc < n_valid ? static_cast<int>(pc) : -1);
-        uint32_t v = 0;
-        if (r >= 0) {
-            const long long sr = gather ? gather[r] : r;
-            v = __ldg(reinterpret_cast<const uint32_t*>(src + sr * cols + c0) + wd);
+    // x runs over source column blocks, so the CTAs in flight read whole source rows
+    const int c0 = blockIdx.x * 64;
+    for (long long yb = blockIdx.y; yb < P / 64; yb += gridDim.y) {
+        const long long pc0 = yb * 64;
+        // load: 64 source rows (one per padded column) x 64 columns = 32 words each;
+        // warp w takes rows w, w + 8, ..., each lane one word of a row, and the
+        // row indices, gathered rows and words of its 8 rows are fetched as
+        // independent loads before any of them is used
+        const int wd = threadIdx.x & 31, w0 = threadIdx.x >> 5;
+        int rsrc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const long long pc = pc0 + w0 + 8 * q;
+            rsrc[q] = src_row ? __ldg(src_row + pc) : (pc < n_valid ? static_cast<int>(pc) : -1);
         }
-        tile[rr][wd] = v;
-    }
-    __syncthreads();
-    // store: 64 destination rows (source columns) x 64 padded columns
-    for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x) {
-        const int cc = i >> 5, wd = i & 31;     // destination row c0 + cc, padded columns 2 wd, 2 wd + 1
-        const long long pc = pc0 + 2 * wd;
-        if (pc >= P) continue;
-        const uint32_t a = tile[2 * wd][cc >> 1], b = tile[2 * wd + 1][cc >> 1];
-        const uint32_t lo = (cc & 1) ? (a >> 16) : (a & 0xffffu);
-        const uint32_t hi = (cc & 1) ? (b >> 16) : (b & 0xffffu);
-        reinterpret_cast<uint32_t*>(dst + static_cast<long long>(c0 + cc) * P + pc)[0] = lo | (hi << 16);
+        if (gather) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) rsrc[q] = rsrc[q] >= 0 ? __ldg(gather + rsrc[q]) : -1;
+        }
+        uint32_t v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            v[q] = rsrc[q] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<long long>(rsrc[q]) * cols + c0) + wd)
+                                : 0u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tile[w0 + 8 * q][wd] = v[q];
+        __syncthreads();
+        // store: 64 destination rows (source columns) x 64 padded columns, one
+        // contiguous 64 x 64 piece of the tiled block (c0 / RB, pc0 / 64)
+        __nv_bfloat16* piece = dst + ((static_cast<long long>(c0 / RB) * (P / 64) + pc0 / 64) * RB + c0 % RB) * 64;
+        for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x) {
+            const int cc = i >> 5, wd = i & 31;     // destination row c0 + cc, padded columns 2 wd, 2 wd + 1
+            const uint32_t a = tile[2 * wd][cc >> 1], b = tile[2 * wd + 1][cc >> 1];
+            const uint32_t lo = (cc & 1) ? (a >> 16) : (a & 0xffffu);
+            const uint32_t hi = (cc & 1) ? (b >> 16) : (b & 0xffffu);
+            reinterpret_cast<uint32_t*>(piece + cc * 64 + 2 * wd)[0] = lo | (hi << 16);
+        }
+        __syncthreads();     // the tile is reused by the next row block
     }
 }
 
@@ -453,10 +472,12 @@ cudaError_t launch_pad_plan(const int* offsets, int G, int n_rows, long long P, 
 }
 
 cudaError_t launch_transpose_pad(const void* src, int cols, const int* src_row, int n_valid, const int* gather,
-                                 long long P, void* dst, cudaStream_t st) {
-    dim3 grid(static_cast<unsigned>((P + 63) / 64), static_cast<unsigned>(cols / 64));
+                                 long long P, int RB, void* dst, cudaStream_t st) {
+    if (P % 64 || cols % 64 || (RB != 128 && RB != 256)) return cudaErrorInvalidValue;
+    const long long yb = P / 64;
+    dim3 grid(static_cast<unsigned>(cols / 64), static_cast<unsigned>(yb < 65535 ? yb : 65535));
     transpose_pad_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), cols, src_row, n_valid, gather,
-                                               P, static_cast<__nv_bfloat16*>(dst));
+                                               P, RB, static_cast<__nv_bfloat16*>(dst));
     count_launch();
     return cudaGetLastError();
 }

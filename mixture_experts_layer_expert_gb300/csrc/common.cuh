@@ -131,6 +131,26 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// 2D tiled store of a box from smem to global (x = inner coordinate, y = row;
+// x * element size a multiple of 16 bytes, both coordinates non-negative);
+// elements outside the tensor are not written.  Completion is tracked by the
+// issuing thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The smem sources of this thread's committed bulk stores have been read.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy smem writes become visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Four rows (y0..y3) of a 2D tensor, columns [x, x + box width), gathered into
 // four consecutive smem rows at dst (tile::gather4; the tensor map's box is
 // one row high).  Same completion and swizzle behaviour as tma_load_2d.

@@ -274,7 +274,18 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                 float* dst = Z + orow * args.ldo + tl.n * BN + c0;
                 const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
                 if (args.accumulate) {
-                    for (int j = 0; j < nv; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + dst[j]);
+                    if (vec && nv == 32) {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const float4 o = reinterpret_cast<const float4*>(dst)[w];
+                            v[4 * w] = __float_as_uint(__uint_as_float(v[4 * w]) + o.x);
+                            v[4 * w + 1] = __float_as_uint(__uint_as_float(v[4 * w + 1]) + o.y);
+                            v[4 * w + 2] = __float_as_uint(__uint_as_float(v[4 * w + 2]) + o.z);
+                            v[4 * w + 3] = __float_as_uint(__uint_as_float(v[4 * w + 3]) + o.w);
+                        }
+                    } else {
+                        for (int j = 0; j < nv; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + dst[j]);
+                    }
                 }
                 if (vec && nv == 32) {
 #pragma unroll
@@ -770,25 +781,40 @@ __global__ void plan_kernel(const int* __restrict__ offsets, int G, int n_rows, 
 struct WArgs {
     const int* kb;
     int G, M, N, m_tiles, n_tiles, max_kb;
-    float* out;
-    float* out2;
     int remap, split;
     int* err;
 };
 
-__device__ __forceinline__ float* wgrad_dst(const WArgs& a, int g, int row, int col) {
-    if (a.remap == 1) {      // packed gate/up row q -> W2 (gate) or W1 (up) row 64 (q / 128) + q % 64
-        const int blk = row >> 7, within = row & 127;
-        const long long drow = static_cast<long long>(g) * (a.M / 2) + blk * 64 + (within & 63);
-        return (within < 64 ? a.out2 : a.out) + drow * a.N + col;
+// The output is written by TMA stores from a 2 KB staging buffer per epilogue
+// warp (32 rows x 16 fp32 columns, 64-byte swizzle): one store instruction per
+// piece instead of 32 rows' worth of 16-byte stores per instruction.
+constexpr int W_STAGE_OFF = (STAGES * STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * 4 + 1023) / 1024 * 1024;
+constexpr int W_PIECE = 32 * 16 * 4;
+constexpr size_t W_SMEM_BYTES = 1024 + W_STAGE_OFF + EPI_WARPS * W_PIECE;
+
+// Destination (map, x, y) of the 32 x 16 piece at output row row0, column col of group g:
+//   remap 0: out [G M, N];  remap 1: packed gate/up rows -> W2 (gate, map 2) or W1 (up, map 1)
+//   row 64 (q / 128) + q % 64 of [G M/2, N];  remap 2: column jj -> [jj / split][row][jj % split]
+__device__ __forceinline__ const CUtensorMap* wgrad_piece(const WArgs& a, const CUtensorMap* o1, const CUtensorMap* o2,
+                                                          int g, int row0, int col, int& x, int& y) {
+    if (a.remap == 1) {
+        x = col;
+        y = g * (a.M / 2) + 64 * (row0 >> 7) + (row0 & 63);
+        return (row0 & 127) < 64 ? o2 : o1;
     }
-    if (a.remap == 2)        // concatenated shared columns jj -> [jj / split][row][jj % split]
-        return a.out + (static_cast<long long>(col / a.split) * a.M + row) * a.split + col % a.split;
-    return a.out + (static_cast<long long>(g) * a.M + row) * a.N + col;
+    if (a.remap == 2) {
+        x = col % a.split;
+        y = (col / a.split) * a.M + row0;
+        return o1;
+    }
+    x = col;
+    y = g * a.M + row0;
+    return o1;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const WArgs args) {
+wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2, const WArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -853,8 +879,8 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     uint8_t* sa = smem + stage * STAGE_BYTES;
-                    tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m * BM);
-                    tma_load_2d(smem_u32(sa + A_STAGE), &tmB, fb, kb * BK, n * BN);
+                    tma_load_3d(smem_u32(sa), &tmA, fb, 0, 0, m * args.max_kb + kb);
+                    tma_load_3d(smem_u32(sa + A_STAGE), &tmB, fb, 0, 0, n * args.max_kb + kb);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -911,7 +937,8 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else {
         const int quarter = warp & 3;
         const int half = (warp - 2) >> 2;
-        const int r = quarter * 32 + lane;
+        uint8_t* piece = smem + W_STAGE_OFF + (warp - 2) * W_PIECE;
+        const uint32_t piece_s = smem_u32(piece);
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const int g = t / per_g, rr = t - g * per_g;
@@ -923,29 +950,42 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            const int row = m * BM + r;
+            const int row0 = m * BM + quarter * 32;       // this warp's 32 rows
             const int rem = args.N - n * BN;
             const int ncols = rem >= BN ? BN : rem;
             const int cend = min(ncols, (half + 1) * (BN / 2));
+            if (row0 < args.M) {
 #pragma unroll 1
-            for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
-                uint32_t v[32];
-                if (any) {
-                    tmem_ld32(tbase + c0, v);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0u;
-                }
-                if (row < args.M) {
-                    float* dst = wgrad_dst(args, g, row, n * BN + c0);
-                    const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
-                    if (nv == 32) {
-#pragma unroll
-                        for (int w = 0; w < 8; ++w)
-                            reinterpret_cast<uint4*>(dst)[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+                for (int c0 = half * (BN / 2); c0 < cend; c0 += 32) {
+                    uint32_t v[32];
+                    if (any) {
+                        tmem_ld32(tbase + c0, v);
+                        tmem_ld_wait();
                     } else {
-                        for (int j = 0; j < nv; ++j) dst[j] = __uint_as_float(v[j]);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0u;
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = n * BN + c0 + 16 * h;
+                        if (col >= args.N) break;
+                        if (lane == 0) bulk_wait_read0();      // the previous piece has left the buffer
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int sw = q ^ ((lane >> 1) & 3);     // 64-byte swizzle of the 16-byte chunks
+                            *reinterpret_cast<uint4*>(piece + lane * 64 + sw * 16) =
+                                make_uint4(v[16 * h + 4 * q], v[16 * h + 4 * q + 1], v[16 * h + 4 * q + 2],
+                                           v[16 * h + 4 * q + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            int x, y;
+                            const CUtensorMap* map = wgrad_piece(args, &tmO1, &tmO2, g, row0, col, x, y);
+                            tma_store_2d(map, piece_s, x, y);
+                            bulk_commit();
+                        }
                     }
                 }
             }
@@ -953,6 +993,8 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
         }
+        if (lane == 0) bulk_wait0();      // every store of this warp has completed
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -1220,20 +1262,57 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
 cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const int* kb, int G, int M, int N, float* out,
                               float* out2, int remap, int split, cudaStream_t st) {
     if (G < 1 || G > kMaxGroups || M < 1 || N < 1 || N % 32 || P % 64) return cudaErrorInvalidValue;
+    if (G > 1 && M % 32) return cudaErrorInvalidValue;      // a 32-row piece never spans two groups
     if (remap == 1 && (M % 128 || !out2)) return cudaErrorInvalidValue;
-    if (remap == 2 && (G != 1 || split < 32 || split % 32 || N % split)) return cudaErrorInvalidValue;
+    if (remap == 2 && (G != 1 || M % 32 || split < 32 || split % 32 || N % split)) return cudaErrorInvalidValue;
     static bool attr_set = false;
     cudaError_t e;
     if (!attr_set) {
         e = cudaFuncSetAttribute(tc::wgrad_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tc::SMEM_BYTES));
+                                 static_cast<int>(tc::W_SMEM_BYTES));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    // tiled operands: A blocks of 128 rows, B blocks of 256 rows, each [rows][64]
     CUtensorMap ta, tb;
-    e = make_map(&ta, A, M, P, tc::BM);
+    const long long mt = (M + tc::BM - 1) / tc::BM, nt = (N + tc::BN - 1) / tc::BN;
+    {
+        e = get_encode();
+        if (e != cudaSuccess) return e;
+        cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(tc::BM), static_cast<cuuint64_t>(mt * (P / 64))};
+        cuuint64_t gstride[2] = {128, static_cast<cuuint64_t>(tc::BM) * 128};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tc::BM), 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A), gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    e = make_map_blocked(&tb, B, nt * (P / 64), tc::BN);
     if (e != cudaSuccess) return e;
-    e = make_map(&tb, B, N, P, tc::BN);
+    // fp32 outputs, written as 32-row x 16-column pieces with the 64-byte swizzle
+    auto out_map = [&](CUtensorMap* mp, float* base, long long rows, long long cols) -> cudaError_t {
+        cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+        cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 4};
+        cuuint32_t box[2] = {16, 32};
+        cuuint32_t estr[2] = {1, 1};
+        return g_encode(mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, gdim, gstride, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+                   ? cudaSuccess
+                   : cudaErrorInvalidValue;
+    };
+    CUtensorMap to1, to2;
+    if (remap == 1) {
+        e = out_map(&to1, out, static_cast<long long>(G) * (M / 2), N);
+        if (e == cudaSuccess) e = out_map(&to2, out2, static_cast<long long>(G) * (M / 2), N);
+    } else if (remap == 2) {
+        e = out_map(&to1, out, static_cast<long long>(N / split) * M, split);
+        to2 = to1;
+    } else {
+        e = out_map(&to1, out, static_cast<long long>(G) * M, N);
+        to2 = to1;
+    }
     if (e != cudaSuccess) return e;
     tc::WArgs args;
     args.kb = kb;
@@ -1243,8 +1322,6 @@ cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const i
     args.m_tiles = (M + tc::BM - 1) / tc::BM;
     args.n_tiles = (N + tc::BN - 1) / tc::BN;
     args.max_kb = static_cast<int>(P / 64);
-    args.out = out;
-    args.out2 = out2;
     args.remap = remap;
     args.split = split;
     args.err = dev_error_ptr();
@@ -1254,7 +1331,7 @@ cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const i
     const long long total = static_cast<long long>(G) * args.m_tiles * args.n_tiles;
     int grid = static_cast<int>(total < sms ? total : sms);
     if (grid < 1) grid = 1;
-    tc::wgrad_gemm_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+    tc::wgrad_gemm_kernel<<<grid, tc::THREADS, tc::W_SMEM_BYTES, st>>>(ta, tb, to1, to2, args);
     count_launch();
     return cudaGetLastError();
 }

@@ -41,10 +41,11 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
                            const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st,
                            const TcExtra* ex = nullptr);
 // Weight-gradient GEMM: for each group g, out_g [M, N] = sum over the group's K
-// segment of A[m, k] B[n, k], with A [M, P] and B [N, P] bf16 (K = P
-// contiguous: transposed activations, every group's segment padded to a
-// multiple of 64 columns) and kb[2g], kb[2g+1] the segment's first and end
-// 64-column blocks (device).  fp32 out; remap 0: out [G][M][N]; remap 1 (packed
+// segment of A[m, k] B[n, k], with A [M, P] and B [N, P] bf16 in the tiled
+// layouts of launch_transpose_pad (A with RB = 128, B with RB = 256; K = P, the
+// transposed activations, every group's segment padded to a multiple of 64
+// columns) and kb[2g], kb[2g+1] the segment's first and end 64-column blocks
+// (device).  fp32 out; remap 0: out [G][M][N]; remap 1 (packed
 // gate/up rows, M = 2c): rows to out2 (gate, W2) and out (up, W1), each
 // [G][c][N]; remap 2 (concatenated shared down columns): [N / split][M][split].
 cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const int* kb, int G, int M, int N, float* out,
@@ -102,7 +103,8 @@ cudaError_t launch_pack_w3_fp8(int G, int d, int c, const void* w3, void* w3p, c
 cudaError_t launch_pack_w3_shared_fp8(int ns, int cs, int d, const void* w3s, void* w3cat, cudaStream_t st);
 cudaError_t launch_quant_rows(const void* x, long long rows, int cols, void* q, cudaStream_t st);
 
-// backward.cu -- memory-bound steps of the MoE block's backward
+// backward.cu -- memory-bound steps of the MoE block's backward (do_prev and du
+// are accumulated into: +=)
 cudaError_t launch_combine_backward(const float* dO, const float* dOs, const void* y_perm, const int32_t* pos,
                                     const float* topk_w, int T, int d, int k, void* dy_perm, float* dw, void* dS,
                                     float* do_prev, cudaStream_t st);
@@ -118,10 +120,12 @@ cudaError_t launch_zero(void* dst, size_t bytes, cudaStream_t st);              
 // padded K segments of the weight-gradient GEMMs: kb [2G], poff [G+1], src_row [P]
 cudaError_t launch_pad_plan(const int* offsets, int G, int n_rows, long long P, int* kb, int* poff, int* src_row,
                             cudaStream_t st);
-// dst [cols, P] = transpose of src [rows, cols] bf16 through the padded column map
-// (src_row NULL: identity for pc < n_valid); gather: read row gather[r]
+// dst = transpose of src [rows, cols] bf16 through the padded column map (src_row
+// NULL: identity for pc < n_valid; gather: read row gather[r]), tiled as
+// [ceil(cols / RB)][P / 64][RB][64] (RB = 128 or 256; rows past cols in the last
+// row block are left as they are)
 cudaError_t launch_transpose_pad(const void* src, int cols, const int* src_row, int n_valid, const int* gather,
-                                 long long P, void* dst, cudaStream_t st);
+                                 long long P, int RB, void* dst, cudaStream_t st);
 // transposed weight packs (mode 0 W13^T, 1 W3^T, 2 W3cat^T, 3 W_R^T) in the tiled layout [G][N'/256][K'/64][256][64]
 cudaError_t launch_pack_t(int mode, int G, int Np, int Kp, int c, int d, int cs, int E, const void* a, const void* b,
                           void* out, cudaStream_t st);
