@@ -49,8 +49,11 @@ constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;   // 320
 constexpr int kGroupM = 16;                    // M-tiles per rasterisation block
 constexpr int BAR_BYTES = 256;
-constexpr size_t SMEM_BYTES =
-    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * sizeof(int);
+// bf16 outputs leave through one 2 KB staging piece per epilogue warp (32 rows x
+// 32 columns, 64-byte swizzle) and TMA stores, after the barriers and the plan
+constexpr int PIECE_OFF = (STAGES * STAGE_BYTES + BAR_BYTES + 2 * (kMaxGroups + 1) * 4 + 1023) / 1024 * 1024;
+constexpr int PIECE_BYTES = 2048;
+constexpr size_t SMEM_BYTES = 1024 + PIECE_OFF + EPI_WARPS * PIECE_BYTES;
 
 struct Args {
     const int* plan;   // [2 (G + 1)]: m-tile prefix (BM rows), then row_start
@@ -71,6 +74,7 @@ struct Args {
     void* aux;               // TcExtra::aux (stored pre-activations out / in)
     long long aux_ld;
     int accumulate;          // EPI_F32: out += acc
+    int tma_out;             // bf16 out (EPI_SWIGLU h, EPI_BF16) through the output tensor map
 };
 
 struct Tile {
@@ -121,11 +125,37 @@ __device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float*
 // CTA (row a_row + r of the output), columns of half `half` of the tile.
 // With F8 the accumulator is scaled by the A row's and the B rows' scales:
 // (acc * a_scale[row]) * b_scale[g N + col].
+// One 32-row x 32-column bf16 piece (pk: this lane's row, 16 bf16 pairs) to
+// global through the warp's staging buffer and a TMA store at (x, y).
+__device__ __forceinline__ void store_piece_bf16(const CUtensorMap* tmo, uint8_t* piece, const uint32_t* pk, int lane,
+                                                 int x, int y) {
+    if (lane == 0) bulk_wait_read0();          // the previous piece has left the buffer
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int sw = q ^ ((lane >> 1) & 3);  // 64-byte swizzle of the 16-byte chunks
+        *reinterpret_cast<uint4*>(piece + lane * 64 + sw * 16) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmo, smem_u32(piece), x, y);
+        bulk_commit();
+    }
+}
+
 template <int EPI, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, int rows_valid, int n, int r, int half,
-                                              const Args& args) {
+                                              const Args& args, const CUtensorMap* tmo = nullptr,
+                                              uint8_t* piece = nullptr) {
     const Tile tl{g, 0, n, a_row, rows_valid, 0};
     const bool row_ok = r < tl.rows_valid;
+    // TMA stores for whole 32-row pieces inside the group; a piece that crosses
+    // the group's last row keeps the masked per-thread stores, so the next
+    // group's rows are never written here
+    const int lane = r & 31, q32 = r & ~31;
+    const bool piece_ok = tmo != nullptr && q32 + 32 <= tl.rows_valid;
     const long long orow = static_cast<long long>(tl.a_row + r);
     float sa = 1.0f;
     if constexpr (F8) {
@@ -183,10 +213,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                         const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
                         pk[q] = pack_bf16x2(h0, h1);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(H + orow * args.ldo + tl.n * 128 + g2 * 64 + j0);
+                    if (piece_ok) {
+                        store_piece_bf16(tmo, piece, pk, lane, tl.n * 128 + g2 * 64 + j0, tl.a_row + q32);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(H + orow * args.ldo + tl.n * 128 + g2 * 64 + j0);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
                 }
             }
         }
@@ -206,10 +240,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
                     pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-                uint4* dst = reinterpret_cast<uint4*>(Y + orow * args.ldo + tl.n * BN + c0);
+                if (piece_ok) {
+                    store_piece_bf16(tmo, piece, pk, lane, tl.n * BN + c0, tl.a_row + q32);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(Y + orow * args.ldo + tl.n * BN + c0);
 #pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    for (int w = 0; w < 4; ++w)
+                        dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                }
             }
         }
     } else if constexpr (EPI == EPI_DSWIGLU) {
@@ -302,7 +340,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
 template <int EPI, bool F8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const Args args) {
+                    const __grid_constant__ CUtensorMap tmO, const Args args) {
     constexpr int BKE = F8 ? 128 : BK;     // K elements per stage (128 bytes per row)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -500,11 +538,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            epilogue_tile<EPI, F8>(tbase, tl.g, tl.a_row, tl.rows_valid, tl.n, r, half, args);
+            epilogue_tile<EPI, F8>(tbase, tl.g, tl.a_row, tl.rows_valid, tl.n, r, half, args,
+                                   args.tma_out ? &tmO : nullptr, smem + PIECE_OFF + (warp - 2) * PIECE_BYTES);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
         }
+        if (args.tma_out && lane == 0) bulk_wait0();     // this warp's TMA stores have completed
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -1058,6 +1099,32 @@ static cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2D bf16 output map [rows, cols] (row stride ldo elements) for 32 x 32 pieces
+// stored with the 64-byte swizzle.
+static cudaError_t make_out_map_bf16(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo) {
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ldo) * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The output map of a launch, when its epilogue stores bf16 pieces by TMA.
+static cudaError_t output_map(int epi, bool pair, void* out, long long out_rows, int out_cols, long long ldo,
+                              CUtensorMap* m, int* use) {
+    *use = 0;
+    if (pair || (epi != EPI_SWIGLU && epi != EPI_BF16)) return cudaSuccess;
+    if (out_cols % 32 || ldo % 8 || (reinterpret_cast<uintptr_t>(out) & 15u) || out_rows < 1) return cudaSuccess;
+    cudaError_t e = make_out_map_bf16(m, out, out_rows, out_cols, ldo);
+    if (e == cudaSuccess) *use = 1;
+    return e;
+}
+
 static int g_num_sms = 0;
 
 static cudaError_t num_sms(int* out) {
@@ -1136,6 +1203,9 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.aux = ex ? ex->aux : nullptr;
     args.aux_ld = ex ? ex->aux_ld : 0;
     args.accumulate = ex ? ex->accumulate : 0;
+    CUtensorMap to = ta;
+    e = output_map(EPI, pair, out, gather_rows ? gather_limit : a_rows, out_cols, ldo, &to, &args.tma_out);
+    if (e != cudaSuccess) return e;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -1148,7 +1218,7 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     } else {
         int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
         if (grid < 1) grid = 1;
-        tc::grouped_gemm_kernel<EPI><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+        tc::grouped_gemm_kernel<EPI><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, to, args);
     }
     count_launch();
     return cudaGetLastError();
@@ -1197,6 +1267,9 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     args.aux = nullptr;
     args.aux_ld = 0;
     args.accumulate = 0;
+    CUtensorMap to = ta;
+    e = output_map(EPI, pair, out, a_rows, out_cols, ldo, &to, &args.tma_out);
+    if (e != cudaSuccess) return e;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -1210,7 +1283,7 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     } else {
         int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
         if (grid < 1) grid = 1;
-        tc::grouped_gemm_kernel<EPI, true><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, args);
+        tc::grouped_gemm_kernel<EPI, true><<<grid, tc::THREADS, tc::SMEM_BYTES, st>>>(ta, tb, to, args);
     }
     count_launch();
     return cudaGetLastError();
