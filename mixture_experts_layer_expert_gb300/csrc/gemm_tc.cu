@@ -125,8 +125,8 @@ __device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float*
 // CTA (row a_row + r of the output), columns of half `half` of the tile.
 // With F8 the accumulator is scaled by the A row's and the B rows' scales:
 // (acc * a_scale[row]) * b_scale[g N + col].
-// One 32-row x 32-column bf16 piece (pk: this lane's row, 16 bf16 pairs) to
-// global through the warp's staging buffer and a TMA store at (x, y).
+// One 32-row x 64-byte piece (pk: this lane's row, 16 words: 32 bf16 or 16
+// fp32) to global through the warp's staging buffer and a TMA store at (x, y).
 __device__ __forceinline__ void store_piece_bf16(const CUtensorMap* tmo, uint8_t* piece, const uint32_t* pk, int lane,
                                                  int x, int y) {
     if (lane == 0) bulk_wait_read0();          // the previous piece has left the buffer
@@ -307,7 +307,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
             uint32_t v[32];
             tmem_ld32(tbase + c0, v);
             tmem_ld_wait();
-            if (row_ok) {
+            if (piece_ok && ncols - c0 >= 32) {       // two 32 x 16 fp32 pieces through TMA stores
+                if constexpr (F8) scale_cols32(v, sa, sb + c0);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pk[j] = v[16 * h + j];
+                    store_piece_bf16(tmo, piece, pk, lane, tl.n * BN + c0 + 16 * h, tl.a_row + q32);
+                }
+            } else if (row_ok) {
                 if constexpr (F8) scale_cols32(v, sa, sb + c0);
                 float* dst = Z + orow * args.ldo + tl.n * BN + c0;
                 const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
@@ -1114,13 +1123,36 @@ static cudaError_t make_out_map_bf16(CUtensorMap* m, void* base, long long rows,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// The output map of a launch, when its epilogue stores bf16 pieces by TMA.
-static cudaError_t output_map(int epi, bool pair, void* out, long long out_rows, int out_cols, long long ldo,
-                              CUtensorMap* m, int* use) {
+// 2D fp32 output map [rows, cols] (row stride ldo elements) for 32 x 16 pieces.
+static cudaError_t make_out_map_f32(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo) {
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ldo) * 4};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, gdim, gstride, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The output map of a launch, when its epilogue stores pieces by TMA: bf16 h
+// and y, and fp32 outputs that are written (not accumulated).
+static cudaError_t output_map(int epi, bool pair, int accumulate, void* out, long long out_rows, int out_cols,
+                              long long ldo, CUtensorMap* m, int* use) {
     *use = 0;
-    if (pair || (epi != EPI_SWIGLU && epi != EPI_BF16)) return cudaSuccess;
-    if (out_cols % 32 || ldo % 8 || (reinterpret_cast<uintptr_t>(out) & 15u) || out_rows < 1) return cudaSuccess;
-    cudaError_t e = make_out_map_bf16(m, out, out_rows, out_cols, ldo);
+    if (pair || out_rows < 1 || (reinterpret_cast<uintptr_t>(out) & 15u)) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    if (epi == EPI_SWIGLU || epi == EPI_BF16) {
+        if (out_cols % 32 || ldo % 8) return cudaSuccess;
+        e = make_out_map_bf16(m, out, out_rows, out_cols, ldo);
+    } else if (epi == EPI_F32 && !accumulate) {
+        if (out_cols % 32 || ldo % 4) return cudaSuccess;
+        e = make_out_map_f32(m, out, out_rows, out_cols, ldo);
+    } else {
+        return cudaSuccess;
+    }
     if (e == cudaSuccess) *use = 1;
     return e;
 }
@@ -1204,7 +1236,8 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.aux_ld = ex ? ex->aux_ld : 0;
     args.accumulate = ex ? ex->accumulate : 0;
     CUtensorMap to = ta;
-    e = output_map(EPI, pair, out, gather_rows ? gather_limit : a_rows, out_cols, ldo, &to, &args.tma_out);
+    e = output_map(EPI, pair, args.accumulate, out, gather_rows ? gather_limit : a_rows, out_cols, ldo, &to,
+                   &args.tma_out);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = num_sms(&sms);
@@ -1268,7 +1301,7 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     args.aux_ld = 0;
     args.accumulate = 0;
     CUtensorMap to = ta;
-    e = output_map(EPI, pair, out, a_rows, out_cols, ldo, &to, &args.tma_out);
+    e = output_map(EPI, pair, 0, out, a_rows, out_cols, ldo, &to, &args.tma_out);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = num_sms(&sms);
