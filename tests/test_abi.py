@@ -155,5 +155,43 @@ def test_fp8_argument_checks(L):
     assert fs.fs_launch_count() == 0
 
 
+def test_training_argument_checks(L):
+    """The training entry points: bf16 and the MoE wirings only; bad arguments
+    are rejected before any launch."""
+    d = desc()
+    assert fs.fs_train_saved_bytes(d, 1) > 0
+    assert fs.fs_train_saved_bytes(d, 2) == 2 * fs.fs_train_saved_bytes(d, 1)
+    assert fs.fs_workspace_bytes_backward(d, 1) > 0
+    assert fs.fs_train_saved_bytes(desc(dtype=2), 1) == 0          # FP8: no backward
+    assert fs.fs_train_saved_bytes(desc(dtype=1), 1) == 0          # fp32: no backward
+    assert fs.fs_workspace_bytes_backward(d, 0) == 0
+    blocks = (fs.BlockWeights * 1)(fs.BlockWeights(FAKE, None, FAKE, FAKE, FAKE, FAKE, None))
+    args = [ctypes.byref(d), 1, 0, blocks, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256), 1 << 40, _vp(FAKE * 256),
+            1 << 40, None]
+    a = list(args); a[2] = 3
+    assert L.fs_farskip_stack_train(*a) == 1                         # attention wiring
+    a = list(args); a[1] = 0
+    assert L.fs_farskip_stack_train(*a) == 1                         # L = 0
+    f32 = desc(dtype=1)
+    a = list(args); a[0] = ctypes.byref(f32)
+    assert L.fs_farskip_stack_train(*a) == 2                         # fp32
+    a = list(args); a[8] = 16
+    assert L.fs_farskip_stack_train(*a) == 3                         # saved buffer too small
+    bt = (fs.BlockWeightsT * 1)(fs.BlockWeightsT(FAKE, FAKE, FAKE, FAKE, FAKE))
+    gr = (fs.BlockGrads * 1)(fs.BlockGrads(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE))
+    bargs = [ctypes.byref(d), 1, 0, blocks, bt, _vp(FAKE * 256), 1 << 40, _vp(FAKE), None, _vp(FAKE), gr,
+             _vp(FAKE * 256), 1 << 40, None]
+    a = list(bargs); a[10] = None
+    assert L.fs_farskip_stack_backward(*a) == 1                      # no gradient array
+    a = list(bargs); a[8] = _vp(MIS)
+    assert L.fs_farskip_stack_backward(*a) == 2                      # misaligned d_os
+    a = list(bargs); a[12] = 16
+    assert L.fs_farskip_stack_backward(*a) == 3                      # workspace too small
+    assert L.fs_pack_w13t(0, 64, 64, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 1
+    assert L.fs_pack_w3t(1, 64, 65, _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_pack_wrt(16, 100, _vp(FAKE), _vp(FAKE), None) == 2
+    assert fs.fs_launch_count() == 0
+
+
 def test_no_launch_on_rejected_calls(L):
     assert fs.fs_launch_count() == 0
