@@ -182,6 +182,15 @@ def run_ours(args, cfg, rank, world, local):
     st, code = fs.fs_get_error()
     if st != 0:
         raise RuntimeError("device error word after warm-up: %d" % code)
+    graph_launches = None
+    if args.graph:      # one CUDA graph of the whole stack, replayed per step
+        l0 = fs.fs_launch_count()
+        stack.capture(x, overlap=args.overlap)
+        graph_launches = fs.fs_launch_count() - l0
+        for _ in range(args.warmup):
+            stack.replay()
+        torch.cuda.synchronize()
+        fwd = lambda _x: stack.replay()
     sampler = ClockSampler(local).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     barrier()
@@ -193,7 +202,7 @@ def run_ours(args, cfg, rank, world, local):
         fwd(x)
     e1.record(stream)
     torch.cuda.synchronize()
-    launches = (fs.fs_launch_count() - l0) // args.steps
+    launches = (fs.fs_launch_count() - l0) // args.steps if graph_launches is None else graph_launches
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
 
@@ -201,7 +210,7 @@ def run_ours(args, cfg, rank, world, local):
     stage_ms = per_stage_timing(cfg, stack, x, args.steps, stream)
 
     # ------------------------------------------- timed region 3: end to end
-    e2e_ms, h2d, d2h = e2e_timing(cfg, stack, x, max(2, args.steps // 2), stream)
+    e2e_ms, h2d, d2h = e2e_timing(cfg, stack, x, max(2, args.steps // 2), stream, graph=args.graph)
     clocks = sampler.stop() if sampler else None
     st, code = fs.fs_get_error()
     if st != 0:
@@ -244,7 +253,9 @@ def run_ours(args, cfg, rank, world, local):
         "vs_baseline": None,
         "dtype": {"bf16": "bf16", "f32": "f32", "fp8": "e4m3"}[cfg.dtype],
         "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), uniform router",
-        "config": {"workload": configs.describe(cfg), "schedule": "two-stream overlap" if args.overlap else "one stream",
+        "config": {"workload": configs.describe(cfg),
+                   "schedule": ("two-stream overlap" if args.overlap else "one stream") + (", CUDA graph" if args.graph
+                                                                                          else ""),
                    "T_per_gpu": T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
                    "c": cfg.c, "n_shared": cfg.n_shared, "c_shared": cfg.c_shared, "L": L, "gate": cfg.gate,
                    "wiring": cfg.wiring,
@@ -325,21 +336,23 @@ def per_stage_timing(cfg, stack, x, steps, stream):
     return {n: v / steps for n, v in tot.items()}
 
 
-def e2e_timing(cfg, stack, x, steps, stream):
-    """Host buffers in, host buffer out: pinned H2D of x, the stack, D2H of o_L."""
+def e2e_timing(cfg, stack, x, steps, stream, graph=False):
+    """Host buffers in, host buffer out: pinned H2D of x, the stack, D2H of o_L.
+    With graph, x is the captured input buffer and the stack is the graph replay."""
     x_host = x.cpu().pin_memory()
     o_host = torch.empty(stack.o_full.shape, dtype=stack.o_full.dtype).pin_memory()
-    x_dev = torch.empty_like(x)
+    x_dev = x if graph else torch.empty_like(x)
+    run = (lambda: stack.replay()) if graph else (lambda: stack.forward(x_dev))
     for _ in range(2):
         x_dev.copy_(x_host, non_blocking=True)
-        stack.forward(x_dev)
+        run()
         o_host.copy_(stack.o_full, non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = cuda_events(2)
     e0.record(stream)
     for _ in range(steps):
         x_dev.copy_(x_host, non_blocking=True)
-        stack.forward(x_dev)
+        run()
         o_host.copy_(stack.o_full, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -523,6 +536,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the stack once as a CUDA graph and replay it per step")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward keeping state + backward) instead of the forward")
     ap.add_argument("--overlap", action="store_true",

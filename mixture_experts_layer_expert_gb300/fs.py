@@ -332,6 +332,28 @@ class FarSkipStack:
                          self.ws, stream)
         return self.o_full, self.o_partial
 
+    def capture(self, x: torch.Tensor, overlap: bool = False):
+        """Record one forward (the library's launches for all L blocks, reading x and
+        writing o_full, o_partial) into a CUDA graph; replay() re-runs it.  Warm the
+        stack up (one eager forward) first so that one-time setup happens outside
+        the capture."""
+        self.graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.o_full.device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                if overlap:
+                    self.forward_overlap(x, stream=s)
+                else:
+                    self.forward(x, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        return self.graph
+
+    def replay(self):
+        """Re-run the captured forward (same x buffer, same outputs)."""
+        self.graph.replay()
+        return self.o_full, self.o_partial
+
     def forward_overlap(self, x: torch.Tensor, stream=None):
         """Two-stream FarSkip schedule (partial/outdated wiring)."""
         if not hasattr(self, "ws_overlap"):
