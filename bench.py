@@ -275,7 +275,9 @@ def run_ours(args, cfg, rank, world, local):
                            "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"], "source": pk_src}},
         "breakdown_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "schedule": "double-buffered: step i+1's H2D and step i's D2H on a copy stream beside step i's compute"
+                if not args.graph else "one CUDA graph replayed per step, copies in between"},
         "gpu_launches": int(launches * args.steps),
         "gpu_launches_per_step": int(launches),
         "clocks": clocks,
@@ -337,8 +339,13 @@ def per_stage_timing(cfg, stack, x, steps, stream):
 
 
 def e2e_timing(cfg, stack, x, steps, stream, graph=False):
-    """Host buffers in, host buffer out: pinned H2D of x, the stack, D2H of o_L.
-    With graph, x is the captured input buffer and the stack is the graph replay."""
+    """Host buffers in, host buffer out: every step copies its x from pinned host
+    memory, runs the stack through the C ABI and copies o_L back.  Double-buffered:
+    step i+1's input upload and step i's result download run on a copy stream
+    beside step i's compute (each step's copies stay inside the timed region).
+    With graph, the single captured input buffer is refilled and replayed in turn."""
+    if not graph:
+        return e2e_timing_pipelined(stack, x, steps, stream)
     x_host = x.cpu().pin_memory()
     o_host = torch.empty(stack.o_full.shape, dtype=stack.o_full.dtype).pin_memory()
     x_dev = x if graph else torch.empty_like(x)
@@ -354,6 +361,57 @@ def e2e_timing(cfg, stack, x, steps, stream, graph=False):
         x_dev.copy_(x_host, non_blocking=True)
         run()
         o_host.copy_(stack.o_full, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    nb = x.numel() * x.element_size()
+    return e0.elapsed_time(e1) / steps, nb, stack.o_full.numel() * stack.o_full.element_size()
+
+
+def e2e_timing_pipelined(stack, x, steps, stream):
+    from mixture_experts_layer_expert_gb300 import fs
+
+    x_host = x.cpu().pin_memory()
+    o_host = torch.empty(stack.o_full.shape, dtype=stack.o_full.dtype).pin_memory()
+    xs = [torch.empty_like(x) for _ in range(2)]
+    outs = [(torch.empty_like(stack.o_full), torch.empty_like(stack.o_partial)) for _ in range(2)]
+    cs = torch.cuda.Stream(device=x.device)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
+    L = len(stack.blocks)
+
+    def upload(i):                            # step i's input, once step i-2 has finished reading the buffer
+        b = i % 2
+        if i >= 2:
+            cs.wait_event(ev["comp"][b])
+        with torch.cuda.stream(cs):
+            xs[b].copy_(x_host, non_blocking=True)
+        ev["h2d"][b].record(cs)
+
+    def run(n):
+        # copy-stream order: upload(i+1) before download(i), so the next input
+        # arrives during this step's compute and this result leaves during the next
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(ev["h2d"][b])
+            if i >= 2:
+                stream.wait_event(ev["d2h"][b])     # step i-2's result has left outs[b]
+            fs.fs_farskip_stack(stack.desc, L, stack.wiring, stack.blocks, xs[b], outs[b][0], outs[b][1], stack.ws,
+                                stream)
+            ev["comp"][b].record(stream)
+            if i + 1 < n:
+                upload(i + 1)
+            cs.wait_event(ev["comp"][b])
+            with torch.cuda.stream(cs):
+                o_host.copy_(outs[b][0], non_blocking=True)
+            ev["d2h"][b].record(cs)
+
+    run(2)
+    torch.cuda.synchronize()
+    e0, e1 = cuda_events(2)
+    e0.record(stream)
+    cs.wait_event(e0)
+    run(steps)
+    stream.wait_stream(cs)
     e1.record(stream)
     torch.cuda.synchronize()
     nb = x.numel() * x.element_size()
@@ -410,7 +468,9 @@ def run_train(args, cfg, rank, world, local):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     ms = fwd_ms + bwd_ms
-    # end to end: x and dO from pinned host memory, dx back to the host
+    # end to end: x and dO from pinned host memory, dx back to the host, every step,
+    # in sequence (beside the training kernels, which keep HBM busy, the copies
+    # slow down about 5x, so overlapping them with the next step loses)
     x_h, d_h = x.cpu().pin_memory(), dO.cpu().pin_memory()
     dx_h = torch.empty(tr.dx.shape, dtype=tr.dx.dtype).pin_memory()
     xd, dd = torch.empty_like(x), torch.empty_like(dO)
@@ -461,7 +521,8 @@ def run_train(args, cfg, rank, world, local):
         "breakdown_ms": {"forward_train": round(fwd_ms, 4), "backward": round(bwd_ms, 4)},
         "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size() + dO.numel() * dO.element_size(),
-                "d2h_bytes_per_step": tr.dx.numel() * tr.dx.element_size(), "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": tr.dx.numel() * tr.dx.element_size(), "ms_per_step": round(e2e_ms, 4),
+                "schedule": "H2D, step, D2H in sequence"},
         "gpu_launches": int(launches * args.steps),
         "gpu_launches_per_step": int(launches),
         "clocks": clocks,

@@ -456,12 +456,16 @@ class FarSkipTrainer:
                                             _p(self.ws), _nbytes(self.ws), _stream(stream)), "fs_farskip_stack_train")
         return self.o_full, self.o_partial
 
-    def backward(self, d_o: torch.Tensor, d_os: torch.Tensor | None = None, stream=None):
+    def backward(self, d_o: torch.Tensor, d_os: torch.Tensor | None = None, stream=None,
+                 dx: torch.Tensor | None = None):
+        """Gradients for the last forward: dx (into `dx` when given, else self.dx)
+        and the weight gradients (self.grads)."""
+        out = self.dx if dx is None else dx
         arr = (BlockWeights * self.L)(*[block_struct(b) for b in self.blocks])
         arr_t = (BlockWeightsT * self.L)(*[_block_t_struct(b) for b in self.blocks_t])
         gr = (BlockGrads * self.L)(*[_grads_struct(g) for g in self.grads])
         _check(lib().fs_farskip_stack_backward(ctypes.byref(self.desc), self.L, WIRINGS[self.wiring], arr, arr_t,
-                                               _p(self.saved), _nbytes(self.saved), _p(d_o), _p(d_os), _p(self.dx),
+                                               _p(self.saved), _nbytes(self.saved), _p(d_o), _p(d_os), _p(out),
                                                gr, _p(self.ws_b), _nbytes(self.ws_b), _stream(stream)),
                "fs_farskip_stack_backward")
-        return self.dx, self.grads
+        return out, self.grads
