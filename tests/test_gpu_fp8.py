@@ -260,3 +260,29 @@ def test_full_size_fp8_sampled(fs, name):
     rows = np.sort(g.choice(cfg.T, size=min(SAMPLE, cfg.T), replace=False))
     blockwise(cfg, prob, stack, cfg.wiring, rows)
     end_to_end(cfg, prob, stack, o, o_star, cfg.wiring, rows)
+
+
+def test_dispatch_noalloc_fp8_matches_dispatch(fs):
+    """The no-allocation Dispatch with FS_FP8 writes the same codes, scales and
+    permutation as fs_dispatch with a workspace."""
+    T, E, k, d = 2049, 64, 6, 384
+    cfg = small(T=T, E=E, k=k, d=d)
+    desc = fs.make_desc(cfg)
+    ws = fs.alloc_workspace(desc, 0)
+    u = synth.make_x(cfg, DEV)
+    idx = _rand_topk(T, E, k, 77).to(DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    outs = []
+    for noalloc in (False, True):
+        c, o = torch.full((E,), -7, **i32), torch.full((E + 1,), -7, **i32)
+        p, pm = torch.full((T * k,), -7, **i32), torch.full((T * k,), -7, **i32)
+        xq = fs.fp8_rows_empty(T * k, d, DEV)
+        xq.fill_(0xAB)
+        if noalloc:
+            fs.fs_dispatch_noalloc(desc, idx, u, c, o, p, pm, xq)
+        else:
+            fs.fs_dispatch(desc, idx, u, c, o, p, pm, xq, ws)
+        outs.append((c, o, p, pm, xq))
+    _no_dev_error()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
