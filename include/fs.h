@@ -23,8 +23,10 @@
  *     inconsistent offsets, a pipeline wait that ran out of time) never trap:
  *     the kernel records a code in the library's device error word and skips
  *     the work; fs_get_error() reads and clears it.
- *   - Row-major layouts throughout.  Activations are [rows, d] with dtype
- *     desc->dtype (bf16 or fp32); gate weights and logits are fp32; indices int32.
+ *   - Row-major layouts throughout.  Activations are [rows, d] in the
+ *     activation type: bf16 for FS_BF16 and FS_FP8, fp32 for FS_F32 (FS_FP8's
+ *     E4M3 operands live inside the expert steps, see FS_FP8); gate weights and
+ *     logits are fp32; indices int32.
  *   - Pointers must be 16-byte aligned; d and c must be multiples of 64;
  *     n_shared * c_shared must be a multiple of 64 (FS_FP8: d, c and c_shared
  *     multiples of 128).  Otherwise FS_ERR_UNSUPPORTED.
@@ -103,7 +105,8 @@ typedef struct {
 } fs_layer_desc;
 
 /* One block's weights in the library's packed layouts (fs_pack_w13, fs_pack_w3,
- * fs_pack_w3_shared).  Element type = desc->dtype. */
+ * fs_pack_w3_shared).  Element type: the router weight in the activation type,
+ * the expert weights in desc->dtype's packed layout (FP8 packs for FS_FP8). */
 typedef struct {
     const void* w_r;        /* [E, d] router (W_R), row-major */
     const float* bias;      /* [E] router bias added to the logits, or NULL */
@@ -224,7 +227,7 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
 /* Routed experts (§2.1 MLP and MoE equations), grouped by expert: for every
  * expert e and every row p in [offsets[e], offsets[e+1]):
  *   h = SiLU(x W2_e^T) * (x W1_e^T)  (fp32 accumulate, stored bf16/fp32 in ws)
- *   y_perm[p] = h W3_e^T             (fp32 accumulate, stored in desc->dtype)
+ *   y_perm[p] = h W3_e^T             (fp32 accumulate, stored in the activation type)
  *   x_perm [T k, d], offsets [E+1] (device; the host never reads them),
  *   w13 = fs_pack_w13(E, c, d), w3 = fs_pack_w3(E, d, c) -> y_perm [T k, d].
  * bf16: persistent tcgen05/TMEM grouped GEMMs fed by TMA; fp32: fp32 FMA.
@@ -262,7 +265,7 @@ fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void*
  *                  o_prev (OUTDATED) or o_k (DISABLED)
  *   u_full[t]    = o_k
  * All sums in fp32, each output rounded once.  y_perm, u_next and u_full have
- * the activation type desc->dtype; shared_out (fs_shared_expert's output) and
+ * the activation type; shared_out (fs_shared_expert's output) and
  * extra (e.g. fs_attn_standin's output) are fp32; the residual stream o_prev
  * (prev_dtype) and o_partial / o_full (out_dtype) are FS_BF16 or FS_F32 each,
  * so a stack can carry its residual in fp32.  shared_out NULL = no shared

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI of libfs: argument validation, workspace planning, the
-// single-step entry points and the L-block FarSkip driver.
+// single-step entry points, the L-block FarSkip drivers (one stream, two
+// streams), the FP8 expert path, and the training forward and backward.
 //
 // "FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
 // Models" (papercache.org summary): §2.1 (MLP, MoE, router, Dispatch, Combine,
