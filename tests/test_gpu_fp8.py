@@ -257,7 +257,9 @@ def test_full_size_fp8_sampled(fs, name):
     prob = synth.make_problem(cfg, DEV)
     stack, o, o_star = _run_gpu(cfg, prob, cfg.wiring)
     g = np.random.default_rng(0)
-    rows = np.sort(g.choice(cfg.T, size=min(SAMPLE, cfg.T), replace=False))
+    # the oracle's FP8 form rounds every weight element it touches per token, so
+    # the sample is half the bf16 one
+    rows = np.sort(g.choice(cfg.T, size=min(SAMPLE // 2, cfg.T), replace=False))
     blockwise(cfg, prob, stack, cfg.wiring, rows)
     end_to_end(cfg, prob, stack, o, o_star, cfg.wiring, rows)
 
