@@ -401,6 +401,12 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
  * offsets, 3 = pipeline wait timed out, 4 = size beyond a kernel limit). */
 fs_status fs_get_error(int32_t* code);
 
+/* Self-test of the kernels' bounded waits: one kernel waits on a barrier that
+ * nothing signals, gives up after limit_us microseconds (1 .. 2,000,000),
+ * records code 3 (a wait timed out) in the device error word and returns; the
+ * context stays usable.  fs_get_error then reports FS_ERR_DEVICE_STATE, 3. */
+fs_status fs_selftest_wait_timeout(int32_t limit_us, void* stream);
+
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t fs_launch_count(void);
 

@@ -1108,6 +1108,12 @@ fs_status fs_get_error(int32_t* code) {
     return v ? FS_ERR_DEVICE_STATE : FS_OK;
 }
 
+fs_status fs_selftest_wait_timeout(int32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 2000000) return FS_ERR_INVALID_ARG;
+    FS_TRY(launch_wait_selftest(static_cast<uint64_t>(limit_us) * 1000ull, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
 uint64_t fs_launch_count(void) { return g_launches.load(); }
 
 const char* fs_last_cuda_error(void) { return g_last_cuda; }

@@ -367,6 +367,20 @@ __global__ void __launch_bounds__(256) pack_t_kernel(TSrc src, int NB, int KB, u
     }
 }
 
+// Self-test of the pipeline's bounded wait: one thread waits on an mbarrier
+// that nothing arrives at, with the given limit, through the helper every
+// GEMM wait uses; the wait gives up, records DEV_ERR_TIMEOUT and returns.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+    }
+}
+
 __global__ void set_pair_kernel(int* dst, int a, int b) {
     dst[0] = a;
     dst[1] = b;
@@ -379,6 +393,12 @@ __global__ void copy_u4_kernel(uint4* __restrict__ dst, const uint4* __restrict_
 }
 
 // --------------------------------------------------------------- launchers
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, dev_error_ptr());
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_set_pair(int* dst, int a, int b, cudaStream_t st) {
     set_pair_kernel<<<1, 1, 0, st>>>(dst, a, b);
     count_launch();

@@ -115,6 +115,7 @@ cudaError_t launch_gate_backward(const float* logits, const float* bias, const i
                                  cudaStream_t st);
 cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t st);
 cudaError_t launch_set_pair(int* dst, int a, int b, cudaStream_t st);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);   // bytes % 16 == 0
 cudaError_t launch_zero(void* dst, size_t bytes, cudaStream_t st);                    // bytes % 16 == 0
 // padded K segments of the weight-gradient GEMMs: kb [2G], poff [G+1], src_row [P]

@@ -88,6 +88,7 @@ _SIGS = {
     "fs_quantize_rows_fp8": (_I32, [ctypes.c_int64, _I32, _VP, _VP, _VP]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "fs_launch_count": (ctypes.c_uint64, []),
+    "fs_selftest_wait_timeout": (_I32, [_I32, _VP]),
     "fs_last_cuda_error": (ctypes.c_char_p, []),
     "fs_status_string": (ctypes.c_char_p, [_I32]),
 }
@@ -262,6 +263,10 @@ def fs_get_error():
     code = ctypes.c_int32(0)
     st = lib().fs_get_error(ctypes.byref(code))
     return int(st), int(code.value)
+
+
+def fs_selftest_wait_timeout(limit_us: int, stream=None):
+    _check(lib().fs_selftest_wait_timeout(limit_us, _stream(stream)), "fs_selftest_wait_timeout")
 
 
 def fs_launch_count() -> int:

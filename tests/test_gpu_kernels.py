@@ -127,6 +127,33 @@ def test_dispatch_bad_index_sets_error(fs):
     assert fs.fs_get_error() == (0, 0)   # read clears it
 
 
+def test_bounded_wait_times_out_and_the_context_survives(fs):
+    """A pipeline wait on a barrier nothing signals gives up after its limit,
+    records the timeout in the device error word and returns; the GPU keeps
+    working (a Dispatch afterwards is correct)."""
+    import time
+    t0 = time.perf_counter()
+    fs.fs_selftest_wait_timeout(50_000)             # 50 ms
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert fs.fs_get_error() == (5, 3)
+    assert 0.04 < elapsed < 5.0, elapsed
+    assert fs.fs_get_error() == (0, 0)
+    T, E, k = 300, 8, 2
+    idx = _rand_topk(T, E, k, seed=3)
+    counts, offs, pos, perm = oracle.dispatch(T, k, E, idx.numpy())
+    cfg = small(T=T, E=E, k=k, d=64)
+    desc = fs.make_desc(cfg)
+    ws = fs.alloc_workspace(desc, 0)
+    z = lambda n: torch.empty(n, dtype=torch.int32, device=DEV)
+    got = [z(E), z(E + 1), z(T * k), z(T * k)]
+    u = synth.make_x(cfg, DEV)
+    fs.fs_dispatch(desc, idx.to(DEV), u, *got, None, ws)
+    _no_dev_error()
+    for a, b in zip(got, (counts, offs, pos, perm)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b)
+
+
 # ----------------------------------------------------------- grouped SwiGLU
 
 def _segments(counts):
