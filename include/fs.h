@@ -338,8 +338,8 @@ size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L);
  * Stored backward operands are bf16 (dy, dg/da, dx per slot, dS, dz); every
  * sum is fp32; the input gradient and the weight gradients are fp32 in the
  * page's layouts.  fs_farskip_stack_train runs the forward and keeps what the
- * backward reads (u_k, logits, routing, Dispatch permutation, pre-activations,
- * hidden, y_perm) in `saved` (fs_train_saved_bytes(desc, L) bytes, 256-byte
+ * backward reads (u_k, logits, routing, Dispatch permutation, x_perm,
+ * pre-activations, hidden, y_perm) in `saved` (fs_train_saved_bytes(desc, L) bytes, 256-byte
  * aligned); it needs ws of fs_workspace_bytes(desc, L).
  * fs_farskip_stack_backward needs ws of fs_workspace_bytes_backward(desc, L). */
 

@@ -754,7 +754,7 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
 // column order) and hidden h, the routed outputs y_perm, and the shared
 // experts' pre-activations and hidden.
 struct SavedLayout {
-    size_t u, logits, idx, w, offsets, pos, perm, gu, h, y, gu_s, h_s, size;
+    size_t u, logits, idx, w, offsets, pos, perm, xp, gu, h, y, gu_s, h_s, size;
 };
 
 static SavedLayout saved_layout(const fs_layer_desc* d) {
@@ -771,6 +771,7 @@ static SavedLayout saved_layout(const fs_layer_desc* d) {
     l.offsets = take((E + 1) * 4);
     l.pos = take(rows * 4);
     l.perm = take(rows * 4);
+    l.xp = take(rows * dm * 2);
     l.gu = take(rows * 2 * c * 2);
     l.h = take(rows * c * 2);
     l.y = take(rows * dm * 2);
@@ -781,12 +782,9 @@ static SavedLayout saved_layout(const fs_layer_desc* d) {
 }
 
 // Workspace of the backward: the gradients of the inner residuals o_1..o_{L-1}
-// and o_1*..o_{L-1}* (fp32), the per-block step buffers, the padded K-segment
-// plan and two transposed-operand buffers that the weight-gradient GEMMs reuse
-// in turn.
+// and o_1*..o_{L-1}* (fp32) and the per-block step buffers.
 struct BwdLayout {
-    size_t go, gos, dy, dw, dS, dgu, dx, dgu_s, dz, plan_r, plan_s, kb, poff, src_row, kb1, ta, tb, end;
-    long long P, Tp;
+    size_t go, gos, dy, dw, dS, dgu, dx, dgu_s, dz, plan_r, plan_s, end;
     int Epad;
 };
 
@@ -796,9 +794,6 @@ static BwdLayout bwd_layout(const fs_layer_desc* d, int L) {
     const size_t rows = T * k, cw = static_cast<size_t>(d->n_shared) * d->c_shared;
     BwdLayout l;
     l.Epad = static_cast<int>(align_up(E, 64));
-    l.Tp = static_cast<long long>(align_up(T, 64));
-    l.P = static_cast<long long>(align_up(rows + 64 * E, 64));
-    const size_t Pm = static_cast<size_t>(l.P > l.Tp ? l.P : l.Tp);
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at_ = o; o = align_up(o + bytes, A); return at_; };
     l.go = take(static_cast<size_t>(L) * T * dm * 4);      // gradients of o_1 .. o_{L-1} (slot b)
@@ -812,20 +807,6 @@ static BwdLayout bwd_layout(const fs_layer_desc* d, int L) {
     l.dz = take(T * l.Epad * 2);
     l.plan_r = take(2 * (E + 1) * sizeof(int));
     l.plan_s = take(4 * sizeof(int));
-    l.kb = take(2 * E * sizeof(int));
-    l.poff = take((E + 1) * sizeof(int));
-    l.src_row = take(static_cast<size_t>(l.P) * sizeof(int));
-    l.kb1 = take(2 * sizeof(int));
-    // tiled transposed operands: A rows in blocks of 128, B rows in blocks of 256
-    size_t ra = dm > 2 * c ? dm : 2 * c;
-    if (2 * cw > ra) ra = 2 * cw;
-    if (static_cast<size_t>(l.Epad) > ra) ra = l.Epad;
-    ra = align_up(ra, 128);
-    size_t rb = c > dm ? c : dm;
-    if (cw > rb) rb = cw;
-    rb = align_up(rb, 256);
-    l.ta = take(ra * Pm * 2);
-    l.tb = take(rb * Pm * 2);
     l.end = o;
     return l;
 }
@@ -917,7 +898,6 @@ fs_status fs_farskip_stack_train(const fs_layer_desc* desc, int32_t L, int32_t w
     const int T = desc->T, rows = desc->T * desc->k, cw = desc->n_shared * desc->c_shared;
     auto sv = [&](int blk, size_t off) { return static_cast<uint8_t*>(saved) + static_cast<size_t>(blk) * sl.size + off; };
     int32_t* counts = at<int32_t>(ws, l.counts);
-    void* x_perm = at<void>(ws, l.x_perm);
     void* s_out = cw > 0 ? at<void>(ws, l.s_out) : nullptr;
     FS_TRY(launch_copy(sv(0, sl.u), x, static_cast<size_t>(T) * desc->d * 2, st));
     const void* o_prev = x;
@@ -933,6 +913,7 @@ fs_status fs_farskip_stack_train(const fs_layer_desc* desc, int32_t L, int32_t w
         int32_t* pos = reinterpret_cast<int32_t*>(sv(blk, sl.pos));
         void* y = sv(blk, sl.y);
         FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, reinterpret_cast<float*>(sv(blk, sl.logits)), ws, st));
+        void* x_perm = sv(blk, sl.xp);      // kept: the weight-gradient GEMMs read it
         FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, reinterpret_cast<int32_t*>(sv(blk, sl.perm)),
                                x_perm, ws, st));
         FS_CHECK(swiglu_impl(desc, x_perm, rows, nullptr, rows, offsets, desc->E, desc->c, bw.w13, bw.w3, y, false,
@@ -1003,12 +984,6 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
     void* dz = at<void>(ws, bl.dz);
     int* plan_r = at<int>(ws, bl.plan_r);
     int* plan_s = at<int>(ws, bl.plan_s);
-    int* kb = at<int>(ws, bl.kb);
-    int* poff = at<int>(ws, bl.poff);
-    int* src_row = at<int>(ws, bl.src_row);
-    int* kb1 = at<int>(ws, bl.kb1);
-    void* ta = at<void>(ws, bl.ta);
-    void* tb = at<void>(ws, bl.tb);
     const int bm = tc_block_m();
     const int max_mt = ceil_div(rows, bm) + E;
     // gradients of o_b (b = 0..L) and o_b* (b = 1..L): the caller's d_o, d_os for
@@ -1025,7 +1000,6 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
         FS_TRY(launch_zero(gos + n, static_cast<size_t>(L - 1) * n * 4, st));
     }
     FS_TRY(launch_plan(nullptr, 1, T, bm, plan_s, st));
-    FS_TRY(launch_set_pair(kb1, 0, static_cast<int>(bl.Tp / 64), st));
     for (int b = L; b >= 1; --b) {
         const int blk = b - 1;
         const fs_block_weights& bw = blocks[blk];
@@ -1036,7 +1010,6 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
         const float* w = reinterpret_cast<const float*>(sv(blk, sl.w));
         const int32_t* offsets = reinterpret_cast<const int32_t*>(sv(blk, sl.offsets));
         const int32_t* pos = reinterpret_cast<const int32_t*>(sv(blk, sl.pos));
-        const int32_t* perm = reinterpret_cast<const int32_t*>(sv(blk, sl.perm));
         // the wiring: block b's do_prev goes to o_{b-1}; its du to where u_b came
         // from (o_{b-1}* partial, o_{b-2} outdated, o_{b-1} disabled, x for b = 1)
         float* target;
@@ -1073,26 +1046,18 @@ fs_status fs_farskip_stack_backward(const fs_layer_desc* desc, int32_t L, int32_
                                     bl.Epad, k, desc->gate, dz, st));
         FS_TRY(launch_tc_gemm(EPI_F32, dz, T, bt.w_rt, 1, dm, bl.Epad, plan_s, ceil_div(T, bm) + 1, target, dm, dm,
                               nullptr, 0, true, st, &acc));
-        // weight gradients: contractions over each expert's padded row segment
-        FS_TRY(launch_pad_plan(offsets, E, rows, bl.P, kb, poff, src_row, st));
-        FS_TRY(launch_transpose_pad(dy, dm, src_row, 0, nullptr, bl.P, 128, ta, st));
-        FS_TRY(launch_transpose_pad(sv(blk, sl.h), c, src_row, 0, nullptr, bl.P, 256, tb, st));
-        FS_TRY(launch_wgrad_gemm(ta, bl.P, tb, kb, E, dm, c, gr.dw3, nullptr, 0, 0, st));
-        FS_TRY(launch_transpose_pad(dgu, 2 * c, src_row, 0, nullptr, bl.P, 128, ta, st));
-        FS_TRY(launch_transpose_pad(u, dm, src_row, 0, perm, bl.P, 256, tb, st));
-        FS_TRY(launch_wgrad_gemm(ta, bl.P, tb, kb, E, 2 * c, dm, gr.dw1, gr.dw2, 1, 0, st));
+        // weight gradients: contractions over each expert's rows (all T rows for
+        // the shared experts and the router), the token-row operands read in place
+        FS_TRY(launch_wgrad_gemm(dy, dm, sv(blk, sl.h), c, rows, offsets, E, dm, c, gr.dw3, nullptr, 0, 0, st));
+        FS_TRY(launch_wgrad_gemm(dgu, 2 * c, sv(blk, sl.xp), dm, rows, offsets, E, 2 * c, dm, gr.dw1, gr.dw2, 1, 0,
+                                 st));
         if (sh) {
-            FS_TRY(launch_transpose_pad(dS, dm, nullptr, T, nullptr, bl.Tp, 128, ta, st));
-            FS_TRY(launch_transpose_pad(sv(blk, sl.h_s), cw, nullptr, T, nullptr, bl.Tp, 256, tb, st));
-            FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, dm, cw, gr.dw3_shared, nullptr, 2, cs, st));
-            FS_TRY(launch_transpose_pad(dgu_s, 2 * cw, nullptr, T, nullptr, bl.Tp, 128, ta, st));
-            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, 256, tb, st));
-            FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, 2 * cw, dm, gr.dw1_shared, gr.dw2_shared, 1, 0, st));
-        } else {
-            FS_TRY(launch_transpose_pad(u, dm, nullptr, T, nullptr, bl.Tp, 256, tb, st));
+            FS_TRY(launch_wgrad_gemm(dS, dm, sv(blk, sl.h_s), cw, T, nullptr, 1, dm, cw, gr.dw3_shared, nullptr, 2, cs,
+                                     st));
+            FS_TRY(launch_wgrad_gemm(dgu_s, 2 * cw, u, dm, T, nullptr, 1, 2 * cw, dm, gr.dw1_shared, gr.dw2_shared, 1,
+                                     0, st));
         }
-        FS_TRY(launch_transpose_pad(dz, bl.Epad, nullptr, T, nullptr, bl.Tp, 128, ta, st));
-        FS_TRY(launch_wgrad_gemm(ta, bl.Tp, tb, kb1, 1, E, dm, gr.dw_r, nullptr, 0, 0, st));
+        FS_TRY(launch_wgrad_gemm(dz, bl.Epad, u, dm, T, nullptr, 1, E, dm, gr.dw_r, nullptr, 0, 0, st));
     }
     return FS_OK;
 }

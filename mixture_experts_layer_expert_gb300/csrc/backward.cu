@@ -1,9 +1,9 @@
 // backward.cu -- the memory-bound kernels of the MoE block's backward (training
 // form of "FarSkip-Collective", §2.1 MoE and Combine, §3 FarSkip update):
 // Combine backward, Dispatch backward (the gather-sum of the permuted input
-// gradients), the gate-rule backward of the router, the transposed copies the
-// weight-gradient GEMMs read, and the transposed weight packs of the
-// input-gradient GEMMs.  The GEMMs themselves run in gemm_tc.cu.
+// gradients), the gate-rule backward of the router and the transposed weight
+// packs of the input-gradient GEMMs.  The GEMMs themselves (the weight-gradient
+// GEMMs read the token-row activations in place) run in gemm_tc.cu.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -195,134 +195,6 @@ __global__ void add_f32_kernel(float4* __restrict__ dst, const float4* __restric
     }
 }
 
-// Padded segments for the weight-gradient GEMMs, from offsets [G + 1]: group g's
-// rows [off_g, off_{g+1}) go to padded columns [poff_g, poff_g + cnt_g), each
-// segment a multiple of 64 long.  kb[2g], kb[2g+1] = poff_g / 64 and the end
-// block.  One block of 1024 threads, a chunked exclusive scan.
-__global__ void pad_plan_kernel(const int* __restrict__ offsets, int G, int n_rows, int* __restrict__ kb,
-                                int* __restrict__ poff, int* err) {
-    __shared__ int warp_sums[32];
-    __shared__ int s_carry;
-    __shared__ int s_bad;
-    if (threadIdx.x == 0) { s_carry = 0; s_bad = 0; }
-    __syncthreads();
-    for (int base = 0; base < G; base += blockDim.x) {
-        const int g = base + threadIdx.x;
-        int cnt = 0;
-        if (g < G) {
-            const int a = offsets[g], b = offsets[g + 1];
-            if (a < 0 || b < a || b > n_rows) s_bad = 1;
-            cnt = b > a ? (b - a + 63) / 64 : 0;
-        }
-        int v = cnt;
-        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += n;
-        }
-        if (lane == 31) warp_sums[wid] = v;
-        __syncthreads();
-        if (wid == 0) {
-            int x = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += n;
-            }
-            warp_sums[lane] = x;
-        }
-        __syncthreads();
-        const int excl = v - cnt + (wid > 0 ? warp_sums[wid - 1] : 0) + s_carry;
-        if (g < G) {
-            kb[2 * g] = excl;
-            kb[2 * g + 1] = excl + cnt;
-            poff[g] = 64 * excl;
-        }
-        __syncthreads();
-        if (threadIdx.x == blockDim.x - 1) s_carry = excl + cnt;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        poff[G] = 64 * s_carry;
-        if (s_bad) {
-            for (int g = 0; g < G; ++g) { kb[2 * g] = 0; kb[2 * g + 1] = 0; }
-            poff[G] = 0;
-            set_dev_error(err, DEV_ERR_OFFSETS);
-        }
-    }
-}
-
-// src_row[pc] for every padded column pc < P: the row of group g at local
-// position pc - poff_g, or -1 in a pad (or past the last segment).
-__global__ void pad_map_kernel(const int* __restrict__ offsets, const int* __restrict__ poff, int G, long long P,
-                               int* __restrict__ src_row) {
-    for (long long pc = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; pc < P;
-         pc += static_cast<long long>(gridDim.x) * blockDim.x) {
-        int lo = 0, hi = G;        // last g with poff[g] <= pc
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (poff[mid] <= pc) lo = mid; else hi = mid;
-        }
-        const long long local = pc - poff[lo];
-        const int cnt = offsets[lo + 1] - offsets[lo];
-        src_row[pc] = (pc < poff[G] && local < cnt) ? offsets[lo] + static_cast<int>(local) : -1;
-    }
-}
-
-// The transpose of src [rows, cols] (bf16) as a [cols, P] operand of the
-// weight-gradient GEMM, stored TILED: element (c, pc) at
-// ((c / RB) (P / 64) + pc / 64) RB 64 + (c % RB) 64 + pc % 64, so every RB x 64
-// box the GEMM loads is one contiguous block (RB = 128 for A, 256 for B).
-// Row r of src goes to padded column pc with src_row[pc] = r (-1 = zeros);
-// with src_row NULL the map is pc -> pc for pc < n_valid.  With gather set,
-// the source row read is gather[r].  64 x 64 tiles through shared memory: each
-// CTA writes one contiguous 8 KB piece of a block.
-__global__ void __launch_bounds__(256)
-transpose_pad_kernel(const __nv_bfloat16* __restrict__ src, int cols, const int* __restrict__ src_row, int n_valid,
-                     const int* __restrict__ gather, long long P, int RB, __nv_bfloat16* __restrict__ dst) {
-    __shared__ uint32_t tile[64][33];       // 64 padded columns x 64 source columns (bf16 pairs), +1 against conflicts
-    // x runs over source column blocks, so the CTAs in flight read whole source rows
-    const int c0 = blockIdx.x * 64;
-    for (long long yb = blockIdx.y; yb < P / 64; yb += gridDim.y) {
-        const long long pc0 = yb * 64;
-        // load: 64 source rows (one per padded column) x 64 columns = 32 words each;
-        // warp w takes rows w, w + 8, ..., each lane one word of a row, and the
-        // row indices, gathered rows and words of its 8 rows are fetched as
-        // independent loads before any of them is used
-        const int wd = threadIdx.x & 31, w0 = threadIdx.x >> 5;
-        int rsrc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const long long pc = pc0 + w0 + 8 * q;
-            rsrc[q] = src_row ? __ldg(src_row + pc) : (pc < n_valid ? static_cast<int>(pc) : -1);
-        }
-        if (gather) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) rsrc[q] = rsrc[q] >= 0 ? __ldg(gather + rsrc[q]) : -1;
-        }
-        uint32_t v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            v[q] = rsrc[q] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<long long>(rsrc[q]) * cols + c0) + wd)
-                                : 0u;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) tile[w0 + 8 * q][wd] = v[q];
-        __syncthreads();
-        // store: 64 destination rows (source columns) x 64 padded columns, one
-        // contiguous 64 x 64 piece of the tiled block (c0 / RB, pc0 / 64)
-        __nv_bfloat16* piece = dst + ((static_cast<long long>(c0 / RB) * (P / 64) + pc0 / 64) * RB + c0 % RB) * 64;
-        for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x) {
-            const int cc = i >> 5, wd = i & 31;     // destination row c0 + cc, padded columns 2 wd, 2 wd + 1
-            const uint32_t a = tile[2 * wd][cc >> 1], b = tile[2 * wd + 1][cc >> 1];
-            const uint32_t lo = (cc & 1) ? (a >> 16) : (a & 0xffffu);
-            const uint32_t hi = (cc & 1) ? (b >> 16) : (b & 0xffffu);
-            reinterpret_cast<uint32_t*>(piece + cc * 64 + 2 * wd)[0] = lo | (hi << 16);
-        }
-        __syncthreads();     // the tile is reused by the next row block
-    }
-}
-
 // Transposed weight packs for the input-gradient GEMMs, in the tiled bf16
 // layout [G][ceil(N'/256)][K'/64][256][64] of the forward packs; one CTA per
 // 32 KB block, thread r = packed row n', 64 consecutive K' elements.
@@ -381,11 +253,6 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns, int* err) {
     }
 }
 
-__global__ void set_pair_kernel(int* dst, int a, int b) {
-    dst[0] = a;
-    dst[1] = b;
-}
-
 __global__ void copy_u4_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, long long n) {
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x)
@@ -395,12 +262,6 @@ __global__ void copy_u4_kernel(uint4* __restrict__ dst, const uint4* __restrict_
 // --------------------------------------------------------------- launchers
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st) {
     wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, dev_error_ptr());
-    count_launch();
-    return cudaGetLastError();
-}
-
-cudaError_t launch_set_pair(int* dst, int a, int b, cudaStream_t st) {
-    set_pair_kernel<<<1, 1, 0, st>>>(dst, a, b);
     count_launch();
     return cudaGetLastError();
 }
@@ -473,31 +334,6 @@ cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream
     if (blocks < 1) blocks = 1;
     add_f32_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(reinterpret_cast<float4*>(dst),
                                                                reinterpret_cast<const float4*>(src), n4);
-    count_launch();
-    return cudaGetLastError();
-}
-
-cudaError_t launch_pad_plan(const int* offsets, int G, int n_rows, long long P, int* kb, int* poff, int* src_row,
-                            cudaStream_t st) {
-    pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, G, n_rows, kb, poff, dev_error_ptr());
-    count_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    long long blocks = (P + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
-    if (blocks < 1) blocks = 1;
-    pad_map_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(offsets, poff, G, P, src_row);
-    count_launch();
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_pad(const void* src, int cols, const int* src_row, int n_valid, const int* gather,
-                                 long long P, int RB, void* dst, cudaStream_t st) {
-    if (P % 64 || cols % 64 || (RB != 128 && RB != 256)) return cudaErrorInvalidValue;
-    const long long yb = P / 64;
-    dim3 grid(static_cast<unsigned>(cols / 64), static_cast<unsigned>(yb < 65535 ? yb : 65535));
-    transpose_pad_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), cols, src_row, n_valid, gather,
-                                               P, RB, static_cast<__nv_bfloat16*>(dst));
     count_launch();
     return cudaGetLastError();
 }

@@ -326,6 +326,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return desc;
 }
 
+// Shared-memory matrix descriptor of an MN-major bf16 tile with the 128-byte
+// swizzle: each K row holds 64 consecutive M (or N) elements (128 B), 8 K rows
+// form a 1024 B atom (SBO = 1024 B between the 8-row groups along K), and the
+// next 64 M/N elements start `mn_stride` bytes further (LBO).  This is what a
+// TMA load of a [64 rows][64 columns] box of a row-major [K, M] matrix writes,
+// boxes for successive column blocks placed mn_stride apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t desc = 0;
+    desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    desc |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+    desc |= static_cast<uint64_t>(1024u >> 4) << 32;
+    desc |= static_cast<uint64_t>(1u) << 46;
+    desc |= static_cast<uint64_t>(2u) << 61;
+    return desc;
+}
+
+// Instruction descriptor, kind::f16, both operands MN-major (transpose bits 15
+// and 16 set); otherwise as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
 // bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.

@@ -823,17 +823,27 @@ __global__ void plan_kernel(const int* __restrict__ offsets, int G, int n_rows, 
 }
 
 // ------------------------------------------------------- weight gradients
-// out_g = A B^T over group g's padded K segment (launch_wgrad_gemm): the warp
-// roles, pipeline and bounded waits of grouped_gemm_kernel, with tiles (g, m,
-// n) of 128 x 256 (m inner, so consecutive tiles share the B slab) and the
-// K blocks [kb[2g], kb[2g+1]) of 64 columns.  A group with an empty segment
-// issues no MMAs and its epilogue writes zeros.
+// out_g = A_g^T B_g (launch_wgrad_gemm): A [P, lda] and B [P, ldb] bf16 with one
+// row per token (as the forward and the input-gradient GEMMs leave them), the
+// contraction over group g's rows [offs[g], offs[g+1]).  The operands are read
+// where they lie: TMA boxes of 64 rows x 64 columns (128-byte swizzle) are
+// MN-major tiles, so no transposed copy is made.  The warp roles, pipeline and
+// bounded waits are those of grouped_gemm_kernel; tiles (g, m, n) of 128 x 256
+// (m inner, so consecutive tiles share the B rows in L2), K blocks of 64 rows
+// from the group's first row.  In a group's last block the rows past its end
+// belong to the next group (or are the zero fill past P): the MMA warp zeroes
+// A's rows up to the next multiple of 16 (B there is finite data or zero fill,
+// so those products vanish) and skips the 16-row steps past it.  A group with
+// no rows issues no MMAs and its epilogue writes zeros.
 struct WArgs {
-    const int* kb;
-    int G, M, N, m_tiles, n_tiles, max_kb;
+    const int* offs;   // [G + 1] row offsets (device), or nullptr: one group [0, P)
+    long long P;
+    int G, M, N, m_tiles, n_tiles;
     int remap, split;
     int* err;
 };
+
+constexpr int W_BOX = 64 * 128;        // one 64-row x 64-column bf16 box, 8 KB
 
 // The output is written by TMA stores from a 2 KB staging buffer per epilogue
 // warp (32 rows x 16 fp32 columns, 64-byte swizzle): one store instruction per
@@ -875,21 +885,14 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint64_t* fin = tempty + NACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* kbs = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);    // [2 G]
+    int* offs = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);    // [G + 1]
+    int* bad = offs + kMaxGroups + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = args.G;
-    for (int i = threadIdx.x; i < G; i += THREADS) {
-        int a = args.kb[2 * i], b = args.kb[2 * i + 1];
-        if (a < 0 || b < a || b > args.max_kb) {     // corrupt plan: record it, treat as empty
-            set_dev_error(args.err, DEV_ERR_OFFSETS);
-            a = b = 0;
-        }
-        kbs[2 * i] = a;
-        kbs[2 * i + 1] = b;
-    }
     if (threadIdx.x == 0) {
+        *bad = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -901,6 +904,25 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         mbar_init(smem_u32(fin), 1);
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i <= G; i += THREADS) {
+        int v;
+        bool ok;
+        if (args.offs) {
+            v = args.offs[i];
+            ok = v >= 0 && v <= args.P && (i == 0 || v >= args.offs[i - 1]);
+        } else {
+            v = i == 0 ? 0 : static_cast<int>(args.P);
+            ok = true;
+        }
+        offs[i] = v;
+        if (!ok) *bad = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *bad) {      // corrupt offsets: record it, every group empty
+        set_dev_error(args.err, DEV_ERR_OFFSETS);
+        for (int i = 0; i <= G; ++i) offs[i] = 0;
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -924,13 +946,16 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const int g = t / per_g, rr = t - g * per_g;
                 const int m = rr % args.m_tiles, n = rr / args.m_tiles;
-                for (int kb = kbs[2 * g]; kb < kbs[2 * g + 1]; ++kb) {
+                for (int r = offs[g]; r < offs[g + 1]; r += 64) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    uint8_t* sa = smem + stage * STAGE_BYTES;
-                    tma_load_3d(smem_u32(sa), &tmA, fb, 0, 0, m * args.max_kb + kb);
-                    tma_load_3d(smem_u32(sa + A_STAGE), &tmB, fb, 0, 0, n * args.max_kb + kb);
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * W_BOX, &tmA, fb, m * BM + 64 * j, r);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sa + A_STAGE + j * W_BOX, &tmB, fb, n * BN + 64 * j, r);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -948,35 +973,60 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            int it = 0;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const int g = t / per_g;
-                const int acc = it & 1;
-                const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (!mbar_wait(smem_u32(&tempty[acc]), (use & 1u) ^ 1u, abort_flag, args.err)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const int kb0 = kbs[2 * g];
-                for (int kb = kb0; kb < kbs[2 * g + 1]; ++kb) {
-                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err)) { ok = false; break; }
-                    tc_fence_after();
-                    uint8_t* sa = smem + stage * STAGE_BYTES;
-                    const uint64_t adesc = smem_desc_sw128(smem_u32(sa));
-                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sa + A_STAGE));
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-                    tc_commit(smem_u32(&empty[stage]));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
+        // the whole warp walks the schedule: lane 0 waits and issues, all lanes
+        // zero the rows past a group's end in its last K block
+        constexpr uint32_t idesc = idesc_bf16_f32_mn(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int it = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+            const int g = t / per_g;
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (lane == 0) ok = mbar_wait(smem_u32(&tempty[acc]), (use & 1u) ^ 1u, abort_flag, args.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            const int r0 = offs[g], r1 = offs[g + 1];
+            for (int r = r0; r < r1; r += 64) {
+                if (lane == 0) ok = mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                tc_commit(smem_u32(&tfull[acc]));
+                uint8_t* sa = smem + stage * STAGE_BYTES;
+                const int nrow = min(64, r1 - r);
+                const int nk = (nrow + 15) >> 4;            // 16-row MMA steps that hold rows of the group
+                const int zrows = 16 * nk - nrow;
+                if (zrows > 0) {
+                    // every lane sees the stage complete (the wait returns at once) before writing into it
+                    if (mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err)) {
+                        for (int i = lane; i < (BM / 64) * zrows * 8; i += 32) {
+                            const int box = i / (zrows * 8), rem = i - box * zrows * 8;
+                            *reinterpret_cast<uint4*>(sa + box * W_BOX + (nrow + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t adesc = smem_desc_sw128_mn(smem_u32(sa), W_BOX);
+                    const uint64_t bdesc = smem_desc_sw128_mn(smem_u32(sa + A_STAGE), W_BOX);
+                    for (int kk = 0; kk < nk; ++kk)       // 16 rows = 2048 B = 128 descriptor units
+                        tc_mma_bf16(d_tmem, adesc + 128ull * kk, bdesc + 128ull * kk, idesc,
+                                    (r > r0 || kk > 0) ? 1u : 0u);
+                    tc_commit(smem_u32(&empty[stage]));
+                }
+                __syncwarp();
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
+            if (!ok) break;
+            if (lane == 0) tc_commit(smem_u32(&tfull[acc]));
+            __syncwarp();
+        }
+        if (lane == 0) {
             tc_commit(smem_u32(fin));
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(smem_u32(fin), 0)) {
@@ -993,7 +1043,7 @@ wgrad_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const int g = t / per_g, rr = t - g * per_g;
             const int m = rr % args.m_tiles, n = rr / args.m_tiles;
-            const bool any = kbs[2 * g + 1] > kbs[2 * g];
+            const bool any = offs[g + 1] > offs[g];
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
@@ -1365,9 +1415,10 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
     }
 }
 
-cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const int* kb, int G, int M, int N, float* out,
-                              float* out2, int remap, int split, cudaStream_t st) {
-    if (G < 1 || G > kMaxGroups || M < 1 || N < 1 || N % 32 || P % 64) return cudaErrorInvalidValue;
+cudaError_t launch_wgrad_gemm(const void* A, int lda, const void* B, int ldb, long long P, const int* offs, int G,
+                              int M, int N, float* out, float* out2, int remap, int split, cudaStream_t st) {
+    if (G < 1 || G > kMaxGroups || M < 1 || N < 1 || N % 32 || P < 1 || P > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (M > lda || N > ldb || lda % 8 || ldb % 8 || (!offs && G != 1)) return cudaErrorInvalidValue;
     if (G > 1 && M % 32) return cudaErrorInvalidValue;      // a 32-row piece never spans two groups
     if (remap == 1 && (M % 128 || !out2)) return cudaErrorInvalidValue;
     if (remap == 2 && (G != 1 || M % 32 || split < 32 || split % 32 || N % split)) return cudaErrorInvalidValue;
@@ -1379,22 +1430,10 @@ cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const i
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    // tiled operands: A blocks of 128 rows, B blocks of 256 rows, each [rows][64]
+    // the operands as they lie: [P rows, lda] and [P rows, ldb], boxes of 64 rows x 64 columns
     CUtensorMap ta, tb;
-    const long long mt = (M + tc::BM - 1) / tc::BM, nt = (N + tc::BN - 1) / tc::BN;
-    {
-        e = get_encode();
-        if (e != cudaSuccess) return e;
-        cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(tc::BM), static_cast<cuuint64_t>(mt * (P / 64))};
-        cuuint64_t gstride[2] = {128, static_cast<cuuint64_t>(tc::BM) * 128};
-        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tc::BM), 1};
-        cuuint32_t estr[3] = {1, 1, 1};
-        if (g_encode(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A), gdim, gstride, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    e = make_map_blocked(&tb, B, nt * (P / 64), tc::BN);
+    e = make_map(&ta, A, P, lda, 64);
+    if (e == cudaSuccess) e = make_map(&tb, B, P, ldb, 64);
     if (e != cudaSuccess) return e;
     // fp32 outputs, written as 32-row x 16-column pieces with the 64-byte swizzle
     auto out_map = [&](CUtensorMap* mp, float* base, long long rows, long long cols) -> cudaError_t {
@@ -1421,13 +1460,13 @@ cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const i
     }
     if (e != cudaSuccess) return e;
     tc::WArgs args;
-    args.kb = kb;
+    args.offs = offs;
+    args.P = P;
     args.G = G;
     args.M = M;
     args.N = N;
     args.m_tiles = (M + tc::BM - 1) / tc::BM;
     args.n_tiles = (N + tc::BN - 1) / tc::BN;
-    args.max_kb = static_cast<int>(P / 64);
     args.remap = remap;
     args.split = split;
     args.err = dev_error_ptr();

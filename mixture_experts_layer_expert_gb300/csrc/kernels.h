@@ -40,16 +40,15 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
                            const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
                            const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st,
                            const TcExtra* ex = nullptr);
-// Weight-gradient GEMM: for each group g, out_g [M, N] = sum over the group's K
-// segment of A[m, k] B[n, k], with A [M, P] and B [N, P] bf16 in the tiled
-// layouts of launch_transpose_pad (A with RB = 128, B with RB = 256; K = P, the
-// transposed activations, every group's segment padded to a multiple of 64
-// columns) and kb[2g], kb[2g+1] the segment's first and end 64-column blocks
-// (device).  fp32 out; remap 0: out [G][M][N]; remap 1 (packed
-// gate/up rows, M = 2c): rows to out2 (gate, W2) and out (up, W1), each
-// [G][c][N]; remap 2 (concatenated shared down columns): [N / split][M][split].
-cudaError_t launch_wgrad_gemm(const void* A, long long P, const void* B, const int* kb, int G, int M, int N, float* out,
-                              float* out2, int remap, int split, cudaStream_t st);
+// Weight-gradient GEMM: for each group g, out_g [M, N] = sum over the group's
+// rows p in [offs[g], offs[g+1]) of A[p, m] B[p, n], with A [P, lda] and B
+// [P, ldb] bf16 row-major (one row per token, read in place as MN-major
+// tiles), offs on the device (nullptr: G = 1, rows [0, P)); M <= lda, N <= ldb.
+// fp32 out; remap 0: out [G][M][N]; remap 1 (packed gate/up rows, M = 2c):
+// rows to out2 (gate, W2) and out (up, W1), each [G][c][N]; remap 2
+// (concatenated shared down columns): [N / split][M][split].
+cudaError_t launch_wgrad_gemm(const void* A, int lda, const void* B, int ldb, long long P, const int* offs, int G,
+                              int M, int N, float* out, float* out2, int remap, int split, cudaStream_t st);
 // FP8 E4M3 operands (kind::f8f6f4): A codes [a_rows, K] with a_scale[a_rows],
 // B packed by quant.cu with b_scale[G N]; the epilogue multiplies the fp32
 // accumulator by a_scale[row] b_scale[g N + col].  Single-CTA kernel only.
@@ -114,19 +113,9 @@ cudaError_t launch_gate_backward(const float* logits, const float* bias, const i
                                  const float* dw, int T, int E, int E_pad, int k, int gate, void* dz,
                                  cudaStream_t st);
 cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t st);
-cudaError_t launch_set_pair(int* dst, int a, int b, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);   // bytes % 16 == 0
 cudaError_t launch_zero(void* dst, size_t bytes, cudaStream_t st);                    // bytes % 16 == 0
-// padded K segments of the weight-gradient GEMMs: kb [2G], poff [G+1], src_row [P]
-cudaError_t launch_pad_plan(const int* offsets, int G, int n_rows, long long P, int* kb, int* poff, int* src_row,
-                            cudaStream_t st);
-// dst = transpose of src [rows, cols] bf16 through the padded column map (src_row
-// NULL: identity for pc < n_valid; gather: read row gather[r]), tiled as
-// [ceil(cols / RB)][P / 64][RB][64] (RB = 128 or 256; rows past cols in the last
-// row block are left as they are)
-cudaError_t launch_transpose_pad(const void* src, int cols, const int* src_row, int n_valid, const int* gather,
-                                 long long P, int RB, void* dst, cudaStream_t st);
 // transposed weight packs (mode 0 W13^T, 1 W3^T, 2 W3cat^T, 3 W_R^T) in the tiled layout [G][N'/256][K'/64][256][64]
 cudaError_t launch_pack_t(int mode, int G, int Np, int Kp, int c, int d, int cs, int E, const void* a, const void* b,
                           void* out, cudaStream_t st);

@@ -25,8 +25,10 @@ REL = 5e-3
 KEYS = ("dW_R", "dW1", "dW2", "dW3", "dW1s", "dW2s", "dW3s")
 
 
-def _run(cfg, wiring, seed=5):
+def _run(cfg, wiring, seed=5, mutate=None):
     prob = synth.make_problem(cfg, DEV)
+    if mutate is not None:
+        mutate(prob)
     x = prob["x"]
     tr = fs.FarSkipTrainer(cfg, prob["blocks"], wiring=wiring)
     o, o_star = tr.forward(x)
@@ -82,8 +84,8 @@ def test_stack_backward_wirings(fs, wiring):
 
 
 def test_backward_multi_tile_ragged(fs):
-    """Several M/N tiles, ragged expert segments (K of the weight-gradient GEMMs
-    padded per expert), 16 experts, top-4."""
+    """Several M/N tiles, ragged expert segments (the last 64-row K block of each
+    expert's weight-gradient contraction partly filled), 16 experts, top-4."""
     cfg = configs.LayerConfig("bwm", T=1000, d=384, E=16, k=4, c=256, n_shared=1, c_shared=256, L=2,
                               gate="sigmoid_norm", dtype="bf16")
     _run(cfg, "partial")
@@ -95,6 +97,26 @@ def test_backward_skewed_routing_and_small_E(fs):
     cfg = configs.LayerConfig("bwz", T=520, d=192, E=16, k=1, c=128, n_shared=0, c_shared=0, L=2,
                               gate="sigmoid", dtype="bf16", zipf_s=1.2)
     _run(cfg, "outdated")
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 64, 65, 130])
+def test_backward_exact_segment_lengths(fs, T):
+    """A router bias that sends every token to experts 0 and 1 (top-2 of 8), so
+    both experts' row segments are exactly T long and the other six are empty.
+    The weight-gradient contractions then see a lone row, a block ending one row
+    short of a 16-row MMA step, whole steps, one whole 64-row block, one row into
+    a second block, and two rows after two full blocks; the shared expert's and
+    the router's contractions run over the same T rows."""
+    cfg = configs.LayerConfig("bwt", T=T, d=256, E=8, k=2, c=128, n_shared=1, c_shared=128, L=2,
+                              gate="softmax_renorm", dtype="bf16")
+
+    def force(prob):
+        for w in prob["blocks"]:
+            b = torch.zeros(cfg.E, device=DEV)
+            b[0], b[1] = 30.0, 29.0
+            w["bias"] = b
+
+    _run(cfg, "partial", mutate=force)
 
 
 # ------------------------------------------------------ full-size workloads
