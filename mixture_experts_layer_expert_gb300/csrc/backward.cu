@@ -184,17 +184,6 @@ gate_backward_kernel(const float* __restrict__ logits, const float* __restrict__
     }
 }
 
-// dst += src (fp32, n multiple of 4).
-__global__ void add_f32_kernel(float4* __restrict__ dst, const float4* __restrict__ src, long long n4) {
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        float4 a = dst[i];
-        const float4 b = src[i];
-        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-        dst[i] = a;
-    }
-}
-
 // Transposed weight packs for the input-gradient GEMMs, in the tiled bf16
 // layout [G][ceil(N'/256)][K'/64][256][64] of the forward packs; one CTA per
 // 32 KB block, thread r = packed row n', 64 consecutive K' elements.
@@ -323,17 +312,6 @@ cudaError_t launch_gate_backward(const float* logits, const float* bias, const i
                                  cudaStream_t st) {
     gate_backward_kernel<<<(T + kBwdWarps - 1) / kBwdWarps, kBwdWarps * 32, 0, st>>>(
         logits, bias, idx, w, dw, T, E, E_pad, k, gate, static_cast<__nv_bfloat16*>(dz), dev_error_ptr());
-    count_launch();
-    return cudaGetLastError();
-}
-
-cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t st) {
-    const long long n4 = n / 4;
-    long long blocks = (n4 + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
-    if (blocks < 1) blocks = 1;
-    add_f32_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(reinterpret_cast<float4*>(dst),
-                                                               reinterpret_cast<const float4*>(src), n4);
     count_launch();
     return cudaGetLastError();
 }

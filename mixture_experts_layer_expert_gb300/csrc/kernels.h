@@ -112,7 +112,6 @@ cudaError_t launch_gather_sum(const void* dx_perm, const int32_t* pos, int T, in
 cudaError_t launch_gate_backward(const float* logits, const float* bias, const int32_t* idx, const float* w,
                                  const float* dw, int T, int E, int E_pad, int k, int gate, void* dz,
                                  cudaStream_t st);
-cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);   // bytes % 16 == 0
 cudaError_t launch_zero(void* dst, size_t bytes, cudaStream_t st);                    // bytes % 16 == 0
