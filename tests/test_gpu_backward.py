@@ -119,6 +119,40 @@ def test_backward_exact_segment_lengths(fs, T):
     _run(cfg, "partial", mutate=force)
 
 
+def _saved_offsets_at(cfg):
+    """Byte offset of block 1's expert offsets inside the training state: u, logits,
+    routing indices and weights come first, each region 256-byte aligned."""
+    up = lambda n: (n + 255) // 256 * 256
+    T, rows = cfg.T, cfg.T * cfg.k
+    return up(T * cfg.d * 2) + up(T * cfg.E * 4) + up(rows * 4) + up(rows * 4)
+
+
+def test_backward_corrupt_offsets_sets_error(fs):
+    """Expert offsets in the training state made inconsistent on the host before
+    the backward: the plans and the weight-gradient GEMM record DEV_ERR_OFFSETS
+    (code 2) and treat every expert as empty (routed weight gradients all zero);
+    the next forward rewrites the offsets and the backward is correct again."""
+    cfg = configs.LayerConfig("bwo", T=300, d=256, E=8, k=2, c=128, n_shared=1, c_shared=128, L=1,
+                              gate="sigmoid_norm", dtype="bf16")
+    prob = synth.make_problem(cfg, DEV)
+    tr = fs.FarSkipTrainer(cfg, prob["blocks"])
+    tr.forward(prob["x"])
+    torch.cuda.synchronize()
+    at = _saved_offsets_at(cfg)
+    offs = tr.saved[at:at + 4 * (cfg.E + 1)].view(torch.int32)
+    want = offs.clone()
+    assert int(want[0]) == 0 and int(want[-1]) == cfg.T * cfg.k and bool((want[1:] >= want[:-1]).all())
+    offs[1] = want[2] + 1                 # offsets[1] > offsets[2]
+    g = torch.Generator(device=DEV).manual_seed(2)
+    dO = torch.randn((cfg.T, cfg.d), generator=g, device=DEV)
+    _, grads = tr.backward(dO)
+    torch.cuda.synchronize()
+    assert fs.fs_get_error() == (5, 2)
+    for key in ("dW1", "dW2", "dW3"):
+        assert not grads[0][key].any(), key
+    _run(cfg, "partial")                  # a fresh trainer: the error word is clear and parity holds
+
+
 # ------------------------------------------------------ full-size workloads
 
 SAMPLE_BWD = 128

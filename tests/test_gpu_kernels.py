@@ -190,6 +190,33 @@ def test_grouped_swiglu(fs, dtype, counts, d, c):
     compare(to64(y), ry, dtype, "y_perm")
 
 
+def test_grouped_swiglu_bad_offsets_sets_error(fs):
+    """Offsets that decrease (made on the host; nothing faults): the plan records
+    DEV_ERR_OFFSETS (code 2) and yields no tiles, so y_perm is left untouched; a
+    consistent call afterwards matches the oracle."""
+    counts = [100, 50, 50]
+    cfg = small("bf16", T=200, E=3, k=1, d=128, c=128)
+    g = torch.Generator(device=DEV).manual_seed(8)
+    x = torch.randn((200, 128), generator=g, device=DEV).to(torch.bfloat16)
+    w = synth.make_block_weights(cfg, 0, DEV)
+    packed = fs.pack_block(cfg, w)
+    desc = fs.make_desc(cfg)
+    ws = fs.alloc_workspace(desc, 0)
+    y = torch.full((200, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    bad = torch.tensor([0, 100, 50, 200], dtype=torch.int32, device=DEV)
+    fs.fs_grouped_swiglu(desc, x, bad, packed["w13"], packed["w3"], y, ws)
+    torch.cuda.synchronize()
+    assert fs.fs_get_error() == (5, 2)
+    assert torch.isnan(y.float()).all(), "rows written from an inconsistent plan"
+    offs = torch.from_numpy(_segments(counts)).to(DEV)
+    fs.fs_grouped_swiglu(desc, x, offs, packed["w13"], packed["w3"], y, ws)
+    _no_dev_error()
+    expert = np.repeat(np.arange(3, dtype=np.int32), counts)
+    _, ry = oracle.expert_rows(oracle_cfg(cfg), synth.to_numpy(x), expert, synth.to_numpy(w["w1"]),
+                               synth.to_numpy(w["w2"]), synth.to_numpy(w["w3"]))
+    compare(to64(y), ry, "bf16", "y_perm")
+
+
 @pytest.mark.parametrize("dtype,T,E,k,d,c,skew", [
     ("bf16", 300, 8, 2, 256, 128, False), ("bf16", 1000, 64, 6, 128, 192, True), ("bf16", 1, 8, 2, 64, 64, False),
     ("bf16", 4097, 16, 4, 192, 128, False), ("f32", 257, 8, 2, 128, 128, False),
