@@ -420,6 +420,56 @@ def e2e_timing_pipelined(stack, x, steps, stream):
 
 # ------------------------------------------------------------ training step
 
+def train_e2e_pipelined(tr, x, dO, steps, stream):
+    """Training steps with their host copies: x, dO (pinned) up and dx down every
+    step, on a copy stream beside the compute.  Copy-stream order per step:
+    upload(i+1) before download(i)."""
+    x_h, d_h = x.cpu().pin_memory(), dO.cpu().pin_memory()
+    dx_h = torch.empty(tr.dx.shape, dtype=tr.dx.dtype).pin_memory()
+    xs = [torch.empty_like(x) for _ in range(2)]
+    ds = [torch.empty_like(dO) for _ in range(2)]
+    dxs = [torch.empty_like(tr.dx) for _ in range(2)]
+    cs = torch.cuda.Stream(device=x.device)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
+
+    def upload(i):                     # step i's inputs, once step i-2 has finished reading them
+        b = i % 2
+        if i >= 2:
+            cs.wait_event(ev["comp"][b])
+        with torch.cuda.stream(cs):
+            xs[b].copy_(x_h, non_blocking=True)
+            ds[b].copy_(d_h, non_blocking=True)
+        ev["h2d"][b].record(cs)
+
+    def run(n):
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(ev["h2d"][b])
+            if i >= 2:
+                stream.wait_event(ev["d2h"][b])      # step i-2's dx has left dxs[b]
+            tr.forward(xs[b], stream=stream)
+            tr.backward(ds[b], stream=stream, dx=dxs[b])
+            ev["comp"][b].record(stream)
+            if i + 1 < n:
+                upload(i + 1)
+            cs.wait_event(ev["comp"][b])
+            with torch.cuda.stream(cs):
+                dx_h.copy_(dxs[b], non_blocking=True)
+            ev["d2h"][b].record(cs)
+
+    run(2)                             # untimed: first writes into the new device buffers
+    torch.cuda.synchronize()
+    e0, e1 = cuda_events(2)
+    e0.record(stream)
+    cs.wait_event(e0)
+    run(steps)
+    stream.wait_stream(cs)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_train(args, cfg, rank, world, local):
     """One step = fs_farskip_stack_train + fs_farskip_stack_backward over T tokens
     (bf16), with a fixed output gradient dO resident on the device."""
@@ -468,30 +518,10 @@ def run_train(args, cfg, rank, world, local):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     ms = fwd_ms + bwd_ms
-    # end to end: x and dO from pinned host memory, dx back to the host, every step,
-    # in sequence (beside the training kernels, which keep HBM busy, the copies
-    # slow down about 5x, so overlapping them with the next step loses)
-    x_h, d_h = x.cpu().pin_memory(), dO.cpu().pin_memory()
-    dx_h = torch.empty(tr.dx.shape, dtype=tr.dx.dtype).pin_memory()
-    xd, dd = torch.empty_like(x), torch.empty_like(dO)
-
-    def e2e_step():
-        xd.copy_(x_h, non_blocking=True)
-        dd.copy_(d_h, non_blocking=True)
-        tr.forward(xd)
-        tr.backward(dd)
-        dx_h.copy_(tr.dx, non_blocking=True)
-
-    e2e_step()          # untimed: the first writes into the new device buffers
-    torch.cuda.synchronize()
-    e0, e1 = cuda_events(2)
-    n_e2e = max(2, args.steps // 2)
-    e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    # end to end: x and dO from pinned host memory, dx back to the host, every step;
+    # double-buffered like the inference stack: step i+1's inputs go up and step
+    # i's dx comes down on a copy stream while step i+1 computes
+    e2e_ms = train_e2e_pipelined(tr, x, dO, max(2, args.steps // 2), stream)
     clocks = sampler.stop() if sampler else None
     st, code = fs.fs_get_error()
     if st != 0:
@@ -528,7 +558,7 @@ def run_train(args, cfg, rank, world, local):
         "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size() + dO.numel() * dO.element_size(),
                 "d2h_bytes_per_step": tr.dx.numel() * tr.dx.element_size(), "ms_per_step": round(e2e_ms, 4),
-                "schedule": "H2D, step, D2H in sequence"},
+                "schedule": "double-buffered: step i+1's H2D and step i's D2H on a copy stream beside step i's compute"},
         "gpu_launches": int(launches * args.steps),
         "gpu_launches_per_step": int(launches),
         "clocks": clocks,
