@@ -68,9 +68,14 @@ CONFIGS = {
                       L=1, gate="sigmoid_norm", dtype="bf16"),
     "v3_decode": LayerConfig("v3_decode", T=1024, d=7168, E=256, k=8, c=2048, n_shared=1,
                              c_shared=2048, L=1, gate="sigmoid_norm", dtype="bf16"),
+    # DeepSeek-V3's per-expert GEMM shapes (d = 7168, c = 2048, 2048 rows per expert)
+    # with 32 of its 256 experts: about 5 GB on the device, small enough for
+    # multi-pass profiler captures of the headline kernels
+    "v3_e32": LayerConfig("v3_e32", T=8192, d=7168, E=32, k=8, c=2048, n_shared=1, c_shared=2048,
+                          L=1, gate="sigmoid_norm", dtype="bf16"),
 }
 # The FP8 expert path on the same shapes (the pages' inference precision).
-for _name in ("v2lite", "qwen3", "scout", "v3", "v3_decode"):
+for _name in ("v2lite", "qwen3", "scout", "v3", "v3_decode", "v3_e32"):
     CONFIGS[_name + "_fp8"] = CONFIGS[_name].with_(name=_name + "_fp8", dtype="fp8")
 
 
