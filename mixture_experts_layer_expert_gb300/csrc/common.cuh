@@ -142,6 +142,14 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
                  "r"(src), "r"(x), "r"(y)
                  : "memory");
 }
+// Element-wise fp32 (the map's type) add of a 2D tile from smem into global
+// through the tensor map (TMA reduction); completion as tma_store_2d.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The smem sources of this thread's committed bulk stores have been read.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

@@ -126,9 +126,10 @@ __device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float*
 // With F8 the accumulator is scaled by the A row's and the B rows' scales:
 // (acc * a_scale[row]) * b_scale[g N + col].
 // One 32-row x 64-byte piece (pk: this lane's row, 16 words: 32 bf16 or 16
-// fp32) to global through the warp's staging buffer and a TMA store at (x, y).
+// fp32) to global through the warp's staging buffer and a TMA store at (x, y),
+// or, with reduce, a TMA add into the fp32 values already there.
 __device__ __forceinline__ void store_piece_bf16(const CUtensorMap* tmo, uint8_t* piece, const uint32_t* pk, int lane,
-                                                 int x, int y) {
+                                                 int x, int y, bool reduce = false) {
     if (lane == 0) bulk_wait_read0();          // the previous piece has left the buffer
     __syncwarp();
 #pragma unroll
@@ -140,7 +141,10 @@ __device__ __forceinline__ void store_piece_bf16(const CUtensorMap* tmo, uint8_t
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        tma_store_2d(tmo, smem_u32(piece), x, y);
+        if (reduce)
+            tma_reduce_add_2d(tmo, smem_u32(piece), x, y);
+        else
+            tma_store_2d(tmo, smem_u32(piece), x, y);
         bulk_commit();
     }
 }
@@ -287,12 +291,17 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                                         dh1 * a1 * (s1 * (1.0f + g1 * (1.0f - s1))));
                     pa[q] = pack_bf16x2(dh0 * (g0 * s0), dh1 * (g1 * s1));
                 }
-                uint4* gd = reinterpret_cast<uint4*>(D + orow * args.ldo + pc);
-                uint4* ad = reinterpret_cast<uint4*>(D + orow * args.ldo + pc + 64);
+                if (piece_ok) {     // dg and da as two 32 x 32 pieces through TMA stores
+                    store_piece_bf16(tmo, piece, pg, lane, static_cast<int>(pc), tl.a_row + q32);
+                    store_piece_bf16(tmo, piece, pa, lane, static_cast<int>(pc) + 64, tl.a_row + q32);
+                } else {
+                    uint4* gd = reinterpret_cast<uint4*>(D + orow * args.ldo + pc);
+                    uint4* ad = reinterpret_cast<uint4*>(D + orow * args.ldo + pc + 64);
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    gd[w] = make_uint4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
-                    ad[w] = make_uint4(pa[4 * w], pa[4 * w + 1], pa[4 * w + 2], pa[4 * w + 3]);
+                    for (int w = 0; w < 4; ++w) {
+                        gd[w] = make_uint4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
+                        ad[w] = make_uint4(pa[4 * w], pa[4 * w + 1], pa[4 * w + 2], pa[4 * w + 3]);
+                    }
                 }
             }
         }
@@ -307,14 +316,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
             uint32_t v[32];
             tmem_ld32(tbase + c0, v);
             tmem_ld_wait();
-            if (piece_ok && ncols - c0 >= 32) {       // two 32 x 16 fp32 pieces through TMA stores
+            if (piece_ok && ncols - c0 >= 32) {       // two 32 x 16 fp32 pieces through TMA stores (adds)
                 if constexpr (F8) scale_cols32(v, sa, sb + c0);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pk[j] = v[16 * h + j];
-                    store_piece_bf16(tmo, piece, pk, lane, tl.n * BN + c0 + 16 * h, tl.a_row + q32);
+                    store_piece_bf16(tmo, piece, pk, lane, tl.n * BN + c0 + 16 * h, tl.a_row + q32, args.accumulate != 0);
                 }
             } else if (row_ok) {
                 if constexpr (F8) scale_cols32(v, sa, sb + c0);
@@ -1188,8 +1197,9 @@ static cudaError_t make_out_map_f32(CUtensorMap* m, void* base, long long rows, 
 }
 
 // The output map of a launch, when its epilogue stores pieces by TMA: bf16 h
-// and y, and fp32 outputs that are written (not accumulated).
-static cudaError_t output_map(int epi, bool pair, int accumulate, void* out, long long out_rows, int out_cols,
+// and y, dg/da of the SwiGLU backward, and fp32 outputs (written, or added by
+// TMA reductions when accumulating).
+static cudaError_t output_map(int epi, bool pair, void* out, long long out_rows, int out_cols,
                               long long ldo, CUtensorMap* m, int* use) {
     *use = 0;
     if (pair || out_rows < 1 || (reinterpret_cast<uintptr_t>(out) & 15u)) return cudaSuccess;
@@ -1197,9 +1207,12 @@ static cudaError_t output_map(int epi, bool pair, int accumulate, void* out, lon
     if (epi == EPI_SWIGLU || epi == EPI_BF16) {
         if (out_cols % 32 || ldo % 8) return cudaSuccess;
         e = make_out_map_bf16(m, out, out_rows, out_cols, ldo);
-    } else if (epi == EPI_F32 && !accumulate) {
+    } else if (epi == EPI_F32) {          // accumulate: the pieces are added by TMA reductions
         if (out_cols % 32 || ldo % 4) return cudaSuccess;
         e = make_out_map_f32(m, out, out_rows, out_cols, ldo);
+    } else if (epi == EPI_DSWIGLU) {      // dg, da in the packed gate/up columns: 2 out_cols wide
+        if (out_cols % 32 || ldo % 8) return cudaSuccess;
+        e = make_out_map_bf16(m, out, out_rows, 2LL * out_cols, ldo);
     } else {
         return cudaSuccess;
     }
@@ -1286,7 +1299,7 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.aux_ld = ex ? ex->aux_ld : 0;
     args.accumulate = ex ? ex->accumulate : 0;
     CUtensorMap to = ta;
-    e = output_map(EPI, pair, args.accumulate, out, gather_rows ? gather_limit : a_rows, out_cols, ldo, &to,
+    e = output_map(EPI, pair, out, gather_rows ? gather_limit : a_rows, out_cols, ldo, &to,
                    &args.tma_out);
     if (e != cudaSuccess) return e;
     int sms = 0;
@@ -1351,7 +1364,7 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     args.aux_ld = 0;
     args.accumulate = 0;
     CUtensorMap to = ta;
-    e = output_map(EPI, pair, 0, out, a_rows, out_cols, ldo, &to, &args.tma_out);
+    e = output_map(EPI, pair, out, a_rows, out_cols, ldo, &to, &args.tma_out);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = num_sms(&sms);
