@@ -97,7 +97,12 @@ typedef enum {
 } fs_wiring;
 
 /* One MoE layer: T tokens of width d, E routed experts of width c, top-k,
- * n_shared shared experts of width c_shared (0 = none), activation dtype, gate. */
+ * n_shared shared experts of width c_shared (0 = none), activation dtype, gate.
+ * Every call validates it first: T, d, E, k, c >= 1, k <= E, n_shared >= 0 and
+ * c_shared >= 1 when n_shared > 0, else FS_ERR_INVALID_ARG (an empty batch,
+ * T = 0, is such an error: the caller skips the call); d, c, c_shared multiples
+ * of 64 (128 for FS_FP8), E <= 512, k <= 16 and T k < 2^31 - 1024, else
+ * FS_ERR_UNSUPPORTED. */
 typedef struct {
     int32_t T, d, E, k, c, n_shared, c_shared;
     int32_t dtype;   /* fs_dtype */
