@@ -135,6 +135,19 @@ def cuda_events(n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
+def routed_alg_bytes(cfg, T):
+    """Algorithmic bytes of one routed gate/up + down launch pair: every expert's
+    weights read once (all E are touched when T k >= E), X_perm read, the hidden h
+    written and read once (bf16), Y_perm written; in the stored precisions (FP8:
+    E4M3 weights with one fp32 scale per output channel, E4M3 X_perm)."""
+    a = 4 if cfg.dtype == "f32" else 2
+    w = 1 if cfg.dtype == "fp8" else a
+    rows = T * cfg.k
+    weights = cfg.E * 3 * cfg.d * cfg.c * w + (cfg.E * (2 * cfg.c + cfg.d) * 4 if cfg.dtype == "fp8" else 0)
+    x_perm = rows * cfg.d * (1 if cfg.dtype == "fp8" else a)
+    return float(weights + x_perm + 2 * rows * cfg.c * a + rows * cfg.d * a)
+
+
 def gemm_traffic(cfg_name):
     """DRAM bytes per launch of the gate/up GEMM from the committed ncu summary,
     valid only while the kernel source is unchanged (null otherwise)."""
@@ -227,12 +240,29 @@ def run_ours(args, cfg, rank, world, local):
     flops = cfg.flops_per_block() * L
     bytes_ = cfg.alg_bytes_per_block() * L
     t_roof = max(flops / (pk["bf16_tflops"] * 1e12), bytes_ / (pk["hbm_gbs"] * 1e9))
-    # dominant kernel: the routed grouped SwiGLU GEMMs (gate/up + down)
+    # dominant kernel: the routed grouped SwiGLU GEMMs (gate/up + down); tensor-bound
+    # at prefill sizes, HBM-bound (expert weight streaming) at decode sizes
     routed_flops = 6.0 * T * cfg.k * cfg.d * cfg.c
     routed_ms = stage_ms["routed"] / L
-    achieved = routed_flops / (routed_ms / 1e3) / 1e12
     fp8 = cfg.dtype == "fp8"
+    routed_bytes = routed_alg_bytes(cfg, T)
     peak = pk["bf16_tflops_sustained"] * (FP8_PER_BF16 if fp8 else 1.0)
+    hbm_bound = routed_bytes / (pk["hbm_gbs"] * 1e9) > routed_flops / (peak * 1e12)
+    if hbm_bound:
+        roof = {"bound": "hbm", "kernel": "grouped_gemm_kernel (routed gate/up + down, tcgen05): expert weight streaming",
+                "achieved": round(routed_bytes / (routed_ms / 1e3) / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(routed_bytes / (routed_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                "peak_kind": "HBM copy, %s" % pk_src, "traffic": gemm_traffic(cfg.name),
+                "bytes_per_launch_pair": routed_bytes, "ms_per_launch_pair": round(routed_ms, 4)}
+    else:
+        achieved = routed_flops / (routed_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel (routed gate/up + down, tcgen05)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "peak_kind": ("fp8 = %.0f x bf16 sustained (nominal ratio), %s" % (FP8_PER_BF16, pk_src)) if fp8
+                else "bf16 sustained, %s" % pk_src,
+                "traffic": gemm_traffic(cfg.name),
+                "flops_per_launch_pair": routed_flops, "ms_per_launch_pair": round(routed_ms, 4)}
     if fp8:   # expert GEMMs at the FP8 rate, the router at the bf16 rate
         expert_flops = cfg.gemm_flops_per_block() * L
         t_flops = (expert_flops / (FP8_PER_BF16 * pk["bf16_tflops"] * 1e12)
@@ -261,13 +291,7 @@ def run_ours(args, cfg, rank, world, local):
                    "wiring": cfg.wiring,
                    "l2": "inputs larger than L2 (x %.2f GB, weights %.1f GB per block)" % (
                        T * cfg.d * 2 / 1e9, cfg.alg_bytes_per_block() / 1e9)},
-        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (routed gate/up + down, tcgen05)",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4),
-                     "peak_kind": ("fp8 = %.0f x bf16 sustained (nominal ratio), %s" % (FP8_PER_BF16, pk_src)) if fp8
-                     else "bf16 sustained, %s" % pk_src,
-                     "traffic": gemm_traffic(cfg.name),
-                     "flops_per_launch_pair": routed_flops, "ms_per_launch_pair": round(routed_ms, 4)},
+        "roofline": roof,
         "layer_roofline": {"bound": "tensor" if t_flops >= bytes_ / (pk["hbm_gbs"] * 1e9)
                            else "hbm", "tokens_per_s_at_roofline": round(T / t_roof, 1),
                            "frac": round((T / (ms / 1e3)) / (T / t_roof), 4),
