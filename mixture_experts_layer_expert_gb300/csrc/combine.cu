@@ -14,9 +14,11 @@
 // wirings) is added into o* and o, and o may also be written rounded to the
 // activation type (the next MoE input of the attention/MoE wiring).
 // The residual stream (o_prev, o*, o) may be fp32 or the activation type; S is
-// fp32; the expert rows and u' are in the activation type.  One warp per token, 8
-// columns per lane step: each lane loads the k expert rows of its columns
-// together (k loads in flight), sums in fp32, rounds once per output.
+// fp32; the expert rows and u' are in the activation type.  One warp per token
+// (or, for few tokens, per run of 256-column steps of a token, so that enough
+// warps are in flight), 8 columns per lane step: each lane loads the k expert
+// rows of its columns together (k loads in flight), sums in fp32, rounds once
+// per output.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -92,10 +94,14 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos, const float* __restrict__ topk_w,
                const void* __restrict__ o_prev, bool prev_bf16, const void* __restrict__ shared_out,
                const float* __restrict__ extra, void* __restrict__ o_partial, void* __restrict__ o_full, bool out_bf16,
-               void* __restrict__ u_next, int u_src, void* __restrict__ u_full, int T, int d, int k) {
+               void* __restrict__ u_next, int u_src, void* __restrict__ u_full, int T, int d, int k, int nch,
+               int cpc) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    const long long wid = static_cast<long long>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+    const int t = static_cast<int>(wid / nch);
     if (t >= T) return;
+    const int c_begin = static_cast<int>(wid - static_cast<long long>(t) * nch) * cpc * 256;   // this warp's columns
+    const int c_end = min(d, c_begin + cpc * 256);
     int my_p = -1;
     float my_w = 0.f;
     if (lane < k) {
@@ -110,7 +116,7 @@ combine_kernel(const void* __restrict__ y_perm, const int32_t* __restrict__ pos,
         ws[s] = __shfl_sync(0xffffffffu, my_w, s);
     }
     const long long row = static_cast<long long>(t) * d;
-    for (int c8 = lane * 8; c8 < d; c8 += 32 * 8) {
+    for (int c8 = c_begin + lane * 8; c8 < c_end; c8 += 32 * 8) {
         Raw8<BF16> yr[KMAX];
 #pragma unroll
         for (int s = 0; s < KMAX; ++s)
@@ -156,12 +162,19 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* 
                            int prev_bf16, const void* shared_out, const float* extra, void* o_partial, void* o_full,
                            int out_bf16, void* u_next, int u_src, void* u_full, int T, int d, int k, int is_bf16,
                            cudaStream_t st) {
-    const int grid = (T + kCombineWarps - 1) / kCombineWarps;
+    // runs of cpc 256-column steps per warp: one run per token when there are
+    // many tokens, up to one step per warp for a few (about 16K warps wanted)
+    const int steps = (d + 255) / 256;
+    const int want = T >= 16384 ? 1 : (16384 + T - 1) / T;
+    const int cpc = (steps + want - 1) / want;
+    const int nch = (steps + cpc - 1) / cpc;
+    const long long warps = static_cast<long long>(T) * nch;
+    const int grid = static_cast<int>((warps + kCombineWarps - 1) / kCombineWarps);
     const int threads = kCombineWarps * 32;
 #define FS_COMBINE(BF, KM)                                                                                  \
     combine_kernel<BF, KM><<<grid, threads, 0, st>>>(y_perm, pos, topk_w, o_prev, prev_bf16 != 0, shared_out,   \
                                                      extra, o_partial, o_full, out_bf16 != 0, u_next, u_src, u_full, \
-                                                     T, d, k)
+                                                     T, d, k, nch, cpc)
     if (is_bf16) {
         if (k <= 8) FS_COMBINE(true, 8); else FS_COMBINE(true, 16);
     } else {

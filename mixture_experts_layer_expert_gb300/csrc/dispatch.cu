@@ -162,18 +162,22 @@ constexpr int kCopyWarps = 8;
 // One warp per token: x_perm[pos[t, s]] = u[t] for every slot s.
 __global__ void __launch_bounds__(kCopyWarps * 32)
 dispatch_copy_kernel(const uint4* __restrict__ u, int T, int row_vecs, int k, const int32_t* __restrict__ pos,
-                     uint4* __restrict__ x_perm) {
+                     uint4* __restrict__ x_perm, int nch, int cpc) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kCopyWarps + (threadIdx.x >> 5);
+    const long long wid = static_cast<long long>(blockIdx.x) * kCopyWarps + (threadIdx.x >> 5);
+    const int t = static_cast<int>(wid / nch);
     if (t >= T) return;
+    // this warp's run of cpc 128-vector steps of the row (the whole row when nch = 1)
+    const int i_begin = static_cast<int>(wid - static_cast<long long>(t) * nch) * cpc * 128;
+    const int i_end = min(row_vecs, i_begin + cpc * 128);
     const int my_p = lane < k ? pos[static_cast<long long>(t) * k + lane] : -1;
     const uint4* src = u + static_cast<long long>(t) * row_vecs;
-    for (int i0 = 0; i0 < row_vecs; i0 += 4 * 32) {
+    for (int i0 = i_begin; i0 < i_end; i0 += 4 * 32) {
         uint4 v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int i = i0 + j * 32 + lane;
-            if (i < row_vecs) v[j] = __ldg(src + i);
+            if (i < i_end) v[j] = __ldg(src + i);
         }
         for (int s = 0; s < k; ++s) {
             const int p = __shfl_sync(0xffffffffu, my_p, s);
@@ -182,7 +186,7 @@ dispatch_copy_kernel(const uint4* __restrict__ u, int T, int row_vecs, int k, co
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = i0 + j * 32 + lane;
-                if (i < row_vecs) dst[i] = v[j];
+                if (i < i_end) dst[i] = v[j];
             }
         }
     }
@@ -272,8 +276,14 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d
         return cudaGetLastError();
     }
     const int row_vecs = d * elem_bytes / 16;
-    dispatch_copy_kernel<<<(T + kCopyWarps - 1) / kCopyWarps, kCopyWarps * 32, 0, st>>>(
-        reinterpret_cast<const uint4*>(u), T, row_vecs, k, pos, reinterpret_cast<uint4*>(x_perm));
+    // one warp per token, or for few tokens per run of 128-vector steps (about 16K warps wanted)
+    const int steps = (row_vecs + 127) / 128;
+    const int want = T >= 16384 ? 1 : (16384 + T - 1) / T;
+    const int cpc = (steps + want - 1) / want;
+    const int nch = (steps + cpc - 1) / cpc;
+    const long long warps = static_cast<long long>(T) * nch;
+    dispatch_copy_kernel<<<static_cast<int>((warps + kCopyWarps - 1) / kCopyWarps), kCopyWarps * 32, 0, st>>>(
+        reinterpret_cast<const uint4*>(u), T, row_vecs, k, pos, reinterpret_cast<uint4*>(x_perm), nch, cpc);
     count_launch();
     return cudaGetLastError();
 }
