@@ -120,7 +120,8 @@ static Layout layout(const fs_layer_desc* d, int L) {
     Layout l;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, A); return at; };
-    l.logits = take(T * E * 4);
+    // router logits, or for few tokens the partial sums of its K ranges
+    l.logits = take(T * E * 4 * static_cast<size_t>(d->dtype == FS_F32 ? 1 : tc_router_ksplit(d->T, d->E, d->d)));
     l.disp = take(dispatch_ws_bytes(d->T, d->E));
     l.plan_z = take(4 * sizeof(int));
     l.plan_r = take(2 * (E + 1) * sizeof(int));
@@ -222,6 +223,16 @@ static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* 
     if (d->dtype != FS_F32) {
         const int bm = tc_block_m();
         FS_TRY(launch_plan(nullptr, 1, d->T, bm, plan, st));
+        TcExtra ex;
+        ex.ksplit = tc_router_ksplit(d->T, d->E, d->d);
+        if (ex.ksplit > 1) {
+            // few tokens: K ranges on more SMs, partials summed in order by the top-k kernel
+            float* zp = at<float>(ws, l.logits);
+            FS_TRY(launch_tc_gemm(EPI_F32, u, d->T, w_r, 1, d->E, d->d, plan, ceil_div(d->T, bm) + 1, zp, d->E,
+                                  d->E, nullptr, 0, false, st, &ex));
+            FS_TRY(launch_topk(zp, ex.ksplit, bias, d->T, d->E, d->k, d->gate, idx, w, logits, st));
+            return FS_OK;
+        }
         FS_TRY(launch_tc_gemm(EPI_F32, u, d->T, w_r, 1, d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E,
                               nullptr, 0, false, st));
     } else {
@@ -230,7 +241,7 @@ static fs_status router_impl(const fs_layer_desc* d, const void* u, const void* 
         FS_TRY(launch_simt_gemm(EPI_F32, static_cast<const float*>(u), d->T, static_cast<const float*>(w_r), 1,
                                 d->E, d->d, plan, ceil_div(d->T, bm) + 1, z, d->E, d->E, nullptr, 0, st));
     }
-    FS_TRY(launch_topk(z, bias, d->T, d->E, d->k, d->gate, idx, w, st));
+    FS_TRY(launch_topk(z, 1, bias, d->T, d->E, d->k, d->gate, idx, w, nullptr, st));
     return FS_OK;
 }
 

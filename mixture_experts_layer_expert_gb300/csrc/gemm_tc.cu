@@ -75,6 +75,8 @@ struct Args {
     long long aux_ld;
     int accumulate;          // EPI_F32: out += acc
     int tma_out;             // bf16 out (EPI_SWIGLU h, EPI_BF16) through the output tensor map
+    int ksplit = 1;          // EPI_F32: K split into ksplit ranges, each written as its own partial
+    long long split_rows = 0;   // rows between the partials of successive K ranges in out
 };
 
 struct Tile {
@@ -405,7 +407,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (threadIdx.x == 0) set_dev_error(args.err, DEV_ERR_OFFSETS);
         total_mtiles = 0;
     }
-    const int total = total_mtiles * args.n_tiles;
+    const int ksplit = args.ksplit;         // tile t: output tile t / ksplit, K range t % ksplit
+    const int total = total_mtiles * args.n_tiles * ksplit;
     const int num_kb = args.K / BKE;
 
     if (!F8 && warp == 0 && args.gather_rows != nullptr) {
@@ -470,8 +473,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const int tt = t / ksplit, ks = t - tt * ksplit;
+                const Tile tl = decode_tile(tt, mt_start, row_start, G, args.n_tiles, BN, args.N);
+                const int kb1 = ((ks + 1) * num_kb) / ksplit;
+                for (int kb = (ks * num_kb) / ksplit; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -512,7 +517,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!mbar_wait(smem_u32(&tempty[acc]), (use & 1u) ^ 1u, abort_flag, args.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const int ks = t % ksplit;
+                const int kb0 = (ks * num_kb) / ksplit, kb1 = ((ks + 1) * num_kb) / ksplit;
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err)) { ok = false; break; }
                     tc_fence_after();
                     uint8_t* sa = smem + stage * STAGE_BYTES;
@@ -523,10 +530,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         // one MMA takes 32 bytes of K (16 bf16 or 32 E4M3): +32 bytes inside the
                         // 128-byte swizzle row = +2 in the >>4 address field
                         if constexpr (F8)
-                            tc_mma_f8(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            tc_mma_f8(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                         else
                             tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc,
-                                        (kb > 0 || kk > 0) ? 1u : 0u);
+                                        (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -549,14 +556,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int r = quarter * 32 + lane;     // row of the tile owned by this thread
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const Tile tl = decode_tile(t, mt_start, row_start, G, args.n_tiles, BN, args.N);
+            const int tt = t / ksplit, ks = t - tt * ksplit;
+            const Tile tl = decode_tile(tt, mt_start, row_start, G, args.n_tiles, BN, args.N);
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            epilogue_tile<EPI, F8>(tbase, tl.g, tl.a_row, tl.rows_valid, tl.n, r, half, args,
+            // K range ks of a split GEMM goes to its own partial, split_rows rows further on
+            epilogue_tile<EPI, F8>(tbase, tl.g, tl.a_row + static_cast<int>(ks * args.split_rows), tl.rows_valid, tl.n, r,
+                                   half, args,
                                    args.tma_out ? &tmO : nullptr, smem + PIECE_OFF + (warp - 2) * PIECE_BYTES);
             tc_fence_before();
             __syncwarp();
@@ -1298,14 +1308,20 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     args.aux = ex ? ex->aux : nullptr;
     args.aux_ld = ex ? ex->aux_ld : 0;
     args.accumulate = ex ? ex->accumulate : 0;
+    int ksplit = ex ? ex->ksplit : 1;
+    if (ksplit < 1 || ksplit > K / tc::BK) return cudaErrorInvalidValue;
+    if (ksplit > 1 && (EPI != EPI_F32 || G != 1 || args.accumulate || gather_rows)) return cudaErrorInvalidValue;
+    if (pair) ksplit = 1;
+    args.ksplit = ksplit;
+    args.split_rows = a_rows;
     CUtensorMap to = ta;
-    e = output_map(EPI, pair, out, gather_rows ? gather_limit : a_rows, out_cols, ldo, &to,
+    e = output_map(EPI, pair, out, (gather_rows ? gather_limit : a_rows) * ksplit, out_cols, ldo, &to,
                    &args.tma_out);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = num_sms(&sms);
     if (e != cudaSuccess) return e;
-    const long long max_tiles = static_cast<long long>(max_mtiles) * args.n_tiles;
+    const long long max_tiles = static_cast<long long>(max_mtiles) * args.n_tiles * ksplit;
     if (pair) {
         long long clusters = sms / 2;
         if (max_tiles < clusters) clusters = max_tiles;
@@ -1495,6 +1511,16 @@ cudaError_t launch_wgrad_gemm(const void* A, int lda, const void* B, int ldb, lo
 }
 
 int tc_block_m() { return use_pair() ? tc::P_BM : tc::BM; }
+
+int tc_router_ksplit(long long T, int E, int d) {
+    if (use_pair() || T < 1) return 1;
+    const long long tiles = ((T + tc::BM - 1) / tc::BM) * ((E + tc::BN - 1) / tc::BN);
+    long long s = 148 / tiles;                  // about one CTA per SM of a 148-152 SM part
+    const long long by_k = (d / tc::BK) / 2;    // at least two k-blocks per range
+    if (s > 16) s = 16;
+    if (s > by_k) s = by_k;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
 int tc_block_m_f8() { return use_pair() ? tc::P_BM : tc::BM; }
 
 }  // namespace fs

@@ -24,6 +24,10 @@ struct TcExtra {
     void* aux = nullptr;
     long long aux_ld = 0;
     int accumulate = 0;
+    // EPI_F32, one group, no accumulate, no gather: the K loop split into ksplit
+    // ranges, range s written to rows [s a_rows, (s + 1) a_rows) of out (partial
+    // sums; the consumer adds them in order).  Ignored (1) by the CTA-pair kernel.
+    int ksplit = 1;
 };
 
 void count_launch();
@@ -32,6 +36,9 @@ int* dev_error_ptr();
 // gemm_tc.cu (bf16 operands, tcgen05)
 int tc_block_m();
 int tc_block_m_f8();
+// K splits of the router logits GEMM for T rows, N = E, K = d: enough CTAs for
+// the SMs when T is small (1 when the CTA-pair kernel is selected or T is large)
+int tc_router_ksplit(long long T, int E, int d);
 cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st);
 // gather_rows (nullable): GEMM row p reads row gather_rows[p] of A (p < gather_limit)
 bool tc_gather_supported();
@@ -63,8 +70,10 @@ cudaError_t launch_simt_gemm(int epi, const float* A, long long a_rows, const fl
                              const int* gather_rows, int gather_limit, cudaStream_t st);
 
 // router.cu
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int gate,
-                        int32_t* topk_idx, float* topk_w, cudaStream_t st);
+// logits: nsplit partial sums [nsplit][T][E] added in order (nsplit = 1: the
+// logits themselves); z_out (nullable) receives the summed logits [T, E].
+cudaError_t launch_topk(const float* logits, int nsplit, const float* bias, int T, int E, int k, int gate,
+                        int32_t* topk_idx, float* topk_w, float* z_out, cudaStream_t st);
 
 // dispatch.cu
 constexpr int kStaticDispatchScratchInts = 65536;   // 256 KiB: fs_dispatch_noalloc's scratch

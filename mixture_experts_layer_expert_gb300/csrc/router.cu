@@ -3,7 +3,9 @@
 // "FarSkip-Collective: Unhobbling Blocking Communication in Mixture of Experts
 // Models", §2.1: G(A) = s(A W_R^T), a linear classifier followed by a sparse
 // selection s().  The logits z = u W_R^T come from the grouped GEMM (tensor
-// cores for bf16, fp32 FMA for fp32); this kernel adds the bias, selects the
+// cores for bf16, fp32 FMA for fp32), for few tokens as partial sums over K
+// ranges that this kernel adds in a fixed order (and stores when asked); it
+// then adds the bias, selects the
 // k largest z (descending, ties to the lower expert index) and computes the
 // gate weights of the configured rule.  One warp per token: each lane holds
 // E/32 logits in registers, k rounds of a warp-shuffle argmax.
@@ -16,17 +18,25 @@ constexpr int kTopkWarps = 8;
 
 template <int EPL>   // experts per lane (E <= 32 * EPL)
 __global__ void __launch_bounds__(kTopkWarps * 32)
-topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k, int gate,
-            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+topk_kernel(const float* __restrict__ logits, int nsplit, const float* __restrict__ bias, int T, int E, int k,
+            int gate, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* __restrict__ z_out) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
     if (t >= T) return;
+    const long long part = static_cast<long long>(T) * E;     // elements between partial sums
     const float* z = logits + static_cast<long long>(t) * E;
     float v[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
-        v[j] = (e < E) ? z[e] + (bias ? bias[e] : 0.0f) : -INFINITY;
+        if (e < E) {
+            float zz = z[e];
+            for (int s = 1; s < nsplit; ++s) zz += z[s * part + e];   // K ranges in order
+            if (z_out) z_out[static_cast<long long>(t) * E + e] = zz;
+            v[j] = zz + (bias ? bias[e] : 0.0f);
+        } else {
+            v[j] = -INFINITY;
+        }
     }
     uint32_t taken = 0;
     float sel_v = 0.f;     // lane s < k keeps slot s
@@ -90,18 +100,22 @@ topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, in
     }
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int gate,
-                        int32_t* topk_idx, float* topk_w, cudaStream_t st) {
+cudaError_t launch_topk(const float* logits, int nsplit, const float* bias, int T, int E, int k, int gate,
+                        int32_t* topk_idx, float* topk_w, float* z_out, cudaStream_t st) {
     const int grid = (T + kTopkWarps - 1) / kTopkWarps;
     const int threads = kTopkWarps * 32;
+    if (nsplit < 1) return cudaErrorInvalidValue;
+#define FS_TOPK(EPL) \
+    topk_kernel<EPL><<<grid, threads, 0, st>>>(logits, nsplit, bias, T, E, k, gate, topk_idx, topk_w, z_out)
     if (E <= 32)
-        topk_kernel<1><<<grid, threads, 0, st>>>(logits, bias, T, E, k, gate, topk_idx, topk_w);
+        FS_TOPK(1);
     else if (E <= 128)
-        topk_kernel<4><<<grid, threads, 0, st>>>(logits, bias, T, E, k, gate, topk_idx, topk_w);
+        FS_TOPK(4);
     else if (E <= 256)
-        topk_kernel<8><<<grid, threads, 0, st>>>(logits, bias, T, E, k, gate, topk_idx, topk_w);
+        FS_TOPK(8);
     else
-        topk_kernel<16><<<grid, threads, 0, st>>>(logits, bias, T, E, k, gate, topk_idx, topk_w);
+        FS_TOPK(16);
+#undef FS_TOPK
     count_launch();
     return cudaGetLastError();
 }
