@@ -446,14 +446,15 @@ def e2e_timing_pipelined(stack, x, steps, stream):
 
 def train_e2e_pipelined(tr, x, dO, steps, stream):
     """Training steps with their host copies: x, dO (pinned) up and dx down every
-    step, on a copy stream beside the compute.  Copy-stream order per step:
-    upload(i+1) before download(i)."""
+    step, beside the compute: uploads on one copy stream, downloads on another
+    (separate copy engines), step i+1's uploads issued before step i's download."""
     x_h, d_h = x.cpu().pin_memory(), dO.cpu().pin_memory()
     dx_h = torch.empty(tr.dx.shape, dtype=tr.dx.dtype).pin_memory()
     xs = [torch.empty_like(x) for _ in range(2)]
     ds = [torch.empty_like(dO) for _ in range(2)]
     dxs = [torch.empty_like(tr.dx) for _ in range(2)]
-    cs = torch.cuda.Stream(device=x.device)
+    cs = torch.cuda.Stream(device=x.device)      # uploads
+    cd = torch.cuda.Stream(device=x.device)      # downloads
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
 
     def upload(i):                     # step i's inputs, once step i-2 has finished reading them
@@ -477,18 +478,20 @@ def train_e2e_pipelined(tr, x, dO, steps, stream):
             ev["comp"][b].record(stream)
             if i + 1 < n:
                 upload(i + 1)
-            cs.wait_event(ev["comp"][b])
-            with torch.cuda.stream(cs):
+            cd.wait_event(ev["comp"][b])
+            with torch.cuda.stream(cd):
                 dx_h.copy_(dxs[b], non_blocking=True)
-            ev["d2h"][b].record(cs)
+            ev["d2h"][b].record(cd)
 
     run(2)                             # untimed: first writes into the new device buffers
     torch.cuda.synchronize()
     e0, e1 = cuda_events(2)
     e0.record(stream)
     cs.wait_event(e0)
+    cd.wait_event(e0)
     run(steps)
     stream.wait_stream(cs)
+    stream.wait_stream(cd)
     e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps
@@ -582,7 +585,7 @@ def run_train(args, cfg, rank, world, local):
         "e2e": {"value": round(T * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size() + dO.numel() * dO.element_size(),
                 "d2h_bytes_per_step": tr.dx.numel() * tr.dx.element_size(), "ms_per_step": round(e2e_ms, 4),
-                "schedule": "double-buffered: step i+1's H2D and step i's D2H on a copy stream beside step i's compute"},
+                "schedule": "double-buffered: step i+1's H2D and step i's D2H on two copy streams beside step i's compute"},
         "gpu_launches": int(launches * args.steps),
         "gpu_launches_per_step": int(launches),
         "clocks": clocks,
