@@ -25,15 +25,28 @@ topk_kernel(const float* __restrict__ logits, int nsplit, const float* __restric
     if (t >= T) return;
     const long long part = static_cast<long long>(T) * E;     // elements between partial sums
     const float* z = logits + static_cast<long long>(t) * E;
+    // the K ranges' partials added in order; the lane's EPL logits are independent
+    // chains, so each range's EPL loads are in flight together
     float v[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
+        v[j] = e < E ? z[e] : 0.0f;
+    }
+    for (int s = 1; s < nsplit; ++s) {
+        const float* zs = z + s * part;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E) v[j] += zs[e];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
         if (e < E) {
-            float zz = z[e];
-            for (int s = 1; s < nsplit; ++s) zz += z[s * part + e];   // K ranges in order
-            if (z_out) z_out[static_cast<long long>(t) * E + e] = zz;
-            v[j] = zz + (bias ? bias[e] : 0.0f);
+            if (z_out) z_out[static_cast<long long>(t) * E + e] = v[j];
+            v[j] += bias ? bias[e] : 0.0f;
         } else {
             v[j] = -INFINITY;
         }
