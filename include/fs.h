@@ -214,17 +214,21 @@ fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const 
  * a plugin or custom-op interface that passes only input and output buffers,
  * or code that must not call cudaMalloc/cudaFree (which can synchronise the
  * device) on its execution path.  Same arguments and results as fs_dispatch,
- * minus ws/ws_bytes.  Its scratch (the per-chunk expert histogram) is a fixed
- * 256 KiB device array inside the library, present on every GPU that loads the
- * library until the process exits; it holds ceil(T / 1024) * E <= 65536 ints
- * (e.g. T <= 65536 tokens with E <= 1024 experts, T <= 262144 with E <= 256).
- * Larger shapes return FS_ERR_WORKSPACE before any launch (fs_last_cuda_error
- * gives the sizes).  Nothing in the scratch needs to start at zero: each call
- * overwrites every entry it reads.  All calls share the one array, so calls
- * that overlap on the GPU (several streams, or several host threads) race and
- * must be serialised by the caller.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture.  Allocates nothing. */
+ * minus ws/ws_bytes (x_perm NULL = no row copy, as there).  Its scratch (the
+ * per-chunk expert histogram) is a fixed 256 KiB device array inside the
+ * library, present on every GPU that loads the library until the process
+ * exits; it holds ceil(T / 1024) * E <= 65536 ints (e.g. T <= 131072 tokens
+ * with E <= 512 experts, T <= 262144 with E <= 256).  Larger shapes return
+ * FS_ERR_WORKSPACE before any launch (fs_last_cuda_error gives the sizes).
+ * Nothing in the scratch needs to start at zero: each call overwrites every
+ * entry it reads.  All calls share the one array, so calls that overlap on the
+ * GPU (several streams, or several host threads) race and must be serialised
+ * by the caller.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and keeps it for
+ * the life of the process; make that first call before any stream capture,
+ * and do not keep using the library after cudaDeviceReset on that device (the
+ * kept address, like the library's error word and events, belongs to the
+ * context that was reset).  Allocates nothing. */
 fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u,
                               int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
                               void* x_perm, void* stream);

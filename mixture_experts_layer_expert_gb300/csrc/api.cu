@@ -497,7 +497,7 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
     FS_CHECK(need(offsets));
     FS_CHECK(need(pos));
     FS_CHECK(need(perm_src));
-    FS_CHECK(need(x_perm));
+    if (x_perm && !aligned16(x_perm)) return FS_ERR_UNSUPPORTED;
     if (dispatch_ws_bytes(desc->T, desc->E) > static_cast<size_t>(kStaticDispatchScratchInts) * sizeof(int32_t)) {
         std::snprintf(g_last_cuda, sizeof g_last_cuda,
                       "fs_dispatch_noalloc: ceil(T/1024) * E = %zu scratch ints exceed the static maximum %d",

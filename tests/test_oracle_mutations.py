@@ -42,6 +42,12 @@ MUTANTS = {
                                      "for (size_t i = 0; i < n; ++i) ubuf[i] = oracle_round(os_k[i], cfg->storage);\n                a_in = abuf;"),
     "attn_output_dropped": ("double op = o_prev[(size_t)t * d + i] + (extra ? extra[(size_t)t * d + i] : 0.0);",
                             "double op = o_prev[(size_t)t * d + i];"),
+    "hidden_storage_rounding_dropped": (
+        "h[j] = oracle_round(silu(gate) * up, storage);\n    }\n    for (int i = 0; i < d; ++i) {\n        double acc = 0.0;\n        for (int j = 0; j < c; ++j) acc += h[j]",
+        "h[j] = silu(gate) * up;\n    }\n    for (int i = 0; i < d; ++i) {\n        double acc = 0.0;\n        for (int j = 0; j < c; ++j) acc += h[j]"),
+    "routed_output_storage_rounding_dropped": (
+        "for (int i = 0; i < d; ++i) R[i] += w * oracle_round(y[i], cfg->storage);",
+        "for (int i = 0; i < d; ++i) R[i] += w * y[i];"),
     "shared_sum_rounded_per_expert": ("for (int i = 0; i < d; ++i) S[i] += y[i];",
                                       "for (int i = 0; i < d; ++i) S[i] += (sh == 0 ? y[i] : 0.0);"),
     # FP8 expert path
@@ -91,6 +97,7 @@ PIN_TESTS = [
     pins.test_golden_mlp,
     pins.test_golden_dispatch,
     pins.test_golden_rounding,
+    pins.test_golden_storage_roundings,
     lambda: [pins.test_router_vs_library(g) for g in ("softmax", "softmax_renorm", "sigmoid", "sigmoid_norm")],
     pins.test_dispatch_vs_library,
     lambda: [pins.test_brute_force_dense_moe(g) for g in ("softmax", "softmax_renorm", "sigmoid", "sigmoid_norm")],

@@ -10,6 +10,8 @@ Pins, and the mistake each one catches:
   golden MLP        -- SiLU on the wrong projection, transposed W3, SiLU special values
   golden dispatch   -- counting sort: counts, offsets, stability, pos/perm_src
   golden rounding   -- bf16 / fp32 round-to-nearest-even at storage points
+  golden storage    -- the stored hidden h and each stored routed output y are
+                       rounded where the layer stores them (dropped roundings)
   library routines  -- logits vs a matmul, top-k vs a stable argsort, softmax/expit,
                        counts vs bincount, permutation vs a stable argsort
   brute force       -- dense sum_j G_j MLP^j over all experts (tiny shapes)
@@ -112,6 +114,33 @@ def test_golden_mlp():
                                   np.array([case["w2"]], np.float64), np.array([case["w3"]], np.float64))
         np.testing.assert_allclose(h[0], case["expect_h"], rtol=1e-12, atol=0)
         np.testing.assert_allclose(y[0], case["expect_y"], rtol=1e-12, atol=0)
+
+
+def test_golden_storage_roundings():
+    """The two bf16 storage points inside a block (tests/golden/storage_rounding.json):
+    the expert hidden h between the projections and each routed output y before
+    the gate-weighted sum, with values that fall strictly between bf16 neighbours,
+    so storage mode and exact mode differ by the hand-derived amounts."""
+    g = gold("storage_rounding.json")
+    m = g["mlp"]
+    for mode, st in (("exact", oracle.EXACT), ("bf16", oracle.STORE_BF16)):
+        cfg = cfg_of(m["d"], 1, 1, m["c"], storage=st)
+        h, y = oracle.expert_rows(cfg, np.array([m["a"]], np.float64), np.zeros(1, np.int32),
+                                  np.array([m["w1"]], np.float64), np.array([m["w2"]], np.float64),
+                                  np.array([m["w3"]], np.float64))
+        assert h[0].tolist() == m[mode]["h"], (mode, h[0])
+        assert y[0].tolist() == m[mode]["y"], (mode, y[0])
+    b = g["block"]
+    w = W(dict(w_r=np.array(b["w_r"], np.float64), w1=np.array(b["w1"], np.float64),
+               w2=np.array(b["w2"], np.float64), w3=np.array(b["w3"], np.float64)))
+    for mode, st in (("exact", oracle.EXACT), ("bf16", oracle.STORE_BF16)):
+        cfg = cfg_of(b["d"], b["E"], b["k"], b["c"], storage=st)
+        out = oracle.stack(cfg, [w], "partial", np.array([b["x"]], np.float64), want_rs=True)
+        assert out["topk_idx"][0, 0].tolist() == [0, 1]
+        assert out["topk_w"][0, 0].tolist() == [0.5, 0.5]
+        assert out["o"][0].tolist() == b[mode]["o"], (mode, out["o"][0])
+        assert out["o_star"][0].tolist() == b[mode]["o_star"], (mode, out["o_star"][0])
+        assert out["R"][0, 0].tolist() == b[mode]["R"], (mode, out["R"][0, 0])
 
 
 def test_golden_dispatch():
