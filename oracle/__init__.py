@@ -100,12 +100,17 @@ def round_storage(x: float, storage: int) -> float:
     return float(lib().oracle_round(float(x), int(storage)))
 
 
+FP8_MODES = {False: 0, True: 1, "row": 1, "mx": 2, 0: 0, 1: 1, 2: 2}
+
+
 def make_cfg(d, E, k, c, n_shared=0, c_shared=0, gate="softmax_renorm", in_dtype=F32,
              storage=EXACT, fp8=False) -> _Cfg:
-    """fp8=True: expert GEMM operands in FP8 E4M3 with one power-of-two scale per
-    row along the contraction (tokens, hidden rows, weight output channels)."""
+    """fp8=True / "row": expert GEMM operands in FP8 E4M3 with one power-of-two
+    scale per row along the contraction (tokens, hidden rows, weight output
+    channels); fp8="mx": one such scale per block of 32 consecutive elements
+    along the contraction."""
     g = GATES[gate] if isinstance(gate, str) else int(gate)
-    return _Cfg(d, E, k, c, n_shared, c_shared, g, in_dtype, storage, int(bool(fp8)))
+    return _Cfg(d, E, k, c, n_shared, c_shared, g, in_dtype, storage, FP8_MODES[fp8])
 
 
 def _check(rc, what):
@@ -132,6 +137,20 @@ def quant_rows(x: np.ndarray, dtype: str | None = None):
     deq = np.zeros((rows, cols), np.float64)
     _check(lib().oracle_quant_rows(ctypes.c_int(rows), ctypes.c_int(cols), _p(x), ctypes.c_int(_dt(x, dtype)),
                                    _p(codes), _p(exps), _p(deq)), "quant_rows")
+    return codes, exps, deq
+
+
+def quant_blocks(x: np.ndarray, blk: int, dtype: str | None = None):
+    """FP8 quantisation of x [rows, cols] in blocks of blk consecutive elements per
+    row (blk = cols: per row): codes [rows, cols] uint8, the block exponents e
+    [rows, cols / blk] (scale 2^e) and the dequantised values."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), np.uint8)
+    exps = np.zeros((rows, cols // blk), np.int32)
+    deq = np.zeros((rows, cols), np.float64)
+    _check(lib().oracle_quant_blocks(ctypes.c_int(rows), ctypes.c_int(cols), ctypes.c_int(blk), _p(x),
+                                     ctypes.c_int(_dt(x, dtype)), _p(codes), _p(exps), _p(deq)), "quant_blocks")
     return codes, exps, deq
 
 

@@ -50,6 +50,13 @@
  *     plain sum over the dequantised values.  The router, Combine and the
  *     residual stream are unchanged.  The shared experts are quantised as the
  *     one MLP over their concatenated width that they sum to (§2.1).
+ *   - Block-scaled FP8 (cfg->fp8 = 2, the MX form): the same, with one
+ *     power-of-two scale per block of 32 consecutive elements along the
+ *     contraction instead of one per row -- every activation row, hidden row
+ *     and weight row is cut into 32-element blocks and each block gets its own
+ *     exponent by the same rule.  A block scale still multiplies every term it
+ *     covers by the same power of two, so the GEMM is again the plain sum over
+ *     the dequantised values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -167,6 +174,41 @@ static int quant_row(double* x, int n, uint8_t* codes) {
     return e;
 }
 
+/* Elements per block of the MX form. */
+#define ORACLE_MX_BLOCK 32
+
+/* Block length of the FP8 operands of cfg along a contraction of length len:
+ * the whole row (row scales) or ORACLE_MX_BLOCK (block scales). */
+static int fp8_blk(const oracle_cfg* cfg, int len) { return cfg->fp8 == 2 ? ORACLE_MX_BLOCK : len; }
+
+/* Quantise x[n] in place as n / blk consecutive blocks of blk elements, each
+ * with its own exponent (quant_row on each block); exps[b] receives block b's
+ * exponent, codes its E4M3 codes (either may be NULL).  blk = n is one row
+ * scale. */
+static void quant_blocks(double* x, int n, int blk, uint8_t* codes, int32_t* exps) {
+    for (int b = 0; b < n / blk; ++b) {
+        int e = quant_row(x + (size_t)b * blk, blk, codes ? codes + (size_t)b * blk : NULL);
+        if (exps) exps[b] = e;
+    }
+}
+
+int oracle_quant_blocks(int rows, int cols, int blk, const void* x, int x_dtype,
+                        uint8_t* codes, int32_t* exps, double* deq) {
+    if (rows < 0 || cols <= 0 || blk <= 0 || cols % blk) return -1;
+    int bad = 0;
+    const int nb = cols / blk;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        double* row = (double*)malloc(sizeof(double) * (size_t)cols);
+        if (!row) { bad = 1; continue; }
+        for (int i = 0; i < cols; ++i) row[i] = elem(x, (size_t)r * cols + i, x_dtype);
+        quant_blocks(row, cols, blk, codes ? codes + (size_t)r * cols : NULL, exps ? exps + (size_t)r * nb : NULL);
+        if (deq) memcpy(deq + (size_t)r * cols, row, sizeof(double) * (size_t)cols);
+        free(row);
+    }
+    return bad ? -2 : 0;
+}
+
 int oracle_quant_rows(int rows, int cols, const void* x, int x_dtype,
                       uint8_t* codes, int32_t* exps, double* deq) {
     if (rows < 0 || cols <= 0) return -1;
@@ -184,22 +226,52 @@ int oracle_quant_rows(int rows, int cols, const void* x, int x_dtype,
     return bad ? -2 : 0;
 }
 
-/* Exponents of `rows` weight rows of length K starting at element `base`. */
-static void weight_row_exps(const void* w, int dt, size_t rows, int K, int32_t* out) {
+/* Exponents of `rows` weight rows of length K, one per block of blk elements
+ * along K (blk = K: one per row): out[r * (K / blk) + b]. */
+static void weight_block_exps(const void* w, int dt, size_t rows, int K, int blk, int32_t* out) {
+    const int nb = K / blk;
 #pragma omp parallel for schedule(static)
     for (long long r = 0; r < (long long)rows; ++r) {
-        double amax = 0.0;
-        for (int i = 0; i < K; ++i) {
-            double v = fabs(elem(w, (size_t)r * K + i, dt));
-            if (v > amax) amax = v;
+        for (int b = 0; b < nb; ++b) {
+            double amax = 0.0;
+            for (int i = b * blk; i < (b + 1) * blk; ++i) {
+                double v = fabs(elem(w, (size_t)r * K + i, dt));
+                if (v > amax) amax = v;
+            }
+            out[(size_t)r * nb + b] = fp8_row_exp(amax);
         }
-        out[r] = fp8_row_exp(amax);
     }
 }
 
 /* One weight element quantised with its row's exponent e. */
+static double wq_value(double v, int e) { return ldexp(oracle_e4m3(ldexp(v, -e)), e); }
+
+/* Memo of wq_value for bf16 weights: a bf16 element has 65536 possible bit
+ * patterns, so for each row exponent e in use the quantised value of every
+ * pattern is computed once (wq_value itself) and then looked up.  The values
+ * are identical to calling wq_value; only the repeated work per token goes. */
+enum { WQ_EMIN = -64, WQ_EMAX = 63 };
+static double* g_wq_tab[WQ_EMAX - WQ_EMIN + 1];
+
+static void wq_tables_for(const int32_t* exps, size_t n) {
+#pragma omp critical(oracle_wq_tables)
+    for (size_t r = 0; r < n; ++r) {
+        int e = exps[r];
+        if (e < WQ_EMIN || e > WQ_EMAX || g_wq_tab[e - WQ_EMIN]) continue;
+        double* t = (double*)malloc(sizeof(double) * 65536);
+        if (!t) continue;    /* no memo: wq computes the value directly */
+        for (uint32_t b = 0; b < 65536; ++b) {
+            uint16_t h = (uint16_t)b;
+            t[b] = wq_value(elem(&h, 0, ORACLE_BF16), e);
+        }
+        g_wq_tab[e - WQ_EMIN] = t;
+    }
+}
+
 static double wq(const void* w, size_t i, int dt, int e) {
-    return ldexp(oracle_e4m3(ldexp(elem(w, i, dt), -e)), e);
+    if (dt == ORACLE_BF16 && e >= WQ_EMIN && e <= WQ_EMAX && g_wq_tab[e - WQ_EMIN])
+        return g_wq_tab[e - WQ_EMIN][((const uint16_t*)w)[i]];
+    return wq_value(elem(w, i, dt), e);
 }
 
 static double silu(double v) { return v / (1.0 + exp(-v)); }
@@ -294,46 +366,51 @@ static void mlp_row(int d, int c, const double* a,
     }
 }
 
-/* The FP8 form of one expert (cfg->fp8 = 1).  aq[d] is the token row already
- * quantised (quant_row; once per token, shared by all its experts).  The
- * expert has width c made of sub-experts of width cw side by side (cw = c for
- * a routed expert; the shared experts form one MLP over their concatenated
- * width, the TP-slicing identity of §2.1).  W1, W2 are [c, d] from element
- * base12, row j quantised with exponent e1[j] / e2[j]; W3 element (i, jj) sits
- * at base3 + (jj / cw) d cw + i cw + jj % cw and row i (over all c) uses e3[i].
+/* The FP8 form of one expert (cfg->fp8 = 1 row scales, 2 block scales).  aq[d]
+ * is the token row already quantised (quant_blocks; once per token, shared by
+ * all its experts).  The expert has width c made of sub-experts of width cw
+ * side by side (cw = c for a routed expert; the shared experts form one MLP
+ * over their concatenated width, the TP-slicing identity of §2.1).  Blocks
+ * along the contraction are bd elements of d (W1, W2 rows) and bc elements of
+ * c (the hidden row and W3 rows); bd = d, bc = c is one scale per row.  W1, W2
+ * are [c, d] from element base12, element (j, i) quantised with the exponent
+ * of its block, e1 / e2[j (d / bd) + i / bd]; W3 element (i, jj) sits at
+ * base3 + (jj / cw) d cw + i cw + jj % cw with exponent e3[i (c / bc) + jj / bc].
  *   gate_j = sum_i aq[i] Wq2[j, i],  up_j = sum_i aq[i] Wq1[j, i]
  *   h_j    = SiLU(gate_j) up_j, rounded per storage (the stored hidden)
- *   hq     = h quantised as one row (quant_row over its c elements)
+ *   hq     = h quantised in blocks of bc (quant_blocks over its c elements)
  *   y_i    = sum_jj hq[jj] Wq3[i, jj]
  * h returns the stored hidden before its quantisation. */
-static void mlp_row_fp8(int d, int c, int cw, const double* aq,
+static void mlp_row_fp8(int d, int c, int cw, int bd, int bc, const double* aq,
                         const void* w1, const void* w2, size_t base12, const int32_t* e1, const int32_t* e2,
                         const void* w3, size_t base3, const int32_t* e3, int wdt, int storage,
                         double* h, double* hq, double* y) {
+    const size_t nbd = (size_t)(d / bd), nbc = (size_t)(c / bc);
     for (int j = 0; j < c; ++j) {
         double gate = 0.0, up = 0.0;
         for (int i = 0; i < d; ++i) {
-            gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[j]);
-            up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[j]);
+            gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[(size_t)j * nbd + i / bd]);
+            up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd + i / bd]);
         }
         h[j] = oracle_round(silu(gate) * up, storage);
         hq[j] = h[j];
     }
-    quant_row(hq, c, NULL);
+    quant_blocks(hq, c, bc, NULL, NULL);
     for (int i = 0; i < d; ++i) {
         double acc = 0.0;
         for (int jj = 0; jj < c; ++jj) {
             size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);
-            acc += hq[jj] * wq(w3, off, wdt, e3[i]);
+            acc += hq[jj] * wq(w3, off, wdt, e3[(size_t)i * nbc + jj / bc]);
         }
         y[i] = acc;
     }
 }
 
-/* Row exponents of one block's FP8 expert weights: routed W1, W2 rows [E c]
+/* Exponents of one block's FP8 expert weights, one per row (row scales) or
+ * per block of 32 along the row (block scales): routed W1, W2 rows [E c]
  * (along d) and W3 rows [E d] (along c); the shared experts' gate/up rows
  * [n_s c_s] and the rows of their concatenated down projection [d] (along the
- * n_s c_s concatenated columns). */
+ * n_s c_s concatenated columns).  Each array holds rows x (row length / block). */
 typedef struct { int32_t *e1, *e2, *e3, *e1s, *e2s, *e3s; } fp8_exps;
 
 static void fp8_exps_free(fp8_exps* x) {
@@ -344,29 +421,46 @@ static int fp8_exps_make(const oracle_cfg* cfg, const void* w1, const void* w2, 
                          const void* w1s, const void* w2s, const void* w3s, fp8_exps* x) {
     const int d = cfg->d, E = cfg->E, c = cfg->c, ns = cfg->n_shared, cs = cfg->c_shared;
     const int wdt = cfg->in_dtype;
+    const int bd = fp8_blk(cfg, d), bc = fp8_blk(cfg, c), bcs = fp8_blk(cfg, ns * cs);
     memset(x, 0, sizeof *x);
-    x->e1 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * c);
-    x->e2 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * c);
-    x->e3 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * d);
+    if (d % bd || c % bc || (ns > 0 && (ns * cs) % bcs)) return -1;
+    const size_t nbd = (size_t)(d / bd), nbc = (size_t)(c / bc);
+    x->e1 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * c * nbd);
+    x->e2 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * c * nbd);
+    x->e3 = (int32_t*)malloc(sizeof(int32_t) * (size_t)E * d * nbc);
     if (!x->e1 || !x->e2 || !x->e3) return -2;
-    weight_row_exps(w1, wdt, (size_t)E * c, d, x->e1);
-    weight_row_exps(w2, wdt, (size_t)E * c, d, x->e2);
-    weight_row_exps(w3, wdt, (size_t)E * d, c, x->e3);
+    weight_block_exps(w1, wdt, (size_t)E * c, d, bd, x->e1);
+    weight_block_exps(w2, wdt, (size_t)E * c, d, bd, x->e2);
+    weight_block_exps(w3, wdt, (size_t)E * d, c, bc, x->e3);
+    const size_t nbs = ns > 0 ? (size_t)(ns * cs / bcs) : 0;
     if (ns > 0 && w1s) {
-        x->e1s = (int32_t*)malloc(sizeof(int32_t) * (size_t)ns * cs);
-        x->e2s = (int32_t*)malloc(sizeof(int32_t) * (size_t)ns * cs);
-        x->e3s = (int32_t*)malloc(sizeof(int32_t) * (size_t)d);
+        x->e1s = (int32_t*)malloc(sizeof(int32_t) * (size_t)ns * cs * nbd);
+        x->e2s = (int32_t*)malloc(sizeof(int32_t) * (size_t)ns * cs * nbd);
+        x->e3s = (int32_t*)malloc(sizeof(int32_t) * (size_t)d * nbs);
         if (!x->e1s || !x->e2s || !x->e3s) return -2;
-        weight_row_exps(w1s, wdt, (size_t)ns * cs, d, x->e1s);
-        weight_row_exps(w2s, wdt, (size_t)ns * cs, d, x->e2s);
+        weight_block_exps(w1s, wdt, (size_t)ns * cs, d, bd, x->e1s);
+        weight_block_exps(w2s, wdt, (size_t)ns * cs, d, bd, x->e2s);
+        /* row i of the concatenated down projection, column jj = sh c_s + j */
         for (int i = 0; i < d; ++i) {
-            double amax = 0.0;
-            for (int sh = 0; sh < ns; ++sh)
-                for (int j = 0; j < cs; ++j) {
+            for (size_t b = 0; b < nbs; ++b) {
+                double amax = 0.0;
+                for (int jj = (int)b * bcs; jj < ((int)b + 1) * bcs; ++jj) {
+                    const int sh = jj / cs, j = jj % cs;
                     double v = fabs(elem(w3s, (size_t)sh * d * cs + (size_t)i * cs + j, wdt));
                     if (v > amax) amax = v;
                 }
-            x->e3s[i] = fp8_row_exp(amax);
+                x->e3s[(size_t)i * nbs + b] = fp8_row_exp(amax);
+            }
+        }
+    }
+    if (wdt == ORACLE_BF16) {
+        wq_tables_for(x->e1, (size_t)E * c * nbd);
+        wq_tables_for(x->e2, (size_t)E * c * nbd);
+        wq_tables_for(x->e3, (size_t)E * d * nbc);
+        if (x->e1s) {
+            wq_tables_for(x->e1s, (size_t)ns * cs * nbd);
+            wq_tables_for(x->e2s, (size_t)ns * cs * nbd);
+            wq_tables_for(x->e3s, (size_t)d * nbs);
         }
     }
     return 0;
@@ -392,9 +486,11 @@ int oracle_expert_rows(const oracle_cfg* cfg, int n_rows, const void* a, int a_d
         for (int i = 0; i < d; ++i) arow[i] = elem(a, (size_t)r * d + i, a_dtype);
         size_t e = (size_t)expert[r];
         if (cfg->fp8) {
-            quant_row(arow, d, NULL);
-            mlp_row_fp8(d, c, c, arow, w1, w2, e * c * d, fx.e1 + e * c, fx.e2 + e * c,
-                        w3, e * d * c, fx.e3 + e * d, cfg->in_dtype, cfg->storage, h, hq, y_out + (size_t)r * d);
+            const int bd = fp8_blk(cfg, d), bc = fp8_blk(cfg, c);
+            quant_blocks(arow, d, bd, NULL, NULL);
+            mlp_row_fp8(d, c, c, bd, bc, arow, w1, w2, e * c * d, fx.e1 + e * c * (d / bd), fx.e2 + e * c * (d / bd),
+                        w3, e * d * c, fx.e3 + e * d * (c / bc), cfg->in_dtype, cfg->storage, h, hq,
+                        y_out + (size_t)r * d);
         } else {
             mlp_row(d, c, arow, w1, e * c * d, w2, e * c * d, w3, e * d * c, cfg->in_dtype,
                     cfg->storage, h, y_out + (size_t)r * d);
@@ -481,15 +577,17 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
         const double* a = u + (size_t)t * d;
         if (cfg->fp8) {     /* the token row quantised once for all of its experts */
             memcpy(aq, a, sizeof(double) * (size_t)d);
-            quant_row(aq, d, NULL);
+            quant_blocks(aq, d, fp8_blk(cfg, d), NULL, NULL);
         }
         /* routed experts: Combine = gate-weighted sum of the k expert outputs */
         for (int s = 0; s < k; ++s) {
             size_t e = (size_t)topk_idx[(size_t)t * k + s];
             double w = topk_w[(size_t)t * k + s];
             if (cfg->fp8)
-                mlp_row_fp8(d, c, c, aq, wts->w1, wts->w2, e * c * d, fx.e1 + e * c, fx.e2 + e * c,
-                            wts->w3, e * d * c, fx.e3 + e * d, cfg->in_dtype, cfg->storage, h, hq, y);
+                mlp_row_fp8(d, c, c, fp8_blk(cfg, d), fp8_blk(cfg, c), aq, wts->w1, wts->w2, e * c * d,
+                            fx.e1 + e * c * (d / fp8_blk(cfg, d)), fx.e2 + e * c * (d / fp8_blk(cfg, d)),
+                            wts->w3, e * d * c, fx.e3 + e * d * (c / fp8_blk(cfg, c)), cfg->in_dtype,
+                            cfg->storage, h, hq, y);
             else
                 mlp_row(d, c, a, wts->w1, e * c * d, wts->w2, e * c * d, wts->w3, e * d * c,
                         cfg->in_dtype, cfg->storage, h, y);
@@ -497,8 +595,8 @@ int oracle_block(const oracle_cfg* cfg, const oracle_weights* wts, int n_tok,
         }
         /* shared experts: every token, gate weight 1 */
         if (cfg->fp8 && ns > 0) {
-            mlp_row_fp8(d, ns * cs, cs, aq, wts->w1s, wts->w2s, 0, fx.e1s, fx.e2s,
-                        wts->w3s, 0, fx.e3s, cfg->in_dtype, cfg->storage, h, hq, y);
+            mlp_row_fp8(d, ns * cs, cs, fp8_blk(cfg, d), fp8_blk(cfg, ns * cs), aq, wts->w1s, wts->w2s, 0, fx.e1s,
+                        fx.e2s, wts->w3s, 0, fx.e3s, cfg->in_dtype, cfg->storage, h, hq, y);
             for (int i = 0; i < d; ++i) S[i] = y[i];    /* one MLP over the concatenated width */
         } else {
             for (int sh = 0; sh < ns; ++sh) {

@@ -27,7 +27,8 @@ typedef struct {
     int gate;                /* ORACLE_GATE_* */
     int in_dtype;            /* element type of the weights: ORACLE_F32 / BF16 / F64 */
     int storage;             /* ORACLE_EXACT / STORE_BF16 / STORE_F32 */
-    int fp8;                 /* 1: expert GEMM operands in FP8 E4M3 with per-row scales (see oracle.c) */
+    int fp8;                 /* expert GEMM operands in FP8 E4M3: 1 with per-row scales, 2 with one scale
+                                per block of 32 along the contraction (MX); see oracle.c */
 } oracle_cfg;
 
 typedef struct {
@@ -47,6 +48,8 @@ double oracle_e4m3(double x);
 int oracle_e4m3_array(int64_t n, const double* x, double* out, uint8_t* codes);
 int oracle_quant_rows(int rows, int cols, const void* x, int x_dtype,
                       uint8_t* codes, int32_t* exps, double* deq);
+int oracle_quant_blocks(int rows, int cols, int blk, const void* x, int x_dtype,
+                        uint8_t* codes, int32_t* exps, double* deq);
 int oracle_router(const oracle_cfg* cfg, int n_tok, const void* u, int u_dtype,
                   const void* w_r, const float* bias,
                   double* logits, int32_t* topk_idx, double* topk_w);

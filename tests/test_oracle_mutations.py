@@ -55,15 +55,25 @@ MUTANTS = {
     "e4m3_ties_away": ("double r = nearbyint(a / q) * q; /* ties to even */", "double r = round(a / q) * q;"),
     "fp8_scale_search_starts_high": ("int s = e - 10;", "int s = e - 8;"),
     "fp8_scale_boundary_exclusive": ("while (amax > ldexp(448.0, s)) ++s;", "while (amax >= ldexp(448.0, s)) ++s;"),
-    "fp8_hidden_not_quantised": ("    quant_row(hq, c, NULL);\n", ""),
-    "fp8_gate_uses_up_row_exponent": ("gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[j]);",
-                                      "gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e1[j]);"),
-    "fp8_down_exponent_by_column": ("acc += hq[jj] * wq(w3, off, wdt, e3[i]);", "acc += hq[jj] * wq(w3, off, wdt, e3[jj % d]);"),
-    "fp8_token_row_not_quantised_in_block": ("            quant_row(aq, d, NULL);\n", ""),
+    "fp8_hidden_not_quantised": ("    quant_blocks(hq, c, bc, NULL, NULL);\n", ""),
+    "fp8_gate_uses_up_row_exponent": (
+        "gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[(size_t)j * nbd + i / bd]);",
+        "gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd + i / bd]);"),
+    "fp8_down_exponent_by_column": ("acc += hq[jj] * wq(w3, off, wdt, e3[(size_t)i * nbc + jj / bc]);",
+                                    "acc += hq[jj] * wq(w3, off, wdt, e3[(size_t)(jj % d) * nbc + jj / bc]);"),
+    "fp8_token_row_not_quantised_in_block": ("            quant_blocks(aq, d, fp8_blk(cfg, d), NULL, NULL);\n", ""),
     "fp8_shared_down_read_as_one_matrix": ("size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);",
                                            "size_t off = base3 + (size_t)i * c + (size_t)jj;"),
-    "fp8_shared_down_exponent_first_expert": ("            for (int sh = 0; sh < ns; ++sh)\n                for (int j = 0; j < cs; ++j) {",
-                                              "            for (int sh = 0; sh < 1; ++sh)\n                for (int j = 0; j < cs; ++j) {"),
+    "fp8_shared_down_exponent_first_expert": ("                    const int sh = jj / cs, j = jj % cs;",
+                                              "                    const int sh = 0, j = jj % cs;"),
+    # block-scaled (MX) FP8
+    "mx_blocks_of_16": ("#define ORACLE_MX_BLOCK 32", "#define ORACLE_MX_BLOCK 16"),
+    "mx_weight_row_uses_first_block_exponent": (
+        "up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd + i / bd]);",
+        "up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd]);"),
+    "mx_hidden_row_scaled": ("    quant_blocks(hq, c, bc, NULL, NULL);\n", "    quant_blocks(hq, c, c, NULL, NULL);\n"),
+    "mx_token_row_scaled_in_block": ("            quant_blocks(aq, d, fp8_blk(cfg, d), NULL, NULL);\n",
+                                     "            quant_blocks(aq, d, d, NULL, NULL);\n"),
     # backward
     "bwd_silu_grad_sign": ("return sg * (1.0 + g * (1.0 - sg));", "return sg * (1.0 - g * (1.0 - sg));"),
     "bwd_dg_without_up": ("dg[jj] = oracle_round(dh * a[jj] * silu_grad(g[jj]), storage);",
@@ -114,6 +124,12 @@ PIN_TESTS = [
     fp8.test_down_projection_reduces_to_the_quantised_hidden,
     fp8.test_down_projection_with_representable_weights_is_a_matmul_of_the_quantised_hidden,
     fp8.test_block_sums_are_the_per_row_fp8_experts,
+    fp8.test_mx_block_scales_brute_force,
+    fp8.test_mx_gate_up_reduces_to_exact_on_representable_operands,
+    fp8.test_mx_down_projection_is_a_matmul_of_the_block_quantised_hidden,
+    lambda: [fp8.test_mx_block_sums_are_the_per_row_mx_experts(w) for w in (False, True)],
+    lambda: [fp8.test_mx_expert_matches_a_library_form_on_a_wide_dynamic_range(l)
+             for l in ("across_blocks", "within_blocks")],
     lambda: [bwd.test_stack_backward_finite_differences_wirings(w) for w in ("partial", "outdated", "disabled")],
     lambda: [bwd.test_stack_backward_finite_differences_gates(g) for g in ("softmax", "softmax_renorm", "sigmoid",
                                                                           "sigmoid_norm")],
