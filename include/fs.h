@@ -63,8 +63,17 @@ typedef enum {
  * smallest integer such that max |x_i| 2^-e <= 448; the code of x_i is
  * x_i 2^-e rounded to E4M3 (nearest, ties to even, saturating at 448).  The
  * tensor cores take the E4M3 codes (kind::f8f6f4, fp32 accumulate) and the
- * GEMM epilogue multiplies by the two row scales. */
-typedef enum { FS_BF16 = 0, FS_F32 = 1, FS_FP8 = 2 } fs_dtype;
+ * GEMM epilogue multiplies by the two row scales.
+ *
+ * FS_MXFP8: the same expert path with block scales (the MX formats): every
+ * operand row along the contraction is cut into blocks of 32 elements and each
+ * block gets its own power-of-two scale by the rule above (clamped to 2^-127 ..
+ * 2^127), stored as a UE8M0 byte (exponent + 127).  The tensor cores apply
+ * both operands' block scales inside the contraction (kind::mxf8f6f4 with
+ * block_scale).  The stored bf16 hidden h is quantised in blocks of 32 by the
+ * gate/up GEMM itself.  Dispatch pads each expert's segment to a multiple of
+ * 128 rows (see fs_dispatch).  d, c, c_shared multiples of 128. */
+typedef enum { FS_BF16 = 0, FS_F32 = 1, FS_FP8 = 2, FS_MXFP8 = 3 } fs_dtype;
 
 /* Gate rule s() applied to the top-k logits z (after the optional bias):
  *   SOFTMAX         w_s = exp(z_s) / sum over ALL experts of exp(z_j)
@@ -141,9 +150,14 @@ size_t fs_workspace_bytes_attn(const fs_layer_desc* desc, int L);
  *   FP8:  E4M3 codes tiled as [G][ceil(N/256)][K/128][256][128] (32 KB blocks,
  *         rows past N zero), then the G N fp32 row scales (output channel n of
  *         group g at index g N + n).  The pack functions take the bf16 weights
- *         and quantise each output-channel row (FS_FP8 in fs_dtype).
+ *         and quantise each output-channel row (FS_FP8 in fs_dtype);
+ *   MXFP8: the codes tiled as for FP8 (rows past N zero), then the UE8M0
+ *         block scales as [G][ceil(N/256)][K/128][1024]: for a 256-row tile and
+ *         128 elements of K, byte (r / 128) 512 + (r % 32) 16 + ((r % 128) / 32) 4 + b
+ *         holds the scale of tile row r, block b (0..3) of those 128 elements
+ *         (rows past N: 127, a unit scale).
  * fs_packed_bytes gives the size (0 for invalid arguments; K % 64 == 0, FP8:
- * K % 128 == 0). */
+ * K % 128 == 0, MXFP8: K and N multiples of 128). */
 size_t fs_packed_bytes(int32_t G, int32_t N, int32_t K, int32_t dtype);
 
 /* Gate/up: the page's W1 (up) and W2 (gate), each [G, c, d], as one packed
@@ -182,6 +196,27 @@ size_t fs_fp8_rows_bytes(int64_t rows, int32_t cols);
  * cols % 128 == 0. */
 fs_status fs_quantize_rows_fp8(int64_t rows, int32_t cols, const void* x, void* q, void* stream);
 
+/* MX matrix [rows, cols] (the FS_MXFP8 activations: x_perm, the shared
+ * experts' quantised input, the hidden): with rows128 = rows rounded up to a
+ * multiple of 128, rows128 * cols E4M3 codes row-major, then from byte offset
+ * rows128 * cols rounded up to a multiple of 256 the UE8M0 block scales in
+ * 512-byte chunks [rows128 / 128][cols / 128][512]: byte
+ * (r % 32) 16 + ((r % 128) / 32) 4 + b of chunk (r / 128, j) holds the scale of
+ * row r, block b (0..3) of columns [128 j, 128 j + 128); element (r, i) =
+ * value(code[r, i]) 2^(scale byte - 127).  Its size in bytes, or 0 for
+ * rows < 1 or cols not a positive multiple of 128. */
+size_t fs_mx_rows_bytes(int64_t rows, int32_t cols);
+
+/* Quantise bf16 rows x [rows, cols] to the MX matrix q (blocks of 32 along
+ * each row; the rows up to rows128 get zero codes and unit scales).
+ * cols % 128 == 0. */
+fs_status fs_quantize_rows_mx(int64_t rows, int32_t cols, const void* x, void* q, void* stream);
+
+/* Rows of fs_dispatch's x_perm and of fs_grouped_swiglu's y_perm for desc:
+ * T k, or for FS_MXFP8 (128-row aligned expert segments) T k + 127 E rounded
+ * up to a multiple of 128.  0 for an invalid desc. */
+int64_t fs_dispatch_rows(const fs_layer_desc* desc);
+
 /* Router (§2.1, G(A) = s(A W_R^T)): logits z = u W_R^T + bias (fp32 accumulate;
  * bf16 operands on the tensor cores for FS_BF16, fp32 FMA for FS_F32), then the
  * top-k selection and gate weights of desc->gate.
@@ -204,7 +239,14 @@ fs_status fs_router_topk(const fs_layer_desc* desc, const void* u, const void* w
  * An index outside [0, E) sets the device error word (reported by
  * fs_get_error) and that pair is dropped.  FS_FP8: u is bf16 and x_perm is an
  * FP8 row-scaled matrix [T k, d] (fs_fp8_rows_bytes(T k, d) bytes): each token
- * row is quantised once and its codes and scale go to all of its k rows. */
+ * row is quantised once and its codes and scale go to all of its k rows.
+ * FS_MXFP8: each expert's segment starts at a multiple of 128 rows: offsets[e]
+ * is the exclusive prefix sum of the counts rounded up to 128 (offsets[E] the
+ * padded total), expert e's rows are [offsets[e], offsets[e] + counts[e]) and
+ * the rows up to offsets[e+1] are padding with unspecified contents; x_perm is
+ * an MX matrix of fs_dispatch_rows(desc) rows (fs_mx_rows_bytes bytes), each
+ * token row quantised once in blocks of 32, and perm_src has
+ * fs_dispatch_rows(desc) entries (those of padding rows unspecified). */
 fs_status fs_dispatch(const fs_layer_desc* desc, const int32_t* topk_idx, const void* u,
                       int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
                       void* x_perm, void* ws, size_t ws_bytes, void* stream);
@@ -242,7 +284,11 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
  * bf16: persistent tcgen05/TMEM grouped GEMMs fed by TMA; fp32: fp32 FMA.
  * FS_FP8: x_perm is fs_dispatch's FP8 row-scaled matrix, the weights are the
  * FP8 packs; h is stored bf16, quantised per row (fs_quantize_rows_fp8) and
- * fed to the down GEMM as E4M3; y_perm is bf16. */
+ * fed to the down GEMM as E4M3; y_perm is bf16.  FS_MXFP8: x_perm is
+ * fs_dispatch's MX matrix, offsets its padded offsets, the weights the MXFP8
+ * packs; every row of each padded segment is computed (padding rows give
+ * unspecified y), h is rounded to bf16 and quantised in blocks of 32 by the
+ * gate/up GEMM's epilogue; y_perm has fs_dispatch_rows(desc) rows. */
 fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const int32_t* offsets,
                             const void* w13, const void* w3, void* y_perm,
                             void* ws, size_t ws_bytes, void* stream);
@@ -285,6 +331,28 @@ fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_
                      const void* shared_out, const float* extra, void* o_partial, void* o_full,
                      int32_t out_dtype, void* u_next, int32_t wiring, void* u_full, void* stream);
 
+/* The shared experts (§2.1) with Combine and the FarSkip update (§3, eq. 8a/8b)
+ * in one pass: fs_shared_expert followed by fs_combine, with the combine done
+ * in the epilogue of the shared experts' down projection, so the fp32 shared
+ * output S never goes to memory and the memory-bound combine overlaps that
+ * projection's tensor-core work.  Results are bit-identical to
+ *   fs_shared_expert(desc, u, w13_shared, w3_shared, S, ...);
+ *   fs_combine(desc, y_perm, pos, topk_w, o_prev, prev_dtype, S, NULL,
+ *              o_partial, o_full, out_dtype, u_next, wiring, NULL, ...).
+ * u [T, d] (the shared experts' input), y_perm, pos, topk_w as for fs_combine
+ * (the routed experts' outputs must be complete when the call's work runs),
+ * o_prev [T, d] in prev_dtype -> o_partial (NULL = not written), o_full in
+ * out_dtype, u_next (NULL = not written) per wiring.  FS_BF16 or FS_FP8 with
+ * n_shared >= 1 and k <= 8, else FS_ERR_UNSUPPORTED (n_shared = 0:
+ * FS_ERR_INVALID_ARG).  Needs ws of fs_workspace_bytes(desc, 0) bytes.
+ * (fs_farskip_stack keeps the two separate calls: at DeepSeek-V3's shapes this
+ * fused pass measured slower than them.) */
+fs_status fs_shared_expert_combine(const fs_layer_desc* desc, const void* u, const void* w13_shared,
+                                   const void* w3_shared, const void* y_perm, const int32_t* pos,
+                                   const float* topk_w, const void* o_prev, int32_t prev_dtype, void* o_partial,
+                                   void* o_full, int32_t out_dtype, void* u_next, int32_t wiring, void* ws,
+                                   size_t ws_bytes, void* stream);
+
 /* Stand-in attention sub-block for the attention wirings: out = a W_att^T
  * (a per-token dense GEMM on the tensor cores for bf16, fp32 FMA for fp32).
  * It stands in for attention (which mixes tokens) so the §3 attention/MoE
@@ -317,7 +385,8 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
  * u_{k+1}, while `stream` runs the routed experts and the final
  * o_k = o_k* + R_k; block k+1's router/dispatch/shared thus run concurrently
  * with block k's routed grouped GEMMs.  Bit-identical to fs_farskip_stack.
- * wiring must be FS_WIRE_PARTIAL or FS_WIRE_OUTDATED; stream2 != stream.
+ * wiring must be FS_WIRE_PARTIAL or FS_WIRE_OUTDATED; stream2 != stream;
+ * FS_MXFP8 is not supported here (FS_ERR_UNSUPPORTED).
  * Work queued on `stream` before the call is complete before stream2 starts,
  * and work queued on `stream` after the call sees all of the stack's results.
  * Needs ws of fs_workspace_bytes_overlap(desc, L) bytes.  The library keeps

@@ -24,8 +24,9 @@ class LayerConfig:
     c_shared: int        # shared expert width
     L: int               # FarSkip blocks
     gate: str            # softmax | softmax_renorm | sigmoid | sigmoid_norm
-    dtype: str           # "bf16" (bf16 storage, fp32 accumulate), "f32", or "fp8"
+    dtype: str           # "bf16" (bf16 storage, fp32 accumulate), "f32", "fp8"
                          # (bf16 storage, FP8 E4M3 expert GEMM operands with row scales)
+                         # or "mxfp8" (the same with one scale per 32-element block)
     zipf_s: float | None = None   # router-bias skew (Zipf exponent) or None
     wiring: str = "partial"
     seed: int = 0
@@ -48,7 +49,8 @@ class LayerConfig:
         """Algorithmic HBM bytes of one block: read u and o_prev, write o* and o,
         read every expert's, the shared experts' and the router's weights once."""
         es = 4 if self.dtype == "f32" else 2
-        wes = 1 if self.dtype == "fp8" else es        # FP8 expert weights: one byte per element
+        # FP8 expert weights: one byte per element (MX: plus one scale byte per 32)
+        wes = 1.0 if self.dtype == "fp8" else (1.0 + 1.0 / 32 if self.dtype == "mxfp8" else es)
         T, d = self.T, self.d
         act = 4.0 * T * d * es
         w = (3.0 * self.E * d * self.c + 3.0 * self.n_shared * d * self.c_shared) * wes + self.E * d * es
@@ -77,6 +79,8 @@ CONFIGS = {
 # The FP8 expert path on the same shapes (the pages' inference precision).
 for _name in ("v2lite", "qwen3", "scout", "v3", "v3_decode", "v3_e32"):
     CONFIGS[_name + "_fp8"] = CONFIGS[_name].with_(name=_name + "_fp8", dtype="fp8")
+    # block-scaled FP8 (MX: one UE8M0 scale per 32 elements along the contraction)
+    CONFIGS[_name + "_mxfp8"] = CONFIGS[_name].with_(name=_name + "_mxfp8", dtype="mxfp8")
 
 
 def describe(cfg: LayerConfig) -> str:

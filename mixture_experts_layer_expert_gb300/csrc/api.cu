@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "fp8.cuh"
 #include "kernels.h"
+#include "mx.cuh"
 
 namespace fs {
 
@@ -82,12 +83,14 @@ static fs_status check_desc(const fs_layer_desc* d) {
     if (!d) return FS_ERR_INVALID_ARG;
     if (d->T < 1 || d->d < 1 || d->E < 1 || d->k < 1 || d->c < 1 || d->n_shared < 0) return FS_ERR_INVALID_ARG;
     if (d->k > d->E) return FS_ERR_INVALID_ARG;
-    if (d->dtype != FS_BF16 && d->dtype != FS_F32 && d->dtype != FS_FP8) return FS_ERR_INVALID_ARG;
+    if (d->dtype != FS_BF16 && d->dtype != FS_F32 && d->dtype != FS_FP8 && d->dtype != FS_MXFP8)
+        return FS_ERR_INVALID_ARG;
     if (d->gate < FS_GATE_SOFTMAX || d->gate > FS_GATE_SIGMOID_NORM) return FS_ERR_INVALID_ARG;
     if (d->n_shared > 0 && d->c_shared < 1) return FS_ERR_INVALID_ARG;
     if (d->d % 64 || d->c % 64) return FS_ERR_UNSUPPORTED;
     if (d->n_shared > 0 && d->c_shared % 64) return FS_ERR_UNSUPPORTED;
-    if (d->dtype == FS_FP8 && (d->d % 128 || d->c % 128 || (d->n_shared > 0 && d->c_shared % 128)))
+    if ((d->dtype == FS_FP8 || d->dtype == FS_MXFP8) &&
+        (d->d % 128 || d->c % 128 || (d->n_shared > 0 && d->c_shared % 128)))
         return FS_ERR_UNSUPPORTED;
     if (d->E > kMaxExperts || d->k > kMaxTopK) return FS_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(d->T) * d->k;
@@ -95,11 +98,20 @@ static fs_status check_desc(const fs_layer_desc* d) {
     return FS_OK;
 }
 
-// Activations (GEMM inputs u_k, y_perm, u_next) are bf16 for FS_BF16 and FS_FP8
-// (whose expert operands are quantised inside the path), fp32 for FS_F32.
+// Activations (GEMM inputs u_k, y_perm, u_next) are bf16 for FS_BF16, FS_FP8
+// and FS_MXFP8 (whose expert operands are quantised inside the path), fp32 for
+// FS_F32.
 static inline int elem_bytes(const fs_layer_desc* d) { return d->dtype == FS_F32 ? 4 : 2; }
 static inline int act_dtype(const fs_layer_desc* d) { return d->dtype == FS_F32 ? FS_F32 : FS_BF16; }
 static inline bool is_fp8(const fs_layer_desc* d) { return d->dtype == FS_FP8; }
+static inline bool is_mx(const fs_layer_desc* d) { return d->dtype == FS_MXFP8; }
+static inline int qmode(const fs_layer_desc* d) { return is_fp8(d) ? kQuantRow : (is_mx(d) ? kQuantMx : kQuantNone); }
+// Rows of x_perm / y_perm: T k, or with the MX path's 128-row-aligned expert
+// segments T k + 127 E rounded up to 128.
+static inline long long perm_rows(const fs_layer_desc* d) {
+    const long long rows = static_cast<long long>(d->T) * d->k;
+    return is_mx(d) ? mx_rows128(rows + 127LL * d->E) : rows;
+}
 
 // ------------------------------------------------------------- workspace
 struct Layout {
@@ -125,13 +137,16 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.disp = take(dispatch_ws_bytes(d->T, d->E));
     l.plan_z = take(4 * sizeof(int));
     l.plan_r = take(2 * (E + 1) * sizeof(int));
-    const bool f8 = is_fp8(d);
-    l.h_r = take(rows * d->c * es);
+    const bool f8 = is_fp8(d), mxq = is_mx(d);
+    const long long prow = perm_rows(d);
+    // MX: the hidden goes straight from the gate/up epilogue into an MX matrix
+    l.h_r = take(mxq ? mx_rows_bytes(prow, d->c) : rows * d->c * es);
     l.hq_r = take(f8 ? fp8_rows_bytes(static_cast<long long>(rows), d->c) : 0);   // FP8: quantised h
     l.plan_s = take(4 * sizeof(int));
-    l.h_s = take(T * cw * es);
+    l.h_s = take(mxq ? (cw ? mx_rows_bytes(static_cast<long long>(T), static_cast<int>(cw)) : 0) : T * cw * es);
     l.hq_s = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), static_cast<int>(cw)) : 0);
-    l.uq = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), d->d) : 0);    // FP8: quantised u_k
+    l.uq = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), d->d)
+                         : (mxq && cw ? mx_rows_bytes(static_cast<long long>(T), d->d) : 0));   // quantised u_k
     l.plan_a = take(4 * sizeof(int));
     l.end0 = o;
     l.topk_idx = take(rows * 4);
@@ -139,9 +154,10 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.counts = take(E * 4);
     l.offsets = take((E + 1) * 4);
     l.pos = take(rows * 4);
-    l.perm = take(rows * 4);
-    l.x_perm = take(f8 ? fp8_rows_bytes(static_cast<long long>(rows), d->d) : rows * dm * es);
-    l.y_perm = take(rows * dm * es);
+    l.perm = take(static_cast<size_t>(perm_rows(d)) * 4);
+    l.x_perm = take(f8 ? fp8_rows_bytes(static_cast<long long>(rows), d->d)
+                       : (mxq ? mx_rows_bytes(prow, d->d) : rows * dm * es));
+    l.y_perm = take(static_cast<size_t>(prow) * dm * es);
     l.s_out = take(cw ? T * dm * 4 : 0);     // S in fp32
     // The residual stream between blocks is fp32; the last block writes the
     // caller's outputs.  o_{b-2}, o_{b-1} (and o_{b-1}*) stay live while block
@@ -252,7 +268,8 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
                                cudaStream_t st, void* u_q = nullptr) {
     const Layout l = layout(d, 0);
     FS_TRY(launch_dispatch(idx, u, d->T, d->d, d->E, d->k, elem_bytes(d), counts, offsets, pos, perm, x_perm,
-                           at<int32_t>(ws, l.disp), st, is_fp8(d), is_fp8(d) ? u_q : nullptr));
+                           at<int32_t>(ws, l.disp), st, qmode(d), qmode(d) != kQuantNone ? u_q : nullptr,
+                           perm_rows(d)));
     return FS_OK;
 }
 
@@ -263,10 +280,26 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 // Dispatch permutation applied inside the first GEMM's operand loads.
 // FS_FP8: x is an FP8 row-scaled matrix [x_rows, d], the weights FP8 packs; h
 // (bf16) is quantised per row into hq before the down GEMM.
+// With cmb set (one group over the T token rows, tensor-core dtypes) the down
+// projection's epilogue is Combine fused with the FarSkip update (y unused).
 static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_rows, const int32_t* gather, int rows,
                              const int32_t* offsets, int G, int cw, const void* w13, const void* w3, void* y,
-                             bool y_f32, int* plan, void* h, void* hq, cudaStream_t st, void* gu_save = nullptr) {
-    if (is_fp8(d)) {
+                             bool y_f32, int* plan, void* h, void* hq, cudaStream_t st, void* gu_save = nullptr,
+                             const CombineEpi* cmb = nullptr) {
+    if (is_mx(d)) {
+        // x: an MX matrix of x_rows rows (a multiple of 128 or the token count);
+        // groups start at multiples of 128; the hidden is written as an MX matrix
+        const long long xr = mx_rows128(x_rows);
+        const int max_mt = ceil_div(xr, 128) + G;
+        const uint8_t* xs = static_cast<const uint8_t*>(x) + mx_sf_offset(xr, d->d);
+        uint8_t* hc = static_cast<uint8_t*>(h);
+        uint8_t* hs = hc + mx_sf_offset(xr, cw);
+        FS_TRY(launch_plan(offsets, G, offsets ? static_cast<int>(xr) : rows, 128, plan, st));
+        FS_TRY(launch_mx_gemm(EPI_SWIGLU, x, xr, xs, w13, packed_sf_mx(w13, G, 2 * cw, d->d), G, 2 * cw, d->d, plan,
+                              max_mt, hc, cw, cw, hs, st));
+        FS_TRY(launch_mx_gemm(y_f32 ? EPI_F32 : EPI_BF16, hc, xr, hs, w3, packed_sf_mx(w3, G, d->d, cw), G, d->d, cw,
+                              plan, max_mt, y, d->d, d->d, nullptr, st));
+    } else if (is_fp8(d)) {
         const int bm = tc_block_m_f8();
         const int max_mt = ceil_div(rows, bm) + G;
         const float* xs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x) + fp8_scale_offset(x_rows, d->d));
@@ -275,8 +308,9 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         FS_TRY(launch_tc_gemm_f8(EPI_SWIGLU, x, x_rows, xs, w13, packed_scales_fp8(w13, G, 2 * cw, d->d), G, 2 * cw,
                                  d->d, plan, max_mt, h, cw, cw, st));
         FS_TRY(launch_quant_rows(h, rows, cw, hq, st));
-        FS_TRY(launch_tc_gemm_f8(y_f32 ? EPI_F32 : EPI_BF16, hq, rows, hs, w3, packed_scales_fp8(w3, G, d->d, cw), G,
-                                 d->d, cw, plan, max_mt, y, d->d, d->d, st));
+        FS_TRY(launch_tc_gemm_f8(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), hq, rows, hs, w3,
+                                 packed_scales_fp8(w3, G, d->d, cw), G, d->d, cw, plan, max_mt, y, d->d, d->d, st,
+                                 cmb));
     } else if (d->dtype == FS_BF16) {
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -286,8 +320,10 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         ex.aux_ld = 2LL * cw;
         FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, gather, rows,
                               true, st, &ex));
-        FS_TRY(launch_tc_gemm(y_f32 ? EPI_F32 : EPI_BF16, h, rows, w3, G, d->d, cw, plan, max_mt, y, d->d, d->d,
-                              nullptr, 0, true, st));
+        TcExtra ex2;
+        ex2.combine = cmb;
+        FS_TRY(launch_tc_gemm(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), h, rows, w3, G, d->d, cw, plan,
+                              max_mt, y, d->d, d->d, nullptr, 0, true, st, &ex2));
     } else {
         const int bm = simt_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -303,7 +339,7 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
 static fs_status routed_impl(const fs_layer_desc* d, const void* x_perm, const int32_t* offsets, const void* w13,
                              const void* w3, void* y_perm, void* ws, cudaStream_t st) {
     const Layout l = layout(d, 0);
-    const int rows = d->T * d->k;
+    const int rows = static_cast<int>(perm_rows(d));
     return swiglu_impl(d, x_perm, rows, nullptr, rows, offsets, d->E, d->c, w13, w3, y_perm, false,
                        at<int>(ws, l.plan_r), at<void>(ws, l.h_r), at<void>(ws, l.hq_r), st);
 }
@@ -319,15 +355,44 @@ static fs_status routed_gather_impl(const fs_layer_desc* d, const void* u, const
 // FS_FP8: the GEMMs read the quantised u_k in ws (written by the stack's
 // Dispatch when u_q_ready, else quantised here from u).
 static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* w13s, const void* w3s, void* s_out,
-                             void* ws, cudaStream_t st, bool u_q_ready = false) {
+                             void* ws, cudaStream_t st, bool u_q_ready = false, const CombineEpi* cmb = nullptr) {
     const Layout l = layout(d, 0);
     const void* x = u;
     if (is_fp8(d)) {
         x = at<void>(ws, l.uq);
         if (!u_q_ready) FS_TRY(launch_quant_rows(u, d->T, d->d, at<void>(ws, l.uq), st));
+    } else if (is_mx(d)) {
+        x = at<void>(ws, l.uq);
+        if (!u_q_ready) FS_TRY(launch_quant_rows_mx(u, d->T, d->d, at<void>(ws, l.uq), st));
     }
     return swiglu_impl(d, x, d->T, nullptr, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
-                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), at<void>(ws, l.hq_s), st);
+                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), at<void>(ws, l.hq_s), st, nullptr, cmb);
+}
+
+// The shared experts with Combine and the FarSkip update in the epilogue of
+// their down projection (tensor-core dtypes, k <= 8): the same results as
+// shared_impl followed by combine_impl, without the fp32 S in memory.
+static bool fused_combine_ok(const fs_layer_desc* d) {
+    return (d->dtype == FS_BF16 || d->dtype == FS_FP8) && d->n_shared > 0 && d->k <= kCombineEpiMaxK;
+}
+
+static fs_status shared_combine_impl(const fs_layer_desc* d, const void* u, const void* w13s, const void* w3s,
+                                     const void* y_perm, const int32_t* pos, const float* w, const void* o_prev,
+                                     int prev_dtype, void* o_partial, void* o_full, int out_dtype, void* u_next,
+                                     int wiring, void* ws, cudaStream_t st, bool u_q_ready = false) {
+    CombineEpi cmb;
+    cmb.y_perm = y_perm;
+    cmb.pos = pos;
+    cmb.topk_w = w;
+    cmb.k = d->k;
+    cmb.o_prev = o_prev;
+    cmb.prev_bf16 = prev_dtype == FS_BF16;
+    cmb.o_partial = o_partial;
+    cmb.o_full = o_full;
+    cmb.out_bf16 = out_dtype == FS_BF16;
+    cmb.u_next = u_next;
+    cmb.u_src = wiring == FS_WIRE_PARTIAL ? 0 : (wiring == FS_WIRE_OUTDATED ? 1 : 2);
+    return shared_impl(d, u, w13s, w3s, nullptr, ws, st, u_q_ready, &cmb);
 }
 
 static fs_status combine_impl(const fs_layer_desc* d, const void* y_perm, const int32_t* pos, const float* w,
@@ -392,18 +457,20 @@ size_t fs_workspace_bytes_overlap(const fs_layer_desc* desc, int L) {
     return layout_overlap(desc, L).end;
 }
 
-static inline bool valid_dtype(int32_t t) { return t == FS_BF16 || t == FS_F32 || t == FS_FP8; }
+static inline bool valid_dtype(int32_t t) { return t == FS_BF16 || t == FS_F32 || t == FS_FP8 || t == FS_MXFP8; }
 
 fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype, const void* w1, const void* w2, void* w13,
                       void* stream) {
     if (G < 1 || c < 1 || d < 1 || !valid_dtype(dtype)) return FS_ERR_INVALID_ARG;
-    const int q = dtype == FS_FP8 ? 128 : 64;
+    const int q = (dtype == FS_FP8 || dtype == FS_MXFP8) ? 128 : 64;
     if (c % q || d % q) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(w1));
     FS_CHECK(need(w2));
     FS_CHECK(need(w13));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == FS_FP8)
+    if (dtype == FS_MXFP8)
+        FS_TRY(launch_pack_w13_mx(G, c, d, w1, w2, w13, st));
+    else if (dtype == FS_FP8)
         FS_TRY(launch_pack_w13_fp8(G, c, d, w1, w2, w13, st));
     else
         FS_TRY(launch_pack_w13(G, c, d, dtype == FS_BF16 ? 2 : 4, w1, w2, w13, st));
@@ -413,17 +480,20 @@ fs_status fs_pack_w13(int32_t G, int32_t c, int32_t d, int32_t dtype, const void
 size_t fs_packed_bytes(int32_t G, int32_t N, int32_t K, int32_t dtype) {
     if (G < 1 || N < 1 || K < 1 || K % 64 || !valid_dtype(dtype)) return 0;
     if (dtype == FS_FP8) return K % 128 ? 0 : packed_bytes_fp8(G, N, K);
+    if (dtype == FS_MXFP8) return (K % 128 || N % 128) ? 0 : packed_bytes_mx(G, N, K);
     return packed_bytes(G, N, K, dtype == FS_BF16 ? 2 : 4);
 }
 
 fs_status fs_pack_w3(int32_t G, int32_t d, int32_t c, int32_t dtype, const void* w3, void* w3p, void* stream) {
     if (G < 1 || c < 1 || d < 1 || !valid_dtype(dtype)) return FS_ERR_INVALID_ARG;
-    const int q = dtype == FS_FP8 ? 128 : 64;
+    const int q = (dtype == FS_FP8 || dtype == FS_MXFP8) ? 128 : 64;
     if (c % q || d % q) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(w3));
     FS_CHECK(need(w3p));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == FS_FP8)
+    if (dtype == FS_MXFP8)
+        FS_TRY(launch_pack_w3_mx(G, d, c, w3, w3p, st));
+    else if (dtype == FS_FP8)
         FS_TRY(launch_pack_w3_fp8(G, d, c, w3, w3p, st));
     else
         FS_TRY(launch_pack_w3(G, d, c, dtype == FS_BF16 ? 2 : 4, w3, w3p, st));
@@ -433,12 +503,14 @@ fs_status fs_pack_w3(int32_t G, int32_t d, int32_t c, int32_t dtype, const void*
 fs_status fs_pack_w3_shared(int32_t n_shared, int32_t c_shared, int32_t d, int32_t dtype, const void* w3s,
                             void* w3cat, void* stream) {
     if (n_shared < 1 || c_shared < 1 || d < 1 || !valid_dtype(dtype)) return FS_ERR_INVALID_ARG;
-    const int q = dtype == FS_FP8 ? 128 : 64;
+    const int q = (dtype == FS_FP8 || dtype == FS_MXFP8) ? 128 : 64;
     if (c_shared % q || d % q) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(w3s));
     FS_CHECK(need(w3cat));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == FS_FP8)
+    if (dtype == FS_MXFP8)
+        FS_TRY(launch_pack_w3_shared_mx(n_shared, c_shared, d, w3s, w3cat, st));
+    else if (dtype == FS_FP8)
         FS_TRY(launch_pack_w3_shared_fp8(n_shared, c_shared, d, w3s, w3cat, st));
     else
         FS_TRY(launch_pack_w3_shared(n_shared, c_shared, d, dtype == FS_BF16 ? 2 : 4, w3s, w3cat, st));
@@ -457,6 +529,25 @@ fs_status fs_quantize_rows_fp8(int64_t rows, int32_t cols, const void* x, void* 
     FS_CHECK(need(q));
     FS_TRY(launch_quant_rows(x, rows, cols, q, static_cast<cudaStream_t>(stream)));
     return FS_OK;
+}
+
+size_t fs_mx_rows_bytes(int64_t rows, int32_t cols) {
+    if (rows < 1 || cols < 1 || cols % 128) return 0;
+    return mx_rows_bytes(rows, cols);
+}
+
+fs_status fs_quantize_rows_mx(int64_t rows, int32_t cols, const void* x, void* q, void* stream) {
+    if (rows < 1 || cols < 1) return FS_ERR_INVALID_ARG;
+    if (cols % 128 || rows > 0x7fffffffLL) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(need(x));
+    FS_CHECK(need(q));
+    FS_TRY(launch_quant_rows_mx(x, rows, cols, q, static_cast<cudaStream_t>(stream)));
+    return FS_OK;
+}
+
+int64_t fs_dispatch_rows(const fs_layer_desc* desc) {
+    if (check_desc(desc) != FS_OK) return 0;
+    return perm_rows(desc);
 }
 
 fs_status fs_router_topk(const fs_layer_desc* desc, const void* u, const void* w_r, const float* bias,
@@ -505,7 +596,8 @@ fs_status fs_dispatch_noalloc(const fs_layer_desc* desc, const int32_t* topk_idx
         return FS_ERR_WORKSPACE;
     }
     FS_TRY(launch_dispatch_noalloc(topk_idx, u, desc->T, desc->d, desc->E, desc->k, elem_bytes(desc), counts, offsets,
-                                   pos, perm_src, x_perm, static_cast<cudaStream_t>(stream), is_fp8(desc)));
+                                   pos, perm_src, x_perm, static_cast<cudaStream_t>(stream), qmode(desc),
+                                   perm_rows(desc)));
     return FS_OK;
 }
 
@@ -532,7 +624,7 @@ fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, con
     FS_CHECK(need(w3));
     FS_CHECK(need(y_perm));
     FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
-    if (is_fp8(desc)) return FS_ERR_UNSUPPORTED;
+    if (is_fp8(desc) || is_mx(desc)) return FS_ERR_UNSUPPORTED;
     if (desc->dtype == FS_BF16 && !tc_gather_supported()) return FS_ERR_UNSUPPORTED;
     return routed_gather_impl(desc, u, perm_src, offsets, w13, w3, y_perm, ws, static_cast<cudaStream_t>(stream));
 }
@@ -569,6 +661,32 @@ fs_status fs_combine(const fs_layer_desc* desc, const void* y_perm, const int32_
     if (extra && !aligned16(extra)) return FS_ERR_UNSUPPORTED;
     return combine_impl(desc, y_perm, pos, topk_w, o_prev, prev_dtype, shared_out, extra, o_partial, o_full,
                         out_dtype, u_next, wiring, u_full, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_shared_expert_combine(const fs_layer_desc* desc, const void* u, const void* w13_shared,
+                                   const void* w3_shared, const void* y_perm, const int32_t* pos, const float* topk_w,
+                                   const void* o_prev, int32_t prev_dtype, void* o_partial, void* o_full,
+                                   int32_t out_dtype, void* u_next, int32_t wiring, void* ws, size_t ws_bytes,
+                                   void* stream) {
+    FS_CHECK(check_desc(desc));
+    if (desc->n_shared < 1) return FS_ERR_INVALID_ARG;
+    FS_CHECK(need(u));
+    FS_CHECK(need(w13_shared));
+    FS_CHECK(need(w3_shared));
+    FS_CHECK(need(y_perm));
+    FS_CHECK(need(pos));
+    FS_CHECK(need(topk_w));
+    FS_CHECK(need(o_prev));
+    FS_CHECK(need(o_full));
+    if ((prev_dtype != FS_BF16 && prev_dtype != FS_F32) || (out_dtype != FS_BF16 && out_dtype != FS_F32))
+        return FS_ERR_INVALID_ARG;
+    if (u_next && (wiring < FS_WIRE_PARTIAL || wiring > FS_WIRE_DISABLED)) return FS_ERR_INVALID_ARG;
+    if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
+    if (u_next && !aligned16(u_next)) return FS_ERR_UNSUPPORTED;
+    if (!fused_combine_ok(desc)) return FS_ERR_UNSUPPORTED;
+    FS_CHECK(check_ws(desc, 0, ws, ws_bytes));
+    return shared_combine_impl(desc, u, w13_shared, w3_shared, y_perm, pos, topk_w, o_prev, prev_dtype, o_partial,
+                               o_full, out_dtype, u_next, wiring, ws, static_cast<cudaStream_t>(stream));
 }
 
 fs_status fs_attn_standin(const fs_layer_desc* desc, const void* a, const void* w_att, float* out, void* ws,
@@ -623,12 +741,12 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
     const void* a_in = x;     // attention input (attention wirings), activation type
     int prev_dtype = act_dtype(desc);
     float* att = at<float>(ws, l.att);
-    void* u_q = is_fp8(desc) && desc->n_shared > 0 ? at<void>(ws, layout(desc, 0).uq) : nullptr;
+    void* u_q = qmode(desc) != kQuantNone && desc->n_shared > 0 ? at<void>(ws, layout(desc, 0).uq) : nullptr;
     for (int b = 1; b <= L; ++b) {
         const fs_block_weights& bw = blocks[b - 1];
         const bool last = (b == L);
         void* o_k = last ? o_full : at<void>(ws, l.ring[(b - 1) % l.nring]);
-        void* os_k = last ? o_partial : at<void>(ws, l.star[(b - 1) % l.nstar]);
+        void* os_k = last ? o_partial : nullptr;      // o_k* of an inner block is not read again
         void* u_next = last ? nullptr : at<void>(ws, l.ubuf[(b - 1) % l.nu]);
         void* a_next = last ? nullptr : at<void>(ws, l.abuf[(b - 1) & 1]);
         const int out_dtype = last ? act_dtype(desc) : FS_F32;
@@ -653,6 +771,10 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
         FS_CHECK(router_impl(desc, u, bw.w_r, bw.bias, idx, w, nullptr, ws, st));
         FS_CHECK(dispatch_impl(desc, idx, u, counts, offsets, pos, perm, x_perm, ws, st, u_q));
         FS_CHECK(routed_impl(desc, x_perm, offsets, bw.w13, bw.w3, y_perm, ws, st));
+        // The shared experts then Combine as two passes: Combine in the shared down
+        // projection's epilogue (fs_shared_expert_combine) measured slower at
+        // DeepSeek-V3's shapes -- its per-row gathers from eight epilogue warps per
+        // SM keep too few loads in flight next to the standalone kernel.
         if (s_out) FS_CHECK(shared_impl(desc, u, bw.w13_shared, bw.w3_shared, s_out, ws, st, u_q != nullptr));
         if (wiring == FS_WIRE_ATTN_FARSKIP) {
             // next attention input bf16(o_k*) = bf16(o_k - R_k), next MoE input bf16(o_k)
@@ -683,6 +805,7 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
     if (L < 1 || !blocks) return FS_ERR_INVALID_ARG;
     if (wiring != FS_WIRE_PARTIAL && wiring != FS_WIRE_OUTDATED) return FS_ERR_INVALID_ARG;
     if (!stream2 || stream2 == stream) return FS_ERR_INVALID_ARG;
+    if (is_mx(desc)) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(x));
     FS_CHECK(need(o_full));
     if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;

@@ -50,9 +50,11 @@ dispatch_count_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
 }
 
 // One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+// pad128: each expert's segment starts at a multiple of 128 rows (the MX
+// path): offsets are the exclusive prefix of the counts rounded up to 128.
 __global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E, int32_t* __restrict__ counts,
-                     int32_t* __restrict__ offsets) {
+                     int32_t* __restrict__ offsets, int pad128) {
     __shared__ int warp_sums[32];
     const int e = threadIdx.x;
     int total = 0;
@@ -77,7 +79,8 @@ dispatch_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E, int32
     }
     // exclusive scan of totals over experts
     const int lane = e & 31, wid = e >> 5;
-    int v = total;
+    const int seg = pad128 ? (total + 127) / 128 * 128 : total;
+    int v = seg;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, o);
@@ -95,10 +98,10 @@ dispatch_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E, int32
         warp_sums[lane] = w;
     }
     __syncthreads();
-    const int excl = v - total + (wid > 0 ? warp_sums[wid - 1] : 0);
+    const int excl = v - seg + (wid > 0 ? warp_sums[wid - 1] : 0);
     if (e < E) {
         offsets[e] = excl;
-        if (e == E - 1) offsets[E] = excl + total;
+        if (e == E - 1) offsets[E] = excl + seg;
         for (int b = 0; b < nchunks; ++b) chunk_hist[static_cast<long long>(b) * E + e] += excl;
     }
 }
@@ -246,14 +249,15 @@ static cudaError_t set_smem_attr(const void* fn, size_t bytes) {
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
-                            int32_t* scratch, cudaStream_t st, bool fp8, void* u_q) {
+                            int32_t* scratch, cudaStream_t st, int qmode, void* u_q, long long rows_cap) {
+    const bool fp8 = qmode == kQuantRow;
     const int nc = n_chunks(T);
     int* err = dev_error_ptr();
     dispatch_count_kernel<<<nc, kChunk, E * sizeof(int32_t), st>>>(topk_idx, T, E, k, scratch, err);
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dispatch_scan_kernel<<<1, 1024, 0, st>>>(scratch, nc, E, counts, offsets);
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(scratch, nc, E, counts, offsets, qmode == kQuantMx ? 1 : 0);
     count_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -265,6 +269,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (!x_perm) return cudaSuccess;     // the caller gathers rows itself (no permuted copy)
+    if (qmode == kQuantMx) return launch_dispatch_copy_mx(u, T, d, k, pos, x_perm, rows_cap, u_q, st);
     if (fp8) {
         const long long rows = static_cast<long long>(T) * k;
         uint8_t* xq = static_cast<uint8_t*>(x_perm);
@@ -318,12 +323,12 @@ static cudaError_t dispatch_scratch_address(int32_t** out) {
 
 cudaError_t launch_dispatch_noalloc(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
-                                    void* x_perm, cudaStream_t st, bool fp8) {
+                                    void* x_perm, cudaStream_t st, int qmode, long long rows_cap) {
     int32_t* scratch = nullptr;
     cudaError_t e = dispatch_scratch_address(&scratch);
     if (e != cudaSuccess) return e;
     return launch_dispatch(topk_idx, u, T, d, E, k, elem_bytes, counts, offsets, pos, perm_src, x_perm, scratch, st,
-                           fp8, nullptr);
+                           qmode, nullptr, rows_cap);
 }
 
 }  // namespace fs

@@ -77,6 +77,7 @@ struct Args {
     int tma_out;             // bf16 out (EPI_SWIGLU h, EPI_BF16) through the output tensor map
     int ksplit = 1;          // EPI_F32: K split into ksplit ranges, each written as its own partial
     long long split_rows = 0;   // rows between the partials of successive K ranges in out
+    CombineEpi cmb;          // EPI_COMBINE: Combine operands and outputs
 };
 
 struct Tile {
@@ -120,6 +121,118 @@ __device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float*
         const float f[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[4 * q4 + i] = __float_as_uint((__uint_as_float(v[4 * q4 + i]) * sa) * f[i]);
+    }
+}
+
+// v[j] <- (v[j] * sa) * sb[j] for 16 fp32 accumulator columns.
+__device__ __forceinline__ void scale_cols16(uint32_t* v, float sa, const float* sb) {
+    const float4* s4 = reinterpret_cast<const float4*>(sb);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 b = __ldg(s4 + q4);
+        const float f[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[4 * q4 + i] = __float_as_uint((__uint_as_float(v[4 * q4 + i]) * sa) * f[i]);
+    }
+}
+
+// 16 consecutive residual values (bf16 or fp32) at element offset off.
+__device__ __forceinline__ void load16_resid(const void* base, long long off, bool bf16, float (&v)[16]) {
+    if (bf16) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+        const uint4 a = __ldg(p), b = __ldg(p + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v[2 * q] = bf16lo(w[q]);
+            v[2 * q + 1] = bf16hi(w[q]);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 a = __ldg(p + q);
+            v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+        }
+    }
+}
+
+__device__ __forceinline__ void store16_resid(void* base, long long off, bool bf16, const float (&v)[16]) {
+    if (bf16) {
+        uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
+        p[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                          pack_bf16x2(v[6], v[7]));
+        p[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                          pack_bf16x2(v[14], v[15]));
+    } else {
+        float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+}
+
+// EPI_COMBINE for the thread owning token row `orow`, columns [c_lo, c_hi) of
+// n-tile n: the accumulator is the shared output S; Combine and the FarSkip
+// update follow combine_kernel's arithmetic (see CombineEpi).  Per 16 columns
+// the k routed rows' 32-byte pieces are loaded together (k loads in flight).
+template <bool F8>
+__device__ __forceinline__ void epilogue_combine(uint32_t tbase, bool row_ok, long long orow, int n, int c_lo, int c_hi,
+                                                 float sa, const float* sb, const Args& args) {
+    const CombineEpi& cb = args.cmb;
+    const long long d = args.ldo;
+    int ps[kCombineEpiMaxK];
+    float wsl[kCombineEpiMaxK];
+#pragma unroll
+    for (int s = 0; s < kCombineEpiMaxK; ++s) {
+        ps[s] = -1;
+        wsl[s] = 0.f;
+        if (row_ok && s < cb.k) {
+            ps[s] = __ldg(cb.pos + orow * cb.k + s);
+            wsl[s] = __ldg(cb.topk_w + orow * cb.k + s);
+        }
+    }
+#pragma unroll 1
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + c0, v);
+        tmem_ld_wait();
+        if (!row_ok) continue;
+        if constexpr (F8) scale_cols16(v, sa, sb + c0);
+        const long long col = static_cast<long long>(n) * BN + c0;
+        uint4 yr[kCombineEpiMaxK][2];
+#pragma unroll
+        for (int s = 0; s < kCombineEpiMaxK; ++s) {
+            if (ps[s] >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(cb.y_perm) +
+                                                                  static_cast<long long>(ps[s]) * d + col);
+                yr[s][0] = __ldg(src);
+                yr[s][1] = __ldg(src + 1);
+            }
+        }
+        float prev[16], base[16], acc[16], full[16];
+        load16_resid(cb.o_prev, orow * d + col, cb.prev_bf16 != 0, prev);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            base[j] = prev[j] + __uint_as_float(v[j]);
+            acc[j] = 0.f;
+        }
+#pragma unroll
+        for (int s = 0; s < kCombineEpiMaxK; ++s) {
+            if (ps[s] >= 0) {
+                const uint32_t q[8] = {yr[s][0].x, yr[s][0].y, yr[s][0].z, yr[s][0].w,
+                                       yr[s][1].x, yr[s][1].y, yr[s][1].z, yr[s][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc[2 * i] = fmaf(wsl[s], bf16lo(q[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wsl[s], bf16hi(q[i]), acc[2 * i + 1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) full[j] = base[j] + acc[j];
+        if (cb.o_partial) store16_resid(cb.o_partial, orow * d + col, cb.out_bf16 != 0, base);
+        store16_resid(cb.o_full, orow * d + col, cb.out_bf16 != 0, full);
+        if (cb.u_next) store16_resid(cb.u_next, orow * d + col, true, cb.u_src == 0 ? base : (cb.u_src == 1 ? prev : full));
     }
 }
 
@@ -256,6 +369,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                 }
             }
         }
+    } else if constexpr (EPI == EPI_COMBINE) {
+        const int rem = args.out_cols - tl.n * BN;
+        const int ncols = rem >= BN ? BN : rem;
+        epilogue_combine<F8>(tbase, row_ok, orow, tl.n, half * (BN / 2), min(ncols, (half + 1) * (BN / 2)), sa,
+                             sb, args);
     } else if constexpr (EPI == EPI_DSWIGLU) {
         // accumulator = dh of hidden columns j = 256 n + c; g_j, a_j sit at packed
         // columns 128 (j / 64) + j % 64 and that + 64 of the aux row, and dg, da
@@ -1143,8 +1261,7 @@ static cudaError_t get_encode() {
 // 2D tensor map over a [rows, cols] row-major matrix of bf16 (f8 = false) or
 // 8-bit codes (f8 = true) with a box of box_rows x 128 bytes and the 128-byte
 // swizzle.
-static cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows,
-                            bool f8 = false) {
+cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows, bool f8) {
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
     const int es = f8 ? 1 : 2;
@@ -1161,8 +1278,7 @@ static cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, lo
 
 // 3D tensor map over the tiled weight layout [nblocks][256][128 bytes] (each
 // block a contiguous 32 KB tile of 256 rows) with a box of box_rows x 128 bytes.
-static cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows,
-                                   bool f8 = false) {
+cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows, bool f8) {
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
     const int es = f8 ? 1 : 2;
@@ -1179,7 +1295,7 @@ static cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long 
 
 // 2D bf16 output map [rows, cols] (row stride ldo elements) for 32 x 32 pieces
 // stored with the 64-byte swizzle.
-static cudaError_t make_out_map_bf16(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo) {
+cudaError_t make_out_map_bf16(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo) {
     cudaError_t e = get_encode();
     if (e != cudaSuccess) return e;
     cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -1232,7 +1348,7 @@ static cudaError_t output_map(int epi, bool pair, void* out, long long out_rows,
 
 static int g_num_sms = 0;
 
-static cudaError_t num_sms(int* out) {
+cudaError_t num_sms(int* out) {
     if (!g_num_sms) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -1314,6 +1430,11 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
     if (pair) ksplit = 1;
     args.ksplit = ksplit;
     args.split_rows = a_rows;
+    if (EPI == EPI_COMBINE) {
+        if (!ex || !ex->combine || G != 1 || gather_rows || ex->combine->k < 1 || ex->combine->k > kCombineEpiMaxK)
+            return cudaErrorInvalidValue;
+        args.cmb = *ex->combine;
+    }
     CUtensorMap to = ta;
     e = output_map(EPI, pair, out, (gather_rows ? gather_limit : a_rows) * ksplit, out_cols, ldo, &to,
                    &args.tma_out);
@@ -1339,7 +1460,8 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
 template <int EPI>
 static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const float* a_scale, const void* B,
                                      const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles,
-                                     void* out, long long ldo, int out_cols, cudaStream_t st) {
+                                     void* out, long long ldo, int out_cols, cudaStream_t st,
+                                     const CombineEpi* cmb = nullptr) {
     const bool pair = use_pair();
     static bool attr_set[2] = {false, false};
     cudaError_t e;
@@ -1379,6 +1501,10 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
     args.aux = nullptr;
     args.aux_ld = 0;
     args.accumulate = 0;
+    if (EPI == EPI_COMBINE) {
+        if (!cmb || G != 1 || cmb->k < 1 || cmb->k > kCombineEpiMaxK) return cudaErrorInvalidValue;
+        args.cmb = *cmb;
+    }
     CUtensorMap to = ta;
     e = output_map(EPI, pair, out, a_rows, out_cols, ldo, &to, &args.tma_out);
     if (e != cudaSuccess) return e;
@@ -1403,8 +1529,11 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
 
 cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const float* a_scale, const void* B,
                               const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles, void* out,
-                              long long ldo, int out_cols, cudaStream_t st) {
+                              long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine) {
     switch (epi) {
+        case EPI_COMBINE:
+            return launch_tc_f8_impl<EPI_COMBINE>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
+                                                  out_cols, st, combine);
         case EPI_SWIGLU:
             return launch_tc_f8_impl<EPI_SWIGLU>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
                                                  out_cols, st);
@@ -1435,6 +1564,9 @@ cudaError_t launch_tc_gemm(int epi, const void* A, long long a_rows, const void*
         case EPI_F32:
             return launch_tc_impl<EPI_F32>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
                                            gather_rows, gather_limit, b_blocked, st, ex);
+        case EPI_COMBINE:
+            return launch_tc_impl<EPI_COMBINE>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,
+                                               gather_rows, gather_limit, b_blocked, st, ex);
         case EPI_DSWIGLU:
             if (!ex || !ex->aux) return cudaErrorInvalidValue;
             return launch_tc_impl<EPI_DSWIGLU>(A, a_rows, B, G, N, K, plan, max_mtiles, out, ldo, out_cols,

@@ -1,6 +1,7 @@
 // kernels.h -- internal launchers of libfs (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,7 +14,32 @@ constexpr int kMaxExperts = 512;   // router top-k kernel limit
 // EPI_DSWIGLU: the accumulator is dh (hidden columns); with the stored
 // pre-activations g, a (TcExtra::aux, packed gate/up column order) it writes
 // dg = dh a SiLU'(g) and da = dh SiLU(g) (bf16) at the same packed columns.
-enum { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_DSWIGLU = 3 };
+// EPI_COMBINE: one group over all T token rows (the shared experts' down
+// projection); the accumulator is the shared output S of token row t, and the
+// epilogue is Combine fused with the FarSkip update (CombineEpi).
+enum { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_DSWIGLU = 3, EPI_COMBINE = 4 };
+
+// Combine in the epilogue of the shared experts' down projection, with the
+// arithmetic of combine_kernel (fp32, rounded once per output):
+//   base = o_prev[t] + S[t]; R = sum_{s<k} w[t, s] y_perm[pos[t k + s]] (slot order)
+//   o_partial[t] = base (if set), o_full[t] = base + R,
+//   u_next[t] = bf16 of base (u_src 0), o_prev (1) or base + R (2) (if set).
+// y_perm and u_next are bf16; the residual o_prev / o_partial / o_full is bf16
+// or fp32; k <= 8.
+struct CombineEpi {
+    const void* y_perm = nullptr;
+    const int32_t* pos = nullptr;
+    const float* topk_w = nullptr;
+    int k = 0;
+    const void* o_prev = nullptr;
+    int prev_bf16 = 0;
+    void* o_partial = nullptr;
+    void* o_full = nullptr;
+    int out_bf16 = 0;
+    void* u_next = nullptr;
+    int u_src = 0;
+};
+constexpr int kCombineEpiMaxK = 8;
 
 // Optional epilogue inputs/outputs of launch_tc_gemm:
 //   aux          EPI_SWIGLU: also store the pre-activations g, a (bf16) here
@@ -28,6 +54,8 @@ struct TcExtra {
     // ranges, range s written to rows [s a_rows, (s + 1) a_rows) of out (partial
     // sums; the consumer adds them in order).  Ignored (1) by the CTA-pair kernel.
     int ksplit = 1;
+    // EPI_COMBINE: the Combine operands and outputs (out is unused)
+    const CombineEpi* combine = nullptr;
 };
 
 void count_launch();
@@ -61,7 +89,36 @@ cudaError_t launch_wgrad_gemm(const void* A, int lda, const void* B, int ldb, lo
 // accumulator by a_scale[row] b_scale[g N + col].  Single-CTA kernel only.
 cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const float* a_scale, const void* B,
                               const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles, void* out,
-                              long long ldo, int out_cols, cudaStream_t st);
+                              long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine = nullptr);
+
+// Tensor maps (gemm_tc.cu): a [rows, cols] row-major matrix of bf16 (f8: 8-bit
+// codes) with a box_rows x 128-byte box and the 128-byte swizzle; the tiled
+// weight layout [nblocks][256][128 bytes]; a bf16 output map for 32 x 32
+// pieces (64-byte swizzle).  num_sms: SMs of the current device.
+cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows, bool f8 = false);
+cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows, bool f8 = false);
+cudaError_t make_out_map_bf16(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo);
+cudaError_t num_sms(int* out);
+
+// gemm_mx.cu: block-scaled FP8 operands (kind::mxf8f6f4.block_scale).  A is an
+// MX matrix of a_rows (a multiple of 128) rows and K columns (codes A, scale
+// chunks a_sf), B MX-packed weights [G, N, K] (codes, chunks b_sf); groups
+// start at multiples of 128 rows.  EPI_SWIGLU writes the hidden as an MX
+// matrix (codes at out with row stride ldo bytes, chunks at h_sf; out_cols = c);
+// EPI_BF16 / EPI_F32 write bf16 / fp32 rows.
+cudaError_t launch_mx_gemm(int epi, const void* A, long long a_rows, const uint8_t* a_sf, const void* B,
+                           const uint8_t* b_sf, int G, int N, int K, const int* plan, int max_mtiles, void* out,
+                           long long ldo, int out_cols, uint8_t* h_sf, cudaStream_t st);
+
+// mx.cu: MX packs and quantisation (layouts in mx.cuh)
+size_t packed_bytes_mx(int G, int N, int K);
+const uint8_t* packed_sf_mx(const void* packed, int G, int N, int K);
+cudaError_t launch_pack_w13_mx(int G, int c, int d, const void* w1, const void* w2, void* w13, cudaStream_t st);
+cudaError_t launch_pack_w3_mx(int G, int d, int c, const void* w3, void* w3p, cudaStream_t st);
+cudaError_t launch_pack_w3_shared_mx(int ns, int cs, int d, const void* w3s, void* w3cat, cudaStream_t st);
+cudaError_t launch_quant_rows_mx(const void* x, long long rows, int cols, void* q, cudaStream_t st);
+cudaError_t launch_dispatch_copy_mx(const void* u, int T, int d, int k, const int32_t* pos, void* x_q,
+                                    long long rows_cap, void* u_q, cudaStream_t st);
 
 // gemm_simt.cu (fp32 operands, fp32 FMA)
 int simt_block_m();
@@ -78,14 +135,19 @@ cudaError_t launch_topk(const float* logits, int nsplit, const float* bias, int 
 // dispatch.cu
 constexpr int kStaticDispatchScratchInts = 65536;   // 256 KiB: fs_dispatch_noalloc's scratch
 size_t dispatch_ws_bytes(int T, int E);
-// fp8: x_perm is an FP8 row-scaled matrix [T k, d] (fp8.cuh) and u (bf16) is
-// quantised per token on the way; u_q (nullable) receives the quantised u [T, d].
+// qmode kQuantRow: x_perm is an FP8 row-scaled matrix [T k, d] (fp8.cuh) and u
+// (bf16) is quantised per token on the way; kQuantMx: each expert's segment
+// starts at a multiple of 128 rows (offsets padded) and x_perm is an MX matrix
+// of rows_cap rows (mx.cuh), u quantised in blocks of 32; u_q (nullable)
+// receives the quantised u [T, d] in the same form.
+enum { kQuantNone = 0, kQuantRow = 1, kQuantMx = 2 };
 cudaError_t launch_dispatch_noalloc(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src,
-                                    void* x_perm, cudaStream_t st, bool fp8);
+                                    void* x_perm, cudaStream_t st, int qmode, long long rows_cap);
 cudaError_t launch_dispatch(const int32_t* topk_idx, const void* u, int T, int d, int E, int k, int elem_bytes,
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* perm_src, void* x_perm,
-                            int32_t* scratch, cudaStream_t st, bool fp8 = false, void* u_q = nullptr);
+                            int32_t* scratch, cudaStream_t st, int qmode = kQuantNone, void* u_q = nullptr,
+                            long long rows_cap = 0);
 
 // combine.cu
 cudaError_t launch_combine(const void* y_perm, const int32_t* pos, const float* topk_w, const void* o_prev,

@@ -34,27 +34,6 @@ quant_rows_kernel(const uint4* __restrict__ x, long long rows, int cols, uint8_t
     }
 }
 
-// Where the 8 bf16 source elements [8v, 8v+8) of packed row n of group g live.
-// mode 0: gate/up interleave of w1 (up), w2 (gate) [G, c, d] (N = 2c, K = d);
-// mode 1: plain [G, N, K];  mode 2: shared down projections w3s [ns, d, cs]
-// side by side (N = d, K = ns cs, element (i, s cs + j) = w3s[s][i][j]).
-struct PackSrc {
-    const uint4* a;
-    const uint4* b;
-    int mode, N, K, c, cs;
-    __device__ __forceinline__ const uint4* chunk(long long g, int n, int v) const {
-        if (mode == 0) {
-            const int blk = n >> 7, within = n & 127;
-            const bool gate = within < 64;
-            const long long row = g * c + blk * 64 + (gate ? within : within - 64);
-            return (gate ? b : a) + (row * K) / 8 + v;
-        }
-        if (mode == 1) return a + ((g * N + n) * static_cast<long long>(K)) / 8 + v;
-        const int jj = 8 * v, s = jj / cs, j = jj - s * cs;
-        return a + ((static_cast<long long>(s) * N + n) * cs + j) / 8;
-    }
-};
-
 // One warp per packed row (grid-stride over G * NB * 256 rows).
 __global__ void __launch_bounds__(256)
 pack_fp8_kernel(PackSrc src, int G, int NB, uint8_t* __restrict__ codes, float* __restrict__ scales) {

@@ -18,8 +18,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfs.so")
 _lib = None
 
-FS_BF16, FS_F32, FS_FP8 = 0, 1, 2
-DTYPES = {"bf16": FS_BF16, "f32": FS_F32, "fp8": FS_FP8}
+FS_BF16, FS_F32, FS_FP8, FS_MXFP8 = 0, 1, 2, 3
+DTYPES = {"bf16": FS_BF16, "f32": FS_F32, "fp8": FS_FP8, "mxfp8": FS_MXFP8}
 GATES = {"softmax": 0, "softmax_renorm": 1, "sigmoid": 2, "sigmoid_norm": 3}
 WIRINGS = {"partial": 0, "outdated": 1, "disabled": 2, "attn_farskip": 3, "attn_plain": 4}
 STATUS = {0: "FS_OK", 1: "FS_ERR_INVALID_ARG", 2: "FS_ERR_UNSUPPORTED", 3: "FS_ERR_WORKSPACE",
@@ -67,6 +67,8 @@ _SIGS = {
     "fs_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _I32, _VP, _I32,
                           _VP, _VP]),
     "fs_attn_standin": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "fs_shared_expert_combine": (_I32, [ctypes.POINTER(LayerDesc), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP,
+                                        _I32, _VP, _I32, _VP, _SZ, _VP]),
     "fs_farskip_stack": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP, _VP,
                                 _VP, _VP, _SZ, _VP]),
     "fs_farskip_stack_overlap": (_I32, [ctypes.POINTER(LayerDesc), _I32, _I32, ctypes.POINTER(BlockWeights), _VP,
@@ -86,6 +88,9 @@ _SIGS = {
                                          ctypes.POINTER(BlockWeightsT), _VP, _SZ, _VP, _VP, _VP,
                                          ctypes.POINTER(BlockGrads), _VP, _SZ, _VP]),
     "fs_quantize_rows_fp8": (_I32, [ctypes.c_int64, _I32, _VP, _VP, _VP]),
+    "fs_mx_rows_bytes": (_SZ, [ctypes.c_int64, _I32]),
+    "fs_quantize_rows_mx": (_I32, [ctypes.c_int64, _I32, _VP, _VP, _VP]),
+    "fs_dispatch_rows": (ctypes.c_int64, [ctypes.POINTER(LayerDesc)]),
     "fs_get_error": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "fs_launch_count": (ctypes.c_uint64, []),
     "fs_selftest_wait_timeout": (_I32, [_I32, _VP]),
@@ -169,6 +174,31 @@ def fs_quantize_rows_fp8(rows, cols, x, q, stream=None):
     _check(lib().fs_quantize_rows_fp8(rows, cols, _p(x), _p(q), _stream(stream)), "fs_quantize_rows_fp8")
 
 
+def fs_mx_rows_bytes(rows: int, cols: int) -> int:
+    return int(lib().fs_mx_rows_bytes(rows, cols))
+
+
+def fs_quantize_rows_mx(rows, cols, x, q, stream=None):
+    _check(lib().fs_quantize_rows_mx(rows, cols, _p(x), _p(q), _stream(stream)), "fs_quantize_rows_mx")
+
+
+def fs_dispatch_rows(desc) -> int:
+    return int(lib().fs_dispatch_rows(ctypes.byref(desc)))
+
+
+def mx_rows_empty(rows: int, cols: int, device="cuda") -> torch.Tensor:
+    """A byte buffer for an MX matrix [rows, cols] (codes, then block-scale chunks)."""
+    return torch.empty(fs_mx_rows_bytes(rows, cols), dtype=torch.uint8, device=device)
+
+
+def mx_rows_split(buf: torch.Tensor, rows: int, cols: int):
+    """Views (codes [rows128, cols] uint8, scale bytes [rows128 / 128, cols / 128, 512]) of an MX matrix."""
+    r128 = (rows + 127) // 128 * 128
+    off = (r128 * cols + 255) // 256 * 256
+    return (buf[:r128 * cols].view(r128, cols),
+            buf[off:off + r128 // 128 * cols // 128 * 512].view(r128 // 128, cols // 128, 512))
+
+
 def fp8_rows_empty(rows: int, cols: int, device="cuda") -> torch.Tensor:
     """A byte buffer for an FP8 row-scaled matrix [rows, cols] (codes, then scales)."""
     return torch.empty(fs_fp8_rows_bytes(rows, cols), dtype=torch.uint8, device=device)
@@ -226,6 +256,18 @@ def fs_combine(desc, y_perm, pos, topk_w, o_prev, shared_out, o_partial, o_full,
     _check(lib().fs_combine(ctypes.byref(desc), _p(y_perm), _p(pos), _p(topk_w), _p(o_prev), _dtype_code(o_prev),
                             _p(shared_out), _p(extra), _p(o_partial), _p(o_full), _dtype_code(o_full), _p(u_next), w,
                             _p(u_full), _stream(stream)), "fs_combine")
+
+
+def fs_shared_expert_combine(desc, u, w13_shared, w3_shared, y_perm, pos, topk_w, o_prev, o_partial, o_full,
+                             u_next=None, wiring="partial", ws=None, stream=None):
+    """fs_shared_expert + fs_combine in one pass; residual dtypes from o_prev and o_full."""
+    if o_partial is not None:
+        assert o_partial.dtype == o_full.dtype
+    w = WIRINGS[wiring] if isinstance(wiring, str) else int(wiring)
+    _check(lib().fs_shared_expert_combine(ctypes.byref(desc), _p(u), _p(w13_shared), _p(w3_shared), _p(y_perm),
+                                          _p(pos), _p(topk_w), _p(o_prev), _dtype_code(o_prev), _p(o_partial),
+                                          _p(o_full), _dtype_code(o_full), _p(u_next), w, _p(ws), _nbytes(ws),
+                                          _stream(stream)), "fs_shared_expert_combine")
 
 
 def fs_attn_standin(desc, a, w_att, out, ws, stream=None):
@@ -290,7 +332,7 @@ def _packed(G, N, K, dt, like):
     n = fs_packed_bytes(G, N, K, dt)
     if n == 0:
         raise FsError(1, "fs_packed_bytes")
-    if dt == FS_FP8:
+    if dt in (FS_FP8, FS_MXFP8):
         return torch.empty(n, dtype=torch.uint8, device=like.device)
     return torch.empty(n // like.element_size(), dtype=like.dtype, device=like.device)
 

@@ -113,6 +113,19 @@ def test_other_entry_points_reject_bad_args(L):
                         _vp(FAKE), 0, _vp(FAKE), 9, None, None) == 1        # bad wiring for u_next
     assert L.fs_combine(ctypes.byref(d), _vp(FAKE), _vp(FAKE), _vp(FAKE), _vp(FAKE), 0, None, _vp(MIS), None,
                         _vp(FAKE), 0, None, 0, None, None) == 2             # misaligned extra
+    # fs_shared_expert_combine(desc, u, w13s, w3s, y, pos, w, o_prev, prev_dtype, o_partial, o_full, out_dtype,
+    #                          u_next, wiring, ws, ws_bytes, st)
+    sc = lambda dd, *a: L.fs_shared_expert_combine(ctypes.byref(dd), *a)
+    V = _vp(FAKE)
+    assert sc(d, V, V, V, V, V, V, V, 0, None, None, 0, None, 0, _vp(FAKE * 256), 1 << 40, None) == 1   # null o_full
+    assert sc(d, V, V, V, V, V, V, V, 2, None, V, 0, None, 0, _vp(FAKE * 256), 1 << 40, None) == 1      # bad dtype
+    assert sc(d, V, V, V, V, V, V, V, 0, None, V, 0, V, 7, _vp(FAKE * 256), 1 << 40, None) == 1         # bad wiring
+    assert sc(d, V, V, V, V, V, V, V, 0, _vp(MIS), V, 0, None, 0, _vp(FAKE * 256), 1 << 40, None) == 2  # misaligned
+    assert sc(desc(n_shared=0), V, V, V, V, V, V, V, 0, None, V, 0, None, 0, _vp(FAKE * 256), 1 << 40,
+              None) == 1                                                                            # no shared expert
+    assert sc(desc(dtype=1), V, V, V, V, V, V, V, 0, None, V, 0, None, 0, _vp(FAKE * 256), 1 << 40,
+              None) == 2                                                                            # fp32: unfused only
+    assert sc(d, V, V, V, V, V, V, V, 0, None, V, 0, None, 0, _vp(FAKE * 256), 16, None) == 3           # small ws
     assert L.fs_attn_standin(ctypes.byref(d), None, _vp(FAKE), _vp(FAKE), _vp(FAKE * 256), 1 << 40, None) == 1
     blocks1 = (fs.BlockWeights * 1)(fs.BlockWeights(FAKE, None, FAKE, FAKE, FAKE, FAKE, None))
     assert L.fs_farskip_stack(ctypes.byref(d), 1, 3, blocks1, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256),
@@ -122,7 +135,7 @@ def test_other_entry_points_reject_bad_args(L):
                               1 << 40, None) == 1
     assert L.fs_pack_w13(0, 64, 64, 0, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 1
     assert L.fs_pack_w13(1, 65, 64, 0, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 2
-    assert L.fs_pack_w3_shared(1, 64, 64, 3, _vp(FAKE), _vp(FAKE), None) == 1
+    assert L.fs_pack_w3_shared(1, 64, 64, 9, _vp(FAKE), _vp(FAKE), None) == 1
     blocks = (fs.BlockWeights * 1)()
     assert L.fs_farskip_stack(ctypes.byref(d), 1, 0, blocks, _vp(FAKE), _vp(FAKE), None, _vp(FAKE * 256),
                               1 << 40, None) == 1              # null block weights
@@ -151,7 +164,7 @@ def test_fp8_argument_checks(L):
     assert L.fs_quantize_rows_fp8(10, 100, _vp(FAKE), _vp(FAKE), None) == 2
     assert L.fs_quantize_rows_fp8(0, 128, _vp(FAKE), _vp(FAKE), None) == 1
     assert L.fs_quantize_rows_fp8(10, 128, _vp(MIS), _vp(FAKE), None) == 2
-    assert L.fs_pack_w13(1, 128, 128, 3, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 1      # unknown dtype
+    assert L.fs_pack_w13(1, 128, 128, 9, _vp(FAKE), _vp(FAKE), _vp(FAKE), None) == 1      # unknown dtype
     assert fs.fs_launch_count() == 0
 
 

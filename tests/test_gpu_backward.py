@@ -8,7 +8,9 @@ so the two sides differ by accumulation order and by bf16 rounding flips of
 stored values, compounded through the L blocks.  Bounds: relative Frobenius
 <= L x 5e-3 (the end-to-end forward bound) for the input gradient and for every weight gradient, computed
 over the tokens whose routing agrees in every block (near-ties are counted
-and bounded as in the forward); a weight gradient sums over all tokens.
+and explained as in the forward: block 1 routes identical inputs, and a later
+block may route a token differently only where the bf16 difference of its
+input explains it); a weight gradient sums over all tokens.
 """
 import numpy as np
 import pytest
@@ -16,13 +18,33 @@ import torch
 
 import oracle
 from mixture_experts_layer_expert_gb300 import configs, fs, synth
-from parity import gpu_stack_stepwise, oracle_cfg, oracle_weights, to64
-from test_gpu_stack import DRIFT_FRAC
+from parity import explained_drift, gpu_stack_stepwise, oracle_cfg, oracle_weights, record, to64, topk_mismatch
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 REL = 5e-3
 KEYS = ("dW_R", "dW1", "dW2", "dW3", "dW1s", "dW2s", "dW3s")
+
+
+def routing_agrees(cfg, blocks, routing, inputs, fwd, rows):
+    """Tokens (of `rows`) routed the same in every block by the GPU stack (routing,
+    inputs: per block over all T tokens) and the oracle forward on those rows:
+    block 1 under the strict near-tie rule, later blocks with every difference
+    explained by the input difference (explained_drift)."""
+    rows_t = torch.as_tensor(rows, device=DEV)
+    same = np.ones(len(rows), bool)
+    for b in range(cfg.L):
+        bias = blocks[b]["bias"]
+        bnp = None if bias is None else synth.to_numpy(bias)
+        if b == 0:
+            z = fwd["logits"][0] - (0 if bnp is None else bnp.astype(np.float64)[None, :])
+            bad = topk_mismatch(routing[0][rows], fwd["topk_idx"][0], z, cfg.k, bnp)
+        else:
+            explained_drift(cfg, synth.to_numpy(blocks[b]["w_r"]), bnp, synth.to_numpy(inputs[b][0][rows_t]),
+                            routing[b][rows], fwd["topk_idx"][b], fwd["logits"][b], "block %d" % (b + 1))
+            bad = np.any(np.sort(routing[b][rows], 1) != np.sort(fwd["topk_idx"][b], 1), axis=1)
+        same &= ~bad
+    return same
 
 
 def _run(cfg, wiring, seed=5, mutate=None):
@@ -34,7 +56,7 @@ def _run(cfg, wiring, seed=5, mutate=None):
     o, o_star = tr.forward(x)
     torch.cuda.synchronize()
     assert fs.fs_get_error() == (0, 0)
-    ref_o, ref_os, routing, _ = gpu_stack_stepwise(cfg, tr.blocks, x, wiring)
+    ref_o, ref_os, routing, inputs = gpu_stack_stepwise(cfg, tr.blocks, x, wiring, keep_inputs=True)
     assert torch.equal(o, ref_o) and torch.equal(o_star, ref_os), "training forward != inference forward"
     g = torch.Generator(device=DEV).manual_seed(seed)
     dO = torch.randn((cfg.T, cfg.d), generator=g, device=DEV)
@@ -45,10 +67,7 @@ def _run(cfg, wiring, seed=5, mutate=None):
     ref = oracle.stack_backward(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x),
                                 to64(dO), to64(dOs))
     fwd = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x))
-    same = np.ones(cfg.T, bool)
-    for b in range(cfg.L):
-        same &= np.all(np.sort(routing[b], 1) == np.sort(fwd["topk_idx"][b], 1), axis=1)
-    assert (~same).sum() <= max(1, int(1e-3 * cfg.T)), "routing differs on %d tokens" % int((~same).sum())
+    same = routing_agrees(cfg, prob["blocks"], routing, inputs, fwd, np.arange(cfg.T))
     bound = REL * cfg.L
     got = to64(dx)[same]
     want = ref["dx"][same]
@@ -64,6 +83,7 @@ def _run(cfg, wiring, seed=5, mutate=None):
             r = np.linalg.norm(gw - rw) / max(np.linalg.norm(rw), 1e-30)
             stats["%s[%d]" % (key, b)] = r
             assert r <= bound, "block %d %s: relative Frobenius %.3e > %.1e" % (b + 1, key, r, bound)
+    record("backward", workload=cfg.name, wiring=wiring, L=cfg.L, excluded=int((~same).sum()), **stats)
     print("backward parity", cfg.name, wiring, {k: "%.2e" % v for k, v in stats.items()})
     return stats
 
@@ -77,7 +97,7 @@ def test_block_backward_gates(fs, gate):
 
 @pytest.mark.parametrize("wiring", ["partial", "outdated", "disabled"])
 def test_stack_backward_wirings(fs, wiring):
-    L = 3 if wiring != "disabled" else 2
+    L = 3
     cfg = configs.LayerConfig("bws", T=333, d=256, E=8, k=2, c=192, n_shared=2, c_shared=128, L=L,
                               gate="softmax_renorm", dtype="bf16")
     _run(cfg, wiring)
@@ -155,7 +175,10 @@ def test_backward_corrupt_offsets_sets_error(fs):
 
 # ------------------------------------------------------ full-size workloads
 
-SAMPLE_BWD = 128
+# sampled tokens per workload: the oracle's backward costs about three forwards per
+# token, so the sample is sized to keep the GPU suite within its time budget
+# (Qwen3, the cheapest, at 1,024 tokens with every weight gradient compared)
+SAMPLE_BWD = {"v2lite": 512, "qwen3": 1024, "scout": 256, "v3": 512}
 
 
 @pytest.mark.slow
@@ -173,7 +196,7 @@ def test_full_size_backward_sampled(fs, name, grads):
     tr = fs.FarSkipTrainer(cfg, prob["blocks"])
     tr.forward(x)
     g = np.random.default_rng(1)
-    rows = np.sort(g.choice(cfg.T, size=SAMPLE_BWD, replace=False))
+    rows = np.sort(g.choice(cfg.T, size=SAMPLE_BWD[name], replace=False))
     rows_t = torch.as_tensor(rows, device=DEV)
     gen = torch.Generator(device=DEV).manual_seed(9)
     dO = torch.zeros((cfg.T, cfg.d), device=DEV)
@@ -187,17 +210,10 @@ def test_full_size_backward_sampled(fs, name, grads):
     others[rows_t] = False
     assert not dx[others].any(), "nonzero input gradient outside the sampled tokens"
     xs = x[rows_t]
-    _, _, routing, _ = gpu_stack_stepwise(cfg, tr.blocks, xs, cfg.wiring)   # rows are independent
+    _, _, routing, inputs = gpu_stack_stepwise(cfg, tr.blocks, x, cfg.wiring, keep_inputs=True)
     ocfg, ow = oracle_cfg(cfg), oracle_weights(prob["blocks"])
     fwd = oracle.stack(ocfg, ow, cfg.wiring, synth.to_numpy(xs))
-    same = np.ones(len(rows), bool)
-    for b in range(cfg.L):
-        same &= np.all(np.sort(routing[b], 1) == np.sort(fwd["topk_idx"][b], 1), axis=1)
-    # block 1 routes identical inputs; later blocks see inputs that differ by bf16
-    # rounding flips of the residual, so near-ties may route differently there
-    # (counted and bounded as in the forward's end-to-end check)
-    assert (~same).sum() <= max(1, int(DRIFT_FRAC * len(rows))), "routing differs on %d sampled tokens" % int(
-        (~same).sum())
+    same = routing_agrees(cfg, prob["blocks"], routing, inputs, fwd, rows)
     ref = oracle.stack_backward(ocfg, ow, cfg.wiring, synth.to_numpy(xs), to64(dO[rows_t]), to64(dOs[rows_t]),
                                 want_grads=grads and same.all())
     bound = REL * cfg.L
@@ -214,4 +230,5 @@ def test_full_size_backward_sampled(fs, name, grads):
                 r = np.linalg.norm(to64(gr[b][key]) - rw) / max(np.linalg.norm(rw), 1e-30)
                 stats["%s[%d]" % (key, b)] = r
                 assert r <= bound, "block %d %s: relative Frobenius %.3e > %.1e" % (b + 1, key, r, bound)
+    record("backward_full_size", workload=name, tokens=len(rows), excluded=int((~same).sum()), **stats)
     print("full-size backward parity", name, {k: "%.2e" % v for k, v in stats.items()})

@@ -273,6 +273,54 @@ def test_shared_expert(fs, dtype, ns, cs, T):
     compare(to64(s), out["S"][0], dtype, "shared")
 
 
+@pytest.mark.parametrize("dtype,T,k,d,ns,cs,resid,partial", [
+    ("bf16", 300, 2, 256, 1, 128, "act", True),
+    ("bf16", 1000, 8, 320, 2, 128, "f32", True),       # ragged M tile, half N tile (d = 320)
+    ("bf16", 77, 6, 512, 1, 192, "f32_in", False),
+    ("bf16", 1, 1, 64, 1, 64, "act", True),
+    ("fp8", 700, 8, 384, 1, 256, "act", True),
+    ("fp8", 333, 4, 256, 2, 128, "f32", False),
+])
+def test_shared_expert_combine_matches_unfused(fs, dtype, T, k, d, ns, cs, resid, partial):
+    """fs_shared_expert_combine (Combine in the shared down projection's epilogue)
+    gives the same bits as fs_shared_expert followed by fs_combine, for every
+    wiring's next input and residual precision."""
+    E = max(k, 8)
+    cfg = small(dtype, T=T, E=E, k=k, d=d, n_shared=ns, c_shared=cs)
+    x = synth.make_x(cfg, DEV)
+    w = synth.make_block_weights(cfg, 0, DEV)
+    packed = fs.pack_block(cfg, w)
+    desc = fs.make_desc(cfg)
+    ws = fs.alloc_workspace(desc, 0)
+    g = torch.Generator(device=DEV).manual_seed(12)
+    idx = _rand_topk(T, E, k, seed=6)
+    _, _, pos, _ = oracle.dispatch(T, k, E, idx.numpy())
+    pos = torch.from_numpy(pos).to(DEV)
+    y = torch.randn((T * k, d), generator=g, device=DEV).to(torch.bfloat16)
+    tw = torch.rand((T, k), generator=g, device=DEV)
+    pdt = torch.bfloat16 if resid == "act" else torch.float32
+    odt = torch.float32 if resid == "f32" else torch.bfloat16
+    op = torch.randn((T, d), generator=g, device=DEV).to(pdt)
+    s = torch.empty((T, d), dtype=torch.float32, device=DEV)
+    fs.fs_shared_expert(desc, x, packed["w13_shared"], packed["w3_shared"], s, ws)
+    for wi in ("partial", "outdated", "disabled"):
+        outs = []
+        for fused in (False, True):
+            o_star = torch.full((T, d), 7.0, dtype=odt, device=DEV) if partial else None
+            o = torch.full((T, d), 7.0, dtype=odt, device=DEV)
+            un = torch.full((T, d), 7.0, dtype=torch.bfloat16, device=DEV)
+            if fused:
+                fs.fs_shared_expert_combine(desc, x, packed["w13_shared"], packed["w3_shared"], y, pos, tw, op,
+                                            o_star, o, un, wi, ws)
+            else:
+                fs.fs_combine(desc, y, pos, tw, op, s, o_star, o, un, wi)
+            outs.append((o_star, o, un))
+        _no_dev_error()
+        for name, a, b in zip(("o*", "o", "u_next"), *outs):
+            if a is not None:
+                assert torch.equal(a, b), "%s: %s differs from the unfused path" % (wi, name)
+
+
 # ----------------------------------------------------------------- combine
 
 @pytest.mark.parametrize("dtype,T,k,d,shared,partial,resid", [

@@ -1,26 +1,32 @@
 """GPU parity of the FarSkip stack against the CPU oracle.
 
 Two kinds of check, for small multi-tile shapes (every token) and for the
-full-size workloads (in the launch configuration the benchmark times, on a
-seeded sample of tokens; token rows are independent through the whole stack):
+full-size workloads (in the launch configuration the benchmark times: the
+stack runs over all T tokens, and the oracle follows every token of V2-Lite,
+Qwen3 and the V3 decode batch, a seeded sample of 2,048 tokens of Scout and V3
+prefill; token rows are independent through the whole stack):
 
 blockwise   every block k is run on the GPU on the oracle's own inputs u_k
-            (bf16) and o_{k-1} (fp32), spliced into the sampled rows of a
+            (bf16) and o_{k-1} (fp32), spliced into the checked rows of a
             full-size GPU input, so both sides route identical inputs: the
             routing rule (top-k sets equal unless the k-th/(k+1)-th gap
             < 1e-4, such tokens < 0.1%) and the output tolerance (relative
-            Frobenius <= 5e-3, max-abs <= 2e-2 rms) hold per block: the
-            tolerance is stated for a layer's outputs.
+            Frobenius <= 5e-3, max-abs <= 2e-2 rms plus the one-flip allowance
+            of a stored bf16 value whose rounding flipped, tokens beyond it
+            < 0.1%) hold per block: the tolerance is stated for a layer's outputs.
 end-to-end  fs_farskip_stack as a whole vs the oracle stack.  After block 1
             the two sides' bf16 block inputs differ by rounding flips of the
-            residual, so later-block routing may differ near ties: such
-            tokens are counted (bounded) and left out.  An L-block stack
-            composes L layers' errors through the residual (and, with random
-            unnormalised weights, the block Jacobians grow with the residual),
-            so the end-to-end bound is L x 5e-3 relative Frobenius; the
-            max-abs bound is a per-layer property and is checked blockwise.
+            residual, so a later block may route a near-tie differently: every
+            such token must be explained by that input difference (its oracle
+            gap is below twice the logit change the GPU's input causes,
+            explained_drift); they are left out of the output comparison.  An
+            L-block stack composes L layers' errors through the residual, so the
+            end-to-end bound is L x 5e-3 relative Frobenius (the per-layer bound
+            added over the layers); the max-abs bound is a per-layer property and
+            is checked blockwise.
 The stack driver is also checked bit-for-bit against the same stack driven
-step by step through the single-step entry points.
+step by step through the single-step entry points (which also gives the
+GPU's routing and block inputs).  Observed statistics go to $FS_PARITY_LOG.
 """
 import os
 
@@ -30,12 +36,11 @@ import torch
 
 import oracle
 from mixture_experts_layer_expert_gb300 import configs, fs, synth
-from parity import (Fp8Flips, GpuBlockRunner, TOL, compare, compare_fp8, gpu_stack_stepwise, kth_gap, oracle_cfg,
-                    oracle_weights, to64, topk_mismatch)
+from parity import (GpuBlockRunner, HiddenFlips, TOL, compare, compare_flips, explained_drift, gpu_attn_layer,
+                    gpu_attn_stepwise, gpu_stack_stepwise, oracle_cfg, oracle_weights, record, to64, topk_mismatch)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-DRIFT_FRAC = 0.05      # end-to-end: tokens whose later-block routing may differ
 
 
 def _run_gpu(cfg, prob, wiring):
@@ -47,99 +52,140 @@ def _run_gpu(cfg, prob, wiring):
     return stack, o, o_star
 
 
-def blockwise(cfg, prob, stack, wiring, rows=None):
-    """Per-block parity on identical inputs (see module docstring)."""
+_REF_CACHE = {}
+
+
+def _fingerprint(prob):
+    """A checksum of a problem's input and weights (position-weighted sums)."""
+    ts = [prob["x"]]
+    for b in prob["blocks"]:
+        ts += [v for v in b.values() if v is not None]
+    out = []
+    for t in ts:
+        f = t.detach().reshape(-1)[:1 << 20].float()
+        out.append(float((f * torch.arange(1, f.numel() + 1, device=f.device, dtype=torch.float32)).sum()))
+    return tuple(out)
+
+
+def oracle_ref(cfg, prob, wiring, rows):
+    """The oracle stack on the rows of x (with its per-block inputs and outputs);
+    the last result is kept for a following test on the same problem."""
+    key = (cfg, wiring, rows.tobytes(), _fingerprint(prob))
+    if key not in _REF_CACHE:
+        _REF_CACHE.clear()
+        x = prob["x"][torch.as_tensor(rows, device=DEV)]
+        _REF_CACHE[key] = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x),
+                                       want_inputs=True)
+    return _REF_CACHE[key]
+
+
+def _ref_logits(ref, b):
+    """Oracle logits of block b including the router bias (the oracle adds it)."""
+    return ref["logits"][b]
+
+
+def blockwise(cfg, prob, blocks, wiring, rows, ref, gpu_inputs, tag=""):
+    """Per-block parity on identical inputs (see module docstring).  gpu_inputs:
+    the full-size GPU stack's (u_k, o_{k-1}) per block."""
     T = cfg.T
-    x = prob["x"]
-    rows = np.arange(T) if rows is None else rows
     rows_t = torch.as_tensor(rows, device=DEV)
-    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x[rows_t]),
-                       want_inputs=True)
-    _, _, _, gpu_inputs = gpu_stack_stepwise(cfg, stack.blocks, x, wiring, keep_inputs=True)
     run = GpuBlockRunner(cfg, T)
-    for b, pw in enumerate(stack.blocks):
+    out = []
+    for b, pw in enumerate(blocks):
         u, o_prev = gpu_inputs[b]
         u = u.clone()
         o_prev = o_prev.clone()
-        if b > 0:   # splice the oracle's inputs into the sampled rows
+        if b > 0:   # splice the oracle's inputs into the checked rows
             u[rows_t] = torch.from_numpy(ref["U"][b]).to(DEV, u.dtype)
             o_prev[rows_t] = torch.from_numpy(ref["P"][b]).to(DEV, o_prev.dtype)
         o_k, o_star, _, idx = run.run(pw, u, o_prev, b == cfg.L - 1, wiring)
         bias = pw["bias"]
         bnp = None if bias is None else bias.cpu().numpy()
-        z = ref["logits"][b] - (0 if bnp is None else bnp.astype(np.float64)[None, :])
+        z = _ref_logits(ref, b) - (0 if bnp is None else bnp.astype(np.float64)[None, :])
         bad = topk_mismatch(idx[rows], ref["topk_idx"][b], z, cfg.k, bnp)
         keep = ~bad
-        if cfg.dtype == "fp8":
-            flips = Fp8Flips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][b].items()},
-                             synth.to_numpy(torch.from_numpy(ref["U"][b]).to(torch.bfloat16)),
-                             ref["topk_idx"][b], ref["topk_w"][b])
+        st = {"block": b + 1, "tokens": int(len(rows)), "routing_near_ties": int(bad.sum())}
+        if cfg.dtype == "f32":
+            compare(to64(o_k[rows_t])[keep], ref["O"][b][keep], cfg.dtype, "block %d o_k" % (b + 1))
+            compare(to64(o_star[rows_t])[keep], ref["OS"][b][keep], cfg.dtype, "block %d o_k*" % (b + 1))
+        else:
+            u16 = synth.to_numpy(torch.from_numpy(ref["U"][b]).to(torch.bfloat16))
+            flips = HiddenFlips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][b].items()},
+                                u16, ref["topk_idx"][b], ref["topk_w"][b])
             kept = np.nonzero(keep)[0]
-            compare_fp8(to64(o_k[rows_t])[keep], ref["O"][b][keep], flips, kept, "block %d o_k" % (b + 1))
-            compare_fp8(to64(o_star[rows_t])[keep], ref["OS"][b][keep], flips, kept, "block %d o_k*" % (b + 1))
-            continue
-        compare(to64(o_k[rows_t])[keep], ref["O"][b][keep], cfg.dtype, "block %d o_k" % (b + 1))
-        compare(to64(o_star[rows_t])[keep], ref["OS"][b][keep], cfg.dtype, "block %d o_k*" % (b + 1))
-    return ref
+            st["o"] = compare_flips(to64(o_k[rows_t])[keep], ref["O"][b][keep], flips, kept,
+                                    "block %d o_k" % (b + 1), cfg.dtype)
+            st["o_star"] = compare_flips(to64(o_star[rows_t])[keep], ref["OS"][b][keep], flips, kept,
+                                         "block %d o_k*" % (b + 1), cfg.dtype)
+        record("blockwise", workload=cfg.name + tag, wiring=wiring, **st)
+        out.append(st)
+    return out
 
 
-def end_to_end(cfg, prob, stack, o, o_star, wiring, rows=None):
-    T = cfg.T
-    rows = np.arange(T) if rows is None else rows
+def end_to_end(cfg, prob, o, o_star, wiring, rows, ref, routing, gpu_inputs, tag=""):
+    """o, o_star: the stack's outputs over all T tokens; routing and gpu_inputs:
+    the GPU's per-block routing and inputs (the stack's, through the single-step
+    calls, checked bit-identical)."""
     rows_t = torch.as_tensor(rows, device=DEV)
-    x_s = prob["x"][rows_t]
-    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(x_s),
-                       want_inputs=True)
-    _, _, routing, _ = gpu_stack_stepwise(cfg, stack.blocks, x_s, wiring)
     bad_any = np.zeros(len(rows), bool)
     drift = []
     for b in range(cfg.L):
         bias = prob["blocks"][b]["bias"]
         bnp = None if bias is None else synth.to_numpy(bias)
-        z = ref["logits"][b] - (0 if bnp is None else bnp.astype(np.float64)[None, :])
+        z = _ref_logits(ref, b) - (0 if bnp is None else bnp.astype(np.float64)[None, :])
         if b == 0:       # identical inputs: the strict rule
-            bad = topk_mismatch(routing[0], ref["topk_idx"][0], z, cfg.k, bnp)
+            bad = topk_mismatch(routing[0][rows], ref["topk_idx"][0], z, cfg.k, bnp)
         else:
-            bad = np.any(np.sort(routing[b], 1) != np.sort(ref["topk_idx"][b], 1), axis=1)
-            zz = ref["logits"][b]
-            drift.append((b + 1, int(bad.sum()), float(kth_gap(zz[bad], cfg.k).max()) if bad.any() else 0.0))
+            u_g = synth.to_numpy(gpu_inputs[b][0][rows_t])
+            n_bad, gmax, dmax = explained_drift(cfg, synth.to_numpy(prob["blocks"][b]["w_r"]), bnp, u_g,
+                                                routing[b][rows], ref["topk_idx"][b], _ref_logits(ref, b),
+                                                "block %d" % (b + 1))
+            bad = np.any(np.sort(routing[b][rows], 1) != np.sort(ref["topk_idx"][b], 1), axis=1)
+            drift.append({"block": b + 1, "tokens": int(bad.sum()), "max_gap": gmax, "max_delta": dmax})
         bad_any |= bad
-    assert bad_any.sum() <= max(1, int(DRIFT_FRAC * len(rows))), "routing drift %s" % drift
     keep = ~bad_any
     got, got_s = to64(o[rows_t])[keep], to64(o_star[rows_t])[keep]
+    st = {"tokens": int(len(rows)), "excluded": int(bad_any.sum()), "drift": drift}
     if cfg.L == 1:
-        if cfg.dtype == "fp8":
-            flips = Fp8Flips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][0].items()},
-                             synth.to_numpy(x_s), ref["topk_idx"][0], ref["topk_w"][0])
+        if cfg.dtype == "f32":
+            compare(got, ref["o"][keep], cfg.dtype, "o_L")
+            compare(got_s, ref["o_star"][keep], cfg.dtype, "o_L*")
+        else:
+            flips = HiddenFlips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][0].items()},
+                                synth.to_numpy(prob["x"][rows_t]), ref["topk_idx"][0], ref["topk_w"][0])
             kept = np.nonzero(keep)[0]
-            compare_fp8(got, ref["o"][keep], flips, kept, "o_L")
-            compare_fp8(got_s, ref["o_star"][keep], flips, kept, "o_L*")
-            return drift
-        compare(got, ref["o"][keep], cfg.dtype, "o_L")
-        compare(got_s, ref["o_star"][keep], cfg.dtype, "o_L*")
-        return drift
-    tol = TOL[cfg.dtype]
-    for g, r, what in ((got, ref["o"][keep], "o_L"), (got_s, ref["o_star"][keep], "o_L*")):
-        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
-        assert rel <= tol["rel_fro"] * cfg.L, "%s: relative Frobenius %.3e > L x %.1e" % (what, rel, tol["rel_fro"])
-        drift.append((what, float(rel), float(np.abs(g - r).max() / np.sqrt(np.mean(r ** 2)))))
-    return drift
+            st["o"] = compare_flips(got, ref["o"][keep], flips, kept, "o_L", cfg.dtype)
+            st["o_star"] = compare_flips(got_s, ref["o_star"][keep], flips, kept, "o_L*", cfg.dtype)
+    else:
+        tol = TOL[cfg.dtype]
+        for g, r, what in ((got, ref["o"][keep], "o_L"), (got_s, ref["o_star"][keep], "o_L*")):
+            rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+            st[what] = {"rel": float(rel), "max_abs_rms": float(np.abs(g - r).max() / np.sqrt(np.mean(r ** 2)))}
+            assert rel <= tol["rel_fro"] * cfg.L, "%s: relative Frobenius %.3e > L x %.1e" % (
+                what, rel, tol["rel_fro"])
+    record("end_to_end", workload=cfg.name + tag, wiring=wiring, L=cfg.L, **st)
+    return st
 
 
-def _check_stack(cfg, prob, wiring):
+def _check_stack(cfg, prob, wiring, rows=None):
     stack, o, o_star = _run_gpu(cfg, prob, wiring)
-    so, so_star, _, _ = gpu_stack_stepwise(cfg, stack.blocks, prob["x"], wiring)
+    so, so_star, routing, inputs = gpu_stack_stepwise(cfg, stack.blocks, prob["x"], wiring, keep_inputs=True)
     assert torch.equal(so, o) and torch.equal(so_star, o_star), "stack driver != single-step calls"
-    blockwise(cfg, prob, stack, wiring)
-    end_to_end(cfg, prob, stack, o, o_star, wiring)
+    rows = np.arange(cfg.T) if rows is None else rows
+    ref = oracle_ref(cfg, prob, wiring, rows)
+    blockwise(cfg, prob, stack.blocks, wiring, rows, ref, inputs)
+    end_to_end(cfg, prob, o, o_star, wiring, rows, ref, routing, inputs)
+    return stack, o, o_star, ref
 
 
-@pytest.mark.parametrize("wiring,L", [("partial", 3), ("outdated", 3), ("disabled", 2)])
+@pytest.mark.parametrize("wiring,L", [("partial", 3), ("outdated", 3), ("disabled", 3)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_small_stack_wirings(fs, wiring, L, dtype):
     # The disabled wiring feeds the whole residual back in; with random weights and
-    # no normalisation the SwiGLU activations grow like |u|^2 and by a third block
-    # the bf16 storage of h alone reaches the max-abs bound, so that case stops at L = 2.
+    # no normalisation the SwiGLU hidden grows like |u|^2 from block to block, and
+    # its heavy tail makes a single flipped bf16 rounding of one hidden unit large
+    # against the output's rms by the third block: the one-flip allowance covers
+    # exactly that, and nothing else is allowed past the max-abs bound.
     cfg = configs.LayerConfig("s", T=333, d=256, E=8, k=2, c=192, n_shared=1, c_shared=128, L=L,
                               gate="softmax_renorm", dtype=dtype)
     _check_stack(cfg, synth.make_problem(cfg, DEV), wiring)
@@ -180,26 +226,55 @@ def test_stack_is_deterministic(fs):
 # ------------------------------------------------------ full-size workloads
 
 FULL = ["v2lite", "qwen3", "scout", "v3", "v3_decode"]
-SAMPLE = int(os.environ.get("FS_PARITY_SAMPLE", "128"))
+# tokens the oracle follows: None = every token, else a seeded sample
+ROWS = {"v2lite": None, "qwen3": None, "scout": 2048, "v3": 2048, "v3_decode": None}
+_CAP = int(os.environ.get("FS_PARITY_CAP", "0"))      # > 0: fewer rows, for quick local runs only
+
+
+def parity_rows(cfg, n):
+    n = cfg.T if n is None else min(n, cfg.T)
+    if _CAP:
+        n = min(n, _CAP)
+    if n >= cfg.T:
+        return np.arange(cfg.T)
+    return np.sort(np.random.default_rng(0).choice(cfg.T, size=n, replace=False))
+
+
+# the two-stream schedule is checked right after the one-stream run of the same
+# workload, so both use one oracle computation
+FULL_CASES = [("v2lite", "one_stream"), ("v2lite", "two_streams"), ("qwen3", "one_stream"), ("scout", "one_stream"),
+              ("scout", "two_streams"), ("v3", "one_stream"), ("v3_decode", "one_stream")]
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(fs, name):
-    """Full-size workload, one fs_farskip_stack call over all T tokens (the
-    benchmark's launch configuration); the oracle follows a seeded sample of
-    tokens through all L blocks, blockwise and end to end."""
+@pytest.mark.parametrize("name,schedule", FULL_CASES)
+def test_full_size_sampled(fs, name, schedule):
+    """Full-size workload, one stack call over all T tokens (the benchmark's
+    launch configuration); the oracle follows every token (V2-Lite, Qwen3, V3
+    decode) or 2,048 sampled tokens (Scout, V3) through all L blocks.
+    one_stream: fs_farskip_stack, blockwise and end to end.  two_streams: the
+    FarSkip overlap schedule (fs_farskip_stack_overlap) at the shapes its overlap
+    is measured on (V2-Lite L = 4, Scout L = 2), end to end against the oracle
+    stack, and bit for bit against the one-stream stack."""
     cfg = configs.CONFIGS[name]
     prob = synth.make_problem(cfg, DEV)
+    rows = parity_rows(cfg, ROWS[name])
+    if schedule == "one_stream":
+        _check_stack(cfg, prob, cfg.wiring, rows)
+        return
     stack, o, o_star = _run_gpu(cfg, prob, cfg.wiring)
-    g = np.random.default_rng(0)
-    rows = np.sort(g.choice(cfg.T, size=min(SAMPLE, cfg.T), replace=False))
-    blockwise(cfg, prob, stack, cfg.wiring, rows)
-    end_to_end(cfg, prob, stack, o, o_star, cfg.wiring, rows)
+    o, o_star = o.clone(), o_star.clone()
+    o2, o2_star = stack.forward_overlap(prob["x"])
+    torch.cuda.synchronize()
+    assert fs.fs_get_error() == (0, 0)
+    _, _, routing, inputs = gpu_stack_stepwise(cfg, stack.blocks, prob["x"], cfg.wiring, keep_inputs=True)
+    ref = oracle_ref(cfg, prob, cfg.wiring, rows)
+    end_to_end(cfg, prob, o2, o2_star, cfg.wiring, rows, ref, routing, inputs, tag=" overlap")
+    assert torch.equal(o2, o) and torch.equal(o2_star, o_star), "two-stream stack != one-stream stack"
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["v3", "qwen3"])
+@pytest.mark.parametrize("name", ["v3", "qwen3", "v2lite", "scout"])
 def test_full_size_routing_all_tokens(fs, name):
     """Block-1 routing of EVERY token at full size against the oracle's router:
     top-k sets equal except near-ties (< 1e-4), and those are < 0.1% of tokens."""
@@ -213,25 +288,37 @@ def test_full_size_routing_all_tokens(fs, name):
     fs.fs_router_topk(desc, x, w["w_r"], w["bias"], idx, tw, None, ws)
     torch.cuda.synchronize()
     bias = synth.to_numpy(w["bias"])
-    z, ridx, _ = oracle.router(oracle_cfg(cfg), synth.to_numpy(x), synth.to_numpy(w["w_r"]), bias)
+    z, ridx, rw = oracle.router(oracle_cfg(cfg), synth.to_numpy(x), synth.to_numpy(w["w_r"]), bias)
     zref = z - (0 if bias is None else bias.astype(np.float64)[None, :])
-    topk_mismatch(idx.cpu().numpy(), ridx, zref, cfg.k, bias)
+    bad = topk_mismatch(idx.cpu().numpy(), ridx, zref, cfg.k, bias)
+    keep = ~bad
+    gw = tw.cpu().numpy().astype(np.float64)[keep]
+    # gate weights of the agreeing tokens, slot for slot (slot order = descending z)
+    same_order = np.all(idx.cpu().numpy()[keep] == ridx[keep], axis=1)
+    werr = float(np.abs(gw[same_order] - rw[keep][same_order]).max()) if same_order.any() else 0.0
+    assert werr < 1e-5, werr
+    record("routing_all_tokens", workload=name, tokens=cfg.T, near_ties=int(bad.sum()),
+           slot_order_differs=int((~same_order).sum()), max_gate_weight_err=werr)
 
 
 @pytest.mark.parametrize("wiring,L,dtype", [("partial", 1, "bf16"), ("partial", 3, "bf16"), ("outdated", 3, "bf16"),
                                            ("partial", 2, "f32"), ("outdated", 4, "bf16")])
-def test_overlap_stack_matches_sequential(fs, wiring, L, dtype):
-    """The two-stream FarSkip schedule gives the same bits as the one-stream stack."""
+def test_overlap_stack_vs_oracle(fs, wiring, L, dtype):
+    """The two-stream FarSkip schedule against the oracle stack (end to end), and
+    bit for bit against the one-stream stack."""
     cfg = configs.LayerConfig("ov", T=700, d=256, E=16, k=4, c=192, n_shared=1, c_shared=128, L=L,
                               gate="sigmoid_norm", dtype=dtype)
     prob = synth.make_problem(cfg, DEV)
-    stack = fs.FarSkipStack(cfg, prob["blocks"], wiring=wiring)
-    o, o_star = stack.forward(prob["x"])
+    stack, o, o_star = _run_gpu(cfg, prob, wiring)
     o, o_star = o.clone(), o_star.clone()
+    _, _, routing, inputs = gpu_stack_stepwise(cfg, stack.blocks, prob["x"], wiring, keep_inputs=True)
+    rows = np.arange(cfg.T)
+    ref = oracle_ref(cfg, prob, wiring, rows)
     for _ in range(2):       # twice: the second call reuses the library's events and slots
         o2, o2_star = stack.forward_overlap(prob["x"])
         torch.cuda.synchronize()
         assert fs.fs_get_error() == (0, 0)
+        end_to_end(cfg, prob, o2, o2_star, wiring, rows, ref, routing, inputs, tag=" overlap")
         assert torch.equal(o2, o) and torch.equal(o2_star, o_star)
 
 
@@ -262,13 +349,19 @@ def test_attn_standin_gemm(fs):
 
 
 @pytest.mark.parametrize("wiring,L,dtype", [("attn_farskip", 1, "bf16"), ("attn_farskip", 3, "bf16"),
-                                           ("attn_plain", 2, "bf16"), ("attn_farskip", 2, "f32"),
-                                           ("attn_plain", 2, "f32")])
+                                           ("attn_plain", 2, "bf16"), ("attn_plain", 3, "bf16"),
+                                           ("attn_farskip", 2, "f32"), ("attn_plain", 2, "f32")])
 def test_attention_wirings_stack(fs, wiring, L, dtype):
     """fs_farskip_stack with a stand-in attention sub-block per layer vs the oracle.
-    Tokens near a routing tie (oracle k-th/(k+1)-th gap < 1e-3 in any layer) can
-    route differently once the bf16 layer inputs differ by rounding; they are
-    counted (at most 2%) and left out; the rest meet L x the per-layer tolerance."""
+    The stack is first checked bit for bit against the same layers driven through
+    the single-step entry points (which gives the GPU's routing and MoE inputs).
+    Per layer, on the oracle's own layer inputs: a MoE input that is identical on
+    both sides (farskip: u_k = bf16(o_{k-1})) is held to the strict routing rule;
+    one the layer forms itself (plain: bf16(o_{k-1} + A_k)) may differ by rounding
+    flips, and a token may then route differently only where explained_drift
+    explains it; outputs meet the per-layer tolerance (with the one-flip allowance
+    for bf16).  End to end: every routing difference explained, L x the per-layer
+    relative Frobenius bound."""
     cfg = configs.LayerConfig("aw", T=400, d=256, E=8, k=2, c=128, n_shared=1, c_shared=128, L=L,
                               gate="softmax_renorm", dtype=dtype)
     prob = synth.make_problem(cfg, DEV)
@@ -277,18 +370,55 @@ def test_attention_wirings_stack(fs, wiring, L, dtype):
     o, o_star = stack.forward(prob["x"])
     torch.cuda.synchronize()
     assert fs.fs_get_error() == (0, 0)
-    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(prob["x"]))
-    near = np.zeros(cfg.T, bool)
+    so, so_star, routing, inputs = gpu_attn_stepwise(cfg, stack.blocks, prob["x"], wiring)
+    assert torch.equal(so, o) and torch.equal(so_star, o_star), "stack driver != single-step calls"
+    ref = oracle.stack(oracle_cfg(cfg), oracle_weights(prob["blocks"]), wiring, synth.to_numpy(prob["x"]),
+                       want_inputs=True)
+    wnp = [{k_: synth.to_numpy(v) for k_, v in b.items()} for b in prob["blocks"]]
+    act = synth.storage_dtype(cfg)
+    rtol = TOL[dtype]["rel_fro"]
+
+    def routing_rule(b, idx, u_gpu, strict):
+        if strict:
+            return topk_mismatch(idx, ref["topk_idx"][b], ref["logits"][b], cfg.k)
+        n_bad, gmax, dmax = explained_drift(cfg, wnp[b]["w_r"], None, synth.to_numpy(u_gpu), idx,
+                                            ref["topk_idx"][b], ref["logits"][b], "layer %d" % (b + 1))
+        return np.any(np.sort(idx, 1) != np.sort(ref["topk_idx"][b], 1), axis=1)
+
+    # per layer on the oracle's layer inputs
+    run = GpuBlockRunner(cfg, cfg.T)
+    for b, pw in enumerate(stack.blocks):
+        a_in = torch.from_numpy(ref["A"][b]).to(DEV, act)
+        u_in = torch.from_numpy(ref["U"][b]).to(DEV, act)
+        o_prev = torch.from_numpy(ref["P"][b]).to(DEV, act if b == 0 else torch.float32)
+        o_k, o_s, idx, u_used, _, _ = gpu_attn_layer(run, pw, wiring, a_in, u_in, o_prev, b == L - 1)
+        bad = routing_rule(b, idx, u_used, wiring == "attn_farskip")
+        keep = ~bad
+        if dtype == "f32":
+            compare(to64(o_k)[keep], ref["O"][b][keep], dtype, "layer %d o_k" % (b + 1))
+            compare(to64(o_s)[keep], ref["OS"][b][keep], dtype, "layer %d o_k*" % (b + 1))
+            continue
+        flips = HiddenFlips(cfg, wnp[b], synth.to_numpy(torch.from_numpy(ref["U"][b]).to(torch.bfloat16)),
+                            ref["topk_idx"][b], ref["topk_w"][b])
+        kept = np.nonzero(keep)[0]
+        st = {"layer": b + 1, "drifted": int(bad.sum())}
+        st["o"] = compare_flips(to64(o_k)[keep], ref["O"][b][keep], flips, kept, "layer %d o_k" % (b + 1))
+        st["o_star"] = compare_flips(to64(o_s)[keep], ref["OS"][b][keep], flips, kept, "layer %d o_k*" % (b + 1))
+        record("attention_layer", wiring=wiring, L=L, **st)
+
+    # end to end
+    bad_any = np.zeros(cfg.T, bool)
     for b in range(L):
-        near |= kth_gap(ref["logits"][b], cfg.k) < 1e-3
-    assert near.mean() <= 0.02, near.mean()
-    keep = ~near
-    tol = 5e-3 if dtype == "bf16" else 1e-5
+        bad_any |= routing_rule(b, routing[b], inputs[b], b == 0 and wiring == "attn_farskip")
+    keep = ~bad_any
+    st = {"excluded": int(bad_any.sum())}
     for got, want, what in ((o, ref["o"], "o_L"), (o_star, ref["o_star"], "o_L*")):
         g = to64(got)[keep]
         r = want[keep]
         rel = np.linalg.norm(g - r) / np.linalg.norm(r)
-        assert rel <= tol * L, "%s: relative Frobenius %.3e" % (what, rel)
+        st[what] = float(rel)
+        assert rel <= rtol * L, "%s: relative Frobenius %.3e" % (what, rel)
+    record("attention_end_to_end", wiring=wiring, L=L, dtype=dtype, **st)
 
 
 @pytest.mark.parametrize("dtype,overlap", [("bf16", False), ("bf16", True), ("fp8", False)])
