@@ -141,8 +141,11 @@ def routed_alg_bytes(cfg, T):
     written and read once (bf16), Y_perm written; in the stored precisions (FP8:
     E4M3 weights with one fp32 scale per output channel, E4M3 X_perm)."""
     a = 4 if cfg.dtype == "f32" else 2
-    w = 1 if cfg.dtype == "fp8" else a
     rows = T * cfg.k
+    if cfg.dtype == "mxfp8":     # E4M3 codes plus one scale byte per 32 elements; the hidden is stored MX
+        q = 1.0 + 1.0 / 32
+        return float(cfg.E * 3 * cfg.d * cfg.c * q + rows * cfg.d * q + 2 * rows * cfg.c * q + rows * cfg.d * a)
+    w = 1 if cfg.dtype == "fp8" else a
     weights = cfg.E * 3 * cfg.d * cfg.c * w + (cfg.E * (2 * cfg.c + cfg.d) * 4 if cfg.dtype == "fp8" else 0)
     x_perm = rows * cfg.d * (1 if cfg.dtype == "fp8" else a)
     return float(weights + x_perm + 2 * rows * cfg.c * a + rows * cfg.d * a)
@@ -244,7 +247,7 @@ def run_ours(args, cfg, rank, world, local):
     # at prefill sizes, HBM-bound (expert weight streaming) at decode sizes
     routed_flops = 6.0 * T * cfg.k * cfg.d * cfg.c
     routed_ms = stage_ms["routed"] / L
-    fp8 = cfg.dtype == "fp8"
+    fp8 = cfg.dtype in ("fp8", "mxfp8")
     routed_bytes = routed_alg_bytes(cfg, T)
     peak = pk["bf16_tflops_sustained"] * (FP8_PER_BF16 if fp8 else 1.0)
     hbm_bound = routed_bytes / (pk["hbm_gbs"] * 1e9) > routed_flops / (peak * 1e12)
@@ -281,7 +284,7 @@ def run_ours(args, cfg, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {"bf16": "bf16", "f32": "f32", "fp8": "e4m3"}[cfg.dtype],
+        "dtype": {"bf16": "bf16", "f32": "f32", "fp8": "e4m3", "mxfp8": "e4m3+ue8m0/32"}[cfg.dtype],
         "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), uniform router",
         "config": {"workload": configs.describe(cfg),
                    "schedule": ("two-stream overlap" if args.overlap else "one stream") + (", CUDA graph" if args.graph
@@ -322,10 +325,15 @@ def per_stage_timing(cfg, stack, x, steps, stream):
     i32 = dict(dtype=torch.int32, device=dev)
     idx, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
     counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
-    pos, perm = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
-    x_perm = (fs.fp8_rows_empty(T * k, d, dev) if cfg.dtype == "fp8"
-              else torch.empty((T * k, d), dtype=x.dtype, device=dev))
-    y_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
+    prow = fs.fs_dispatch_rows(desc)      # T k, or the MX path's 128-row-padded capacity
+    pos, perm = torch.empty(T * k, **i32), torch.empty(prow, **i32)
+    if cfg.dtype == "fp8":
+        x_perm = fs.fp8_rows_empty(T * k, d, dev)
+    elif cfg.dtype == "mxfp8":
+        x_perm = fs.mx_rows_empty(prow, d, dev)
+    else:
+        x_perm = torch.empty((T * k, d), dtype=x.dtype, device=dev)
+    y_perm = torch.empty((prow, d), dtype=x.dtype, device=dev)
     s = torch.empty((T, d), dtype=torch.float32, device=dev) if cfg.n_shared else None
     L = len(stack.blocks)
     o_bufs = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(3)]
@@ -599,7 +607,7 @@ def oracle_cfg_for(cfg):
     dt = oracle.F32 if cfg.dtype == "f32" else oracle.BF16
     st = oracle.STORE_F32 if cfg.dtype == "f32" else oracle.STORE_BF16
     return oracle.make_cfg(cfg.d, cfg.E, cfg.k, cfg.c, cfg.n_shared, cfg.c_shared, cfg.gate, dt, st,
-                           fp8=cfg.dtype == "fp8")
+                           fp8={"fp8": "row", "mxfp8": "mx"}.get(cfg.dtype, False))
 
 
 def cpu_baseline(cfg, host_blocks, x, sample):
@@ -640,7 +648,7 @@ def run_reference(args, cfg, rank, world):
     sec = (time.perf_counter() - t0) / args.steps
     value = T / sec
     sample = "%d of the %d tokens per step, all L=%d blocks" % (T, cfg.T, cfg.L)
-    return {"impl": "reference", "metric": METRIC_FP8 if cfg.dtype == "fp8" else METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+    return {"impl": "reference", "metric": METRIC_FP8 if cfg.dtype in ("fp8", "mxfp8") else METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in)",

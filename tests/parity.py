@@ -311,22 +311,24 @@ def explained_drift(cfg, w_r, bias, u_gpu: np.ndarray, gpu_idx: np.ndarray, ref_
     return n_bad, float(gaps.max()), float(delta.max())
 
 
-def gpu_attn_layer(run, pw, wiring, a_in, u, o_prev, last):
+def gpu_attn_layer(run, pw, wiring, a_in, u, o_prev, last, u_plain=None):
     """One layer of the attention-wiring stack (FS_WIRE_ATTN_FARSKIP / _PLAIN)
     through the single-step entry points, as fs_farskip_stack runs it: the
     stand-in attention A_k on the attention input a_in, then the MoE block on
     the MoE input u (farskip) or on u = bf16(h_k), h_k = o_prev + A_k(a_in)
     (plain; that fp32 add and its bf16 rounding are formed here with torch --
     the same single IEEE roundings as the library's kernel, which the caller
-    checks against fs_farskip_stack bit for bit).  Returns (o_k, o_k*, topk_idx
-    numpy, the MoE input u, next attention input, next MoE input)."""
+    checks against fs_farskip_stack bit for bit); u_plain, when given, replaces
+    the plain layer's bf16(h_k) as the MoE input (a per-layer check on the
+    oracle's own MoE input).  Returns (o_k, o_k*, topk_idx numpy, the MoE input
+    u, next attention input, next MoE input)."""
     fs, cfg, T, d, dt = run.fs, run.cfg, run.T, run.cfg.d, run.dt
     att = torch.empty((T, d), dtype=torch.float32, device=run.dev)
     fs.fs_attn_standin(run.desc, a_in, pw["w_att"], att, run.ws)
     base, extra = o_prev, att
     if wiring == "attn_plain":
         base = o_prev.float() + att
-        u = base.to(dt)
+        u = base.to(dt) if u_plain is None else u_plain
         extra = None
     fs.fs_router_topk(run.desc, u, pw["w_r"], pw["bias"], run.idx, run.w, None, run.ws)
     idx = run.idx.cpu().numpy().copy()

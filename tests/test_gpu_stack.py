@@ -355,12 +355,11 @@ def test_attention_wirings_stack(fs, wiring, L, dtype):
     """fs_farskip_stack with a stand-in attention sub-block per layer vs the oracle.
     The stack is first checked bit for bit against the same layers driven through
     the single-step entry points (which gives the GPU's routing and MoE inputs).
-    Per layer, on the oracle's own layer inputs: a MoE input that is identical on
-    both sides (farskip: u_k = bf16(o_{k-1})) is held to the strict routing rule;
-    one the layer forms itself (plain: bf16(o_{k-1} + A_k)) may differ by rounding
-    flips, and a token may then route differently only where explained_drift
-    explains it; outputs meet the per-layer tolerance (with the one-flip allowance
-    for bf16).  End to end: every routing difference explained, L x the per-layer
+    Per layer, on the oracle's own layer inputs (attention input, residual and
+    MoE input -- for the plain layer the oracle's bf16(o_{k-1} + A_k) replaces the
+    one the layer would form), routing meets the strict rule and the outputs the
+    per-layer tolerance (with the one-flip allowance for bf16).  End to end: every
+    routing difference explained by the input difference, L x the per-layer
     relative Frobenius bound."""
     cfg = configs.LayerConfig("aw", T=400, d=256, E=8, k=2, c=128, n_shared=1, c_shared=128, L=L,
                               gate="softmax_renorm", dtype=dtype)
@@ -391,8 +390,9 @@ def test_attention_wirings_stack(fs, wiring, L, dtype):
         a_in = torch.from_numpy(ref["A"][b]).to(DEV, act)
         u_in = torch.from_numpy(ref["U"][b]).to(DEV, act)
         o_prev = torch.from_numpy(ref["P"][b]).to(DEV, act if b == 0 else torch.float32)
-        o_k, o_s, idx, u_used, _, _ = gpu_attn_layer(run, pw, wiring, a_in, u_in, o_prev, b == L - 1)
-        bad = routing_rule(b, idx, u_used, wiring == "attn_farskip")
+        o_k, o_s, idx, u_used, _, _ = gpu_attn_layer(run, pw, wiring, a_in, u_in, o_prev, b == L - 1,
+                                                     u_plain=u_in if wiring == "attn_plain" else None)
+        bad = routing_rule(b, idx, u_used, True)
         keep = ~bad
         if dtype == "f32":
             compare(to64(o_k)[keep], ref["O"][b][keep], dtype, "layer %d o_k" % (b + 1))
