@@ -388,9 +388,12 @@ static void mlp_row_fp8(int d, int c, int cw, int bd, int bc, const double* aq,
     const size_t nbd = (size_t)(d / bd), nbc = (size_t)(c / bc);
     for (int j = 0; j < c; ++j) {
         double gate = 0.0, up = 0.0;
-        for (int i = 0; i < d; ++i) {
-            gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[(size_t)j * nbd + i / bd]);
-            up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd + i / bd]);
+        for (size_t b = 0; b < nbd; ++b) {          /* i in index order, block by block */
+            const int eg = e2[(size_t)j * nbd + b], eu = e1[(size_t)j * nbd + b];
+            for (int i = (int)b * bd; i < ((int)b + 1) * bd; ++i) {
+                gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, eg);
+                up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, eu);
+            }
         }
         h[j] = oracle_round(silu(gate) * up, storage);
         hq[j] = h[j];
@@ -398,9 +401,12 @@ static void mlp_row_fp8(int d, int c, int cw, int bd, int bc, const double* aq,
     quant_blocks(hq, c, bc, NULL, NULL);
     for (int i = 0; i < d; ++i) {
         double acc = 0.0;
-        for (int jj = 0; jj < c; ++jj) {
-            size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);
-            acc += hq[jj] * wq(w3, off, wdt, e3[(size_t)i * nbc + jj / bc]);
+        for (size_t b = 0; b < nbc; ++b) {          /* jj in index order, block by block */
+            const int ed = e3[(size_t)i * nbc + b];
+            for (int jj = (int)b * bc; jj < ((int)b + 1) * bc; ++jj) {
+                size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);
+                acc += hq[jj] * wq(w3, off, wdt, ed);
+            }
         }
         y[i] = acc;
     }

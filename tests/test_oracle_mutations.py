@@ -56,11 +56,10 @@ MUTANTS = {
     "fp8_scale_search_starts_high": ("int s = e - 10;", "int s = e - 8;"),
     "fp8_scale_boundary_exclusive": ("while (amax > ldexp(448.0, s)) ++s;", "while (amax >= ldexp(448.0, s)) ++s;"),
     "fp8_hidden_not_quantised": ("    quant_blocks(hq, c, bc, NULL, NULL);\n", ""),
-    "fp8_gate_uses_up_row_exponent": (
-        "gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e2[(size_t)j * nbd + i / bd]);",
-        "gate += aq[i] * wq(w2, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd + i / bd]);"),
-    "fp8_down_exponent_by_column": ("acc += hq[jj] * wq(w3, off, wdt, e3[(size_t)i * nbc + jj / bc]);",
-                                    "acc += hq[jj] * wq(w3, off, wdt, e3[(size_t)(jj % d) * nbc + jj / bc]);"),
+    "fp8_gate_uses_up_row_exponent": ("const int eg = e2[(size_t)j * nbd + b], eu = e1[(size_t)j * nbd + b];",
+                                      "const int eg = e1[(size_t)j * nbd + b], eu = e1[(size_t)j * nbd + b];"),
+    "fp8_down_exponent_by_column": ("const int ed = e3[(size_t)i * nbc + b];",
+                                    "const int ed = e3[(size_t)((int)b * bc % d) * nbc + b];"),
     "fp8_token_row_not_quantised_in_block": ("            quant_blocks(aq, d, fp8_blk(cfg, d), NULL, NULL);\n", ""),
     "fp8_shared_down_read_as_one_matrix": ("size_t off = base3 + (size_t)(jj / cw) * d * cw + (size_t)i * cw + (size_t)(jj % cw);",
                                            "size_t off = base3 + (size_t)i * c + (size_t)jj;"),
@@ -68,9 +67,8 @@ MUTANTS = {
                                               "                    const int sh = 0, j = jj % cs;"),
     # block-scaled (MX) FP8
     "mx_blocks_of_16": ("#define ORACLE_MX_BLOCK 32", "#define ORACLE_MX_BLOCK 16"),
-    "mx_weight_row_uses_first_block_exponent": (
-        "up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd + i / bd]);",
-        "up += aq[i] * wq(w1, base12 + (size_t)j * d + i, wdt, e1[(size_t)j * nbd]);"),
+    "mx_weight_row_uses_first_block_exponent": ("const int eg = e2[(size_t)j * nbd + b], eu = e1[(size_t)j * nbd + b];",
+                                                "const int eg = e2[(size_t)j * nbd + b], eu = e1[(size_t)j * nbd];"),
     "mx_hidden_row_scaled": ("    quant_blocks(hq, c, bc, NULL, NULL);\n", "    quant_blocks(hq, c, c, NULL, NULL);\n"),
     "mx_token_row_scaled_in_block": ("            quant_blocks(aq, d, fp8_blk(cfg, d), NULL, NULL);\n",
                                      "            quant_blocks(aq, d, d, NULL, NULL);\n"),
