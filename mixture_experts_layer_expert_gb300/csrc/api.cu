@@ -116,7 +116,7 @@ static inline long long perm_rows(const fs_layer_desc* d) {
 // ------------------------------------------------------------- workspace
 struct Layout {
     // single-step regions (L = 0)
-    size_t logits, disp, plan_z, plan_r, h_r, hq_r, plan_s, h_s, hq_s, uq, plan_a, end0;
+    size_t logits, disp, plan_z, plan_r, plan_r2, h_r, hq_r, plan_s, plan_s2, h_s, hq_s, uq, plan_a, end0;
     // stack regions (L >= 1)
     size_t topk_idx, topk_w, counts, offsets, pos, perm, x_perm, y_perm, s_out, ring[3], star[2], ubuf[2], end;
     size_t att, hbuf, abuf[2], end_attn;   // attention wirings only: A_k output, h_k, attention inputs
@@ -137,12 +137,14 @@ static Layout layout(const fs_layer_desc* d, int L) {
     l.disp = take(dispatch_ws_bytes(d->T, d->E));
     l.plan_z = take(4 * sizeof(int));
     l.plan_r = take(2 * (E + 1) * sizeof(int));
+    l.plan_r2 = take(2 * (E + 1) * sizeof(int));    // the down projection's plan when it runs on CTA pairs
     const bool f8 = is_fp8(d), mxq = is_mx(d);
     const long long prow = perm_rows(d);
     // MX: the hidden goes straight from the gate/up epilogue into an MX matrix
     l.h_r = take(mxq ? mx_rows_bytes(prow, d->c) : rows * d->c * es);
     l.hq_r = take(f8 ? fp8_rows_bytes(static_cast<long long>(rows), d->c) : 0);   // FP8: quantised h
     l.plan_s = take(4 * sizeof(int));
+    l.plan_s2 = take(4 * sizeof(int));
     l.h_s = take(mxq ? (cw ? mx_rows_bytes(static_cast<long long>(T), static_cast<int>(cw)) : 0) : T * cw * es);
     l.hq_s = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), static_cast<int>(cw)) : 0);
     l.uq = take(f8 && cw ? fp8_rows_bytes(static_cast<long long>(T), d->d)
@@ -282,10 +284,15 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 // (bf16) is quantised per row into hq before the down GEMM.
 // With cmb set (one group over the T token rows, tensor-core dtypes) the down
 // projection's epilogue is Combine fused with the FarSkip update (y unused).
+// plan2 (nullable): room for a second plan, used when the down projection runs
+// on the CTA-pair kernel (tc_down_pair) while the gate/up GEMM does not.
 static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_rows, const int32_t* gather, int rows,
                              const int32_t* offsets, int G, int cw, const void* w13, const void* w3, void* y,
                              bool y_f32, int* plan, void* h, void* hq, cudaStream_t st, void* gu_save = nullptr,
-                             const CombineEpi* cmb = nullptr) {
+                             const CombineEpi* cmb = nullptr, int* plan2 = nullptr) {
+    // down projection on CTA pairs: its own plan of 256-row tiles
+    const bool dp = plan2 && tc_down_pair() && tc_block_m() == 128;
+    const int max_mt2 = ceil_div(rows, 256) + G;
     if (is_mx(d)) {
         // x: an MX matrix of x_rows rows (a multiple of 128 or the token count);
         // groups start at multiples of 128; the hidden is written as an MX matrix
@@ -308,9 +315,10 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         FS_TRY(launch_tc_gemm_f8(EPI_SWIGLU, x, x_rows, xs, w13, packed_scales_fp8(w13, G, 2 * cw, d->d), G, 2 * cw,
                                  d->d, plan, max_mt, h, cw, cw, st));
         FS_TRY(launch_quant_rows(h, rows, cw, hq, st));
+        if (dp) FS_TRY(launch_plan(offsets, G, rows, 256, plan2, st));
         FS_TRY(launch_tc_gemm_f8(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), hq, rows, hs, w3,
-                                 packed_scales_fp8(w3, G, d->d, cw), G, d->d, cw, plan, max_mt, y, d->d, d->d, st,
-                                 cmb));
+                                 packed_scales_fp8(w3, G, d->d, cw), G, d->d, cw, dp ? plan2 : plan,
+                                 dp ? max_mt2 : max_mt, y, d->d, d->d, st, cmb, dp ? 1 : -1));
     } else if (d->dtype == FS_BF16) {
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -322,8 +330,12 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
                               true, st, &ex));
         TcExtra ex2;
         ex2.combine = cmb;
-        FS_TRY(launch_tc_gemm(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), h, rows, w3, G, d->d, cw, plan,
-                              max_mt, y, d->d, d->d, nullptr, 0, true, st, &ex2));
+        if (dp) {
+            FS_TRY(launch_plan(offsets, G, rows, 256, plan2, st));
+            ex2.variant = 1;
+        }
+        FS_TRY(launch_tc_gemm(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), h, rows, w3, G, d->d, cw,
+                              dp ? plan2 : plan, dp ? max_mt2 : max_mt, y, d->d, d->d, nullptr, 0, true, st, &ex2));
     } else {
         const int bm = simt_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
@@ -341,7 +353,8 @@ static fs_status routed_impl(const fs_layer_desc* d, const void* x_perm, const i
     const Layout l = layout(d, 0);
     const int rows = static_cast<int>(perm_rows(d));
     return swiglu_impl(d, x_perm, rows, nullptr, rows, offsets, d->E, d->c, w13, w3, y_perm, false,
-                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), at<void>(ws, l.hq_r), st);
+                       at<int>(ws, l.plan_r), at<void>(ws, l.h_r), at<void>(ws, l.hq_r), st, nullptr, nullptr,
+                       at<int>(ws, l.plan_r2));
 }
 
 static fs_status routed_gather_impl(const fs_layer_desc* d, const void* u, const int32_t* perm_src,
@@ -366,7 +379,8 @@ static fs_status shared_impl(const fs_layer_desc* d, const void* u, const void* 
         if (!u_q_ready) FS_TRY(launch_quant_rows_mx(u, d->T, d->d, at<void>(ws, l.uq), st));
     }
     return swiglu_impl(d, x, d->T, nullptr, d->T, nullptr, 1, d->n_shared * d->c_shared, w13s, w3s, s_out, true,
-                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), at<void>(ws, l.hq_s), st, nullptr, cmb);
+                       at<int>(ws, l.plan_s), at<void>(ws, l.h_s), at<void>(ws, l.hq_s), st, nullptr, cmb,
+                       at<int>(ws, l.plan_s2));
 }
 
 // The shared experts with Combine and the FarSkip update in the epilogue of

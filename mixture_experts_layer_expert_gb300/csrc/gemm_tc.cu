@@ -1367,22 +1367,25 @@ cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan
 }
 
 // Kernel variant: the single-CTA kernel, or the CTA-pair kernel when the
-// environment sets FS_TC_VARIANT=pair.
-static bool use_pair() {
+// environment sets FS_TC_VARIANT=pair; FS_TC_VARIANT=pair_down keeps the
+// single-CTA kernel except for the forward down projections.
+static int variant_mode() {
     static int mode = -1;
     if (mode < 0) {
         const char* e = getenv("FS_TC_VARIANT");
-        mode = (e && std::strcmp(e, "pair") == 0) ? 1 : 0;
+        mode = (e && std::strcmp(e, "pair") == 0) ? 1 : ((e && std::strcmp(e, "pair_down") == 0) ? 2 : 0);
     }
-    return mode == 1;
+    return mode;
 }
+static bool use_pair() { return variant_mode() == 1; }
+bool tc_down_pair() { return variant_mode() == 2; }
 
 template <int EPI>
 static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,
                                   const int* plan, int max_mtiles, void* out, long long ldo, int out_cols,
                                   const int* gather_rows, int gather_limit, bool b_blocked, cudaStream_t st,
                                   const TcExtra* ex) {
-    const bool pair = use_pair();
+    const bool pair = (ex && ex->variant >= 0) ? ex->variant == 1 : use_pair();
     if (pair && gather_rows) return cudaErrorNotSupported;
     static bool attr_set[2] = {false, false};
     cudaError_t e;
@@ -1461,8 +1464,8 @@ template <int EPI>
 static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const float* a_scale, const void* B,
                                      const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles,
                                      void* out, long long ldo, int out_cols, cudaStream_t st,
-                                     const CombineEpi* cmb = nullptr) {
-    const bool pair = use_pair();
+                                     const CombineEpi* cmb = nullptr, int variant = -1) {
+    const bool pair = variant >= 0 ? variant == 1 : use_pair();
     static bool attr_set[2] = {false, false};
     cudaError_t e;
     if (!attr_set[pair]) {
@@ -1529,20 +1532,20 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
 
 cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const float* a_scale, const void* B,
                               const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles, void* out,
-                              long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine) {
+                              long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine, int variant) {
     switch (epi) {
         case EPI_COMBINE:
             return launch_tc_f8_impl<EPI_COMBINE>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
-                                                  out_cols, st, combine);
+                                                  out_cols, st, combine, variant);
         case EPI_SWIGLU:
             return launch_tc_f8_impl<EPI_SWIGLU>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
-                                                 out_cols, st);
+                                                 out_cols, st, nullptr, variant);
         case EPI_BF16:
             return launch_tc_f8_impl<EPI_BF16>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
-                                               out_cols, st);
+                                               out_cols, st, nullptr, variant);
         case EPI_F32:
             return launch_tc_f8_impl<EPI_F32>(A, a_rows, a_scale, B, b_scale, G, N, K, plan, max_mtiles, out, ldo,
-                                              out_cols, st);
+                                              out_cols, st, nullptr, variant);
         default:
             return cudaErrorInvalidValue;
     }

@@ -56,6 +56,9 @@ struct TcExtra {
     int ksplit = 1;
     // EPI_COMBINE: the Combine operands and outputs (out is unused)
     const CombineEpi* combine = nullptr;
+    // -1: the library-wide kernel variant; 0: single-CTA kernel; 1: CTA-pair kernel
+    // (its plan must then be built with 256-row tiles)
+    int variant = -1;
 };
 
 void count_launch();
@@ -89,7 +92,11 @@ cudaError_t launch_wgrad_gemm(const void* A, int lda, const void* B, int ldb, lo
 // accumulator by a_scale[row] b_scale[g N + col].  Single-CTA kernel only.
 cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const float* a_scale, const void* B,
                               const float* b_scale, int G, int N, int K, const int* plan, int max_mtiles, void* out,
-                              long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine = nullptr);
+                              long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine = nullptr,
+                              int variant = -1);
+// The forward down projections (y = h W3^T) on the CTA-pair kernel while the
+// other GEMMs keep the library-wide variant (FS_TC_VARIANT=pair_down).
+bool tc_down_pair();
 
 // Tensor maps (gemm_tc.cu): a [rows, cols] row-major matrix of bf16 (f8: 8-bit
 // codes) with a box_rows x 128-byte box and the 128-byte swizzle; the tiled
