@@ -110,8 +110,8 @@ typedef enum {
  * Every call validates it first: T, d, E, k, c >= 1, k <= E, n_shared >= 0 and
  * c_shared >= 1 when n_shared > 0, else FS_ERR_INVALID_ARG (an empty batch,
  * T = 0, is such an error: the caller skips the call); d, c, c_shared multiples
- * of 64 (128 for FS_FP8), E <= 512, k <= 16 and T k < 2^31 - 1024, else
- * FS_ERR_UNSUPPORTED. */
+ * of 64 (128 for FS_FP8 and FS_MXFP8), E <= 512, k <= 16 and T k < 2^31 - 1024
+ * (FS_MXFP8: T k + 127 E + 128 < 2^31 - 1024), else FS_ERR_UNSUPPORTED. */
 typedef struct {
     int32_t T, d, E, k, c, n_shared, c_shared;
     int32_t dtype;   /* fs_dtype */

@@ -95,6 +95,8 @@ static fs_status check_desc(const fs_layer_desc* d) {
     if (d->E > kMaxExperts || d->k > kMaxTopK) return FS_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(d->T) * d->k;
     if (rows > 0x7fffffffLL - 1024) return FS_ERR_UNSUPPORTED;
+    // MX: the 128-row-padded expert segments must fit the same bound
+    if (d->dtype == FS_MXFP8 && rows + 127LL * d->E + 128 > 0x7fffffffLL - 1024) return FS_ERR_UNSUPPORTED;
     return FS_OK;
 }
 

@@ -54,6 +54,20 @@ def desc(**kw):
     return d
 
 
+def test_mx_sizes(L):
+    d = desc(dtype=3)                                     # FS_MXFP8, V3 shapes
+    assert fs.fs_dispatch_rows(d) == (65536 * 8 + 127 * 256 + 127) // 128 * 128
+    assert fs.fs_dispatch_rows(desc()) == 65536 * 8
+    assert fs.fs_mx_rows_bytes(300, 256) == 384 * 256 + 3 * 2 * 512          # rows rounded up to 128
+    assert fs.fs_mx_rows_bytes(300, 200) == 0                                # cols % 128
+    assert fs.fs_packed_bytes(2, 384, 256, 3) == 2 * 512 * 256 + 2 * 2 * 2 * 1024
+    assert fs.fs_packed_bytes(2, 320, 256, 3) == 0                           # N % 128
+    big = desc(dtype=3, T=(2 ** 31 - 1024 - 127 * 256 - 64) // 8, k=8)
+    assert fs.fs_workspace_bytes(big, 0) == 0                                # padded rows beyond int32
+    assert L.fs_quantize_rows_mx(10, 200, _vp(FAKE), _vp(FAKE), None) == 2
+    assert L.fs_quantize_rows_mx(0, 256, _vp(FAKE), _vp(FAKE), None) == 1
+
+
 def test_workspace_bytes(L):
     assert fs.fs_workspace_bytes(desc(), 0) > 0
     assert fs.fs_workspace_bytes(desc(), 1) > fs.fs_workspace_bytes(desc(), 0)
