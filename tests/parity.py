@@ -150,23 +150,28 @@ Fp8Flips = HiddenFlips
 
 
 def compare_flips(got: np.ndarray, ref: np.ndarray, flips: HiddenFlips, tokens: np.ndarray, what: str = "",
-                  dtype: str = "bf16"):
+                  dtype: str = "bf16", out_bf16: bool = False):
     """Outputs [n, d] against the oracle with the one-flip allowance (see the
     rounding-flips note above); tokens[r] = the token of row r in the flips'
-    inputs.  Returns a dict of what was seen."""
+    inputs.  out_bf16: the GPU's output is itself stored in bf16 (a stack's last
+    block) while the oracle returns it at residual precision, so each element
+    also carries its own rounding, half a bf16 step: 2^-9 |ref| (for a
+    heavy-tailed residual an element 10x the rms rounds by 0.02 rms on its own).
+    Returns a dict of what was seen."""
     tol = TOL[dtype]
     err = got - ref
     nref = np.linalg.norm(ref)
     rel = np.linalg.norm(err) / max(nref, 1e-300)
     rms = nref / np.sqrt(max(ref.size, 1))
     assert rel <= tol["rel_fro"], "%s: relative Frobenius %.3e > %.1e" % (what, rel, tol["rel_fro"])
-    base = tol["max_abs_rms"] * rms
+    base = tol["max_abs_rms"] * rms + (2.0 ** -9 * np.abs(ref) if out_bf16 else 0.0)
     over = np.argwhere(np.abs(err) > base)
     unexplained = set()
     for r, i in over:
         if r in unexplained:
             continue
-        if abs(err[r, i]) > base + flips.allowance(int(tokens[r]), int(i)):
+        b = base[r, i] if out_bf16 else base
+        if abs(err[r, i]) > b + flips.allowance(int(tokens[r]), int(i)):
             unexplained.add(int(r))
     n = got.shape[0]
     assert len(unexplained) <= allowed_tokens(n), (

@@ -113,10 +113,11 @@ def blockwise(cfg, prob, blocks, wiring, rows, ref, gpu_inputs, tag=""):
             flips = HiddenFlips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][b].items()},
                                 u16, ref["topk_idx"][b], ref["topk_w"][b])
             kept = np.nonzero(keep)[0]
+            last = b == cfg.L - 1          # the last block's outputs are stored in bf16
             st["o"] = compare_flips(to64(o_k[rows_t])[keep], ref["O"][b][keep], flips, kept,
-                                    "block %d o_k" % (b + 1), cfg.dtype)
+                                    "block %d o_k" % (b + 1), cfg.dtype, out_bf16=last)
             st["o_star"] = compare_flips(to64(o_star[rows_t])[keep], ref["OS"][b][keep], flips, kept,
-                                         "block %d o_k*" % (b + 1), cfg.dtype)
+                                         "block %d o_k*" % (b + 1), cfg.dtype, out_bf16=last)
         record("blockwise", workload=cfg.name + tag, wiring=wiring, **st)
         out.append(st)
     return out
@@ -154,8 +155,8 @@ def end_to_end(cfg, prob, o, o_star, wiring, rows, ref, routing, gpu_inputs, tag
             flips = HiddenFlips(cfg, {k_: synth.to_numpy(v) for k_, v in prob["blocks"][0].items()},
                                 synth.to_numpy(prob["x"][rows_t]), ref["topk_idx"][0], ref["topk_w"][0])
             kept = np.nonzero(keep)[0]
-            st["o"] = compare_flips(got, ref["o"][keep], flips, kept, "o_L", cfg.dtype)
-            st["o_star"] = compare_flips(got_s, ref["o_star"][keep], flips, kept, "o_L*", cfg.dtype)
+            st["o"] = compare_flips(got, ref["o"][keep], flips, kept, "o_L", cfg.dtype, out_bf16=True)
+            st["o_star"] = compare_flips(got_s, ref["o_star"][keep], flips, kept, "o_L*", cfg.dtype, out_bf16=True)
     else:
         tol = TOL[cfg.dtype]
         for g, r, what in ((got, ref["o"][keep], "o_L"), (got_s, ref["o_star"][keep], "o_L*")):
@@ -402,8 +403,11 @@ def test_attention_wirings_stack(fs, wiring, L, dtype):
                             ref["topk_idx"][b], ref["topk_w"][b])
         kept = np.nonzero(keep)[0]
         st = {"layer": b + 1, "drifted": int(bad.sum())}
-        st["o"] = compare_flips(to64(o_k)[keep], ref["O"][b][keep], flips, kept, "layer %d o_k" % (b + 1))
-        st["o_star"] = compare_flips(to64(o_s)[keep], ref["OS"][b][keep], flips, kept, "layer %d o_k*" % (b + 1))
+        last = b == L - 1
+        st["o"] = compare_flips(to64(o_k)[keep], ref["O"][b][keep], flips, kept, "layer %d o_k" % (b + 1),
+                                out_bf16=last)
+        st["o_star"] = compare_flips(to64(o_s)[keep], ref["OS"][b][keep], flips, kept, "layer %d o_k*" % (b + 1),
+                                     out_bf16=last)
         record("attention_layer", wiring=wiring, L=L, **st)
 
     # end to end
