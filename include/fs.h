@@ -24,11 +24,11 @@
  *     the kernel records a code in the library's device error word and skips
  *     the work; fs_get_error() reads and clears it.
  *   - Row-major layouts throughout.  Activations are [rows, d] in the
- *     activation type: bf16 for FS_BF16 and FS_FP8, fp32 for FS_F32 (FS_FP8's
- *     E4M3 operands live inside the expert steps, see FS_FP8); gate weights and
+ *     activation type: bf16 for FS_BF16, FS_FP8 and FS_MXFP8, fp32 for FS_F32 (the
+ *     FP8 paths' E4M3 operands live inside the expert steps, see FS_FP8); gate weights and
  *     logits are fp32; indices int32.
  *   - Pointers must be 16-byte aligned; d and c must be multiples of 64;
- *     n_shared * c_shared must be a multiple of 64 (FS_FP8: d, c and c_shared
+ *     n_shared * c_shared must be a multiple of 64 (FS_FP8, FS_MXFP8: d, c and c_shared
  *     multiples of 128).  Otherwise FS_ERR_UNSUPPORTED.
  *   - Workspace: `ws` is caller-owned device scratch of at least
  *     fs_workspace_bytes(desc, L) bytes (L = 0 for the single-step calls),
@@ -120,7 +120,8 @@ typedef struct {
 
 /* One block's weights in the library's packed layouts (fs_pack_w13, fs_pack_w3,
  * fs_pack_w3_shared).  Element type: the router weight in the activation type,
- * the expert weights in desc->dtype's packed layout (FP8 packs for FS_FP8). */
+ * the expert weights in desc->dtype's packed layout (FP8 / MX packs for FS_FP8 /
+ * FS_MXFP8). */
 typedef struct {
     const void* w_r;        /* [E, d] router (W_R), row-major */
     const float* bias;      /* [E] router bias added to the logits, or NULL */
@@ -299,7 +300,7 @@ fs_status fs_grouped_swiglu(const fs_layer_desc* desc, const void* x_perm, const
  * never written or read.  u [T, d], perm_src [T k] (fs_dispatch's output),
  * offsets [E+1] -> y_perm [T k, d].  Results are bit-identical to
  * fs_dispatch + fs_grouped_swiglu.  FS_ERR_UNSUPPORTED with the CTA-pair GEMM
- * variant and for FS_FP8. */
+ * variant and for FS_FP8 and FS_MXFP8. */
 fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, const int32_t* perm_src,
                                    const int32_t* offsets, const void* w13, const void* w3,
                                    void* y_perm, void* ws, size_t ws_bytes, void* stream);
@@ -307,7 +308,8 @@ fs_status fs_grouped_swiglu_gather(const fs_layer_desc* desc, const void* u, con
 /* Shared expert(s) (§2.1): S = sum_i MLP_shared_i(u) over all T tokens, as one
  * MLP of width n_shared c_shared.  u [T, d] -> s_out [T, d] in fp32 (S is only
  * ever added into the residual stream, so it keeps fp32 accumulator precision).
- * FS_FP8: u is bf16 and is quantised per token in ws; the weights are FP8 packs. */
+ * FS_FP8: u is bf16 and is quantised per token in ws; the weights are FP8 packs.
+ * FS_MXFP8: u is quantised in blocks of 32 in ws; the weights are MX packs. */
 fs_status fs_shared_expert(const fs_layer_desc* desc, const void* u, const void* w13_shared,
                            const void* w3_shared, void* s_out, void* ws, size_t ws_bytes,
                            void* stream);
