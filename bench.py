@@ -226,7 +226,7 @@ def run_ours(args, cfg, rank, world, local):
     stage_ms = per_stage_timing(cfg, stack, x, args.steps, stream)
 
     # ------------------------------------------- timed region 3: end to end
-    e2e_ms, h2d, d2h = e2e_timing(cfg, stack, x, max(2, args.steps // 2), stream, graph=args.graph)
+    e2e_ms, h2d, d2h = e2e_timing(cfg, stack, x, max(2, args.steps), stream, graph=args.graph)
     clocks = sampler.stop() if sampler else None
     st, code = fs.fs_get_error()
     if st != 0:
@@ -556,7 +556,7 @@ def run_train(args, cfg, rank, world, local):
     # end to end: x and dO from pinned host memory, dx back to the host, every step;
     # double-buffered like the inference stack: step i+1's inputs go up and step
     # i's dx comes down on a copy stream while step i+1 computes
-    e2e_ms = train_e2e_pipelined(tr, x, dO, max(2, args.steps // 2), stream)
+    e2e_ms = train_e2e_pipelined(tr, x, dO, max(2, args.steps), stream)
     clocks = sampler.stop() if sampler else None
     st, code = fs.fs_get_error()
     if st != 0:
