@@ -112,27 +112,38 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* mt_start, const in
     return r;
 }
 
-// v[j] <- (v[j] * sa) * sb[j] for 32 fp32 accumulator columns.
-__device__ __forceinline__ void scale_cols32(uint32_t* v, float sa, const float* sb) {
-    const float4* s4 = reinterpret_cast<const float4*>(sb);
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-        const float4 b = __ldg(s4 + q4);
-        const float f[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[4 * q4 + i] = __float_as_uint((__uint_as_float(v[4 * q4 + i]) * sa) * f[i]);
-    }
+// FP8 dequantisation scales of one epilogue thread: its A row's scale, and
+// the B scales of the 128 tile columns its warp covers (half `half` of the
+// tile), spread over the lanes: lane l holds columns 4l .. 4l + 3 of the half.
+// Loaded before the accumulator is ready, so the loads' latency overlaps the
+// tile's MMAs instead of stalling each column block of the epilogue.
+struct EpiScales {
+    float sa = 1.0f;
+    float4 sb = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+};
+
+__device__ __forceinline__ EpiScales load_epi_scales(const float* a_scale, const float* b_scale, int N, int g, int n,
+                                                     long long orow, bool row_ok, int half, int lane) {
+    EpiScales s;
+    if (row_ok) s.sa = __ldg(a_scale + orow);
+    static_assert(tc::BN == 256, "the epilogue's B scales cover 2 x 128 columns per tile");
+    const int col = n * tc::BN + half * (tc::BN / 2) + 4 * lane;
+    if (col < N) s.sb = __ldg(reinterpret_cast<const float4*>(b_scale + static_cast<long long>(g) * N + col));
+    return s;
 }
 
-// v[j] <- (v[j] * sa) * sb[j] for 16 fp32 accumulator columns.
-__device__ __forceinline__ void scale_cols16(uint32_t* v, float sa, const float* sb) {
-    const float4* s4 = reinterpret_cast<const float4*>(sb);
+// v[j] <- (v[j] * sa) * sb[rel + j] for NC (16 or 32) accumulator columns
+// starting at column rel (a multiple of 16) of the warp's half; the B scales
+// come from the lanes holding them.  Every lane of the warp must call it.
+template <int NC>
+__device__ __forceinline__ void scale_cols(uint32_t* v, const EpiScales& s, int rel) {
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 b = __ldg(s4 + q4);
-        const float f[4] = {b.x, b.y, b.z, b.w};
+    for (int q4 = 0; q4 < NC / 4; ++q4) {
+        const int src = (rel >> 2) + q4;
+        const float f[4] = {__shfl_sync(0xffffffffu, s.sb.x, src), __shfl_sync(0xffffffffu, s.sb.y, src),
+                            __shfl_sync(0xffffffffu, s.sb.z, src), __shfl_sync(0xffffffffu, s.sb.w, src)};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[4 * q4 + i] = __float_as_uint((__uint_as_float(v[4 * q4 + i]) * sa) * f[i]);
+        for (int i = 0; i < 4; ++i) v[4 * q4 + i] = __float_as_uint((__uint_as_float(v[4 * q4 + i]) * s.sa) * f[i]);
     }
 }
 
@@ -177,7 +188,7 @@ __device__ __forceinline__ void store16_resid(void* base, long long off, bool bf
 // the k routed rows' 32-byte pieces are loaded together (k loads in flight).
 template <bool F8>
 __device__ __forceinline__ void epilogue_combine(uint32_t tbase, bool row_ok, long long orow, int n, int c_lo, int c_hi,
-                                                 float sa, const float* sb, const Args& args) {
+                                                 int half, const EpiScales& sc, const Args& args) {
     const CombineEpi& cb = args.cmb;
     const long long d = args.ldo;
     int ps[kCombineEpiMaxK];
@@ -196,8 +207,8 @@ __device__ __forceinline__ void epilogue_combine(uint32_t tbase, bool row_ok, lo
         uint32_t v[16];
         tmem_ld16(tbase + c0, v);
         tmem_ld_wait();
+        if constexpr (F8) scale_cols<16>(v, sc, c0 - half * (BN / 2));
         if (!row_ok) continue;
-        if constexpr (F8) scale_cols16(v, sa, sb + c0);
         const long long col = static_cast<long long>(n) * BN + c0;
         uint4 yr[kCombineEpiMaxK][2];
 #pragma unroll
@@ -266,7 +277,7 @@ __device__ __forceinline__ void store_piece_bf16(const CUtensorMap* tmo, uint8_t
 
 template <int EPI, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, int rows_valid, int n, int r, int half,
-                                              const Args& args, const CUtensorMap* tmo = nullptr,
+                                              const Args& args, const EpiScales& sc, const CUtensorMap* tmo = nullptr,
                                               uint8_t* piece = nullptr) {
     const Tile tl{g, 0, n, a_row, rows_valid, 0};
     const bool row_ok = r < tl.rows_valid;
@@ -276,11 +287,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
     const int lane = r & 31, q32 = r & ~31;
     const bool piece_ok = tmo != nullptr && q32 + 32 <= tl.rows_valid;
     const long long orow = static_cast<long long>(tl.a_row + r);
-    float sa = 1.0f;
-    if constexpr (F8) {
-        if (row_ok) sa = __ldg(args.a_scale + orow);
-    }
-    const float* sb = F8 ? args.b_scale + static_cast<long long>(g) * args.N + tl.n * BN : nullptr;
     if constexpr (EPI == EPI_SWIGLU) {
         // packed tile columns: [gate 64 | up 64] x 2 -> 128 expert columns
         const int rem = args.N - tl.n * BN;
@@ -293,21 +299,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                 tmem_ld32(tbase + g2 * 128 + j0, gv);
                 tmem_ld32(tbase + g2 * 128 + 64 + j0, uv);
                 tmem_ld_wait();
+                if constexpr (F8) {          // g2 == half: gate columns j0.., up columns 64 + j0.. of the half
+                    scale_cols<32>(gv, sc, j0);
+                    scale_cols<32>(uv, sc, 64 + j0);
+                }
                 if (row_ok) {
-                    if constexpr (F8) {
-                        const float4* sg4 = reinterpret_cast<const float4*>(sb + g2 * 128 + j0);
-                        const float4* su4 = reinterpret_cast<const float4*>(sb + g2 * 128 + 64 + j0);
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            const float4 a = __ldg(sg4 + q4), b = __ldg(su4 + q4);
-                            const float fg[4] = {a.x, a.y, a.z, a.w}, fu[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                gv[4 * q4 + i] = __float_as_uint((__uint_as_float(gv[4 * q4 + i]) * sa) * fg[i]);
-                                uv[4 * q4 + i] = __float_as_uint((__uint_as_float(uv[4 * q4 + i]) * sa) * fu[i]);
-                            }
-                        }
-                    }
                     if (args.aux) {   // training forward: keep g, a (bf16) for the backward
                         uint32_t pg[16], pu[16];
 #pragma unroll
@@ -353,8 +349,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
             uint32_t v[32];
             tmem_ld32(tbase + c0, v);
             tmem_ld_wait();
+            if constexpr (F8) scale_cols<32>(v, sc, c0 - half * (BN / 2));
             if (row_ok) {
-                if constexpr (F8) scale_cols32(v, sa, sb + c0);
                 uint32_t pk[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
@@ -372,8 +368,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
     } else if constexpr (EPI == EPI_COMBINE) {
         const int rem = args.out_cols - tl.n * BN;
         const int ncols = rem >= BN ? BN : rem;
-        epilogue_combine<F8>(tbase, row_ok, orow, tl.n, half * (BN / 2), min(ncols, (half + 1) * (BN / 2)), sa,
-                             sb, args);
+        epilogue_combine<F8>(tbase, row_ok, orow, tl.n, half * (BN / 2), min(ncols, (half + 1) * (BN / 2)), half,
+                             sc, args);
     } else if constexpr (EPI == EPI_DSWIGLU) {
         // accumulator = dh of hidden columns j = 256 n + c; g_j, a_j sit at packed
         // columns 128 (j / 64) + j % 64 and that + 64 of the aux row, and dg, da
@@ -436,8 +432,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
             uint32_t v[32];
             tmem_ld32(tbase + c0, v);
             tmem_ld_wait();
+            if constexpr (F8) scale_cols<32>(v, sc, c0 - half * (BN / 2));
             if (piece_ok && ncols - c0 >= 32) {       // two 32 x 16 fp32 pieces through TMA stores (adds)
-                if constexpr (F8) scale_cols32(v, sa, sb + c0);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[16];
@@ -446,7 +442,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int g, int a_row, 
                     store_piece_bf16(tmo, piece, pk, lane, tl.n * BN + c0 + 16 * h, tl.a_row + q32, args.accumulate != 0);
                 }
             } else if (row_ok) {
-                if constexpr (F8) scale_cols32(v, sa, sb + c0);
                 float* dst = Z + orow * args.ldo + tl.n * BN + c0;
                 const int nv = ncols - c0 >= 32 ? 32 : ncols - c0;
                 if (args.accumulate) {
@@ -678,13 +673,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const Tile tl = decode_tile(tt, mt_start, row_start, G, args.n_tiles, BN, args.N);
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
+            EpiScales sc;
+            if constexpr (F8)
+                sc = load_epi_scales(args.a_scale, args.b_scale, args.N, tl.g, tl.n, static_cast<long long>(tl.a_row) + r,
+                                     r < tl.rows_valid, half, lane);
             if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             // K range ks of a split GEMM goes to its own partial, split_rows rows further on
             epilogue_tile<EPI, F8>(tbase, tl.g, tl.a_row + static_cast<int>(ks * args.split_rows), tl.rows_valid, tl.n, r,
-                                   half, args,
+                                   half, args, sc,
                                    args.tma_out ? &tmO : nullptr, smem + PIECE_OFF + (warp - 2) * PIECE_BYTES);
             tc_fence_before();
             __syncwarp();
@@ -881,11 +880,15 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             rows_valid = rows_valid < 0 ? 0 : (rows_valid > 128 ? 128 : rows_valid);
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
+            EpiScales sc;
+            if constexpr (F8)
+                sc = load_epi_scales(args.a_scale, args.b_scale, args.N, tl.g, tl.n, static_cast<long long>(a_row) + r,
+                                     r < rows_valid, half, lane);
             if (!mbar_wait(smem_u32(&tfull[acc]), use & 1u, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            epilogue_tile<EPI, F8>(tbase, tl.g, a_row, rows_valid, tl.n, r, half, args);
+            epilogue_tile<EPI, F8>(tbase, tl.g, a_row, rows_valid, tl.n, r, half, args, sc);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(map_to_cta(smem_u32(&tempty[acc]), 0));
