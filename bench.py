@@ -303,7 +303,7 @@ def run_ours(args, cfg, rank, world, local):
         "breakdown_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "schedule": "double-buffered: step i+1's H2D and step i's D2H on a copy stream beside step i's compute"
+                "schedule": "double-buffered: step i+1's H2D and step i's D2H on two copy streams beside step i's compute"
                 if not args.graph else "one CUDA graph replayed per step, copies in between"},
         "gpu_launches": int(launches * args.steps),
         "gpu_launches_per_step": int(launches),
@@ -400,13 +400,17 @@ def e2e_timing(cfg, stack, x, steps, stream, graph=False):
 
 
 def e2e_timing_pipelined(stack, x, steps, stream):
+    """Uploads on one copy stream and downloads on another (separate copy engines;
+    with both directions on one stream the overlap with compute depended on the
+    box), step i+1's upload issued before step i's download."""
     from mixture_experts_layer_expert_gb300 import fs
 
     x_host = x.cpu().pin_memory()
     o_host = torch.empty(stack.o_full.shape, dtype=stack.o_full.dtype).pin_memory()
     xs = [torch.empty_like(x) for _ in range(2)]
     outs = [(torch.empty_like(stack.o_full), torch.empty_like(stack.o_partial)) for _ in range(2)]
-    cs = torch.cuda.Stream(device=x.device)
+    cs = torch.cuda.Stream(device=x.device)      # uploads
+    cd = torch.cuda.Stream(device=x.device)      # downloads
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
     L = len(stack.blocks)
 
@@ -419,8 +423,8 @@ def e2e_timing_pipelined(stack, x, steps, stream):
         ev["h2d"][b].record(cs)
 
     def run(n):
-        # copy-stream order: upload(i+1) before download(i), so the next input
-        # arrives during this step's compute and this result leaves during the next
+        # the next input arrives during this step's compute and this result
+        # leaves during the next
         upload(0)
         for i in range(n):
             b = i % 2
@@ -432,18 +436,20 @@ def e2e_timing_pipelined(stack, x, steps, stream):
             ev["comp"][b].record(stream)
             if i + 1 < n:
                 upload(i + 1)
-            cs.wait_event(ev["comp"][b])
-            with torch.cuda.stream(cs):
+            cd.wait_event(ev["comp"][b])
+            with torch.cuda.stream(cd):
                 o_host.copy_(outs[b][0], non_blocking=True)
-            ev["d2h"][b].record(cs)
+            ev["d2h"][b].record(cd)
 
-    run(2)
+    run(2)                                    # untimed: first writes into the new device buffers
     torch.cuda.synchronize()
     e0, e1 = cuda_events(2)
     e0.record(stream)
     cs.wait_event(e0)
+    cd.wait_event(e0)
     run(steps)
     stream.wait_stream(cs)
+    stream.wait_stream(cd)
     e1.record(stream)
     torch.cuda.synchronize()
     nb = x.numel() * x.element_size()
