@@ -286,14 +286,15 @@ static fs_status dispatch_impl(const fs_layer_desc* d, const int32_t* idx, const
 // (bf16) is quantised per row into hq before the down GEMM.
 // With cmb set (one group over the T token rows, tensor-core dtypes) the down
 // projection's epilogue is Combine fused with the FarSkip update (y unused).
-// plan2 (nullable): room for a second plan, used when the down projection runs
-// on the CTA-pair kernel (tc_down_pair) while the gate/up GEMM does not.
+// plan2 (nullable): room for a second plan, used when one of the two GEMMs runs
+// on the CTA-pair kernel (tc_down_pair, tc_up_pair) and the other does not.
 static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_rows, const int32_t* gather, int rows,
                              const int32_t* offsets, int G, int cw, const void* w13, const void* w3, void* y,
                              bool y_f32, int* plan, void* h, void* hq, cudaStream_t st, void* gu_save = nullptr,
                              const CombineEpi* cmb = nullptr, int* plan2 = nullptr) {
-    // down projection on CTA pairs: its own plan of 256-row tiles
+    // down (dp) or gate/up (up) projection on CTA pairs: its own plan of 256-row tiles
     const bool dp = plan2 && tc_down_pair() && tc_block_m() == 128;
+    const bool up = plan2 && tc_up_pair() && tc_block_m() == 128 && !gather;
     const int max_mt2 = ceil_div(rows, 256) + G;
     if (is_mx(d)) {
         // x: an MX matrix of x_rows rows (a multiple of 128 or the token count);
@@ -314,10 +315,11 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         const float* xs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x) + fp8_scale_offset(x_rows, d->d));
         const float* hs = reinterpret_cast<const float*>(static_cast<const uint8_t*>(hq) + fp8_scale_offset(rows, cw));
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
+        if (dp || up) FS_TRY(launch_plan(offsets, G, rows, 256, plan2, st));
         FS_TRY(launch_tc_gemm_f8(EPI_SWIGLU, x, x_rows, xs, w13, packed_scales_fp8(w13, G, 2 * cw, d->d), G, 2 * cw,
-                                 d->d, plan, max_mt, h, cw, cw, st));
+                                 d->d, up ? plan2 : plan, up ? max_mt2 : max_mt, h, cw, cw, st, nullptr,
+                                 up ? 1 : -1));
         FS_TRY(launch_quant_rows(h, rows, cw, hq, st));
-        if (dp) FS_TRY(launch_plan(offsets, G, rows, 256, plan2, st));
         FS_TRY(launch_tc_gemm_f8(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), hq, rows, hs, w3,
                                  packed_scales_fp8(w3, G, d->d, cw), G, d->d, cw, dp ? plan2 : plan,
                                  dp ? max_mt2 : max_mt, y, d->d, d->d, st, cmb, dp ? 1 : -1));
@@ -325,17 +327,16 @@ static fs_status swiglu_impl(const fs_layer_desc* d, const void* x, long long x_
         const int bm = tc_block_m();
         const int max_mt = ceil_div(rows, bm) + G;
         FS_TRY(launch_plan(offsets, G, rows, bm, plan, st));
+        if (dp || up) FS_TRY(launch_plan(offsets, G, rows, 256, plan2, st));
         TcExtra ex;
         ex.aux = gu_save;            // training forward: keep the pre-activations for the backward
         ex.aux_ld = 2LL * cw;
-        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, plan, max_mt, h, cw, cw, gather, rows,
-                              true, st, &ex));
+        if (up) ex.variant = 1;
+        FS_TRY(launch_tc_gemm(EPI_SWIGLU, x, x_rows, w13, G, 2 * cw, d->d, up ? plan2 : plan, up ? max_mt2 : max_mt,
+                              h, cw, cw, gather, rows, true, st, &ex));
         TcExtra ex2;
         ex2.combine = cmb;
-        if (dp) {
-            FS_TRY(launch_plan(offsets, G, rows, 256, plan2, st));
-            ex2.variant = 1;
-        }
+        if (dp) ex2.variant = 1;
         FS_TRY(launch_tc_gemm(cmb ? EPI_COMBINE : (y_f32 ? EPI_F32 : EPI_BF16), h, rows, w3, G, d->d, cw,
                               dp ? plan2 : plan, dp ? max_mt2 : max_mt, y, d->d, d->d, nullptr, 0, true, st, &ex2));
     } else {

@@ -1370,18 +1370,22 @@ cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan
 }
 
 // Kernel variant: the single-CTA kernel, or the CTA-pair kernel when the
-// environment sets FS_TC_VARIANT=pair; FS_TC_VARIANT=pair_down keeps the
-// single-CTA kernel except for the forward down projections.
+// environment sets FS_TC_VARIANT=pair; FS_TC_VARIANT=pair_down (pair_up) keeps
+// the single-CTA kernel except for the forward down (gate/up) projections.
 static int variant_mode() {
     static int mode = -1;
     if (mode < 0) {
         const char* e = getenv("FS_TC_VARIANT");
-        mode = (e && std::strcmp(e, "pair") == 0) ? 1 : ((e && std::strcmp(e, "pair_down") == 0) ? 2 : 0);
+        mode = 0;
+        if (e && std::strcmp(e, "pair") == 0) mode = 1;
+        if (e && std::strcmp(e, "pair_down") == 0) mode = 2;
+        if (e && std::strcmp(e, "pair_up") == 0) mode = 3;
     }
     return mode;
 }
 static bool use_pair() { return variant_mode() == 1; }
 bool tc_down_pair() { return variant_mode() == 2; }
+bool tc_up_pair() { return variant_mode() == 3; }
 
 template <int EPI>
 static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B, int G, int N, int K,

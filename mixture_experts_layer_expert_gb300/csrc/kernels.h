@@ -95,8 +95,10 @@ cudaError_t launch_tc_gemm_f8(int epi, const void* A, long long a_rows, const fl
                               long long ldo, int out_cols, cudaStream_t st, const CombineEpi* combine = nullptr,
                               int variant = -1);
 // The forward down projections (y = h W3^T) on the CTA-pair kernel while the
-// other GEMMs keep the library-wide variant (FS_TC_VARIANT=pair_down).
+// other GEMMs keep the library-wide variant (FS_TC_VARIANT=pair_down); the
+// forward gate/up projections on it (FS_TC_VARIANT=pair_up).
 bool tc_down_pair();
+bool tc_up_pair();
 
 // Tensor maps (gemm_tc.cu): a [rows, cols] row-major matrix of bf16 (f8: 8-bit
 // codes) with a box_rows x 128-byte box and the 128-byte swizzle; the tiled
