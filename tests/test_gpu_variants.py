@@ -8,6 +8,7 @@ comparisons of the grouped and shared expert GEMMs (bf16 and FP8) and of the
 small FarSkip stacks: the same tolerances, the same seeded inputs.
 """
 import os
+import re
 import subprocess
 import sys
 
@@ -30,8 +31,13 @@ CASES = [
 def test_kernel_variant_against_oracle(variant):
     env = dict(os.environ, FS_TC_VARIANT=variant)
     env.pop("FS_PARITY_LOG", None)
-    cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider"] + CASES
-    r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, env=env, cwd=ROOT)
+    cmd = [sys.executable, "-m", "pytest", "-q", "-m", "gpu", "-p", "no:cacheprovider"]
+    c = subprocess.run(cmd + ["--collect-only"] + CASES, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    n = re.search(r"(\d+) tests? collected", c.stdout)
+    assert n, c.stdout[-2000:]
+    r = subprocess.run(cmd + ["-x"] + CASES, capture_output=True, text=True, timeout=900, env=env, cwd=ROOT)
     tail = "\n".join((r.stdout + r.stderr).strip().splitlines()[-15:])
     assert r.returncode == 0, "FS_TC_VARIANT=%s:\n%s" % (variant, tail)
-    assert " passed" in r.stdout, tail
+    m = re.search(r"(\d+) passed", r.stdout)
+    assert m and m.group(1) == n.group(1), tail      # every parametrised case of CASES ran
+    print("FS_TC_VARIANT=%s: %s cases passed" % (variant, m.group(1)))
