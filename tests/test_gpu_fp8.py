@@ -124,7 +124,8 @@ def _rand_topk(T, E, k, seed):
     return torch.rand((T, E), generator=g).argsort(dim=1)[:, :k].to(torch.int32).contiguous()
 
 
-@pytest.mark.parametrize("T,E,k,d", [(1, 8, 2, 128), (300, 8, 2, 256), (2049, 64, 6, 384), (1000, 256, 8, 7168)])
+@pytest.mark.parametrize("T,E,k,d", [(1, 8, 2, 128), (300, 8, 2, 256), (2049, 64, 6, 384), (1000, 256, 8, 7168),
+                                     (257, 512, 16, 128)])     # the largest E and k the library takes
 def test_dispatch_fp8_bit_exact(fs, T, E, k, d):
     cfg = small(T=T, E=E, k=k, d=d)
     desc = fs.make_desc(cfg)

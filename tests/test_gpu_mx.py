@@ -140,7 +140,8 @@ def _padded(counts):
     return offs
 
 
-@pytest.mark.parametrize("T,E,k,d", [(1, 8, 2, 128), (300, 8, 2, 256), (2049, 64, 6, 384), (1000, 256, 8, 7168)])
+@pytest.mark.parametrize("T,E,k,d", [(1, 8, 2, 128), (300, 8, 2, 256), (2049, 64, 6, 384), (1000, 256, 8, 7168),
+                                     (257, 512, 16, 128)])     # the largest E and k the library takes
 def test_dispatch_mx_bit_exact(fs, T, E, k, d):
     """Counts as the counting sort gives them; offsets the exclusive prefix of the
     counts rounded up to 128; each (token, slot) at its padded segment start plus
