@@ -105,16 +105,20 @@ gather_sum_kernel(const uint4* __restrict__ dx_perm, const int32_t* __restrict__
     if (t >= T) return;
     const int nv = d / 8;
     const int my_p = lane < k ? pos[static_cast<long long>(t) * k + lane] : -1;
-    for (int v = lane; v < nv; v += 32) {
+    // steps counted for the whole warp: every lane takes part in the shuffles
+    for (int v0 = 0; v0 < nv; v0 += 32) {
+        const int v = v0 + lane;
+        const bool act = v < nv;
         float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int s = 0; s < k; ++s) {
             const int p = __shfl_sync(0xffffffffu, my_p, s);
-            if (p < 0) continue;
+            if (p < 0 || !act) continue;
             float x[8];
             unpack8(__ldg(dx_perm + static_cast<long long>(p) * nv + v), x);
 #pragma unroll
             for (int i = 0; i < 8; ++i) sum[i] += x[i];
         }
+        if (!act) continue;
         float4* o = reinterpret_cast<float4*>(du + static_cast<long long>(t) * d + 8 * v);
         const float4 a = o[0], b = o[1];
         o[0] = make_float4(a.x + sum[0], a.y + sum[1], a.z + sum[2], a.w + sum[3]);

@@ -7,7 +7,9 @@
 // In every kernel a warp walks a row 8 elements (one 16-byte vector) per lane
 // and step, so the 4 lanes 4q .. 4q+3 of a step hold one 32-element block:
 // its largest magnitude is a 4-lane shuffle maximum, and lane 4q writes the
-// block's scale byte.
+// block's scale byte.  The steps are counted for the whole warp (a row of
+// 16-byte vectors that is not a multiple of 32 leaves lanes idle in its last
+// step, they still take part in the shuffles).
 #include "kernels.h"
 #include "mx.cuh"
 
@@ -29,13 +31,17 @@ quant_rows_mx_kernel(const uint4* __restrict__ x, long long rows, int cols, uint
     const long long r128 = mx_rows128(rows);
     for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < r128; r += nwarps) {
         uint2* dst = reinterpret_cast<uint2*>(q + r * cols);
-        for (int v = lane; v < nv; v += 32) {
+        for (int v0 = 0; v0 < nv; v0 += 32) {
+            const int v = v0 + lane;
+            const bool act = v < nv;
             if (r < rows) {
-                const uint4 a = __ldg(x + r * nv + v);
+                const uint4 a = act ? __ldg(x + r * nv + v) : make_uint4(0, 0, 0, 0);
                 const MxQuant m = mx_quant(group4_max(absmax_bf16x8(a)));
-                dst[v] = mx_codes(a, m);
-                if ((lane & 3) == 0) sf[mx_sf_byte(r, v / 4, cols)] = m.ue8m0;
-            } else {
+                if (act) {
+                    dst[v] = mx_codes(a, m);
+                    if ((lane & 3) == 0) sf[mx_sf_byte(r, v / 4, cols)] = m.ue8m0;
+                }
+            } else if (act) {
                 dst[v] = make_uint2(0, 0);
                 if ((lane & 3) == 0) sf[mx_sf_byte(r, v / 4, cols)] = 127;
             }
@@ -57,18 +63,20 @@ dispatch_copy_mx_kernel(const uint4* __restrict__ u, int T, int d, int k, const 
     uint8_t* xsf = x_q + mx_sf_offset(rows_cap, d);
     uint8_t* usf = u_q ? u_q + mx_sf_offset(T, d) : nullptr;
     const uint4* src = u + static_cast<long long>(t) * nv;
-    for (int v = lane; v < nv; v += 32) {
-        const uint4 a = __ldg(src + v);
+    for (int v0 = 0; v0 < nv; v0 += 32) {
+        const int v = v0 + lane;
+        const bool act = v < nv;
+        const uint4 a = act ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
         const MxQuant m = mx_quant(group4_max(absmax_bf16x8(a)));
         const uint2 c = mx_codes(a, m);
         const bool lead = (lane & 3) == 0;
         for (int s = 0; s < k; ++s) {
             const int p = __shfl_sync(0xffffffffu, my_p, s);
-            if (p < 0) continue;
+            if (p < 0 || !act) continue;
             reinterpret_cast<uint2*>(x_q + static_cast<long long>(p) * d)[v] = c;
             if (lead) xsf[mx_sf_byte(p, v / 4, d)] = m.ue8m0;
         }
-        if (u_q) {
+        if (u_q && act) {
             reinterpret_cast<uint2*>(u_q + static_cast<long long>(t) * d)[v] = c;
             if (lead) usf[mx_sf_byte(t, v / 4, d)] = m.ue8m0;
         }
@@ -89,18 +97,22 @@ pack_mx_kernel(PackSrc src, int G, int NB, uint8_t* __restrict__ codes, uint8_t*
         const int nr = static_cast<int>(R - g * NB * 256);
         const int nb = nr >> 8, rr = nr & 255;
         uint8_t* blk0 = codes + ((g * NB + nb) * KB) * 32768LL + rr * 128;
-        for (int v = lane; v < nv; v += 32) {
+        for (int v0 = 0; v0 < nv; v0 += 32) {
+            const int v = v0 + lane;
+            const bool act = v < nv;
             const int kk = 8 * v;
             uint2 c = make_uint2(0, 0);
             uint8_t byte = 127;
             if (nr < N) {
-                const uint4 a = __ldg(src.chunk(g, nr, v));
+                const uint4 a = act ? __ldg(src.chunk(g, nr, v)) : make_uint4(0, 0, 0, 0);
                 const MxQuant m = mx_quant(group4_max(absmax_bf16x8(a)));
                 c = mx_codes(a, m);
                 byte = m.ue8m0;
             }
-            *reinterpret_cast<uint2*>(blk0 + (kk >> 7) * 32768LL + (kk & 127)) = c;
-            if ((lane & 3) == 0) sf[mx_w_sf_byte(g, NB, nb, rr, v / 4, K)] = byte;
+            if (act) {
+                *reinterpret_cast<uint2*>(blk0 + (kk >> 7) * 32768LL + (kk & 127)) = c;
+                if ((lane & 3) == 0) sf[mx_w_sf_byte(g, NB, nb, rr, v / 4, K)] = byte;
+            }
         }
     }
 }
