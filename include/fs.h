@@ -387,8 +387,9 @@ fs_status fs_farskip_stack(const fs_layer_desc* desc, int32_t L, int32_t wiring,
  * u_{k+1}, while `stream` runs the routed experts and the final
  * o_k = o_k* + R_k; block k+1's router/dispatch/shared thus run concurrently
  * with block k's routed grouped GEMMs.  Bit-identical to fs_farskip_stack.
- * wiring must be FS_WIRE_PARTIAL or FS_WIRE_OUTDATED; stream2 != stream;
- * FS_MXFP8 is not supported here (FS_ERR_UNSUPPORTED).
+ * wiring must be FS_WIRE_PARTIAL or FS_WIRE_OUTDATED; stream2 != stream.
+ * Every dtype (FS_FP8 / FS_MXFP8: stream2's Dispatch also quantises u_k for
+ * the shared experts).
  * Work queued on `stream` before the call is complete before stream2 starts,
  * and work queued on `stream` after the call sees all of the stack's results.
  * Needs ws of fs_workspace_bytes_overlap(desc, L) bytes.  The library keeps

@@ -195,6 +195,7 @@ static OverlapLayout layout_overlap(const fs_layer_desc* d, int L) {
     const size_t es = elem_bytes(d);
     const size_t T = d->T, E = d->E, k = d->k, dm = d->d;
     const size_t rows = T * k;
+    const long long prow = perm_rows(d);     // MX: every expert's segment padded to 128 rows
     OverlapLayout l;
     size_t o = layout(d, 0).end0;
     l.end0 = o;
@@ -207,14 +208,16 @@ static OverlapLayout layout_overlap(const fs_layer_desc* d, int L) {
         l.counts[i] = on ? take(E * 4) : 0;
         l.offsets[i] = on ? take((E + 1) * 4) : 0;
         l.pos[i] = on ? take(rows * 4) : 0;
-        l.perm[i] = on ? take(rows * 4) : 0;
-        l.x_perm[i] = on ? take(is_fp8(d) ? fp8_rows_bytes(static_cast<long long>(rows), d->d) : rows * dm * es) : 0;
+        l.perm[i] = on ? take(static_cast<size_t>(prow) * 4) : 0;
+        l.x_perm[i] = on ? take(is_fp8(d) ? fp8_rows_bytes(static_cast<long long>(rows), d->d)
+                                          : (is_mx(d) ? mx_rows_bytes(prow, d->d) : rows * dm * es))
+                         : 0;
         l.s_out[i] = on ? take(T * dm * 4) : 0;
         l.ostar[i] = on ? take(T * dm * 4) : 0;
         l.oring[i] = on ? take(T * dm * 4) : 0;
         l.ubuf[i] = on ? take(T * dm * es) : 0;
     }
-    l.y_perm = take(rows * dm * es);
+    l.y_perm = take(static_cast<size_t>(prow) * dm * es);
     l.end = o;
     return l;
 }
@@ -822,7 +825,6 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
     if (L < 1 || !blocks) return FS_ERR_INVALID_ARG;
     if (wiring != FS_WIRE_PARTIAL && wiring != FS_WIRE_OUTDATED) return FS_ERR_INVALID_ARG;
     if (!stream2 || stream2 == stream) return FS_ERR_INVALID_ARG;
-    if (is_mx(desc)) return FS_ERR_UNSUPPORTED;
     FS_CHECK(need(x));
     FS_CHECK(need(o_full));
     if (o_partial && !aligned16(o_partial)) return FS_ERR_UNSUPPORTED;
@@ -847,7 +849,8 @@ fs_status fs_farskip_stack_overlap(const fs_layer_desc* desc, int32_t L, int32_t
     cudaStream_t sb = static_cast<cudaStream_t>(stream2);    // router, dispatch, shared expert, o_k*
     const int act = act_dtype(desc);
     void* y_perm = at<void>(ws, l.y_perm);
-    void* u_q = is_fp8(desc) && desc->n_shared > 0 ? at<void>(ws, layout(desc, 0).uq) : nullptr;
+    // FP8 / MX: Dispatch also writes the quantised u_k for the shared experts (both on stream2)
+    void* u_q = qmode(desc) != kQuantNone && desc->n_shared > 0 ? at<void>(ws, layout(desc, 0).uq) : nullptr;
 
     // fork: stream2 starts after everything already queued on stream (x ready)
     FS_TRY(cudaEventRecord(evA, sa));

@@ -249,13 +249,20 @@ def test_small_stack_mx_gates(fs, gate, E, k, ns):
     _check_stack(cfg, synth.make_problem(cfg, DEV), "partial")
 
 
-def test_overlap_stack_rejects_mx(fs):
-    cfg = small(T=64, L=1)
+@pytest.mark.parametrize("wiring,L,ns", [("partial", 3, 1), ("outdated", 2, 1), ("partial", 2, 0)])
+def test_overlap_stack_mx_matches_sequential(fs, wiring, L, ns):
+    """The two-stream schedule on the MX path (stream2's Dispatch also quantising
+    u_k for the shared experts; padded expert segments in both slots) against
+    the one-stream stack, which the tests above check against the oracle."""
+    cfg = small(T=700, E=16, k=4, gate="sigmoid_norm", L=L, n_shared=ns, c_shared=128 if ns else 0)
     prob = synth.make_problem(cfg, DEV)
-    stack = fs.FarSkipStack(cfg, prob["blocks"])
-    with pytest.raises(fs.FsError) as e:
-        stack.forward_overlap(prob["x"])
-    assert e.value.status == 2
+    stack = fs.FarSkipStack(cfg, prob["blocks"], wiring=wiring)
+    o, o_star = stack.forward(prob["x"])
+    o, o_star = o.clone(), o_star.clone()
+    o2, o2_star = stack.forward_overlap(prob["x"])
+    torch.cuda.synchronize()
+    assert fs.fs_get_error() == (0, 0)
+    assert torch.equal(o2, o) and torch.equal(o2_star, o_star)
 
 
 ROWS_MX = {"v3_mxfp8": 1024, "v3_decode_mxfp8": None, "qwen3_mxfp8": 2048}
