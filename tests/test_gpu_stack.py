@@ -351,7 +351,9 @@ def test_attn_standin_gemm(fs):
 
 @pytest.mark.parametrize("wiring,L,dtype", [("attn_farskip", 1, "bf16"), ("attn_farskip", 3, "bf16"),
                                            ("attn_plain", 2, "bf16"), ("attn_plain", 3, "bf16"),
-                                           ("attn_farskip", 2, "f32"), ("attn_plain", 2, "f32")])
+                                           ("attn_farskip", 2, "f32"), ("attn_plain", 2, "f32"),
+                                           ("attn_farskip", 2, "fp8"), ("attn_plain", 2, "fp8"),
+                                           ("attn_farskip", 2, "mxfp8"), ("attn_plain", 2, "mxfp8")])
 def test_attention_wirings_stack(fs, wiring, L, dtype):
     """fs_farskip_stack with a stand-in attention sub-block per layer vs the oracle.
     The stack is first checked bit for bit against the same layers driven through
