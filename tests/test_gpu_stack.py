@@ -427,7 +427,8 @@ def test_attention_wirings_stack(fs, wiring, L, dtype):
     record("attention_end_to_end", wiring=wiring, L=L, dtype=dtype, **st)
 
 
-@pytest.mark.parametrize("dtype,overlap", [("bf16", False), ("bf16", True), ("fp8", False)])
+@pytest.mark.parametrize("dtype,overlap", [("bf16", False), ("bf16", True), ("fp8", False), ("fp8", True),
+                                           ("mxfp8", False), ("mxfp8", True)])
 def test_graph_replay_matches_eager(fs, dtype, overlap):
     """The stack captured once as a CUDA graph and replayed gives the same bits as
     the eager call, also after the input buffer is refilled."""
