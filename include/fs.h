@@ -33,6 +33,13 @@
  *   - Workspace: `ws` is caller-owned device scratch of at least
  *     fs_workspace_bytes(desc, L) bytes (L = 0 for the single-step calls),
  *     256-byte aligned.  Contents need not be initialised.
+ *   - Environment, read once per process: FS_TC_VARIANT=pair runs the bf16 and
+ *     FP8 tensor-core GEMMs on the CTA-pair kernel (256-row tiles over two SMs),
+ *     pair_down / pair_up only the experts' down / gate/up projections; unset,
+ *     the single-CTA kernel (the faster one under this GPU's power cap).  Every
+ *     variant gives results within the same bounds of the definition; the
+ *     gathered-row GEMM (fs_grouped_swiglu_gather) has no pair form and answers
+ *     FS_ERR_UNSUPPORTED under FS_TC_VARIANT=pair.
  */
 #ifndef FARSKIP_FS_H
 #define FARSKIP_FS_H
