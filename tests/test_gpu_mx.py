@@ -265,7 +265,9 @@ def test_overlap_stack_mx_matches_sequential(fs, wiring, L, ns):
     assert torch.equal(o2, o) and torch.equal(o2_star, o_star)
 
 
-ROWS_MX = {"v3_mxfp8": 1024, "v3_decode_mxfp8": None, "qwen3_mxfp8": 2048}
+# V2-Lite: L = 4, c = 1408 (11 stages of 128 along the down projection's
+# contraction; weight rows of 176 16-byte vectors, not a multiple of 32)
+ROWS_MX = {"v3_mxfp8": 1024, "v3_decode_mxfp8": None, "qwen3_mxfp8": 2048, "v2lite_mxfp8": 1024}
 
 
 @pytest.mark.slow
