@@ -397,14 +397,9 @@ template <int EPI>
 static cudaError_t launch_mx_impl(const void* A, long long a_rows, const uint8_t* a_sf, const void* B,
                                   const uint8_t* b_sf, int G, int N, int K, const int* plan, int max_mtiles, void* out,
                                   long long ldo, int out_cols, uint8_t* h_sf, cudaStream_t st) {
-    static bool attr_set = false;
-    cudaError_t e;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(mx::mx_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(mx::SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static bool set_mx[kMaxDevices];
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(mx::mx_gemm_kernel<EPI>), mx::SMEM_BYTES, set_mx);
+    if (e != cudaSuccess) return e;
     if (K % 128 || N % 128 || a_rows % 128 || G < 1 || G > kMaxGroups) return cudaErrorInvalidValue;
     CUtensorMap ta, tb, to;
     e = make_map(&ta, A, a_rows, K, 128, true);

@@ -1349,18 +1349,30 @@ static cudaError_t output_map(int epi, bool pair, void* out, long long out_rows,
     return e;
 }
 
-static int g_num_sms = 0;
+static int g_num_sms[kMaxDevices];
 
 cudaError_t num_sms(int* out) {
-    if (!g_num_sms) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_num_sms[dev]) {
+        e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    *out = g_num_sms;
+    *out = g_num_sms[dev];
     return cudaSuccess;
+}
+
+cudaError_t smem_attr_once(const void* fn, size_t bytes, bool (&set)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (set[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) set[dev] = true;
+    return e;
 }
 
 cudaError_t launch_plan(const int* offsets, int G, int n_rows, int bm, int* plan, cudaStream_t st) {
@@ -1394,18 +1406,12 @@ static cudaError_t launch_tc_impl(const void* A, long long a_rows, const void* B
                                   const TcExtra* ex) {
     const bool pair = (ex && ex->variant >= 0) ? ex->variant == 1 : use_pair();
     if (pair && gather_rows) return cudaErrorNotSupported;
-    static bool attr_set[2] = {false, false};
-    cudaError_t e;
-    if (!attr_set[pair]) {
-        if (pair)
-            e = cudaFuncSetAttribute(tc::pair_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(tc::P_SMEM_BYTES));
-        else
-            e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(tc::SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        attr_set[pair] = true;
-    }
+    static bool set_single[kMaxDevices], set_pair[kMaxDevices];
+    cudaError_t e = pair ? smem_attr_once(reinterpret_cast<const void*>(tc::pair_gemm_kernel<EPI>), tc::P_SMEM_BYTES,
+                                          set_pair)
+                         : smem_attr_once(reinterpret_cast<const void*>(tc::grouped_gemm_kernel<EPI>), tc::SMEM_BYTES,
+                                          set_single);
+    if (e != cudaSuccess) return e;
     CUtensorMap ta, tb;
     e = make_map(&ta, A, a_rows, K, gather_rows ? 1 : 128);
     if (e != cudaSuccess) return e;
@@ -1473,18 +1479,12 @@ static cudaError_t launch_tc_f8_impl(const void* A, long long a_rows, const floa
                                      void* out, long long ldo, int out_cols, cudaStream_t st,
                                      const CombineEpi* cmb = nullptr, int variant = -1) {
     const bool pair = variant >= 0 ? variant == 1 : use_pair();
-    static bool attr_set[2] = {false, false};
-    cudaError_t e;
-    if (!attr_set[pair]) {
-        if (pair)
-            e = cudaFuncSetAttribute(tc::pair_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(tc::P_SMEM_BYTES));
-        else
-            e = cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(tc::SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        attr_set[pair] = true;
-    }
+    static bool set_single[kMaxDevices], set_pair[kMaxDevices];
+    cudaError_t e = pair ? smem_attr_once(reinterpret_cast<const void*>(tc::pair_gemm_kernel<EPI, true>),
+                                          tc::P_SMEM_BYTES, set_pair)
+                         : smem_attr_once(reinterpret_cast<const void*>(tc::grouped_gemm_kernel<EPI, true>),
+                                          tc::SMEM_BYTES, set_single);
+    if (e != cudaSuccess) return e;
     if (K % 128 || N % 128) return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
     e = make_map(&ta, A, a_rows, K, 128, true);
@@ -1593,14 +1593,9 @@ cudaError_t launch_wgrad_gemm(const void* A, int lda, const void* B, int ldb, lo
     if (G > 1 && M % 32) return cudaErrorInvalidValue;      // a 32-row piece never spans two groups
     if (remap == 1 && (M % 128 || !out2)) return cudaErrorInvalidValue;
     if (remap == 2 && (G != 1 || M % 32 || split < 32 || split % 32 || N % split)) return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    cudaError_t e;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(tc::wgrad_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tc::W_SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static bool set_w[kMaxDevices];
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(tc::wgrad_gemm_kernel), tc::W_SMEM_BYTES, set_w);
+    if (e != cudaSuccess) return e;
     // the operands as they lie: [P rows, lda] and [P rows, ldb], boxes of 64 rows x 64 columns
     CUtensorMap ta, tb;
     e = make_map(&ta, A, P, lda, 64);

@@ -108,6 +108,11 @@ cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, long long
 cudaError_t make_map_blocked(CUtensorMap* m, const void* base, long long nblocks, int box_rows, bool f8 = false);
 cudaError_t make_out_map_bf16(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo);
 cudaError_t num_sms(int* out);
+// Raise fn's dynamic shared memory limit to `bytes` on the current device, once
+// per device (the attribute belongs to each device's copy of the kernel; set[d]
+// records device d).  num_sms is cached per device too.
+constexpr int kMaxDevices = 64;
+cudaError_t smem_attr_once(const void* fn, size_t bytes, bool (&set)[kMaxDevices]);
 
 // gemm_mx.cu: block-scaled FP8 operands (kind::mxf8f6f4.block_scale).  A is an
 // MX matrix of a_rows (a multiple of 128) rows and K columns (codes A, scale
